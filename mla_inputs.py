@@ -1,0 +1,285 @@
+"""Seeded synthetic workloads for batched paged MLA decode.
+
+This module draws inputs and nothing else: query rows, a paged latent KV pool,
+page tables, KV lengths, packed query offsets and the two scale factors.  It
+holds none of the attention arithmetic, so both the fp64 oracle (``oracle/``)
+and the CUDA library (``paged_mla_decode_03_gb300``) can be fed from it without
+sharing any computation.
+
+Shapes follow the problem statement of the FlashInfer page
+"prims_ts_batch_decode_with_kv_cache_mla" (signature and parameter text):
+
+* fixed query   ``[B, SQ, H, 576]``; packed query ``[total_q, H, 576]`` with
+  ``qo_indptr`` holding B + 1 cumulative offsets;
+* ``kv_cache``  ``[num_pages, page_size, 576]`` (512 latent + 64 RoPE dims, one
+  copy: V is the first 512 dims of the same rows);
+* ``block_tables`` ``[B, max_pages_per_req]`` int32, ``seq_lens`` ``[B]`` int32.
+
+Values are N(0, 1) rounded to bf16 (round-to-nearest-even).  The fp8 variant
+quantises N(0, 1) KV to e4m3 with a per-tensor ``k_scale = amax / 448`` and
+folds it into both scales, as the vLLM ``FlashInferMLAImpl.forward_mqa`` page
+does for a quantised cache (``bmm1 *= k_scale``, ``bmm2 *= k_scale``).
+
+Memory the computation must never touch is poisoned: rows at or past
+``seq_lens[b]`` in a request's last page and every page no request uses hold
+NaN, and page-table entries past a request's last page hold -1 or an
+out-of-range page id.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+HEAD_DIM_QK = 576      # 512 latent (kv_lora_rank) + 64 RoPE dims
+HEAD_DIM_V = 512       # V = first 512 dims of each cache row
+BF16_NAN = 0x7FC0
+E4M3_NAN = 0x7F
+E4M3_MAX = 448.0
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    seed: int
+    batch: int
+    num_heads: int
+    page_size: int
+    packed: bool
+    causal: bool
+    return_lse: bool
+    kv_dtype: str                      # "bf16" or "e4m3"
+    q_lens: np.ndarray                 # [B] int32 (uniform when fixed)
+    seq_lens: np.ndarray               # [B] int32
+    max_seq_len_q: int
+    max_seq_len: int
+    query: np.ndarray                  # uint16 bf16 bits, [B,SQ,H,576] or [total_q,H,576]
+    qo_indptr: Optional[np.ndarray]    # [B+1] int32 when packed
+    kv_cache: np.ndarray               # uint16 (bf16) or uint8 (e4m3), [pages, ps, 576]
+    block_tables: np.ndarray           # [B, max_pages_per_req] int32
+    bmm1_scale: float                  # exactly representable in fp32
+    bmm2_scale: float
+    k_scale: Optional[float] = None
+
+    @property
+    def total_q(self) -> int:
+        return int(self.q_lens.sum())
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.kv_cache.shape[0])
+
+    @property
+    def sq(self) -> int:
+        """Per-request query length of a fixed launch (the bound when packed)."""
+        return int(self.max_seq_len_q)
+
+    def q_start(self) -> np.ndarray:
+        """[B+1] token offsets of each request's first query row."""
+        if self.packed:
+            return self.qo_indptr.astype(np.int64)
+        return np.arange(self.batch + 1, dtype=np.int64) * self.sq
+
+    def query_rows(self) -> np.ndarray:
+        """The query viewed as [tokens, H, 576] (fixed shape flattened)."""
+        return self.query.reshape(-1, self.num_heads, HEAD_DIM_QK)
+
+
+def f32(x: float) -> float:
+    """Round a Python float to the nearest fp32 value."""
+    return float(np.float32(x))
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 array -> bf16 bit patterns (round to nearest even) as uint16."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """float32 array -> float8_e4m3fn bit patterns (round to nearest even)."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _normal(rng: np.random.Generator, shape) -> np.ndarray:
+    return rng.standard_normal(size=shape, dtype=np.float32)
+
+
+def build(name: str, seed: int, *, num_heads: int, page_size: int,
+          seq_lens, q_lens, packed: bool, causal: bool = True,
+          return_lse: bool = False, kv_dtype: str = "bf16",
+          pool_factor: float = 1.25, bmm1_scale: float = 1.0 / math.sqrt(192.0),
+          bmm2_scale: float = 1.0, num_pages: Optional[int] = None,
+          block_tables: Optional[np.ndarray] = None, poison: bool = True,
+          max_seq_len_q: Optional[int] = None, max_seq_len: Optional[int] = None,
+          rng: Optional[np.random.Generator] = None) -> Workload:
+    """Draw one workload.  Draw order: pool permutation, query, KV values."""
+    rng = rng if rng is not None else np.random.default_rng(seed)
+    seq_lens = np.asarray(seq_lens, dtype=np.int32)
+    q_lens = np.asarray(q_lens, dtype=np.int32)
+    B = int(seq_lens.shape[0])
+    H = int(num_heads)
+    ps = int(page_size)
+    if not packed and B > 0:
+        assert np.all(q_lens == q_lens[0]), "fixed-shape launches share one q_len"
+    n_pages = (seq_lens.astype(np.int64) + ps - 1) // ps
+    needed = int(n_pages.sum())
+    max_pages = max(1, int(n_pages.max()) if B else 1)
+
+    if block_tables is None:
+        pool = num_pages if num_pages is not None else max(1, math.ceil(pool_factor * needed))
+        assert pool >= needed
+        perm = rng.permutation(pool).astype(np.int32)
+        block_tables = np.empty((B, max_pages), dtype=np.int32)
+        pos = 0
+        for b in range(B):
+            k = int(n_pages[b])
+            block_tables[b, :k] = perm[pos:pos + k]
+            pos += k
+            tail = block_tables[b, k:]
+            # unused entries: alternate -1 and an out-of-range page id
+            tail[0::2] = -1
+            tail[1::2] = pool + 7
+    else:
+        block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        pool = int(num_pages)
+
+    if packed:
+        qo_indptr = np.zeros(B + 1, dtype=np.int32)
+        qo_indptr[1:] = np.cumsum(q_lens)
+        total_q = int(qo_indptr[-1])
+        qshape = (total_q, H, HEAD_DIM_QK)
+        sq = int(max_seq_len_q if max_seq_len_q is not None else (q_lens.max() if B else 1))
+    else:
+        qo_indptr = None
+        sq = int(q_lens[0]) if B else int(max_seq_len_q or 1)
+        qshape = (B, sq, H, HEAD_DIM_QK)
+    query = bf16_bits(_normal(rng, qshape))
+
+    kv32 = _normal(rng, (pool, ps, HEAD_DIM_QK))
+    used = np.zeros((pool, ps), dtype=bool)
+    for b in range(B):
+        L = int(seq_lens[b])
+        for p in range(int(n_pages[b])):
+            rows = min(ps, L - p * ps)
+            used[block_tables[b, p], :rows] = True
+
+    k_scale = None
+    if kv_dtype == "bf16":
+        kv = bf16_bits(kv32)
+        if poison:
+            kv[~used] = BF16_NAN
+    elif kv_dtype == "e4m3":
+        amax = float(np.abs(kv32[used]).max()) if used.any() else 1.0
+        k_scale = f32(amax / E4M3_MAX)
+        kv = e4m3_bits(kv32 / np.float32(k_scale))
+        if poison:
+            kv[~used] = E4M3_NAN
+        bmm1_scale = bmm1_scale * k_scale
+        bmm2_scale = bmm2_scale * k_scale
+    else:
+        raise ValueError(kv_dtype)
+    del kv32
+
+    return Workload(
+        name=name, seed=seed, batch=B, num_heads=H, page_size=ps, packed=packed,
+        causal=causal, return_lse=return_lse, kv_dtype=kv_dtype, q_lens=q_lens,
+        seq_lens=seq_lens,
+        max_seq_len_q=sq,
+        max_seq_len=int(max_seq_len if max_seq_len is not None else (seq_lens.max() if B else 1)),
+        query=query, qo_indptr=qo_indptr, kv_cache=kv, block_tables=block_tables,
+        bmm1_scale=f32(bmm1_scale), bmm2_scale=f32(bmm2_scale), k_scale=k_scale)
+
+
+# ---------------------------------------------------------------------------
+# The five workloads.  Seeds are 1000 + workload index.  ``scale`` < 1 shrinks
+# the batch and the length ranges for parity runs the oracle finishes quickly;
+# ``scale`` = 1 is the full-size workload.
+# ---------------------------------------------------------------------------
+
+def tiny(seed: int = 1001, poison: bool = True) -> Workload:
+    """B=2, H=16, q_len=1, seq_lens {37, 64}, page_size 32, 8 physical pages,
+    block_tables = a seeded permutation of the 8 pages viewed as [2, 4]."""
+    rng = np.random.default_rng(seed)
+    bt = rng.permutation(8).astype(np.int32).reshape(2, 4)
+    return build("tiny_b2_h16_q1_ps32", seed, num_heads=16, page_size=32,
+                 seq_lens=[37, 64], q_lens=[1, 1], packed=False, return_lse=True,
+                 num_pages=8, block_tables=bt, poison=poison, rng=rng)
+
+
+def _uniform_lens(rng, lo, hi, n):
+    return rng.integers(lo, hi, size=n, endpoint=True).astype(np.int32)
+
+
+def deepseek_v3(seed: int = 1002, batch: int = 64, lo: int = 1024, hi: int = 8192,
+                return_lse: bool = False, poison: bool = True) -> Workload:
+    """B=64, H=128, q_len=1, page_size 64, seq_lens ~ U[1024, 8192]."""
+    rng = np.random.default_rng(seed)
+    L = _uniform_lens(rng, lo, hi, batch)
+    return build(f"deepseek_v3_b{batch}_h128_q1_ps64", seed, num_heads=128, page_size=64,
+                 seq_lens=L, q_lens=np.ones(batch, np.int32), packed=False,
+                 return_lse=return_lse, poison=poison, rng=rng)
+
+
+def mtp(seed: int = 1003, batch: int = 32, lo: int = 2048, hi: int = 16384,
+        q_len: int = 4, return_lse: bool = False, poison: bool = True) -> Workload:
+    """B=32, H=128, fixed q_len=4, bottom-right causal, seq_lens ~ U[2048, 16384]."""
+    rng = np.random.default_rng(seed)
+    L = _uniform_lens(rng, lo, hi, batch)
+    return build(f"mtp_b{batch}_h128_q{q_len}_ps64", seed, num_heads=128, page_size=64,
+                 seq_lens=L, q_lens=np.full(batch, q_len, np.int32), packed=False,
+                 return_lse=return_lse, poison=poison, rng=rng)
+
+
+def ragged(seed: int = 1004, batch: int = 128, median: float = 4096.0, sigma: float = 1.0,
+           max_len: int = 32768, poison: bool = True) -> Workload:
+    """B=128, H=16, packed q_len ~ U{1..8} via qo_indptr (max_seq_len_q = 8),
+    page_size 32, seq_lens lognormal (median 4096, sigma 1) clipped to
+    [q_len, 32768], output plus LSE."""
+    rng = np.random.default_rng(seed)
+    q = rng.integers(1, 8, size=batch, endpoint=True).astype(np.int32)
+    raw = np.rint(np.exp(rng.normal(math.log(median), sigma, size=batch)))
+    L = np.clip(raw, q, max_len).astype(np.int32)
+    return build(f"ragged_b{batch}_h16_packed_ps32", seed, num_heads=16, page_size=32,
+                 seq_lens=L, q_lens=q, packed=True, return_lse=True, max_seq_len_q=8,
+                 poison=poison, rng=rng)
+
+
+def fp8_long(seed: int = 1005, batch: int = 8, lo: int = 65536, hi: int = 131072,
+             q_len: int = 2, return_lse: bool = False, poison: bool = True) -> Workload:
+    """B=8, H=128, fixed q_len=2, page_size 64, seq_lens ~ U[65536, 131072],
+    e4m3 KV with k_scale = amax/448 folded into bmm1 and bmm2."""
+    rng = np.random.default_rng(seed)
+    L = _uniform_lens(rng, lo, hi, batch)
+    return build(f"fp8_long_b{batch}_h128_q{q_len}_ps64", seed, num_heads=128, page_size=64,
+                 seq_lens=L, q_lens=np.full(batch, q_len, np.int32), packed=False,
+                 kv_dtype="e4m3", return_lse=return_lse, poison=poison, rng=rng)
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "deepseek_v3": deepseek_v3,
+    "mtp": mtp,
+    "ragged": ragged,
+    "fp8_long": fp8_long,
+}
+
+
+def permute_pages(w: Workload, seed: int) -> Workload:
+    """Same logical cache with physical pages shuffled and block_tables rewritten.
+
+    Every valid entry of ``block_tables`` is remapped; poisoned entries are kept.
+    """
+    rng = np.random.default_rng(seed)
+    P = w.num_pages
+    perm = rng.permutation(P)               # old page p moves to slot perm[p]
+    kv = np.empty_like(w.kv_cache)
+    kv[perm] = w.kv_cache
+    bt = w.block_tables.copy()
+    valid = (bt >= 0) & (bt < P)
+    bt[valid] = perm[bt[valid]]
+    return dataclasses.replace(w, kv_cache=kv, block_tables=bt.astype(np.int32))
