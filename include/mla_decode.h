@@ -1,0 +1,163 @@
+/*
+ * Batched paged Multi-head Latent Attention (MLA) decode -- C ABI.
+ *
+ * The operation (problem statement of the FlashInfer page
+ * "prims_ts_batch_decode_with_kv_cache_mla", signature and parameter text):
+ * for request b with KV length L = seq_lens[b] and q query rows, every query
+ * row i and head h attends over the rows of a paged latent cache,
+ *
+ *   s_j = bmm1_scale * <Q[b,i,h,0:576], K_b[j,0:576]>
+ *   O[b,i,h,:] = bmm2_scale * sum_j softmax_j(s) * K_b[j,0:512]
+ *   lse[b,i,h] = ln sum_j exp(s_j)                       (natural log)
+ *
+ * where K_b[j] = kv_cache[block_tables[b][j / page_size]][j % page_size], the
+ * 576-wide rows concatenate 512 latent and 64 RoPE dims, and V is the first
+ * 512 dims of the same rows (one-copy cache).  Causal masking is bottom-right
+ * aligned: row i sees KV rows 0 .. L - q + i; dense masking sees 0 .. L - 1.
+ * The natural-log LSE follows the vLLM "FlashInferMLAImpl" page (its LSE
+ * contract is base e); the scales are the folded bmm1/bmm2 factors of the
+ * FlashInfer pull request "dynamic scale factor interface and one-copy
+ * kvcache on trtllm-gen mla" (bmm1 from q/k/softmax scales, bmm2 from v/o).
+ *
+ * Calling sequence:  mla_decode_plan (host only; before any graph capture)
+ * -> mla_decode_run (any number of times; capture-safe) -> mla_decode_destroy.
+ *
+ * Every tensor argument is a DEVICE pointer owned by the caller.  The library
+ * allocates no device memory, performs no device-to-host copy and never
+ * synchronises the stream: all per-launch metadata (seq_lens, qo_indptr,
+ * block_tables) is read on the device.  Status codes are returned only for
+ * what the host can check; violations of the device-side contract below are
+ * undefined behaviour, except that out-of-range lengths and offsets are
+ * clamped on the device so that no access leaves the given buffers, and a
+ * nonzero status word is left in the workspace (mla_decode_status_offset).
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_HEAD_DIM_QK 576 /* 512 latent + 64 RoPE */
+#define MLA_HEAD_DIM_V 512  /* V = first 512 dims of each cache row */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1,        /* null pointer, negative size, bad enum */
+  MLA_ERR_UNSUPPORTED = -2,        /* head count / page size outside the supported set */
+  MLA_ERR_WORKSPACE_TOO_SMALL = -3,
+  MLA_ERR_ALIGNMENT = -4,          /* a tensor pointer is not 16-byte aligned */
+  MLA_ERR_CUDA = -5                /* a CUDA runtime call failed (launch, attribute) */
+} mla_status;
+
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
+typedef enum { MLA_MASK_CAUSAL = 0, MLA_MASK_DENSE = 1 } mla_mask;
+
+/*
+ * Static parameters of a launch (the "semantic key" of the problem
+ * statement): everything that sizes grids and the workspace.  Runtime
+ * lengths live on the device and may change between launches of one plan
+ * (and between replays of a captured graph) within these bounds.
+ */
+typedef struct mla_decode_params {
+  int32_t batch;             /* B >= 0 requests */
+  int32_t num_heads;         /* H in {16, 32, 64, 128} */
+  int32_t max_seq_len_q;     /* fixed launch: the q_len SQ of every request;
+                                packed launch: static bound on each q_len (required) */
+  int32_t max_seq_len;       /* static bound on every seq_lens[b] (>= 1) */
+  int32_t page_size;         /* 32 or 64 rows per page */
+  int32_t max_pages_per_req; /* row stride of block_tables (>= ceil(max_seq_len / page_size)) */
+  int64_t num_pages;         /* physical pages in kv_cache */
+  int32_t packed;            /* 0: query [B, SQ, H, 576]; 1: query [total_q, H, 576] + qo_indptr */
+  int64_t max_total_q;       /* packed: bound on total_q (query.shape[0]); fixed: ignored */
+  int32_t kv_dtype;          /* mla_kv_dtype */
+  int32_t mask;              /* mla_mask */
+  int32_t return_lse;        /* nonzero: mla_decode_run writes lse */
+  int32_t device;            /* CUDA device ordinal the plan is for */
+} mla_decode_params;
+
+typedef struct mla_plan_s mla_plan_t; /* opaque; host memory only */
+
+/*
+ * Validate the static parameters, query the device (SM count, shared memory)
+ * and size the workspace.  Host only; not capture-safe (it sets kernel
+ * attributes).  On success *plan receives a new plan (free with
+ * mla_decode_destroy) and *workspace_bytes the number of bytes the caller must
+ * provide to every mla_decode_run of this plan.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_CUDA.
+ */
+int mla_decode_plan(const mla_decode_params *params, mla_plan_t **plan,
+                    size_t *workspace_bytes);
+
+/*
+ * Enqueue one decode on `stream` (a cudaStream_t; NULL = legacy default).
+ *
+ * query        bf16, fixed [B, SQ, H, 576] or packed [total_q, H, 576], contiguous.
+ * kv_cache     bf16 or fp8-e4m3 (per params.kv_dtype), [num_pages, page_size, 576]
+ *              (a rank-4 [num_pages, 1, page_size, 576] cache is the same memory).
+ * block_tables int32 [B, max_pages_per_req]; entries at or past a request's
+ *              ceil(seq_lens[b] / page_size) pages are never read.
+ * seq_lens     int32 [B]; 1 <= seq_lens[b] <= max_seq_len; for causal masking
+ *              q_len(b) <= seq_lens[b].
+ * qo_indptr    packed: int32 [B + 1], qo_indptr[0] = 0, strictly increasing,
+ *              qo_indptr[B] = total_q, every delta <= max_seq_len_q.
+ *              fixed: must be NULL.
+ * total_q      packed: query.shape[0] (<= max_total_q); fixed: ignored.
+ * bmm1_scale   multiplies the 576-dim dot products (softmax scale and any
+ *              q/k dequantisation scales already folded in by the caller).
+ * bmm2_scale   multiplies the normalised output (v/o scales folded in).
+ * out          bf16, [B, SQ, H, 512] or [total_q, H, 512]; required.
+ * lse          fp32, [B * SQ or total_q, H]; required iff params.return_lse.
+ * workspace    caller-owned device scratch of >= the planned size, 256-byte
+ *              aligned, exclusive to one in-flight launch (or one captured
+ *              graph) and not overlapping any other argument.  Needs no
+ *              zeroing: every launch re-initialises what it uses.
+ *
+ * Errors (synchronous, nothing enqueued): MLA_ERR_INVALID_ARG,
+ * MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_ALIGNMENT; MLA_ERR_CUDA if a launch fails.
+ */
+int mla_decode_run(const mla_plan_t *plan, const void *query, const void *kv_cache,
+                   const int32_t *block_tables, const int32_t *seq_lens,
+                   const int32_t *qo_indptr, int64_t total_q, float bmm1_scale,
+                   float bmm2_scale, void *out, float *lse, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * mla_decode_run, plus two CUDA events (cudaEvent_t, may be NULL) recorded on
+ * `stream` immediately before and after the decode kernel, so that a caller
+ * can time that kernel alone with cudaEventElapsedTime.  Same arguments,
+ * errors and capture rules as mla_decode_run.
+ */
+int mla_decode_run_profiled(const mla_plan_t *plan, const void *query, const void *kv_cache,
+                            const int32_t *block_tables, const int32_t *seq_lens,
+                            const int32_t *qo_indptr, int64_t total_q, float bmm1_scale,
+                            float bmm2_scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, void *stream, void *event_before_decode,
+                            void *event_after_decode);
+
+/* Free a plan (NULL is allowed). */
+void mla_decode_destroy(mla_plan_t *plan);
+
+/* Workspace bytes of a plan (the value mla_decode_plan returned). */
+size_t mla_decode_workspace_size(const mla_plan_t *plan);
+
+/*
+ * Byte offset, inside the workspace, of the int32 device status word the last
+ * run left behind (0 = every length and offset was within the contract; bit 0:
+ * a seq_len out of [1, max_seq_len]; bit 1: a q_len out of [1, max_seq_len_q]
+ * or a qo_indptr offset out of range; bit 2: causal q_len > seq_len).  Reading
+ * it is the caller's choice (a device-to-host copy after the stream syncs).
+ */
+size_t mla_decode_status_offset(void);
+
+/* Human-readable name of a status code. */
+const char *mla_decode_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

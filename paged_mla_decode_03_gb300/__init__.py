@@ -1,0 +1,290 @@
+"""Batched paged MLA decode on GB300 (sm_103a): thin Python binding.
+
+Every step of the computation runs in the CUDA kernels of ``libmla_decode.so``
+behind the C ABI in ``include/mla_decode.h``; this module only marshals
+arguments (torch tensors for device memory and streams) and caches plans.
+There is no CPU fallback: if the library is missing, every call raises.
+
+The high-level entry point mirrors the FlashInfer page
+"prims_ts_batch_decode_with_kv_cache_mla" (signature): fixed
+``[B, SQ, H, 576]`` or packed ``[total_q, H, 576]`` queries (``qo_indptr``),
+a rank-3 or rank-4 paged cache, ``block_tables``/``seq_lens`` on the device,
+caller-owned workspace, ``bmm1_scale``/``bmm2_scale``, causal or dense
+masking, bf16 output and an optional natural-log LSE.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Tuple
+
+import torch
+
+__all__ = [
+    "MLA_OK", "MlaDecodeError", "MlaDecodeParams", "load_library", "library_path",
+    "mla_decode_plan", "mla_decode_run", "mla_decode_run_profiled", "mla_decode_destroy", "mla_decode_workspace_size",
+    "mla_decode_status_offset", "mla_decode_status_string", "Plan", "decode",
+    "HEAD_DIM_QK", "HEAD_DIM_V",
+]
+
+HEAD_DIM_QK = 576
+HEAD_DIM_V = 512
+MLA_OK = 0
+KV_BF16, KV_FP8_E4M3 = 0, 1
+MASK_CAUSAL, MASK_DENSE = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libmla_decode.so")
+_lib = None
+
+
+class MlaDecodeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {mla_decode_status_string(status)} ({status})")
+        self.status = status
+
+
+class MlaDecodeParams(ctypes.Structure):
+    """Mirror of ``mla_decode_params`` (natural C alignment)."""
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("max_seq_len_q", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("max_pages_per_req", ctypes.c_int32),
+        ("num_pages", ctypes.c_int64),
+        ("packed", ctypes.c_int32),
+        ("max_total_q", ctypes.c_int64),
+        ("kv_dtype", ctypes.c_int32),
+        ("mask", ctypes.c_int32),
+        ("return_lse", ctypes.c_int32),
+        ("device", ctypes.c_int32),
+    ]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libmla_decode.so (built by ``paged_mla_decode_03_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "`python -m paged_mla_decode_03_gb300.build` (no fallback exists)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.mla_decode_plan.argtypes = [ctypes.POINTER(MlaDecodeParams), ctypes.POINTER(vp),
+                                    ctypes.POINTER(sz)]
+    lib.mla_decode_plan.restype = ctypes.c_int
+    lib.mla_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, i64, ctypes.c_float, ctypes.c_float,
+                                   vp, vp, vp, sz, vp]
+    lib.mla_decode_run.restype = ctypes.c_int
+    lib.mla_decode_run_profiled.argtypes = lib.mla_decode_run.argtypes + [vp, vp]
+    lib.mla_decode_run_profiled.restype = ctypes.c_int
+    lib.mla_decode_destroy.argtypes = [vp]
+    lib.mla_decode_destroy.restype = None
+    lib.mla_decode_workspace_size.argtypes = [vp]
+    lib.mla_decode_workspace_size.restype = sz
+    lib.mla_decode_status_offset.argtypes = []
+    lib.mla_decode_status_offset.restype = sz
+    lib.mla_decode_status_string.argtypes = [ctypes.c_int]
+    lib.mla_decode_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def mla_decode_status_string(status: int) -> str:
+    return load_library().mla_decode_status_string(int(status)).decode()
+
+
+def mla_decode_status_offset() -> int:
+    return int(load_library().mla_decode_status_offset())
+
+
+def mla_decode_plan(params: MlaDecodeParams) -> Tuple[int, int]:
+    """-> (plan handle, workspace bytes).  Raises MlaDecodeError on failure."""
+    lib = load_library()
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    rc = lib.mla_decode_plan(ctypes.byref(params), ctypes.byref(handle), ctypes.byref(ws))
+    if rc != MLA_OK:
+        raise MlaDecodeError(rc, "mla_decode_plan")
+    return handle.value, ws.value
+
+
+def mla_decode_destroy(plan: Optional[int]) -> None:
+    if plan:
+        load_library().mla_decode_destroy(ctypes.c_void_p(plan))
+
+
+def mla_decode_workspace_size(plan: int) -> int:
+    return int(load_library().mla_decode_workspace_size(ctypes.c_void_p(plan)))
+
+
+def _nbytes(x) -> int:
+    if x is None or isinstance(x, int):
+        return 0
+    return x.numel() * x.element_size()
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def mla_decode_run(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q: int,
+                   bmm1_scale: float, bmm2_scale: float, out, lse, workspace,
+                   workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """Enqueue one decode (arguments: tensors or raw device pointers)."""
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    rc = lib.mla_decode_run(ctypes.c_void_p(plan), _ptr(query), _ptr(kv_cache), _ptr(block_tables),
+                            _ptr(seq_lens), _ptr(qo_indptr), int(total_q), float(bmm1_scale),
+                            float(bmm2_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                            int(workspace_bytes), stream)
+    if rc != MLA_OK:
+        raise MlaDecodeError(rc, "mla_decode_run")
+
+
+def mla_decode_run_profiled(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr,
+                            total_q: int, bmm1_scale: float, bmm2_scale: float, out, lse,
+                            workspace, workspace_bytes: Optional[int] = None, stream=None,
+                            events=None) -> None:
+    """``mla_decode_run`` that also records ``events = (before, after)``
+    (torch.cuda.Event) around the decode kernel on the same stream."""
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if not isinstance(stream, torch.cuda.Stream):
+        raise TypeError("stream must be a torch.cuda.Stream")
+    ev0 = ev1 = None
+    if events is not None:
+        # make sure the events exist (torch creates them lazily on first record)
+        events[0].record(stream)
+        events[1].record(stream)
+        ev0, ev1 = events[0].cuda_event, events[1].cuda_event
+    rc = lib.mla_decode_run_profiled(ctypes.c_void_p(plan), _ptr(query), _ptr(kv_cache),
+                                     _ptr(block_tables), _ptr(seq_lens), _ptr(qo_indptr),
+                                     int(total_q), float(bmm1_scale), float(bmm2_scale),
+                                     _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                     stream.cuda_stream, ev0, ev1)
+    if rc != MLA_OK:
+        raise MlaDecodeError(rc, "mla_decode_run_profiled")
+
+
+class Plan:
+    """Owns one C plan; ``run`` enqueues a decode with it."""
+
+    def __init__(self, *, batch: int, num_heads: int, max_seq_len_q: int, max_seq_len: int,
+                 page_size: int, max_pages_per_req: int, num_pages: int, packed: bool,
+                 max_total_q: int = 0, kv_dtype: str = "bf16", causal: bool = True,
+                 return_lse: bool = False, device: int = 0):
+        self.params = MlaDecodeParams(
+            batch=batch, num_heads=num_heads, max_seq_len_q=max_seq_len_q,
+            max_seq_len=max_seq_len, page_size=page_size, max_pages_per_req=max_pages_per_req,
+            num_pages=num_pages, packed=int(bool(packed)), max_total_q=max_total_q,
+            kv_dtype=KV_FP8_E4M3 if kv_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else KV_BF16,
+            mask=MASK_CAUSAL if causal else MASK_DENSE, return_lse=int(bool(return_lse)),
+            device=device)
+        self.handle, self.workspace_bytes = mla_decode_plan(self.params)
+
+    def run(self, query, kv_cache, block_tables, seq_lens, out, *, qo_indptr=None, total_q=0,
+            lse=None, workspace=None, bmm1_scale=1.0, bmm2_scale=1.0, stream=None):
+        mla_decode_run(self.handle, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q,
+                       bmm1_scale, bmm2_scale, out, lse, workspace, None, stream)
+
+    def close(self):
+        if self.handle:
+            mla_decode_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_plans: Dict[tuple, Plan] = {}
+
+
+def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.Tensor,
+           block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, *,
+           qo_indptr: Optional[torch.Tensor] = None, max_seq_len_q: Optional[int] = None,
+           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+           bmm1_scale: float = 1.0, bmm2_scale: float = 1.0, mask_type: str = "causal",
+           return_lse: bool = False):
+    """Paged MLA decode.  Returns ``out`` (and ``lse`` when ``return_lse``).
+
+    ``query``: bf16 ``[B, SQ, H, 576]`` (qo_indptr None) or ``[total_q, H, 576]``.
+    ``kv_cache``: bf16 or float8_e4m3fn, ``[pages, page_size, 576]`` or
+    ``[pages, 1, page_size, 576]``.  ``workspace_buffer`` must hold at least
+    the plan's workspace bytes (see ``Plan``).  Plans are cached per static key.
+    """
+    if query.dtype != torch.bfloat16 or not query.is_cuda:
+        raise ValueError("query must be a bf16 CUDA tensor")
+    if kv_cache.dim() == 4:
+        if kv_cache.shape[1] != 1:
+            raise ValueError("rank-4 kv_cache must be [pages, 1, page_size, 576]")
+        kv_cache = kv_cache.squeeze(1)
+    if kv_cache.dim() != 3 or kv_cache.shape[-1] != HEAD_DIM_QK:
+        raise ValueError("kv_cache must be [pages, page_size, 576]")
+    if kv_cache.dtype == torch.bfloat16:
+        kv_dtype = "bf16"
+    elif kv_cache.dtype in (torch.float8_e4m3fn, torch.uint8):
+        kv_dtype = "e4m3"
+    else:
+        raise ValueError(f"unsupported kv_cache dtype {kv_cache.dtype}")
+    packed = qo_indptr is not None
+    H = int(query.shape[-2])
+    B = int(seq_lens.shape[0])
+    if packed:
+        if max_seq_len_q is None:
+            raise ValueError("max_seq_len_q is required for packed launches")
+        total_q = int(query.shape[0])
+        sq = int(max_seq_len_q)
+        out_shape = (total_q, H, HEAD_DIM_V)
+        lse_shape = (total_q, H)
+    else:
+        total_q = 0
+        sq = int(query.shape[1])
+        out_shape = (B, sq, H, HEAD_DIM_V)
+        lse_shape = (B * sq, H)
+    causal = mask_type == "causal"
+    if mask_type not in ("causal", "dense"):
+        raise ValueError(mask_type)
+    key = (B, H, sq, int(max_seq_len), int(kv_cache.shape[1]), int(block_tables.shape[1]),
+           int(kv_cache.shape[0]), packed, total_q if packed else 0, kv_dtype, causal,
+           bool(return_lse), query.device.index or 0)
+    plan = _plans.get(key)
+    if plan is None:
+        plan = Plan(batch=B, num_heads=H, max_seq_len_q=sq, max_seq_len=int(max_seq_len),
+                    page_size=int(kv_cache.shape[1]), max_pages_per_req=int(block_tables.shape[1]),
+                    num_pages=int(kv_cache.shape[0]), packed=packed, max_total_q=total_q,
+                    kv_dtype=kv_dtype, causal=causal, return_lse=return_lse,
+                    device=query.device.index or 0)
+        _plans[key] = plan
+    if workspace_buffer.numel() * workspace_buffer.element_size() < plan.workspace_bytes:
+        raise ValueError(f"workspace_buffer needs {plan.workspace_bytes} bytes")
+    if out is None:
+        out = torch.empty(out_shape, dtype=torch.bfloat16, device=query.device)
+    if return_lse and lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=query.device)
+    plan.run(query, kv_cache, block_tables, seq_lens, out, qo_indptr=qo_indptr, total_q=total_q,
+             lse=lse if return_lse else None, workspace=workspace_buffer,
+             bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale)
+    return (out, lse) if return_lse else out

@@ -1,0 +1,227 @@
+// C ABI of the paged MLA decode library (declared in include/mla_decode.h).
+//
+// mla_decode_plan sizes the workspace from the static parameters (the
+// problem statement's "semantic key": head count, page size, the static
+// q_len / KV-length / total_q bounds) and the device's SM count.
+// mla_decode_run checks what the host can check and enqueues three kernels
+// on the caller's stream: the split-KV partitioner, the decode kernel and the
+// combine kernel.  Grid sizes depend only on plan-time values, and nothing
+// here allocates, copies or synchronises, so a run can be captured in a CUDA
+// graph and replayed with new seq_lens / qo_indptr values.
+#include <algorithm>
+#include <new>
+
+#include "../../include/mla_decode.h"
+#include "mla_common.cuh"
+
+namespace mla {
+cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cudaStream_t stream);
+cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
+                           cudaStream_t stream);
+cudaError_t decode_simt_setup();
+cudaError_t decode_sm103_setup(int sm_count, int* n_pairs);
+cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
+                                cudaStream_t stream);
+size_t decode_simt_smem_bytes();
+cudaError_t launch_decode_simt(const Problem& p, const Layout& lay, void* ws,
+                               cudaStream_t stream);
+}  // namespace mla
+
+struct mla_plan_s {
+  mla_decode_params prm;
+  mla::Layout lay;
+  int sm_count;
+  int combine_grid;
+  int tensor_core;  // 1: tcgen05 CTA-pair kernel (bf16 KV); 0: CUDA-core kernel
+};
+
+namespace {
+
+constexpr size_t kHeaderBytes = sizeof(int) * mla::kHdrWords;
+
+bool supported_heads(int h) { return h == 16 || h == 32 || h == 64 || h == 128; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int rows_per_group,
+                mla::Layout* lay) {
+  using namespace mla;
+  const long long B = prm.batch;
+  const long long R = rows_per_group;
+  const long long g_max = ceil_div((long long)prm.max_seq_len_q * prm.num_heads, R);
+  long long groups = B * g_max;
+  if (prm.packed) groups = std::min(groups, B + ceil_div(prm.max_total_q * prm.num_heads, R));
+  groups = std::max(groups, 1LL);
+  // each range boundary between two workers cuts at most one group
+  const long long max_items = groups + n_workers;
+  if (max_items > (1LL << 30)) return MLA_ERR_UNSUPPORTED;
+  lay->rows_per_group = rows_per_group;
+  lay->n_workers = n_workers;
+  lay->n_ctas = n_ctas;
+  lay->max_groups = (int)groups;
+  lay->max_items = (int)max_items;
+  lay->max_combine = (int)std::min(groups, (long long)n_workers);
+  lay->max_partials = (int)std::min(max_items, 2LL * n_workers);
+  size_t off = kHeaderBytes;
+  lay->items = off;
+  off = align_up(off + sizeof(WorkItem) * lay->max_items, 256);
+  lay->combine = off;
+  off = align_up(off + sizeof(CombineItem) * lay->max_combine, 256);
+  lay->worker_ranges = off;
+  off = align_up(off + sizeof(int) * (n_workers + 1), 256);
+  lay->req_scratch = off;
+  off = align_up(off + sizeof(int) * 4 * std::max(B, 1LL), 256);
+  lay->group_scratch = off;
+  off = align_up(off + sizeof(long long) * lay->max_groups + sizeof(int) * 5 * lay->max_groups +
+                     sizeof(int) * lay->max_items,
+                 256);
+  lay->part_o = off;
+  off = align_up(off + sizeof(float) * R * kVDim * (size_t)lay->max_partials, 256);
+  lay->part_lse = off;
+  off = align_up(off + sizeof(float) * R * (size_t)lay->max_partials, 256);
+  lay->total = off;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* workspace_bytes) {
+  if (!params || !plan || !workspace_bytes) return MLA_ERR_INVALID_ARG;
+  *plan = nullptr;
+  const mla_decode_params& p = *params;
+  if (p.batch < 0 || p.max_seq_len_q < 1 || p.max_seq_len < 1 || p.max_pages_per_req < 1 ||
+      p.num_pages < 1 || p.device < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (p.packed != 0 && p.packed != 1) return MLA_ERR_INVALID_ARG;
+  if (p.packed && p.max_total_q < 0) return MLA_ERR_INVALID_ARG;
+  if (p.kv_dtype != MLA_KV_BF16 && p.kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p.mask != MLA_MASK_CAUSAL && p.mask != MLA_MASK_DENSE) return MLA_ERR_INVALID_ARG;
+  if (!supported_heads(p.num_heads)) return MLA_ERR_UNSUPPORTED;
+  if (p.page_size != 32 && p.page_size != 64) return MLA_ERR_UNSUPPORTED;
+  if ((long long)p.max_pages_per_req * p.page_size < p.max_seq_len) return MLA_ERR_INVALID_ARG;
+  if (!p.packed && (long long)p.batch * p.max_seq_len_q > (1LL << 31) / 128)
+    return MLA_ERR_UNSUPPORTED;
+
+  int dev_count = 0;
+  if (cudaGetDeviceCount(&dev_count) != cudaSuccess || p.device >= dev_count) return MLA_ERR_CUDA;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaSetDevice(p.device) != cudaSuccess) return MLA_ERR_CUDA;
+  int sms = 0, n_pairs = 0;
+  const bool tensor_core = p.kv_dtype == MLA_KV_BF16;
+  cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
+  if (e == cudaSuccess) e = tensor_core ? mla::decode_sm103_setup(sms, &n_pairs) : mla::decode_simt_setup();
+  cudaSetDevice(prev);
+  if (e != cudaSuccess || sms <= 0) return MLA_ERR_CUDA;
+
+  mla_plan_s* pl = new (std::nothrow) mla_plan_s;
+  if (!pl) return MLA_ERR_INVALID_ARG;
+  pl->prm = p;
+  pl->sm_count = sms;
+  pl->tensor_core = tensor_core ? 1 : 0;
+  const int rc = tensor_core ? make_layout(p, n_pairs, 2 * n_pairs, 128, &pl->lay)
+                             : make_layout(p, sms, sms, 64, &pl->lay);
+  if (rc != MLA_OK) {
+    delete pl;
+    return rc;
+  }
+  pl->combine_grid = std::min(pl->lay.max_combine, 4 * sms);
+  *plan = pl;
+  *workspace_bytes = pl->lay.total;
+  return MLA_OK;
+}
+
+int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const void* kv_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* qo_indptr, int64_t total_q, float bmm1_scale,
+                            float bmm2_scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream, void* event_before_decode,
+                            void* event_after_decode) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  const mla_decode_params& prm = plan->prm;
+  if (prm.batch == 0) return MLA_OK;
+  if (!query || !kv_cache || !block_tables || !seq_lens || !out || !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (prm.return_lse && !lse) return MLA_ERR_INVALID_ARG;
+  if (prm.packed) {
+    if (!qo_indptr || total_q < 0 || total_q > prm.max_total_q) return MLA_ERR_INVALID_ARG;
+  } else if (qo_indptr) {
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (workspace_bytes < plan->lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(query, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+      (lse && !aligned(lse, 4)) || (qo_indptr && !aligned(qo_indptr, 4)))
+    return MLA_ERR_ALIGNMENT;
+
+  mla::Problem p;
+  p.batch = prm.batch;
+  p.num_heads = prm.num_heads;
+  p.max_q = prm.max_seq_len_q;
+  p.max_seq_len = prm.max_seq_len;
+  p.page_size = prm.page_size;
+  p.max_pages = prm.max_pages_per_req;
+  p.packed = prm.packed;
+  p.kv_dtype = prm.kv_dtype;
+  p.causal = prm.mask == MLA_MASK_CAUSAL;
+  p.return_lse = prm.return_lse != 0;
+  p.num_pages = prm.num_pages;
+  p.total_q = prm.packed ? total_q : (long long)prm.batch * prm.max_seq_len_q;
+  p.bmm1_scale = bmm1_scale;
+  p.bmm2_scale = bmm2_scale;
+  p.query = query;
+  p.kv_cache = kv_cache;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.qo_indptr = prm.packed ? qo_indptr : nullptr;
+  p.out = out;
+  p.lse = prm.return_lse ? lse : nullptr;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mla::launch_partition(p, plan->lay, workspace, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (event_before_decode &&
+      cudaEventRecord(static_cast<cudaEvent_t>(event_before_decode), s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  const cudaError_t ke = plan->tensor_core ? mla::launch_decode_sm103(p, plan->lay, workspace, s)
+                                           : mla::launch_decode_simt(p, plan->lay, workspace, s);
+  if (ke != cudaSuccess) return MLA_ERR_CUDA;
+  if (event_after_decode &&
+      cudaEventRecord(static_cast<cudaEvent_t>(event_after_decode), s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (mla::launch_combine(p, plan->lay, workspace, plan->combine_grid, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+int mla_decode_run(const mla_plan_t* plan, const void* query, const void* kv_cache,
+                   const int32_t* block_tables, const int32_t* seq_lens, const int32_t* qo_indptr,
+                   int64_t total_q, float bmm1_scale, float bmm2_scale, void* out, float* lse,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  return mla_decode_run_profiled(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q,
+                                 bmm1_scale, bmm2_scale, out, lse, workspace, workspace_bytes,
+                                 stream, nullptr, nullptr);
+}
+
+void mla_decode_destroy(mla_plan_t* plan) { delete plan; }
+
+size_t mla_decode_workspace_size(const mla_plan_t* plan) { return plan ? plan->lay.total : 0; }
+
+size_t mla_decode_status_offset(void) { return sizeof(int) * mla::kHdrStatus; }
+
+const char* mla_decode_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE_TOO_SMALL: return "MLA_ERR_WORKSPACE_TOO_SMALL";
+    case MLA_ERR_ALIGNMENT: return "MLA_ERR_ALIGNMENT";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

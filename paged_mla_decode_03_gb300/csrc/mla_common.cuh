@@ -1,0 +1,77 @@
+// Shared definitions of the paged MLA decode kernels: the problem record
+// passed by value to every kernel, the split-KV work items, and the layout of
+// the caller-owned workspace.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kQkDim = 576;       // 512 latent + 64 RoPE
+constexpr int kVDim = 512;        // V = the latent part of each cache row
+constexpr int kKvTile = 64;       // KV rows per pipeline tile
+
+// Problem record: static plan parameters plus the per-run pointers/scales.
+struct Problem {
+  int batch, num_heads, max_q, max_seq_len, page_size, max_pages;
+  int packed, kv_dtype, causal, return_lse;
+  long long num_pages, total_q;  // total_q: rows of the query tensor (tokens)
+  float bmm1_scale, bmm2_scale;
+  const void* query;             // bf16 [tokens, H, 576]
+  const void* kv_cache;          // bf16 or e4m3 [num_pages, page_size, 576]
+  const int* block_tables;       // [B, max_pages]
+  const int* seq_lens;           // [B]
+  const int* qo_indptr;          // [B + 1] or nullptr
+  void* out;                     // bf16 [tokens, H, 512]
+  float* lse;                    // fp32 [tokens, H] or nullptr
+};
+
+// One unit of work of the decode kernel: query rows [R g, R g + R) of request
+// b (R = Layout::rows_per_group, clipped to its q_len * H rows) against KV rows
+// [kv_begin, kv_end).
+// slot < 0: the item covers the whole KV range and writes `out` directly;
+// otherwise it writes a normalised fp32 partial (O and natural-log LSE) into
+// partial slot `slot` for the combine kernel.
+struct WorkItem {
+  int b, g, kv_begin, kv_end;
+  int slot, q_len, seq_len, q_start;  // q_start: first token of request b
+};
+
+// One split (request, row group): partials live in slots first + k * stride.
+struct CombineItem {
+  int b, g, first_slot, stride;
+  int n_chunks, q_len, q_start, pad;
+};
+
+// Header words at the start of the workspace.
+enum HeaderWord {
+  kHdrStatus = 0,     // contract-violation bits (see mla_decode_status_offset)
+  kHdrNumItems = 1,
+  kHdrWorkCounter = 2,
+  kHdrNumCombine = 3,
+  kHdrChunkTiles = 4,
+  kHdrCombineCounter = 5,
+  kHdrWords = 64
+};
+
+// Byte layout of the workspace; computed on the host at plan time.
+struct Layout {
+  size_t items;          // WorkItem[max_items]
+  size_t combine;        // CombineItem[max_combine]
+  size_t worker_ranges;  // int[n_workers + 1]: worker w owns items [r[w], r[w+1])
+  size_t req_scratch;    // int[4 * batch]: partitioner scratch
+  size_t group_scratch;  // partitioner scratch per row group / item
+  size_t part_o;         // float[max_partials][rows_per_group][512]
+  size_t part_lse;       // float[max_partials][rows_per_group]
+  size_t total;
+  int max_items, max_combine, max_partials, max_groups;
+  int n_workers;       // persistent workers (CTAs, or CTA pairs)
+  int n_ctas;          // CTAs of the decode grid
+  int rows_per_group;  // query rows per work item
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace mla

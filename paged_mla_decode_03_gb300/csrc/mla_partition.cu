@@ -1,0 +1,285 @@
+// On-device split-KV work partitioner.
+//
+// Reads seq_lens / qo_indptr on the device (the problem statement of the
+// FlashInfer page "prims_ts_batch_decode_with_kv_cache_mla" forbids
+// device-to-host metadata reads on this path) and writes into the workspace
+// (a) the list of work items of the decode kernel and, for every persistent
+// worker, the contiguous range of items it owns, and (b) the list of split
+// (request, row group) pairs the combine kernel merges.
+//
+// Cost model: a request with q query rows and H heads has G = ceil(q H / R)
+// row groups of R rows; each group costs c0 + T units, T = ceil(L / 64) KV
+// tiles plus a fixed overhead c0 (query load, epilogue).  Laying all groups
+// end to end gives W units; worker p owns units [floor(p W / n),
+// floor((p+1) W / n)).  A group that straddles a range boundary is cut at the
+// corresponding tile and each piece becomes a separate item writing a
+// partial; every other group is one item writing the output directly.  So
+// workers are balanced to within one tile plus one overhead, and there are at
+// most n + #groups items and n - 1 cut points.  One CTA of 1024 threads.
+#include "mla_common.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr long long kOverheadTiles = 2;  // c0: query load + epilogue, in tile units
+
+struct Shared {
+  long long warp_ll[32];
+  int warp_i[32];
+  int carry;
+  long long carry_ll;
+};
+
+__device__ int block_or(int v, Shared& sh) {
+  for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) sh.warp_i[warp] = v;
+  __syncthreads();
+  int t = 0;
+  for (int w = 0; w < kThreads / 32; ++w) t |= sh.warp_i[w];
+  __syncthreads();
+  return t;
+}
+
+// In-place exclusive prefix sum of data[0, n); returns the total.
+template <typename T>
+__device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) sh.carry_ll = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += kThreads) {
+    const int i = base + threadIdx.x;
+    const T v = i < n ? data[i] : T(0);
+    T x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const T y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) sh.warp_ll[warp] = (long long)x;
+    __syncthreads();
+    if (warp == 0) {
+      long long w = sh.warp_ll[lane];
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      sh.warp_ll[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const long long warp_excl = warp ? sh.warp_ll[warp - 1] : 0;
+    const long long carry = sh.carry_ll;
+    if (i < n) data[i] = (T)(carry + warp_excl + (long long)(x - v));
+    __syncthreads();
+    if (threadIdx.x == 0) sh.carry_ll = carry + sh.warp_ll[31];
+    __syncthreads();
+  }
+  return (T)sh.carry_ll;
+}
+
+// Start unit of worker p's range: floor(p * W / n).
+__device__ __forceinline__ long long boundary(long long p, long long W, long long n) {
+  return (p * W) / n;
+}
+
+// Tile cut position of range boundary p inside a group starting at unit S.
+__device__ __forceinline__ int cut_tile(long long p, long long W, long long n, long long S,
+                                        int T) {
+  const long long t = boundary(p, W, n) - S - kOverheadTiles;
+  return (int)min(max(t, 0LL), (long long)T);
+}
+
+// Worker that owns unit x: the largest p with boundary(p) <= x.
+__device__ int owner_of(long long x, long long W, long long n) {
+  long long p = W > 0 ? min((x * n) / W, n - 1) : 0;
+  while (p + 1 < n && boundary(p + 1, W, n) <= x) ++p;
+  while (p > 0 && boundary(p, W, n) > x) --p;
+  return (int)p;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1)
+partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
+  __shared__ Shared sh;
+  int* hdr = reinterpret_cast<int*>(ws);
+  WorkItem* items = reinterpret_cast<WorkItem*>(ws + lay.items);
+  CombineItem* comb = reinterpret_cast<CombineItem*>(ws + lay.combine);
+  int* worker_begin = reinterpret_cast<int*>(ws + lay.worker_ranges);
+  const int B = p.batch;
+  const int R = lay.rows_per_group;
+  const int H = p.num_heads;
+  // per-request scratch
+  int* r_qlen = reinterpret_cast<int*>(ws + lay.req_scratch);
+  int* r_qstart = r_qlen + B;
+  int* r_len = r_qstart + B;
+  int* r_gbase = r_len + B;  // first group index of the request
+  // per-group scratch
+  long long* g_start = reinterpret_cast<long long*>(ws + lay.group_scratch);  // unit offset
+  int* g_items = reinterpret_cast<int*>(g_start + lay.max_groups);              // -> item base
+  int* g_req = g_items + lay.max_groups;
+  int* g_nch = g_req + lay.max_groups;
+  int* g_slot = g_nch + lay.max_groups;  // partial-slot base
+  int* g_comb = g_slot + lay.max_groups;  // combine-entry base
+  int* it_owner = g_comb + lay.max_groups;  // per item: owning worker
+
+  // 1. Per-request lengths, clamped so that nothing downstream leaves the
+  //    caller's buffers; contract violations are flagged in the status word.
+  int status = 0;
+  for (int b = threadIdx.x; b < B; b += kThreads) {
+    int q, qs;
+    if (p.packed) {
+      int lo = p.qo_indptr[b], hi = p.qo_indptr[b + 1];
+      const int tq = (int)p.total_q;
+      if (lo < 0 || hi > tq || hi - lo < 1 || hi - lo > p.max_q) status |= 2;
+      lo = min(max(lo, 0), tq);
+      hi = min(max(hi, lo), tq);
+      q = min(hi - lo, p.max_q);
+      qs = lo;
+    } else {
+      q = p.max_q;
+      qs = b * p.max_q;
+    }
+    int L = p.seq_lens[b];
+    if (L < 1 || L > p.max_seq_len) status |= 1;
+    L = min(max(L, 0), p.max_seq_len);
+    if (p.causal && q > L) status |= 4;
+    r_qlen[b] = q;
+    r_qstart[b] = qs;
+    r_len[b] = L;
+    r_gbase[b] = (L > 0) ? (q * H + R - 1) / R : 0;
+  }
+  status = __syncthreads_or(status) ? block_or(status, sh) : 0;
+  __syncthreads();
+  int n_groups = block_exclusive_scan(r_gbase, B, sh);
+  if (n_groups > lay.max_groups) {  // unreachable within the contract
+    status |= 8;
+    n_groups = 0;
+  }
+
+  // 2. Groups in request order with their unit costs.
+  for (int b = threadIdx.x; b < B; b += kThreads) {
+    const int gb = r_gbase[b];
+    const int ge = (b + 1 < B) ? r_gbase[b + 1] : n_groups;
+    const int T = (r_len[b] + kKvTile - 1) / kKvTile;
+    for (int g = gb; g < ge && g < n_groups; ++g) {
+      g_req[g] = b;
+      g_start[g] = kOverheadTiles + T;  // cost; scanned into the start unit below
+    }
+  }
+  __syncthreads();
+  const long long W = block_exclusive_scan(g_start, n_groups, sh);
+  const long long n = lay.n_workers;
+
+  // 3. Cut points inside each group -> chunk counts.
+  for (int g = threadIdx.x; g < n_groups; g += kThreads) {
+    const int b = g_req[g];
+    const int T = (r_len[b] + kKvTile - 1) / kKvTile;
+    const long long S = g_start[g], c = kOverheadTiles + T;
+    int nch = 1;
+    if (W > 0) {
+      const long long p_lo = ((S + 1) * n + W - 1) / W;
+      const long long p_hi = ((S + c) * n + W - 1) / W - 1;
+      int prev = 0;
+      for (long long q = max(p_lo, 1LL); q <= min(p_hi, n - 1); ++q) {
+        const int t = cut_tile(q, W, n, S, T);
+        if (t > prev && t < T) {
+          ++nch;
+          prev = t;
+        }
+      }
+    }
+    g_nch[g] = nch;
+    g_items[g] = nch;
+    g_slot[g] = nch > 1 ? nch : 0;
+    g_comb[g] = nch > 1 ? 1 : 0;
+  }
+  __syncthreads();
+  int n_items = block_exclusive_scan(g_items, n_groups, sh);
+  const int n_partials = block_exclusive_scan(g_slot, n_groups, sh);
+  const int n_combine = block_exclusive_scan(g_comb, n_groups, sh);
+  if (n_items > lay.max_items || n_partials > lay.max_partials || n_combine > lay.max_combine) {
+    status |= 8;  // unreachable within the contract
+    n_items = 0;
+  }
+
+  // 4. Items (group order, then chunk order) and combine entries.
+  if (n_items > 0) {
+    for (int g = threadIdx.x; g < n_groups; g += kThreads) {
+      const int b = g_req[g];
+      const int L = r_len[b];
+      const int T = (L + kKvTile - 1) / kKvTile;
+      const long long S = g_start[g], c = kOverheadTiles + T;
+      const int nch = g_nch[g];
+      const int g_local = g - r_gbase[b];
+      int k = 0, prev = 0;
+      long long start_unit = S;
+      auto emit = [&](int t0, int t1, long long unit) {
+        WorkItem it;
+        it.b = b;
+        it.g = g_local;
+        it.kv_begin = t0 * kKvTile;
+        it.kv_end = min(L, t1 * kKvTile);
+        it.slot = nch > 1 ? g_slot[g] + k : -1;
+        it.q_len = r_qlen[b];
+        it.seq_len = L;
+        it.q_start = r_qstart[b];
+        items[g_items[g] + k] = it;
+        it_owner[g_items[g] + k] = owner_of(unit, W, n);
+        ++k;
+      };
+      if (nch > 1 && W > 0) {
+        const long long p_lo = ((S + 1) * n + W - 1) / W;
+        const long long p_hi = ((S + c) * n + W - 1) / W - 1;
+        for (long long q = max(p_lo, 1LL); q <= min(p_hi, n - 1); ++q) {
+          const int t = cut_tile(q, W, n, S, T);
+          if (t > prev && t < T) {
+            emit(prev, t, start_unit);
+            start_unit = S + kOverheadTiles + t;
+            prev = t;
+          }
+        }
+      }
+      emit(prev, T, start_unit);
+      if (nch > 1) {
+        CombineItem ci;
+        ci.b = b;
+        ci.g = g_local;
+        ci.first_slot = g_slot[g];
+        ci.stride = 1;
+        ci.n_chunks = nch;
+        ci.q_len = r_qlen[b];
+        ci.q_start = r_qstart[b];
+        ci.pad = 0;
+        comb[g_comb[g]] = ci;
+      }
+    }
+  }
+  __syncthreads();
+  // 5. Worker ranges: worker w owns items [begin[w], begin[w + 1]).
+  for (int w = threadIdx.x; w <= (int)n; w += kThreads) {
+    int lo = 0, hi = n_items;  // first item with owner >= w
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (it_owner[mid] < w) lo = mid + 1; else hi = mid;
+    }
+    worker_begin[w] = (w == (int)n) ? n_items : lo;
+  }
+  if (threadIdx.x == 0) {
+    hdr[kHdrStatus] = status;
+    hdr[kHdrNumItems] = n_items;
+    hdr[kHdrWorkCounter] = 0;
+    hdr[kHdrNumCombine] = n_items > 0 ? n_combine : 0;
+    hdr[kHdrChunkTiles] = (int)min(W, (long long)1 << 30);
+    hdr[kHdrCombineCounter] = 0;
+  }
+}
+
+cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cudaStream_t stream) {
+  partition_kernel<<<1, kThreads, 0, stream>>>(p, lay, static_cast<char*>(ws));
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Reduced-size variants of the five workloads are compared element by element
+on every output; the full-size workloads, in the launch configuration the
+bench times, are compared on sampled (token, head) pairs the oracle computes
+one by one.  Edge cases: L = 1, L = q, ragged page tails, NaN-poisoned unused
+memory, many-way KV splits, dense masking, packed ragged batches.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import mla_inputs as mi
+import oracle
+from harness import check, device_status, results, run, sample_pairs, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def full_parity(w, **kw):
+    d = to_device(w, **kw)
+    run(w, d)
+    out, lse = results(d)
+    ref_o, ref_l = oracle.run(w, causal=kw.get("causal"))
+    H = w.num_heads
+    rel = check(w.kv_dtype, out.reshape(-1, H, 512), ref_o, lse, ref_l if lse is not None else None,
+                what=w.name)
+    return d, out, lse, rel
+
+
+REDUCED = {
+    "tiny": lambda: mi.tiny(),
+    "deepseek_v3": lambda: mi.deepseek_v3(batch=6, lo=100, hi=700),
+    "mtp": lambda: mi.mtp(batch=4, lo=64, hi=400, return_lse=True),
+    "ragged": lambda: mi.ragged(batch=12, median=200.0, max_len=1000),
+    "fp8_long": lambda: mi.fp8_long(batch=3, lo=500, hi=1500, return_lse=True),
+}
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+def test_reduced_workload_full_parity(name):
+    full_parity(REDUCED[name]())
+
+
+@pytest.mark.parametrize("name", ["deepseek_v3", "mtp", "ragged", "fp8_long"])
+def test_full_size_workload_sampled_parity(name):
+    w = mi.WORKLOADS[name]()
+    d = to_device(w)
+    run(w, d)
+    out, lse = results(d)
+    sel = sample_pairs(w, 48, seed=1)
+    ref_o, ref_l = oracle.run(w, sel=sel)
+    got_o = out.reshape(-1, w.num_heads, 512)[sel[:, 0], sel[:, 1]]
+    got_l = lse[sel[:, 0], sel[:, 1]] if lse is not None else None
+    check(w.kv_dtype, got_o, ref_o, got_l, ref_l if got_l is not None else None, what=w.name)
+    assert np.isfinite(out).all()
+    assert device_status(d) == 0
+
+
+def test_many_way_split_and_long_combine():
+    """One long request on a 16-head group: the partitioner cuts it into far
+    more than 32 chunks, exercising the multi-pass LSE merge."""
+    w = mi.build("split", 77, num_heads=16, page_size=64, seq_lens=[9000], q_lens=[1],
+                 packed=False, return_lse=True)
+    full_parity(w)
+
+
+def test_mixed_split_and_unsplit_requests():
+    w = mi.build("mixed", 78, num_heads=64, page_size=32, seq_lens=[5, 4000, 33, 1200, 64, 2],
+                 q_lens=[2] * 6, packed=False, return_lse=True)
+    full_parity(w)
+
+
+def test_seq_len_one_and_minimum_causal_length():
+    w = mi.build("L1", 79, num_heads=128, page_size=64, seq_lens=[1, 1, 1], q_lens=[1, 1, 1],
+                 packed=False, return_lse=True)
+    full_parity(w)
+    w = mi.build("Lq", 80, num_heads=32, page_size=32, seq_lens=[4, 4, 9], q_lens=[4, 4, 4],
+                 packed=False, return_lse=True)
+    full_parity(w)
+
+
+def test_dense_mask_multi_token():
+    w = mi.build("dense", 81, num_heads=32, page_size=64, seq_lens=[70, 300, 129],
+                 q_lens=[3, 3, 3], packed=False, causal=False, return_lse=True)
+    full_parity(w)
+
+
+def test_ragged_packed_every_q_len():
+    w = mi.build("ragq", 82, num_heads=16, page_size=32, seq_lens=[8, 40, 100, 63, 64, 65, 300, 9],
+                 q_lens=[1, 2, 3, 4, 5, 6, 7, 8], packed=True, return_lse=True, max_seq_len_q=8)
+    full_parity(w)
+
+
+def test_page_permutation_is_bitwise_invariant():
+    w = REDUCED["ragged"]()
+    w2 = mi.permute_pages(w, seed=9)
+    d1 = to_device(w)
+    d2 = to_device(w2)
+    run(w, d1)
+    run(w2, d2)
+    o1, l1 = results(d1)
+    o2, l2 = results(d2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_packed_uniform_equals_fixed_bitwise():
+    w = REDUCED["mtp"]()
+    qo = (np.arange(w.batch + 1) * w.sq).astype(np.int32)
+    wp = dataclasses.replace(w, packed=True, qo_indptr=qo,
+                             query=w.query.reshape(-1, w.num_heads, 576))
+    d1 = to_device(w)
+    d2 = to_device(wp)
+    run(w, d1)
+    run(wp, d2)
+    o1, l1 = results(d1)
+    o2, l2 = results(d2)
+    assert np.array_equal(o1.reshape(o2.shape), o2) and np.array_equal(l1, l2)
+
+
+def test_repeat_runs_are_bitwise_deterministic_with_dirty_workspace():
+    w = REDUCED["deepseek_v3"]()
+    d = to_device(w, return_lse=True, workspace_fill=0xFF)
+    run(w, d)
+    o1, l1 = results(d)
+    d.workspace.fill_(0x7F)
+    run(w, d)
+    o2, l2 = results(d)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_rank4_cache_through_decode_api():
+    import paged_mla_decode_03_gb300 as mla
+    w = REDUCED["tiny"]()
+    d = to_device(w)
+    ws = torch.empty(d.plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    o3, l3 = mla.decode(d.query, d.kv_cache, ws, d.block_tables, d.seq_lens, w.max_seq_len,
+                        bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, return_lse=True)
+    o4, l4 = mla.decode(d.query, d.kv_cache.unsqueeze(1), ws, d.block_tables, d.seq_lens,
+                        w.max_seq_len, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
+                        return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o3, o4) and torch.equal(l3, l4)
+    ref_o, ref_l = oracle.run(w)
+    check("bf16", o3.float().cpu().numpy().reshape(-1, w.num_heads, 512).astype(np.float64),
+          ref_o, l3.cpu().numpy().astype(np.float64), ref_l)
+
+
+def test_cuda_graph_replay_with_new_lengths():
+    """Capture one run, then change seq_lens / qo_indptr values in place and
+    replay: the device-side metadata is re-read on every replay."""
+    w = mi.build("graph", 83, num_heads=16, page_size=32, seq_lens=[300, 120, 77],
+                 q_lens=[2, 3, 1], packed=True, return_lse=True, max_seq_len_q=4)
+    d = to_device(w)
+    run(w, d)  # warm (plan already made outside capture)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            run(w, d, stream=s)
+    for new_lens, new_q in (([250, 64, 77], [3, 2, 1]), ([300, 1, 40], [1, 1, 4])):
+        w2 = mi.build("graph", 83, num_heads=16, page_size=32, seq_lens=new_lens, q_lens=new_q,
+                      packed=True, return_lse=True, max_seq_len_q=4,
+                      block_tables=w.block_tables, num_pages=w.num_pages)
+        # same storage, new values (query / KV contents of the first draw kept)
+        w2 = dataclasses.replace(w2, query=w.query, kv_cache=w.kv_cache, max_seq_len=w.max_seq_len)
+        d.seq_lens.copy_(torch.from_numpy(w2.seq_lens))
+        d.qo_indptr.copy_(torch.from_numpy(w2.qo_indptr))
+        d.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        out, lse = results(d)
+        ref_o, ref_l = oracle.run(w2)
+        check("bf16", out, ref_o, lse, ref_l, what="graph replay")
+
+
+def test_large_packed_total_q():
+    """Prefill-through-decode shape: thousands of packed query tokens."""
+    rng = np.random.default_rng(84)
+    B = 400
+    q = rng.integers(1, 9, size=B)
+    L = rng.integers(8, 200, size=B)
+    L = np.maximum(L, q)
+    w = mi.build("bigq", 84, num_heads=16, page_size=32, seq_lens=L, q_lens=q, packed=True,
+                 return_lse=True, max_seq_len_q=8)
+    d = to_device(w)
+    run(w, d)
+    out, lse = results(d)
+    sel = sample_pairs(w, 64, seed=2)
+    ref_o, ref_l = oracle.run(w, sel=sel)
+    check("bf16", out[sel[:, 0], sel[:, 1]], ref_o, lse[sel[:, 0], sel[:, 1]], ref_l)
+
+
+def test_out_of_contract_lengths_set_status_without_faulting():
+    w = mi.build("bad", 85, num_heads=16, page_size=32, seq_lens=[50, 70], q_lens=[1, 1],
+                 packed=False, return_lse=True)
+    d = to_device(w)
+    d.seq_lens.copy_(torch.tensor([50, w.max_seq_len + 500], dtype=torch.int32))
+    run(w, d)
+    torch.cuda.synchronize()
+    assert device_status(d) & 1
+    d.seq_lens.copy_(torch.from_numpy(w.seq_lens))
+    run(w, d)
+    out, lse = results(d)
+    assert device_status(d) == 0
+    ref_o, ref_l = oracle.run(w)
+    check("bf16", out, ref_o, lse, ref_l)
+
+
+def test_empty_batch_is_a_no_op():
+    import paged_mla_decode_03_gb300 as mla
+    plan = mla.Plan(batch=0, num_heads=16, max_seq_len_q=1, max_seq_len=64, page_size=32,
+                    max_pages_per_req=2, num_pages=4, packed=False)
+    plan.run(0, 0, 0, 0, 0, workspace=0)
+    torch.cuda.synchronize()
+
+
+def test_host_side_errors():
+    import paged_mla_decode_03_gb300 as mla
+    w = REDUCED["tiny"]()
+    d = to_device(w)
+    with pytest.raises(mla.MlaDecodeError) as e:
+        d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=d.lse,
+                   workspace=d.workspace[: d.plan.workspace_bytes // 2],
+                   bmm1_scale=w.bmm1_scale)
+    assert e.value.status == -3
+    with pytest.raises(mla.MlaDecodeError) as e:
+        d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=None,
+                   workspace=d.workspace)
+    assert e.value.status == -1
+    with pytest.raises(mla.MlaDecodeError) as e:
+        d.plan.run(d.query.view(-1)[1:], d.kv_cache, d.block_tables, d.seq_lens, d.out,
+                   lse=d.lse, workspace=d.workspace)
+    assert e.value.status == -4
