@@ -11,23 +11,30 @@
 // streaming the KV range in 64-row tiles with an online (running-max) softmax.
 //
 // GB300 mapping.  A 128 x 512 fp32 accumulator fills a whole SM's TMEM and a
-// 128 x 576 bf16 query tile nearly half its shared memory, so one work item
+// 128 x 576 bf16 query tile needs 144 KB of shared memory, so one work item
 // is shared by the two CTAs of a cluster:
-//  * the QK contraction is split along its 576 dims: CTA r holds 64-dim
-//    chunks 4r .. 4r+4 of Q and of every KV tile and contracts 288 of the 576
-//    dims (18 MMA K-steps of 16) into a partial S (M = 128 query rows,
-//    N = 64 KV rows, fp32 in TMEM);
-//  * the partial scores are exchanged through distributed shared memory, so
-//    both CTAs hold the full S and run identical (bitwise equal) softmaxes;
-//  * CTA r accumulates O^T for V dims [256 r, 256 r + 256) (its local chunks
-//    0..3): O^T = V^T P^T with M = 128 V dims, N = 128 query rows, K = 64
+//  * the QK contraction is split along its 576 dims: CTA r holds latent dims
+//    [256 r, 256 r + 256) and RoPE dims [512 + 32 r, 512 + 32 r + 32) of Q
+//    and of every KV tile (18 MMA K-steps of 16) and forms a partial
+//    S_r (M = 128 query rows, N = 64 KV rows, fp32 in TMEM);
+//  * the softmax is split by rows: CTA r owns query rows [64 r, 64 r + 64).
+//    Its "sender" warps push the partial scores of the peer's rows into the
+//    peer's shared memory with st.async (completing the peer's mbarrier
+//    transaction count); its softmax warps add the peer's partial for their
+//    own rows, normalise, write bf16 P rows and per-row rescale factors, and
+//    a bulk DSMEM copy hands those to the peer, so both CTAs hold all 128
+//    rows of P;
+//  * CTA r accumulates O^T for V dims [256 r, 256 r + 256), i.e. its latent
+//    chunks: O^T = V^T P^T with M = 128 V dims, N = 128 query rows, K = 64
 //    KV rows -- two 128 x 128 fp32 TMEM blocks.
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM
-// owner), warps 4-7 softmax (thread = query row = TMEM lane), warps 8-11
-// O correction and epilogue (thread = V dim = TMEM lane).  The running max
-// is only raised (and O^T rescaled) when it grows by more than 2^8, so most
-// tiles need no correction pass.  Every wait is bounded; a timeout sets an
-// error bit in the workspace status word and the kernel unwinds.
+// Warp roles (320 threads): warp 0 TMA producer (3-stage KV ring), warp 1
+// MMA issuer and TMEM owner, warps 2-5 scores (64 senders + 64 softmax
+// rows), warps 6-9 O correction and epilogue (thread = V dim = TMEM lane).
+// A warp reaches TMEM lanes 32 (w mod 4) .. + 31, so each group of four
+// consecutive warps covers all 128 lanes.
+// The running max is only raised, and O^T rescaled, when it grows by more
+// than 2^8.  Every wait is bounded; a timeout sets an error bit in the
+// workspace status word and the kernel unwinds.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -43,33 +50,37 @@ namespace {
 using namespace ptx;
 
 constexpr int kRows = 128;        // query rows per work item
+constexpr int kHalfRows = 64;     // rows whose softmax each CTA owns
 constexpr int kTile = kKvTile;    // 64 KV rows per tile
-constexpr int kLocalChunks = 5;   // 64-dim chunks each CTA holds (4r .. 4r+4)
-constexpr int kQkSteps = 18;      // 16-wide K steps of the QK contraction per CTA
-constexpr int kThreads = 384;
+constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
+constexpr int kStages = 3;        // KV ring depth
+constexpr int kThreads = 320;
 constexpr uint32_t kWaitLimit = 1u << 26;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // shared-memory layout (bytes from a 1024-aligned base)
-constexpr uint32_t kChunkQ = kRows * 128;   // one 64-dim chunk of Q: 128 rows x 128 B
-constexpr uint32_t kChunkKV = kTile * 128;  // one 64-dim chunk of a KV tile
-constexpr uint32_t kStageBytes = kLocalChunks * kChunkKV;
+constexpr uint32_t kChunkQ = kRows * 128;   // 64-dim chunk of Q, 128B-swizzled rows
+constexpr uint32_t kRopeQ = kRows * 64;     // 32-dim RoPE half of Q, 64B-swizzled rows
+constexpr uint32_t kChunkKV = kTile * 128;  // 64-dim chunk of a KV tile
+constexpr uint32_t kRopeKV = kTile * 64;    // 32-dim RoPE half of a KV tile
+constexpr uint32_t kStageBytes = kLatChunks * kChunkKV + kRopeKV;  // 36 KB
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = OFF_Q + kLocalChunks * kChunkQ;
-constexpr uint32_t OFF_P = OFF_KV + 2 * kStageBytes;
-constexpr uint32_t OFF_X = OFF_P + kRows * 128;
-constexpr uint32_t OFF_MISC = OFF_X + kRows * kTile * 4;
-constexpr uint32_t OFF_BARS = OFF_MISC;
-constexpr uint32_t OFF_FAC = OFF_MISC + 512;          // float[2][128]
-constexpr uint32_t OFF_STAT_M = OFF_FAC + 1024;       // float[2][128]
-constexpr uint32_t OFF_STAT_L = OFF_STAT_M + 1024;    // float[2][128]
-constexpr uint32_t OFF_FLAG = OFF_STAT_L + 1024;      // int[2] tile ids needing correction
-constexpr uint32_t OFF_TMEM = OFF_FLAG + 16;
+constexpr uint32_t OFF_QROPE = OFF_Q + kLatChunks * kChunkQ;
+constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
+constexpr uint32_t OFF_P = OFF_KV + kStages * kStageBytes;
+constexpr uint32_t OFF_X = OFF_P + kRows * 128;        // peer's partial scores of my rows
+constexpr uint32_t OFF_BARS = OFF_X + kHalfRows * kTile * 4;
+constexpr uint32_t kSliceBytes = 272;                  // per warp: fac[32], l[32], flag[4]
+constexpr uint32_t kPartBytes = 2 * kSliceBytes;       // per rank: two warp slices
+constexpr uint32_t OFF_FAC = OFF_BARS + 512;           // [2 tile parities][2 ranks] parts
+constexpr uint32_t OFF_TMEM = OFF_FAC + 4 * kPartBytes;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
 constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0, "alignment");
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
@@ -77,12 +88,12 @@ constexpr uint32_t TM_O = 0;    // two 128-column O^T blocks
 constexpr uint32_t TM_S = 256;  // two 64-column S buffers
 
 enum Bar {
-  Q_FULL, Q_FREE, KV_FULL0, KV_FULL1, KV_EMPTY0, KV_EMPTY1, S_FULL0, S_FULL1, S_FREE0, S_FREE1,
-  P_FULL, P_FREE, PV_DONE, CORR_REQ, CORR_DONE, X_FULL, X_FREE, STATS_READY, STATS_FREE, NUM_BARS
+  Q_FULL, Q_FREE, KV_FULL0, KV_FULL1, KV_FULL2, KV_EMPTY0, KV_EMPTY1, KV_EMPTY2,
+  S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, P_FREE, PV_DONE, CORR_REQ, CORR_DONE,
+  X_FULL, PEER_X_FREE, PEER_P_FREE, NUM_BARS
 };
 
 struct Ctx {
-  unsigned char* sm;
   uint64_t* bars;
   volatile int* abort;
   int* status;
@@ -119,12 +130,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Pointer into the per-tile factor block: parity b, rank part k.
+__device__ __forceinline__ unsigned char* fac_part(unsigned char* sm, int b, int k) {
+  return sm + OFF_FAC + (2 * b + k) * kPartBytes;
+}
+
 }  // namespace
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                     const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_kv) {
+                    const __grid_constant__ CUtensorMap tm_q_rope,
+                    const __grid_constant__ CUtensorMap tm_kv,
+                    const __grid_constant__ CUtensorMap tm_kv_rope) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -139,24 +157,26 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
 
   Ctx c;
-  c.sm = sm;
   c.bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
   c.abort = reinterpret_cast<volatile int*>(sm + OFF_ABORT);
   c.status = &hdr[kHdrStatus];
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
-  float* fac = reinterpret_cast<float*>(sm + OFF_FAC);
-  float* stat_m = reinterpret_cast<float*>(sm + OFF_STAT_M);
-  float* stat_l = reinterpret_cast<float*>(sm + OFF_STAT_L);
-  volatile int* flag = reinterpret_cast<volatile int*>(sm + OFF_FLAG);
 
   if (tid == 0) {
-    const uint32_t counts[NUM_BARS] = {1, 1, 1, 1, 1, 1, 1, 1, 128, 128,
-                                       128, 1, 1, 128, 128, 128, 128, 128, 128};
+    uint32_t counts[NUM_BARS];
+    for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
+    counts[S_FREE0] = counts[S_FREE1] = 128;
+    counts[P_FULL] = counts[CORR_REQ] = counts[PEER_X_FREE] = kHalfRows;
+    counts[CORR_DONE] = 128;
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(&c.bars[i], counts[i]);
     *c.abort = 0;
-    flag[0] = -1;
-    flag[1] = -1;
+    for (int b = 0; b < 2; ++b)
+      for (int k = 0; k < 2; ++k)
+        for (int w = 0; w < 2; ++w)
+          reinterpret_cast<int*>(fac_part(sm, b, k) + w * kSliceBytes + 256)[0] = -1;
     fence_mbar_init();
+    // the first tile's peer scores may arrive as soon as the cluster is up
+    mbar_arrive_expect_tx(&c.bars[X_FULL], kHalfRows * kTile * 4);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -165,7 +185,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers exist before any remote arrive
+  cluster_sync();  // the peer's barriers exist before any remote access
   const uint32_t tmem = *tmem_slot;
   const int item_begin = worker_begin[worker], item_end = worker_begin[worker + 1];
   const int H = p.num_heads;
@@ -174,50 +194,72 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_q_rope);
       tma_prefetch_desc(&tm_kv);
+      tma_prefetch_desc(&tm_kv_rope);
       uint32_t g = 0;
       int n_item = 0;
       const int ps = p.page_size;
+      const int npg = kTile / ps;
       for (int idx = item_begin; idx < item_end; ++idx) {
         const WorkItem it = items[idx];
         const int nt = n_tiles_of(it);
         if (nt <= 0) continue;
+        const int* bt = p.block_tables + (size_t)it.b * p.max_pages;
+        // page ids of the first tile (later tiles are read one tile ahead)
+        int pages[2] = {-1, -1};
+        for (int pg = 0; pg < npg; ++pg) {
+          const int jr = it.kv_begin + pg * ps;
+          if (jr < it.kv_end) pages[pg] = bt[jr / ps];
+        }
         if (!wait_bar(c, Q_FREE, (n_item & 1) ^ 1)) goto done_producer;
         ++n_item;
         {
-          mbar_arrive_expect_tx(&c.bars[Q_FULL], kLocalChunks * kChunkQ);
+          mbar_arrive_expect_tx(&c.bars[Q_FULL], kLatChunks * kChunkQ + kRopeQ);
           const int qrow = it.q_start * H + it.g * kRows;
-          for (int lc = 0; lc < kLocalChunks; ++lc)
-            tma_load_2d(sm + OFF_Q + lc * kChunkQ, &tm_q, 64 * (4 * (int)rank + lc), qrow,
+          for (int lc = 0; lc < kLatChunks; ++lc)
+            tma_load_2d(sm + OFF_Q + lc * kChunkQ, &tm_q, 256 * (int)rank + 64 * lc, qrow,
                         &c.bars[Q_FULL]);
+          tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank, qrow, &c.bars[Q_FULL]);
         }
         for (int t = 0; t < nt; ++t, ++g) {
-          const int s = g & 1;
-          if (!wait_bar(c, KV_EMPTY0 + s, ((g >> 1) & 1) ^ 1)) goto done_producer;
+          const int s = g % kStages;
+          const uint32_t use = g / kStages;
+          // read the next tile's page ids while this tile's slot drains
+          int next[2] = {-1, -1};
+          if (t + 1 < nt)
+            for (int pg = 0; pg < npg; ++pg) {
+              const int jr = it.kv_begin + (t + 1) * kTile + pg * ps;
+              if (jr < it.kv_end) next[pg] = bt[jr / ps];
+            }
+          if (!wait_bar(c, KV_EMPTY0 + s, (use & 1) ^ 1)) goto done_producer;
           const int j0 = it.kv_begin + t * kTile;
-          int pages[2];
           uint32_t bytes = 0;
-          const int npg = kTile / ps;
           for (int pg = 0; pg < npg; ++pg) {
-            const int jr = j0 + pg * ps;
-            pages[pg] = -1;
-            if (jr >= it.kv_end) continue;
-            const int page = p.block_tables[(size_t)it.b * p.max_pages + jr / ps];
-            if (page < 0 || (long long)page >= p.num_pages) {
-              atomicOr(c.status, 16);
+            if (j0 + pg * ps >= it.kv_end) {
+              pages[pg] = -1;
               continue;
             }
-            pages[pg] = page;
-            bytes += kLocalChunks * ps * 128;
+            if (pages[pg] < 0 || (long long)pages[pg] >= p.num_pages) {
+              atomicOr(c.status, 16);
+              pages[pg] = -1;
+              continue;
+            }
+            bytes += ps * (kLatChunks * 128 + 64);
           }
           mbar_arrive_expect_tx(&c.bars[KV_FULL0 + s], bytes);
           unsigned char* stage = sm + OFF_KV + s * kStageBytes;
           for (int pg = 0; pg < npg; ++pg) {
             if (pages[pg] < 0) continue;
-            for (int lc = 0; lc < kLocalChunks; ++lc)
-              tma_load_2d(stage + lc * kChunkKV + pg * ps * 128, &tm_kv, 64 * (4 * (int)rank + lc),
-                          pages[pg] * ps, &c.bars[KV_FULL0 + s]);
+            const int y = pages[pg] * ps;
+            for (int lc = 0; lc < kLatChunks; ++lc)
+              tma_load_2d(stage + lc * kChunkKV + pg * ps * 128, &tm_kv, 256 * (int)rank + 64 * lc,
+                          y, &c.bars[KV_FULL0 + s]);
+            tma_load_2d(stage + kLatChunks * kChunkKV + pg * ps * 64, &tm_kv_rope,
+                        512 + 32 * (int)rank, y, &c.bars[KV_FULL0 + s]);
           }
+          pages[0] = next[0];
+          pages[1] = next[1];
         }
       }
     done_producer:;
@@ -228,27 +270,33 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       constexpr uint32_t idesc_qk = idesc_f16(128, 64, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, 128, true, false);
       const uint32_t q_base = smem_u32(sm + OFF_Q);
+      const uint32_t qr_base = smem_u32(sm + OFF_QROPE);
       const uint32_t kv_base = smem_u32(sm + OFF_KV);
       const uint32_t p_base = smem_u32(sm + OFF_P);
       uint32_t g = 0;
       int n_item = 0;
       bool ok = true;
       auto issue_qk = [&](uint32_t gq) -> bool {
-        const int s = gq & 1;
-        if (!wait_bar(c, KV_FULL0 + s, (gq >> 1) & 1)) return false;
-        if (!wait_bar(c, S_FREE0 + s, ((gq >> 1) & 1) ^ 1)) return false;
+        const int s = gq % kStages;
+        const int sb = gq & 1;
+        if (!wait_bar(c, KV_FULL0 + s, (gq / kStages) & 1)) return false;
+        if (!wait_bar(c, S_FREE0 + sb, ((gq >> 1) & 1) ^ 1)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + TM_S + 64 * s;
-        for (int k = 0; k < kQkSteps; ++k) {
-          const int gk = kQkSteps * (int)rank + k;  // global K step 0..35
-          const int lc = gk / 4 - 4 * (int)rank;
-          const int ks = gk % 4;
+        const uint32_t d = tmem + TM_S + 64 * sb;
+        const uint32_t stage = kv_base + s * kStageBytes;
+        for (int k = 0; k < 4 * kLatChunks; ++k) {
+          const int lc = k >> 2, ks = k & 3;
           const uint64_t a = smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
-          const uint64_t b = smem_desc(kv_base + s * kStageBytes + lc * kChunkKV + ks * 32, 16,
-                                       1024, kSwizzle128B);
+          const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
           mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
         }
-        mma_commit(&c.bars[S_FULL0 + s]);
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
+          const uint64_t b = smem_desc(stage + kLatChunks * kChunkKV + ks * 32, 16, 512,
+                                       kSwizzle64B);
+          mma_bf16_ss(d, a, b, idesc_qk, 1u);
+        }
+        mma_commit(&c.bars[S_FULL0 + sb]);
         return true;
       };
       for (int idx = item_begin; idx < item_end && ok; ++idx) {
@@ -267,12 +315,12 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           }
           if (!wait_bar(c, P_FULL, g & 1) || !wait_bar(c, CORR_DONE, g & 1)) { ok = false; break; }
           tc_fence_after();
-          const int s = g & 1;
+          const int s = g % kStages;
+          const uint32_t stage = kv_base + s * kStageBytes;
           for (int bb = 0; bb < 2; ++bb) {
             for (int ks = 0; ks < kTile / 16; ++ks) {
-              const uint64_t a = smem_desc(kv_base + s * kStageBytes + (2 * bb) * kChunkKV +
-                                               ks * 16 * 128,
-                                           8192, 1024, kSwizzle128B);
+              const uint64_t a = smem_desc(stage + (2 * bb) * kChunkKV + ks * 16 * 128, 8192, 1024,
+                                           kSwizzle128B);
               const uint64_t b = smem_desc(p_base + ks * 32, 16, 1024, kSwizzle128B);
               mma_bf16_ss(tmem + TM_O + 128 * bb, a, b, idesc_pv, (t == 0 && ks == 0) ? 0u : 1u);
             }
@@ -283,165 +331,231 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ softmax
-    const int r = tid - 128;  // query row within the item == TMEM lane
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------------------ scores
+    const int q = 32 * (warp & 3) + lane;  // query row within the item == TMEM lane
+    const bool mine = (q >> 6) == (int)rank;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const float scale = p.bmm1_scale * kLog2e;
-    const uint32_t x_local = smem_u32(sm + OFF_X + r * 256);
-    const uint32_t x_peer = map_to_rank(x_local, peer);
-    const uint32_t xfull_peer = map_to_rank(smem_u32(&c.bars[X_FULL]), peer);
-    const uint32_t xfree_peer = map_to_rank(smem_u32(&c.bars[X_FREE]), peer);
     uint32_t g = 0;
-    int n_item = 0;
-    for (int idx = item_begin; idx < item_end; ++idx) {
-      const WorkItem it = items[idx];
-      const int nt = n_tiles_of(it);
-      if (nt <= 0) continue;
-      const int rows_total = it.q_len * H;
-      const int row0 = it.g * kRows;
-      const bool row_ok = r < rows_total - row0;
-      const int qi = (row0 + r) / H;
-      const int last = p.causal ? it.seq_len - it.q_len + qi : it.seq_len - 1;
-      float m_ref = -INFINITY, l_sum = 0.f;
-      for (int t = 0; t < nt; ++t, ++g) {
-        const int s = g & 1;
-        float sv[kTile];
-        if (!wait_bar(c, S_FULL0 + s, (g >> 1) & 1)) goto done_softmax;
-        tc_fence_after();
+    if (!mine) {
+      // sender: partial scores of the peer's rows -> peer's X buffer
+      const int pr = q & 63;  // row index inside the peer's buffer
+      const uint32_t x_peer = map_to_rank(smem_u32(sm + OFF_X + pr * 256), peer);
+      const uint32_t xfull_peer = map_to_rank(smem_u32(&c.bars[X_FULL]), peer);
+      for (int idx = item_begin; idx < item_end; ++idx) {
+        const WorkItem it = items[idx];
+        const int nt = n_tiles_of(it);
+        if (nt <= 0) continue;
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int sb = g & 1;
+          if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_scores;
+          tc_fence_after();
+          uint32_t v[4][16];
 #pragma unroll
-        for (int q4 = 0; q4 < kTile / 16; ++q4) {
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * s + 16 * q4, v);
+          for (int k = 0; k < 4; ++k)
+            tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * sb + 16 * k, v[k]);
           tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) sv[16 * q4 + j] = __uint_as_float(v[j]);
-        }
-        tc_fence_before();
-        mbar_arrive(&c.bars[S_FREE0 + s]);
-        // exchange partial scores with the peer CTA
-        if (!wait_bar(c, X_FREE, (g & 1) ^ 1)) goto done_softmax;
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          st_cluster_v4(x_peer + (uint32_t)((k ^ (r & 7)) << 4),
-                        make_float4(sv[4 * k], sv[4 * k + 1], sv[4 * k + 2], sv[4 * k + 3]));
-        mbar_arrive_cluster(xfull_peer);
-        if (!wait_bar_cluster(c, X_FULL, g & 1)) goto done_softmax;
-        {
-          const float4* xs = reinterpret_cast<const float4*>(sm + OFF_X + r * 256);
+          tc_fence_before();
+          mbar_arrive(&c.bars[S_FREE0 + sb]);
+          if (!wait_bar_cluster(c, PEER_X_FREE, (g & 1) ^ 1)) goto done_scores;
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float4 v = xs[k ^ (r & 7)];
-            sv[4 * k] += v.x;
-            sv[4 * k + 1] += v.y;
-            sv[4 * k + 2] += v.z;
-            sv[4 * k + 3] += v.w;
+            const uint32_t* w = &v[k >> 2][4 * (k & 3)];
+            st_async_v4(x_peer + (uint32_t)((k ^ (pr & 7)) << 4),
+                        make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]),
+                                    __uint_as_float(w[2]), __uint_as_float(w[3])),
+                        xfull_peer);
           }
-        }
-        mbar_arrive_cluster(xfree_peer);
-        // mask, scale, online softmax
-        const int j0 = it.kv_begin + t * kTile;
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kTile; ++j) {
-          const int col = j0 + j;
-          const bool ok = row_ok && col <= last && col < it.kv_end;
-          sv[j] = ok ? sv[j] * scale : -INFINITY;
-          tmax = fmaxf(tmax, sv[j]);
-        }
-        const float m_new = fmaxf(m_ref, tmax);
-        bool need = false;
-        float f = 1.f;
-        if (t == 0) {
-          m_ref = m_new;
-        } else if (m_new > m_ref + kRescaleThreshold) {
-          f = exp2f(m_ref - m_new);  // m_ref = -inf gives 0
-          need = true;
-          l_sum *= f;
-          m_ref = m_new;
-        }
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float rs = 0.f;
-#pragma unroll
-        for (int j = 0; j < kTile; ++j) {
-          sv[j] = exp2f(sv[j] - m_use);
-          rs += sv[j];
-        }
-        l_sum += rs;
-        // zero V rows past the end of the KV range in the last tile
-        const int valid = it.kv_end - j0;
-        if (valid < kTile) {
-          unsigned char* stage = sm + OFF_KV + s * kStageBytes;
-          const int nz = (kTile - valid) * 4 * 8;  // 16-byte units over 4 chunks
-          for (int e = r; e < nz; e += 128) {
-            const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
-            *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-        // P (bf16) into the PV B-operand tile: row r, 128-byte swizzled
-        if (!wait_bar(c, P_FREE, (g & 1) ^ 1)) goto done_softmax;
-        {
-          unsigned char* prow = sm + OFF_P + r * 128;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint4 w;
-            w.x = pack_bf16(sv[8 * k + 0], sv[8 * k + 1]);
-            w.y = pack_bf16(sv[8 * k + 2], sv[8 * k + 3]);
-            w.z = pack_bf16(sv[8 * k + 4], sv[8 * k + 5]);
-            w.w = pack_bf16(sv[8 * k + 6], sv[8 * k + 7]);
-            *reinterpret_cast<uint4*>(prow + ((k ^ (r & 7)) << 4)) = w;
-          }
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&c.bars[P_FULL]);
-        fac[(g & 1) * kRows + r] = f;
-        if (__any_sync(0xffffffffu, need) && lane == 0) flag[g & 1] = (int)g;
-        mbar_arrive(&c.bars[CORR_REQ]);
-      }
-      // final row statistics for the epilogue, LSE from CTA 0
-      if (!wait_bar(c, STATS_FREE, (n_item & 1) ^ 1)) goto done_softmax;
-      stat_m[(n_item & 1) * kRows + r] = m_ref;
-      stat_l[(n_item & 1) * kRows + r] = l_sum;
-      mbar_arrive(&c.bars[STATS_READY]);
-      if (rank == 0 && row_ok) {
-        const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-        const size_t grow = (size_t)it.q_start * H + row0 + r;
-        if (it.slot < 0) {
-          if (p.return_lse) p.lse[grow] = lse;
-        } else {
-          part_lse[(size_t)it.slot * kRows + r] = lse;
         }
       }
-      ++n_item;
+    } else {
+      // softmax of my 64 rows (two warps; each warp hands its 32 rows to the peer)
+      const int mr = q & 63;  // my row index (0..63)
+      const int hw = mr >> 5;  // which of my two warps
+      const bool leader = mr == 0;
+      const float scale = p.bmm1_scale * kLog2e;
+      const uint32_t pfree_peer = map_to_rank(smem_u32(&c.bars[PEER_P_FREE]), peer);
+      const uint32_t xfree_peer = map_to_rank(smem_u32(&c.bars[PEER_X_FREE]), peer);
+      const uint32_t pfull_peer = map_to_rank(smem_u32(&c.bars[P_FULL]), peer);
+      const uint32_t corr_peer = map_to_rank(smem_u32(&c.bars[CORR_REQ]), peer);
+      const uint32_t p_rows_off = OFF_P + (uint32_t)(kHalfRows * (int)rank + 32 * hw) * 128;
+      const uint32_t p_peer = map_to_rank(smem_u32(sm + p_rows_off), peer);
+      const float4* xs = reinterpret_cast<const float4*>(sm + OFF_X + mr * 256);
+      for (int idx = item_begin; idx < item_end; ++idx) {
+        const WorkItem it = items[idx];
+        const int nt = n_tiles_of(it);
+        if (nt <= 0) continue;
+        const int rows_total = it.q_len * H;
+        const int row0 = it.g * kRows;
+        const bool row_ok = q < rows_total - row0;
+        const int qi = (row0 + q) / H;
+        const int last = p.causal ? it.seq_len - it.q_len + qi : it.seq_len - 1;
+        // tiles ending at or before `clean_end` need no mask for any valid row
+        const int first_qi = row0 / H;
+        const int clean_end =
+            min(it.kv_end, p.causal ? it.seq_len - it.q_len + first_qi + 1 : it.seq_len);
+        float m_ref = -INFINITY, l_sum = 0.f;
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int sb = g & 1;
+          float sv[kTile];
+          if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_scores;
+          tc_fence_after();
+          {
+            uint32_t v[4][16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * sb + 16 * k, v[k]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < kTile; ++j) sv[j] = __uint_as_float(v[j >> 4][j & 15]);
+          }
+          tc_fence_before();
+          mbar_arrive(&c.bars[S_FREE0 + sb]);
+          // add the peer's partial for my rows, then release the row to the peer
+          if (!wait_bar(c, X_FULL, g & 1)) goto done_scores;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float4 x = xs[k ^ (mr & 7)];
+            sv[4 * k] += x.x;
+            sv[4 * k + 1] += x.y;
+            sv[4 * k + 2] += x.z;
+            sv[4 * k + 3] += x.w;
+          }
+          if (leader) mbar_arrive_expect_tx(&c.bars[X_FULL], kHalfRows * kTile * 4);  // next tile
+          mbar_arrive_cluster_relaxed(xfree_peer);
+          // mask, scale, online softmax
+          const int j0 = it.kv_begin + t * kTile;
+          float f = 1.f;
+          bool need = false;
+          if (row_ok) {
+            float tmax = -INFINITY;
+            if (j0 + kTile <= clean_end) {
+#pragma unroll
+              for (int j = 0; j < kTile; ++j) {
+                sv[j] *= scale;
+                tmax = fmaxf(tmax, sv[j]);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < kTile; ++j) {
+                const int col = j0 + j;
+                sv[j] = (col <= last && col < it.kv_end) ? sv[j] * scale : -INFINITY;
+                tmax = fmaxf(tmax, sv[j]);
+              }
+            }
+            const float m_new = fmaxf(m_ref, tmax);
+            if (t == 0) {
+              m_ref = m_new;
+            } else if (m_new > m_ref + kRescaleThreshold) {
+              f = ex2(m_ref - m_new);  // m_ref = -inf gives 0
+              need = true;
+              l_sum *= f;
+              m_ref = m_new;
+            }
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < kTile; ++j) {
+              sv[j] = ex2(sv[j] - m_use);
+              rs += sv[j];
+            }
+            l_sum += rs;
+          } else {
+#pragma unroll
+            for (int j = 0; j < kTile; ++j) sv[j] = 0.f;
+          }
+          // zero V rows past the end of the KV range (last tile of the item)
+          const int valid = it.kv_end - j0;
+          if (valid < kTile) {
+            unsigned char* stage = sm + OFF_KV + (g % kStages) * kStageBytes;
+            const int nz = (kTile - valid) * kLatChunks * 8;  // 16-byte units
+            for (int e = mr; e < nz; e += kHalfRows) {
+              const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
+              *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+          }
+          // my P rows may be overwritten once the local PV of the previous tile is done
+          if (!wait_bar(c, P_FREE, (g & 1) ^ 1)) goto done_scores;
+          if (leader) {
+            // expect the peer's P rows and factor slices, then let the peer send them
+            mbar_expect_tx(&c.bars[P_FULL], kHalfRows * 128);
+            mbar_expect_tx(&c.bars[CORR_REQ], kPartBytes);
+            mbar_arrive_cluster_relaxed(pfree_peer);
+          }
+          {
+            unsigned char* prow = sm + OFF_P + q * 128;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              uint4 w;
+              w.x = pack_bf16(sv[8 * k + 0], sv[8 * k + 1]);
+              w.y = pack_bf16(sv[8 * k + 2], sv[8 * k + 3]);
+              w.z = pack_bf16(sv[8 * k + 4], sv[8 * k + 5]);
+              w.w = pack_bf16(sv[8 * k + 6], sv[8 * k + 7]);
+              *reinterpret_cast<uint4*>(prow + ((k ^ (q & 7)) << 4)) = w;
+            }
+          }
+          unsigned char* slice = fac_part(sm, g & 1, rank) + hw * kSliceBytes;
+          reinterpret_cast<float*>(slice)[lane] = f;
+          reinterpret_cast<float*>(slice + 128)[lane] = l_sum;
+          const bool any = __any_sync(0xffffffffu, need);
+          if (lane == 0 && any) reinterpret_cast<volatile int*>(slice + 256)[0] = (int)g;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (!wait_bar_cluster(c, PEER_P_FREE, g & 1)) goto done_scores;
+            bulk_copy_to_peer(p_peer, sm + p_rows_off, 32 * 128, pfull_peer);
+            bulk_copy_to_peer(map_to_rank(smem_u32(slice), peer), slice, kSliceBytes, corr_peer);
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          __syncwarp();
+          mbar_arrive(&c.bars[P_FULL]);
+          mbar_arrive(&c.bars[CORR_REQ]);
+        }
+        // LSE of my rows
+        if (row_ok) {
+          const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+          const size_t grow = (size_t)it.q_start * H + row0 + q;
+          if (it.slot < 0) {
+            if (p.return_lse) p.lse[grow] = lse;
+          } else {
+            part_lse[(size_t)it.slot * kRows + q] = lse;
+          }
+        }
+      }
     }
-  done_softmax:;
-  } else if (warp >= 8) {
+  done_scores:;
+  } else if (warp >= 6) {
     // ------------------------------------------------------------ correction + epilogue
-    const int v = tid - 256;  // V dim within each 128-wide O^T block == TMEM lane
+    const int v = 32 * (warp & 3) + lane;  // V dim within each 128-wide O^T block == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     uint32_t g = 0;
-    int n_item = 0;
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
       const int nt = n_tiles_of(it);
       if (nt <= 0) continue;
       for (int t = 0; t < nt; ++t, ++g) {
         if (!wait_bar(c, CORR_REQ, g & 1)) goto done_epi;
-        if (t > 0 && flag[g & 1] == (int)g) {
+        bool rescale = false;
+        for (int k = 0; k < 4; ++k)
+          rescale |= reinterpret_cast<volatile int*>(fac_part(sm, g & 1, k >> 1) +
+                                                     (k & 1) * kSliceBytes + 256)[0] == (int)g;
+        if (t > 0 && rescale) {
           if (!wait_bar(c, PV_DONE, (g - 1) & 1)) goto done_epi;
           tc_fence_after();
-          const float* f = fac + (g & 1) * kRows;
           for (int bb = 0; bb < 2; ++bb) {
 #pragma unroll 1
             for (int q16 = 0; q16 < kRows / 16; ++q16) {
+              const float* f = reinterpret_cast<const float*>(
+                                   fac_part(sm, g & 1, q16 >> 2) + ((q16 >> 1) & 1) * kSliceBytes) +
+                               16 * (q16 & 1);
               uint32_t x[16];
               const uint32_t addr = tmem + lane_base + TM_O + 128 * bb + 16 * q16;
               tmem_ld_32x32b_x16(addr, x);
               tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; ++j)
-                x[j] = __float_as_uint(__uint_as_float(x[j]) * f[16 * q16 + j]);
+              for (int j = 0; j < 16; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * f[j]);
               tmem_st_32x32b_x16(addr, x);
             }
           }
@@ -450,42 +564,44 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         tc_fence_before();
         mbar_arrive(&c.bars[CORR_DONE]);
       }
-      if (!wait_bar(c, STATS_READY, n_item & 1)) goto done_epi;
+      // epilogue: O = O^T(transposed) / l, from the last tile's factor block
       if (!wait_bar(c, PV_DONE, (g - 1) & 1)) goto done_epi;
       tc_fence_after();
       {
         const int rows_total = it.q_len * H;
         const int row0 = it.g * kRows;
         const int n_rows = min(kRows, rows_total - row0);
-        const float* lrow = stat_l + (n_item & 1) * kRows;
         const size_t grow0 = (size_t)it.q_start * H + row0;
+        const int lb = (g - 1) & 1;
         for (int bb = 0; bb < 2; ++bb) {
           const int vd = 256 * (int)rank + 128 * bb + v;  // output V dim
 #pragma unroll 1
           for (int q16 = 0; q16 < kRows / 16; ++q16) {
+            if (16 * q16 >= n_rows) break;
+            const float* lrow = reinterpret_cast<const float*>(
+                                    fac_part(sm, lb, q16 >> 2) + ((q16 >> 1) & 1) * kSliceBytes +
+                                    128) +
+                                16 * (q16 & 1);
             uint32_t x[16];
             tmem_ld_32x32b_x16(tmem + lane_base + TM_O + 128 * bb + 16 * q16, x);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int q = 16 * q16 + j;
-              if (q >= n_rows) break;
-              const float l = lrow[q];
+              const int qq = 16 * q16 + j;
+              if (qq >= n_rows) break;
+              const float l = lrow[j];
               const float inv = l > 0.f ? 1.f / l : 0.f;
               const float o = __uint_as_float(x[j]) * inv;
               if (it.slot < 0) {
-                reinterpret_cast<__nv_bfloat16*>(p.out)[(grow0 + q) * kVDim + vd] =
+                reinterpret_cast<__nv_bfloat16*>(p.out)[(grow0 + qq) * kVDim + vd] =
                     __float2bfloat16_rn(o * p.bmm2_scale);
               } else {
-                part_o[((size_t)it.slot * kRows + q) * kVDim + vd] = o;
+                part_o[((size_t)it.slot * kRows + qq) * kVDim + vd] = o;
               }
             }
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&c.bars[STATS_FREE]);
-      ++n_item;
     }
   done_epi:;
   }
@@ -516,16 +632,16 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base,
-               uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows) {
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_inner,
+               uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * elem_bytes};
+  cuuint64_t dims[2] = {(cuuint64_t)kQkDim, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kQkDim * 2};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -556,15 +672,16 @@ cudaError_t decode_sm103_setup(int sm_count, int* n_pairs) {
 
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                                 cudaStream_t stream) {
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q, tm_q_rope, tm_kv, tm_kv_rope;
   const uint64_t q_rows = std::max<uint64_t>(1, (uint64_t)p.total_q * p.num_heads);
-  if (!encode_2d(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.query, kQkDim, q_rows, 64, kRows))
+  const uint64_t kv_rows = (uint64_t)p.num_pages * p.page_size;
+  if (!encode_2d(&tm_q, p.query, q_rows, 64, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_q_rope, p.query, q_rows, 32, kRows, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_2d(&tm_kv, p.kv_cache, kv_rows, 64, p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_kv_rope, p.kv_cache, kv_rows, 32, p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  if (!encode_2d(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv_cache, kQkDim,
-                 (uint64_t)p.num_pages * p.page_size, 64, p.page_size))
-    return cudaErrorInvalidValue;
-  decode_sm103_kernel<<<lay.n_ctas, kThreads, kSmemBytes, stream>>>(p, lay, static_cast<char*>(ws),
-                                                                     tm_q, tm_kv);
+  decode_sm103_kernel<<<lay.n_ctas, kThreads, kSmemBytes, stream>>>(
+      p, lay, static_cast<char*>(ws), tm_q, tm_q_rope, tm_kv, tm_kv_rope);
   return cudaGetLastError();
 }
 

@@ -215,7 +215,8 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
       const int nch = g_nch[g];
       const int g_local = g - r_gbase[b];
       int k = 0, prev = 0;
-      long long start_unit = S;
+      // an item belongs to the worker whose range holds its first KV tile
+      long long start_unit = S + kOverheadTiles;
       auto emit = [&](int t0, int t1, long long unit) {
         WorkItem it;
         it.b = b;

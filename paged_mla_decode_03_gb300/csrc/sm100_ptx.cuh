@@ -230,3 +230,58 @@ __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_
 
 }  // namespace ptx
 }  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+constexpr uint32_t kSwizzle64B = 4;
+
+// expect-tx without an arrival
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Asynchronous 16-byte store into a peer CTA's shared memory that completes
+// `bytes` of the transaction count of the peer's mbarrier `remote_bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(remote_addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+      : "memory");
+}
+// Bulk copy from this CTA's shared memory into a peer CTA's shared memory,
+// completing the transaction count of the peer's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const void* src,
+                                                  uint32_t bytes, uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(remote_dst),
+      "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+// Relaxed remote arrive: orders nothing, only counts (for write-after-read
+// hand-offs whose reads have already returned their values).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Named barrier over `nthreads` threads (id 1..15).
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace ptx
+}  // namespace mla
