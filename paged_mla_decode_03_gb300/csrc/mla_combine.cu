@@ -7,6 +7,11 @@
 // which is exactly the single-pass result.  The natural-log LSE is the form
 // the vLLM "FlashInferMLAImpl" page uses to merge partial attention across
 // decode-context-parallel shards; here the shards are KV chunks of one GPU.
+//
+// Grid: (row blocks of 4 rows) x (combine entries), 256 threads; 64 threads
+// per row, 8 output dims per thread, all chunk loads of a thread issued
+// together.  Blocks past the live number of entries exit at once, so the
+// grid depends only on plan-time bounds.
 #include <cuda_bf16.h>
 
 #include "mla_common.cuh"
@@ -15,7 +20,9 @@ namespace mla {
 
 namespace {
 constexpr int kThreads = 256;
-}
+constexpr int kRowsPerBlock = 4;
+constexpr int kUnroll = 8;
+}  // namespace
 
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
@@ -24,70 +31,69 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   const float* part_o = reinterpret_cast<const float*>(ws + lay.part_o);
   const float* part_lse = reinterpret_cast<const float*>(ws + lay.part_lse);
   const int n_combine = hdr[kHdrNumCombine];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = p.num_heads;
   const int R = lay.rows_per_group;
+  const int row_in_block = threadIdx.x >> 6;  // 0..3
+  const int t = threadIdx.x & 63;             // output dims [8 t, 8 t + 8)
 
-  for (int ci = blockIdx.x; ci < n_combine; ci += gridDim.x) {
+  for (int ci = blockIdx.y; ci < n_combine; ci += gridDim.y) {
     const CombineItem c = comb[ci];
-    const int rows_total = c.q_len * H;
-    const int rows = min(R, rows_total - c.g * R);
-    for (int r = warp; r < rows; r += kThreads / 32) {
-      // weights: each lane holds up to one chunk's lse per 32-chunk pass
-      float m = -INFINITY;
-      for (int k = lane; k < c.n_chunks; k += 32) {
-        const int slot = c.first_slot + k * c.stride;
-        m = fmaxf(m, part_lse[(size_t)slot * R + r]);
-      }
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const float m_use = (m == -INFINITY) ? 0.f : m;
-      float sum = 0.f;
-      for (int k = lane; k < c.n_chunks; k += 32) {
-        const int slot = c.first_slot + k * c.stride;
-        sum += expf(part_lse[(size_t)slot * R + r] - m_use);
-      }
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      const float inv = sum > 0.f ? 1.f / sum : 0.f;
-      // each lane owns 16 output dims: d = lane * 4 + 128 * v, v = 0..3
-      float4 acc[4];
+    const int rows = min(R, c.q_len * H - c.g * R);
+    const int r = blockIdx.x * kRowsPerBlock + row_in_block;
+    if (r >= rows) continue;
+    float m = -INFINITY;
+    for (int k = 0; k < c.n_chunks; ++k)
+      m = fmaxf(m, part_lse[(size_t)(c.first_slot + k * c.stride) * R + r]);
+    const float m_use = (m == -INFINITY) ? 0.f : m;
+    float sum = 0.f;
+    float acc[8];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k = 0; k < c.n_chunks; ++k) {
-        const int slot = c.first_slot + k * c.stride;
-        const float w = expf(part_lse[(size_t)slot * R + r] - m_use) * inv;
-        const float4* src = reinterpret_cast<const float4*>(
-            part_o + ((size_t)slot * R + r) * kVDim);
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int k0 = 0; k0 < c.n_chunks; k0 += kUnroll) {
+      float4 x[kUnroll][2];
+      float w[kUnroll];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const float4 x = src[lane + 32 * v];
-          acc[v].x += w * x.x;
-          acc[v].y += w * x.y;
-          acc[v].z += w * x.z;
-          acc[v].w += w * x.w;
+      for (int u = 0; u < kUnroll; ++u) {
+        w[u] = 0.f;
+        x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k0 + u < c.n_chunks) {
+          const size_t slot = (size_t)(c.first_slot + (k0 + u) * c.stride);
+          const float4* src =
+              reinterpret_cast<const float4*>(part_o + (slot * R + r) * kVDim) + 2 * t;
+          x[u][0] = src[0];
+          x[u][1] = src[1];
+          w[u] = expf(part_lse[slot * R + r] - m_use);
         }
       }
-      const size_t grow = (size_t)c.q_start * H + (size_t)c.g * R + r;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kVDim;
-      const float s2 = p.bmm2_scale;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[v].x * s2, acc[v].y * s2);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[v].z * s2, acc[v].w * s2);
-        uint2 packed;
-        packed.x = *reinterpret_cast<uint32_t*>(&lo);
-        packed.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(dst + 4 * (lane + 32 * v)) = packed;
+      for (int u = 0; u < kUnroll; ++u) {
+        sum += w[u];
+        acc[0] += w[u] * x[u][0].x;
+        acc[1] += w[u] * x[u][0].y;
+        acc[2] += w[u] * x[u][0].z;
+        acc[3] += w[u] * x[u][0].w;
+        acc[4] += w[u] * x[u][1].x;
+        acc[5] += w[u] * x[u][1].y;
+        acc[6] += w[u] * x[u][1].z;
+        acc[7] += w[u] * x[u][1].w;
       }
-      if (p.return_lse && lane == 0)
-        p.lse[grow] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
     }
+    const float s2 = sum > 0.f ? p.bmm2_scale / sum : 0.f;
+    const size_t grow = (size_t)c.q_start * H + (size_t)c.g * R + r;
+    __nv_bfloat162 o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kVDim + 8 * t) =
+        *reinterpret_cast<uint4*>(o);
+    if (p.return_lse && t == 0) p.lse[grow] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
   }
 }
 
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  combine_kernel<<<grid, kThreads, 0, stream>>>(p, lay, static_cast<char*>(ws));
+  const dim3 g((lay.rows_per_group + kRowsPerBlock - 1) / kRowsPerBlock, grid, 1);
+  combine_kernel<<<g, kThreads, 0, stream>>>(p, lay, static_cast<char*>(ws));
   return cudaGetLastError();
 }
 

@@ -27,11 +27,12 @@
 //  * CTA r accumulates O^T for V dims [256 r, 256 r + 256), i.e. its latent
 //    chunks: O^T = V^T P^T with M = 128 V dims, N = 128 query rows, K = 64
 //    KV rows -- two 128 x 128 fp32 TMEM blocks.
-// Warp roles (320 threads): warp 0 TMA producer (3-stage KV ring), warp 1
-// MMA issuer and TMEM owner, warps 2-5 scores (64 senders + 64 softmax
-// rows), warps 6-9 O correction and epilogue (thread = V dim = TMEM lane).
-// A warp reaches TMEM lanes 32 (w mod 4) .. + 31, so each group of four
-// consecutive warps covers all 128 lanes.
+// Warp roles (448 threads): warp 0 TMA producer (3-stage KV ring), warp 1
+// MMA issuer and TMEM owner, warps 2-9 scores (two threads per row; the
+// warps on the peer's rows send, the warps on this CTA's rows run the
+// softmax), warps 10-13 O correction and epilogue (thread = V dim = TMEM
+// lane).  A warp reaches TMEM lanes 32 (w mod 4) .. + 31, so each group of
+// four consecutive warps covers all 128 lanes.
 // The running max is only raised, and O^T rescaled, when it grows by more
 // than 2^8.  Every wait is bounded; a timeout sets an error bit in the
 // workspace status word and the kernel unwinds.
@@ -54,7 +55,7 @@ constexpr int kHalfRows = 64;     // rows whose softmax each CTA owns
 constexpr int kTile = kKvTile;    // 64 KV rows per tile
 constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
 constexpr int kStages = 3;        // KV ring depth
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr uint32_t kWaitLimit = 1u << 26;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -72,8 +73,8 @@ constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
 constexpr uint32_t OFF_P = OFF_KV + kStages * kStageBytes;
 constexpr uint32_t OFF_X = OFF_P + kRows * 128;        // peer's partial scores of my rows
 constexpr uint32_t OFF_BARS = OFF_X + kHalfRows * kTile * 4;
-constexpr uint32_t kSliceBytes = 272;                  // per warp: fac[32], l[32], flag[4]
-constexpr uint32_t kPartBytes = 2 * kSliceBytes;       // per rank: two warp slices
+constexpr uint32_t kSliceBytes = 144;                  // per warp: fac[16], l[16], flag[4]
+constexpr uint32_t kPartBytes = 4 * kSliceBytes;       // per rank: four warp slices
 constexpr uint32_t OFF_FAC = OFF_BARS + 512;           // [2 tile parities][2 ranks] parts
 constexpr uint32_t OFF_TMEM = OFF_FAC + 4 * kPartBytes;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
@@ -89,9 +90,13 @@ constexpr uint32_t TM_S = 256;  // two 64-column S buffers
 
 enum Bar {
   Q_FULL, Q_FREE, KV_FULL0, KV_FULL1, KV_FULL2, KV_EMPTY0, KV_EMPTY1, KV_EMPTY2,
-  S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, P_FREE, PV_DONE, CORR_REQ, CORR_DONE,
-  X_FULL, PEER_X_FREE, PEER_P_FREE, NUM_BARS
+  S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, P_FREE, O_STABLE, CORR_DONE, CE_FREE, O_FINAL,
+  EPI_DONE, X_FULL, PEER_X_FREE, PEER_P_FREE, NUM_BARS
 };
+
+// True if any of the eight 16-row groups (2 CTAs x 4 warps) asked for an O^T
+// rescale at global tile g.
+__device__ __forceinline__ bool rescale_requested(unsigned char* sm, uint32_t g);
 
 struct Ctx {
   uint64_t* bars;
@@ -135,6 +140,22 @@ __device__ __forceinline__ unsigned char* fac_part(unsigned char* sm, int b, int
   return sm + OFF_FAC + (2 * b + k) * kPartBytes;
 }
 
+__device__ __forceinline__ bool rescale_requested(unsigned char* sm, uint32_t g) {
+  bool r = false;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    r |= reinterpret_cast<volatile int*>(fac_part(sm, g & 1, k >> 2) + (k & 3) * kSliceBytes +
+                                         128)[0] == (int)g;
+  return r;
+}
+
+// Factor-block entry of query row q (0..127) for tile parity b: fac at +0,
+// running sum l at +64 bytes.
+__device__ __forceinline__ float* fac_of_row(unsigned char* sm, int b, int q) {
+  return reinterpret_cast<float*>(fac_part(sm, b, q >> 6) + ((q >> 4) & 3) * kSliceBytes) +
+         (q & 15);
+}
+
 }  // namespace
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -165,15 +186,15 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   if (tid == 0) {
     uint32_t counts[NUM_BARS];
     for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
-    counts[S_FREE0] = counts[S_FREE1] = 128;
-    counts[P_FULL] = counts[CORR_REQ] = counts[PEER_X_FREE] = kHalfRows;
-    counts[CORR_DONE] = 128;
+    counts[S_FREE0] = counts[S_FREE1] = 256;
+    counts[P_FULL] = counts[PEER_X_FREE] = 2 * kHalfRows;
+    counts[CORR_DONE] = counts[CE_FREE] = counts[EPI_DONE] = 128;
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(&c.bars[i], counts[i]);
     *c.abort = 0;
     for (int b = 0; b < 2; ++b)
       for (int k = 0; k < 2; ++k)
-        for (int w = 0; w < 2; ++w)
-          reinterpret_cast<int*>(fac_part(sm, b, k) + w * kSliceBytes + 256)[0] = -1;
+        for (int w = 0; w < 4; ++w)
+          reinterpret_cast<int*>(fac_part(sm, b, k) + w * kSliceBytes + 128)[0] = -1;
     fence_mbar_init();
     // the first tile's peer scores may arrive as soon as the cluster is up
     mbar_arrive_expect_tx(&c.bars[X_FULL], kHalfRows * kTile * 4);
@@ -273,7 +294,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const uint32_t qr_base = smem_u32(sm + OFF_QROPE);
       const uint32_t kv_base = smem_u32(sm + OFF_KV);
       const uint32_t p_base = smem_u32(sm + OFF_P);
-      uint32_t g = 0;
+      uint32_t g = 0, n_rescale = 0;
       int n_item = 0;
       bool ok = true;
       auto issue_qk = [&](uint32_t gq) -> bool {
@@ -313,7 +334,17 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           } else {
             mma_commit(&c.bars[Q_FREE]);
           }
-          if (!wait_bar(c, P_FULL, g & 1) || !wait_bar(c, CORR_DONE, g & 1)) { ok = false; break; }
+          if (!wait_bar(c, P_FULL, g & 1)) { ok = false; break; }
+          if (t > 0 && rescale_requested(sm, g)) {
+            // let the correction warps rescale O^T once the previous PV is done
+            mma_commit(&c.bars[O_STABLE]);
+            if (!wait_bar(c, CORR_DONE, n_rescale & 1)) { ok = false; break; }
+            ++n_rescale;
+          }
+          if (t == 0 && n_item > 1) {
+            // O^T of the previous item must have been read out before it is overwritten
+            if (!wait_bar(c, EPI_DONE, (n_item - 2) & 1)) { ok = false; break; }
+          }
           tc_fence_after();
           const int s = g % kStages;
           const uint32_t stage = kv_base + s * kStageBytes;
@@ -327,18 +358,23 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           }
           mma_commit(&c.bars[KV_EMPTY0 + s]);
           mma_commit(&c.bars[P_FREE]);
-          mma_commit(&c.bars[PV_DONE]);
+          if (t + 1 == nt) mma_commit(&c.bars[O_FINAL]);
         }
       }
     }
-  } else if (warp >= 2 && warp < 6) {
+  } else if (warp >= 2 && warp < 10) {
     // ------------------------------------------------------------ scores
-    const int q = 32 * (warp & 3) + lane;  // query row within the item == TMEM lane
+    // Warp w reads TMEM lanes 32 (w mod 4) + 16 grp + 0..15 (grp = 0 for
+    // warps 2-5, 1 for warps 6-9) with two threads per row: thread t handles
+    // row (t mod 16) of its 16 and columns [32 h, 32 h + 32), h = t / 16.
+    const int sp = warp & 3, grp = (warp - 2) >> 2;
+    const int half = lane >> 4;
+    const int q = 32 * sp + 16 * grp + (lane & 15);  // query row == TMEM lane
     const bool mine = (q >> 6) == (int)rank;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t lane_addr = (uint32_t)(32 * sp + 16 * grp) << 16;
     uint32_t g = 0;
     if (!mine) {
-      // sender: partial scores of the peer's rows -> peer's X buffer
+      // sender: my half of the partial scores of a peer row -> peer's X buffer
       const int pr = q & 63;  // row index inside the peer's buffer
       const uint32_t x_peer = map_to_rank(smem_u32(sm + OFF_X + pr * 256), peer);
       const uint32_t xfull_peer = map_to_rank(smem_u32(&c.bars[X_FULL]), peer);
@@ -350,37 +386,99 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           const int sb = g & 1;
           if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_scores;
           tc_fence_after();
-          uint32_t v[4][16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * sb + 16 * k, v[k]);
+          uint32_t v[32];
+          tmem_ld_16x32bx2_x32(tmem + lane_addr + TM_S + 64 * sb, v);
           tmem_wait_ld();
           tc_fence_before();
           mbar_arrive(&c.bars[S_FREE0 + sb]);
           if (!wait_bar_cluster(c, PEER_X_FREE, (g & 1) ^ 1)) goto done_scores;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const uint32_t* w = &v[k >> 2][4 * (k & 3)];
-            st_async_v4(x_peer + (uint32_t)((k ^ (pr & 7)) << 4),
-                        make_float4(__uint_as_float(w[0]), __uint_as_float(w[1]),
-                                    __uint_as_float(w[2]), __uint_as_float(w[3])),
+          for (int k = 0; k < 8; ++k) {
+            const int chunk = 8 * half + k;
+            st_async_v4(x_peer + (uint32_t)((chunk ^ (pr & 7)) << 4),
+                        make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                    __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])),
                         xfull_peer);
           }
         }
       }
     } else {
-      // softmax of my 64 rows (two warps; each warp hands its 32 rows to the peer)
-      const int mr = q & 63;  // my row index (0..63)
-      const int hw = mr >> 5;  // which of my two warps
-      const bool leader = mr == 0;
+      // softmax of my 64 rows: 4 warps x 16 rows x 2 threads per row.  Each
+      // tile ends with its hand-off: bf16 P rows and rescale factors are
+      // written locally and copied to the peer, then P_FULL is signalled.
+      const int mr = q & 63;                  // my row index (0..63)
+      const int wslice = mr >> 4;             // this warp's 16-row slice (0..3)
+      const bool leader = mr == 0 && half == 0;
       const float scale = p.bmm1_scale * kLog2e;
       const uint32_t pfree_peer = map_to_rank(smem_u32(&c.bars[PEER_P_FREE]), peer);
       const uint32_t xfree_peer = map_to_rank(smem_u32(&c.bars[PEER_X_FREE]), peer);
       const uint32_t pfull_peer = map_to_rank(smem_u32(&c.bars[P_FULL]), peer);
-      const uint32_t corr_peer = map_to_rank(smem_u32(&c.bars[CORR_REQ]), peer);
-      const uint32_t p_rows_off = OFF_P + (uint32_t)(kHalfRows * (int)rank + 32 * hw) * 128;
+      const uint32_t p_rows_off = OFF_P + (uint32_t)(32 * sp + 16 * grp) * 128;
       const uint32_t p_peer = map_to_rank(smem_u32(sm + p_rows_off), peer);
       const float4* xs = reinterpret_cast<const float4*>(sm + OFF_X + mr * 256);
+      // state of the tile whose hand-off is pending
+      float pv[32];
+      float pf = 1.f, pl = 0.f, plse = 0.f;
+      bool pneed = false, pending = false, plse_valid = false, copy_pending = false;
+      int pslot = 0;
+      size_t plse_idx = 0;
+      uint32_t pg = 0;
+      // hand-off of tile `pg`: P rows, factor slice, copies to the peer, P_FULL
+      auto handoff = [&]() -> bool {
+        if (!wait_bar(c, P_FREE, (pg & 1) ^ 1)) return false;
+        if (!wait_bar(c, CE_FREE, (pg & 1) ^ 1)) return false;
+        if (copy_pending) {  // the previous copy has finished reading my P rows
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+          copy_pending = false;
+        }
+        if (leader) {
+          // expect the peer's P rows and factor slices, then let the peer send them
+          mbar_expect_tx(&c.bars[P_FULL], kHalfRows * 128 + kPartBytes);
+          mbar_arrive_cluster_relaxed(pfree_peer);
+        }
+        unsigned char* prow = sm + OFF_P + q * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 w;
+          w.x = pack_bf16(pv[8 * k + 0], pv[8 * k + 1]);
+          w.y = pack_bf16(pv[8 * k + 2], pv[8 * k + 3]);
+          w.z = pack_bf16(pv[8 * k + 4], pv[8 * k + 5]);
+          w.w = pack_bf16(pv[8 * k + 6], pv[8 * k + 7]);
+          *reinterpret_cast<uint4*>(prow + (((4 * half + k) ^ (q & 7)) << 4)) = w;
+        }
+        unsigned char* slice = fac_part(sm, pg & 1, rank) + wslice * kSliceBytes;
+        if (half == 0) {
+          reinterpret_cast<float*>(slice)[lane] = pf;
+          reinterpret_cast<float*>(slice + 64)[lane] = pl;
+        }
+        const bool any = __any_sync(0xffffffffu, pneed);
+        if (lane == 0 && any) reinterpret_cast<volatile int*>(slice + 128)[0] = (int)pg;
+        fence_proxy_async_smem();
+        __syncwarp();
+        bool ok = true;
+        if (lane == 0) {
+          ok = wait_bar_cluster(c, PEER_P_FREE, pg & 1);
+          if (ok) {
+            bulk_copy_to_peer(p_peer, sm + p_rows_off, 16 * 128, pfull_peer);
+            bulk_copy_to_peer(map_to_rank(smem_u32(slice), peer), slice, kSliceBytes, pfull_peer);
+            bulk_commit();
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) return false;
+        copy_pending = true;
+        mbar_arrive(&c.bars[P_FULL]);
+        if (plse_valid) {
+          if (pslot < 0) {
+            if (p.return_lse) p.lse[plse_idx] = plse;
+          } else {
+            part_lse[plse_idx] = plse;
+          }
+        }
+        pending = false;
+        return true;
+      };
       for (int idx = item_begin; idx < item_end; ++idx) {
         const WorkItem it = items[idx];
         const int nt = n_tiles_of(it);
@@ -394,28 +492,26 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         const int first_qi = row0 / H;
         const int clean_end =
             min(it.kv_end, p.causal ? it.seq_len - it.q_len + first_qi + 1 : it.seq_len);
-        float m_ref = -INFINITY, l_sum = 0.f;
+        float m_ref = -INFINITY, l_half = 0.f;  // l_half: this thread's columns only
         for (int t = 0; t < nt; ++t, ++g) {
           const int sb = g & 1;
-          float sv[kTile];
+          float sv[32];
           if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_scores;
           tc_fence_after();
           {
-            uint32_t v[4][16];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * sb + 16 * k, v[k]);
+            uint32_t v[32];
+            tmem_ld_16x32bx2_x32(tmem + lane_addr + TM_S + 64 * sb, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < kTile; ++j) sv[j] = __uint_as_float(v[j >> 4][j & 15]);
+            for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]);
           }
           tc_fence_before();
           mbar_arrive(&c.bars[S_FREE0 + sb]);
-          // add the peer's partial for my rows, then release the row to the peer
+          // add the peer's partial for my half row, then release it to the peer
           if (!wait_bar(c, X_FULL, g & 1)) goto done_scores;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float4 x = xs[k ^ (mr & 7)];
+          for (int k = 0; k < 8; ++k) {
+            const float4 x = xs[(8 * half + k) ^ (mr & 7)];
             sv[4 * k] += x.x;
             sv[4 * k + 1] += x.y;
             sv[4 * k + 2] += x.z;
@@ -423,133 +519,102 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           }
           if (leader) mbar_arrive_expect_tx(&c.bars[X_FULL], kHalfRows * kTile * 4);  // next tile
           mbar_arrive_cluster_relaxed(xfree_peer);
-          // mask, scale, online softmax
+          // mask, online softmax (scale folded into the exponent)
           const int j0 = it.kv_begin + t * kTile;
+          const int c0 = j0 + 32 * half;  // KV index of sv[0]
           float f = 1.f;
           bool need = false;
+          float tmax = -INFINITY;
           if (row_ok) {
-            float tmax = -INFINITY;
             if (j0 + kTile <= clean_end) {
 #pragma unroll
-              for (int j = 0; j < kTile; ++j) {
-                sv[j] *= scale;
-                tmax = fmaxf(tmax, sv[j]);
-              }
+              for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, sv[j]);
             } else {
 #pragma unroll
-              for (int j = 0; j < kTile; ++j) {
-                const int col = j0 + j;
-                sv[j] = (col <= last && col < it.kv_end) ? sv[j] * scale : -INFINITY;
+              for (int j = 0; j < 32; ++j) {
+                const int col = c0 + j;
+                sv[j] = (col <= last && col < it.kv_end) ? sv[j] : -INFINITY;
                 tmax = fmaxf(tmax, sv[j]);
               }
             }
-            const float m_new = fmaxf(m_ref, tmax);
+          }
+          // both threads of a row live in the same warp (lanes t and t + 16)
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+          if (row_ok) {
+            const float m_new = fmaxf(m_ref, tmax * scale);
             if (t == 0) {
               m_ref = m_new;
             } else if (m_new > m_ref + kRescaleThreshold) {
               f = ex2(m_ref - m_new);  // m_ref = -inf gives 0
               need = true;
-              l_sum *= f;
+              l_half *= f;
               m_ref = m_new;
             }
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
             float rs = 0.f;
 #pragma unroll
-            for (int j = 0; j < kTile; ++j) {
-              sv[j] = ex2(sv[j] - m_use);
+            for (int j = 0; j < 32; ++j) {
+              sv[j] = ex2(fmaf(sv[j], scale, -m_use));
               rs += sv[j];
             }
-            l_sum += rs;
+            l_half += rs;
           } else {
 #pragma unroll
-            for (int j = 0; j < kTile; ++j) sv[j] = 0.f;
+            for (int j = 0; j < 32; ++j) sv[j] = 0.f;
           }
+          const float l_row = l_half + __shfl_xor_sync(0xffffffffu, l_half, 16);
           // zero V rows past the end of the KV range (last tile of the item)
           const int valid = it.kv_end - j0;
           if (valid < kTile) {
             unsigned char* stage = sm + OFF_KV + (g % kStages) * kStageBytes;
             const int nz = (kTile - valid) * kLatChunks * 8;  // 16-byte units
-            for (int e = mr; e < nz; e += kHalfRows) {
+            for (int e = 2 * mr + half; e < nz; e += 2 * kHalfRows) {
               const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
               *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
                   make_uint4(0, 0, 0, 0);
             }
           }
-          // my P rows may be overwritten once the local PV of the previous tile is done
-          if (!wait_bar(c, P_FREE, (g & 1) ^ 1)) goto done_scores;
-          if (leader) {
-            // expect the peer's P rows and factor slices, then let the peer send them
-            mbar_expect_tx(&c.bars[P_FULL], kHalfRows * 128);
-            mbar_expect_tx(&c.bars[CORR_REQ], kPartBytes);
-            mbar_arrive_cluster_relaxed(pfree_peer);
-          }
-          {
-            unsigned char* prow = sm + OFF_P + q * 128;
+          // hand-off of this tile
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              uint4 w;
-              w.x = pack_bf16(sv[8 * k + 0], sv[8 * k + 1]);
-              w.y = pack_bf16(sv[8 * k + 2], sv[8 * k + 3]);
-              w.z = pack_bf16(sv[8 * k + 4], sv[8 * k + 5]);
-              w.w = pack_bf16(sv[8 * k + 6], sv[8 * k + 7]);
-              *reinterpret_cast<uint4*>(prow + ((k ^ (q & 7)) << 4)) = w;
-            }
+          for (int j = 0; j < 32; ++j) pv[j] = sv[j];
+          pf = f;
+          pl = l_row;
+          pneed = need;
+          pg = g;
+          pending = true;
+          plse_valid = (t + 1 == nt) && row_ok && half == 0;
+          if (plse_valid) {
+            plse = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
+            pslot = it.slot;
+            const size_t grow = (size_t)it.q_start * H + row0 + q;
+            plse_idx = it.slot < 0 ? grow : (size_t)it.slot * kRows + q;
           }
-          unsigned char* slice = fac_part(sm, g & 1, rank) + hw * kSliceBytes;
-          reinterpret_cast<float*>(slice)[lane] = f;
-          reinterpret_cast<float*>(slice + 128)[lane] = l_sum;
-          const bool any = __any_sync(0xffffffffu, need);
-          if (lane == 0 && any) reinterpret_cast<volatile int*>(slice + 256)[0] = (int)g;
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            if (!wait_bar_cluster(c, PEER_P_FREE, g & 1)) goto done_scores;
-            bulk_copy_to_peer(p_peer, sm + p_rows_off, 32 * 128, pfull_peer);
-            bulk_copy_to_peer(map_to_rank(smem_u32(slice), peer), slice, kSliceBytes, corr_peer);
-            bulk_commit();
-            bulk_wait_read0();
-          }
-          __syncwarp();
-          mbar_arrive(&c.bars[P_FULL]);
-          mbar_arrive(&c.bars[CORR_REQ]);
-        }
-        // LSE of my rows
-        if (row_ok) {
-          const float lse = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-          const size_t grow = (size_t)it.q_start * H + row0 + q;
-          if (it.slot < 0) {
-            if (p.return_lse) p.lse[grow] = lse;
-          } else {
-            part_lse[(size_t)it.slot * kRows + q] = lse;
-          }
+          if (!handoff()) goto done_scores;
         }
       }
+      if (copy_pending && lane == 0) bulk_wait_read0();
     }
   done_scores:;
-  } else if (warp >= 6) {
+  } else if (warp >= 10) {
     // ------------------------------------------------------------ correction + epilogue
     const int v = 32 * (warp & 3) + lane;  // V dim within each 128-wide O^T block == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    uint32_t g = 0;
+    uint32_t g = 0, n_rescale = 0;
+    int n_item = 0;
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
       const int nt = n_tiles_of(it);
       if (nt <= 0) continue;
       for (int t = 0; t < nt; ++t, ++g) {
-        if (!wait_bar(c, CORR_REQ, g & 1)) goto done_epi;
-        bool rescale = false;
-        for (int k = 0; k < 4; ++k)
-          rescale |= reinterpret_cast<volatile int*>(fac_part(sm, g & 1, k >> 1) +
-                                                     (k & 1) * kSliceBytes + 256)[0] == (int)g;
-        if (t > 0 && rescale) {
-          if (!wait_bar(c, PV_DONE, (g - 1) & 1)) goto done_epi;
+        if (!wait_bar(c, P_FULL, g & 1)) goto done_epi;
+        if (t > 0 && rescale_requested(sm, g)) {
+          if (!wait_bar(c, O_STABLE, n_rescale & 1)) goto done_epi;
+          ++n_rescale;
           tc_fence_after();
           for (int bb = 0; bb < 2; ++bb) {
 #pragma unroll 1
             for (int q16 = 0; q16 < kRows / 16; ++q16) {
-              const float* f = reinterpret_cast<const float*>(
-                                   fac_part(sm, g & 1, q16 >> 2) + ((q16 >> 1) & 1) * kSliceBytes) +
-                               16 * (q16 & 1);
+              const float* f = fac_of_row(sm, g & 1, 16 * q16);
               uint32_t x[16];
               const uint32_t addr = tmem + lane_base + TM_O + 128 * bb + 16 * q16;
               tmem_ld_32x32b_x16(addr, x);
@@ -560,12 +625,13 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
             }
           }
           tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&c.bars[CORR_DONE]);
         }
-        tc_fence_before();
-        mbar_arrive(&c.bars[CORR_DONE]);
+        mbar_arrive(&c.bars[CE_FREE]);
       }
       // epilogue: O = O^T(transposed) / l, from the last tile's factor block
-      if (!wait_bar(c, PV_DONE, (g - 1) & 1)) goto done_epi;
+      if (!wait_bar(c, O_FINAL, n_item & 1)) goto done_epi;
       tc_fence_after();
       {
         const int rows_total = it.q_len * H;
@@ -578,10 +644,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
 #pragma unroll 1
           for (int q16 = 0; q16 < kRows / 16; ++q16) {
             if (16 * q16 >= n_rows) break;
-            const float* lrow = reinterpret_cast<const float*>(
-                                    fac_part(sm, lb, q16 >> 2) + ((q16 >> 1) & 1) * kSliceBytes +
-                                    128) +
-                                16 * (q16 & 1);
+            const float* lrow = fac_of_row(sm, lb, 16 * q16) + 16;
             uint32_t x[16];
             tmem_ld_32x32b_x16(tmem + lane_base + TM_O + 128 * bb + 16 * q16, x);
             tmem_wait_ld();
@@ -602,6 +665,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&c.bars[EPI_DONE]);
+      ++n_item;
     }
   done_epi:;
   }
