@@ -138,6 +138,38 @@ int mla_decode_run_profiled(const mla_plan_t *plan, const void *query, const voi
                             size_t workspace_bytes, void *stream, void *event_before_decode,
                             void *event_after_decode);
 
+/*
+ * Size of the library-owned scratch array used by
+ * mla_decode_run_static_workspace (48 MiB on every GPU that loads the
+ * library, held until the process exits).
+ */
+#define MLA_STATIC_WORKSPACE_BYTES (48u * 1024u * 1024u)
+
+/*
+ * mla_decode_run without a caller-provided workspace.  The source pages have
+ * no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory when they enqueue a decode -- for example code that
+ * runs while a CUDA graph is being captured (where cudaMalloc is not
+ * allowed), or a plug-in inside a runtime that owns all device memory and
+ * offers it no allocator.  Its scratch is a fixed array of
+ * MLA_STATIC_WORKSPACE_BYTES in the library's own device memory; the call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call).
+ *
+ * Same arguments and errors as mla_decode_run, minus the workspace.  Returns
+ * MLA_ERR_WORKSPACE_TOO_SMALL if the plan needs more scratch than
+ * MLA_STATIC_WORKSPACE_BYTES.  The first call on each device resolves the
+ * array's device address (cudaGetSymbolAddress, with that device current);
+ * make that first call before any stream capture that includes this entry
+ * point.  All calls on a device share the one array: calls that may overlap
+ * on the GPU race, so the caller must order them (one stream, or events).
+ * Nothing needs clearing between calls; each run re-initialises what it uses.
+ */
+int mla_decode_run_static_workspace(const mla_plan_t *plan, const void *query,
+                                    const void *kv_cache, const int32_t *block_tables,
+                                    const int32_t *seq_lens, const int32_t *qo_indptr,
+                                    int64_t total_q, float bmm1_scale, float bmm2_scale,
+                                    void *out, float *lse, void *stream);
+
 /* Free a plan (NULL is allowed). */
 void mla_decode_destroy(mla_plan_t *plan);
 

@@ -30,6 +30,7 @@ __all__ = [
 HEAD_DIM_QK = 576
 HEAD_DIM_V = 512
 MLA_OK = 0
+MLA_STATIC_WORKSPACE_BYTES = 48 * 1024 * 1024  # scratch of mla_decode_run_static_workspace
 KV_BF16, KV_FP8_E4M3 = 0, 1
 MASK_CAUSAL, MASK_DENSE = 0, 1
 
