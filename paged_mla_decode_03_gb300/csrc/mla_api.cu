@@ -18,13 +18,9 @@ namespace mla {
 cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cudaStream_t stream);
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream);
-cudaError_t decode_simt_setup();
-cudaError_t decode_sm103_setup(int sm_count, int* n_pairs);
+cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs);
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                                 cudaStream_t stream);
-size_t decode_simt_smem_bytes();
-cudaError_t launch_decode_simt(const Problem& p, const Layout& lay, void* ws,
-                               cudaStream_t stream);
 }  // namespace mla
 
 struct mla_plan_s {
@@ -32,7 +28,6 @@ struct mla_plan_s {
   mla::Layout lay;
   int sm_count;
   int combine_grid;
-  int tensor_core;  // 1: tcgen05 CTA-pair kernel (bf16 KV); 0: CUDA-core kernel
 };
 
 namespace {
@@ -112,9 +107,8 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (cudaGetDevice(&prev) != cudaSuccess) return MLA_ERR_CUDA;
   if (cudaSetDevice(p.device) != cudaSuccess) return MLA_ERR_CUDA;
   int sms = 0, n_pairs = 0;
-  const bool tensor_core = p.kv_dtype == MLA_KV_BF16;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
-  if (e == cudaSuccess) e = tensor_core ? mla::decode_sm103_setup(sms, &n_pairs) : mla::decode_simt_setup();
+  if (e == cudaSuccess) e = mla::decode_sm103_setup(p.kv_dtype, sms, &n_pairs);
   cudaSetDevice(prev);
   if (e != cudaSuccess || sms <= 0) return MLA_ERR_CUDA;
 
@@ -122,9 +116,8 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (!pl) return MLA_ERR_INVALID_ARG;
   pl->prm = p;
   pl->sm_count = sms;
-  pl->tensor_core = tensor_core ? 1 : 0;
-  const int rc = tensor_core ? make_layout(p, n_pairs, 2 * n_pairs, 128, &pl->lay)
-                             : make_layout(p, sms, sms, 64, &pl->lay);
+  // one work item = 128 query rows on one CTA pair
+  const int rc = make_layout(p, n_pairs, 2 * n_pairs, 128, &pl->lay);
   if (rc != MLA_OK) {
     delete pl;
     return rc;
@@ -186,9 +179,7 @@ int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const voi
   if (event_before_decode &&
       cudaEventRecord(static_cast<cudaEvent_t>(event_before_decode), s) != cudaSuccess)
     return MLA_ERR_CUDA;
-  const cudaError_t ke = plan->tensor_core ? mla::launch_decode_sm103(p, plan->lay, workspace, s)
-                                           : mla::launch_decode_simt(p, plan->lay, workspace, s);
-  if (ke != cudaSuccess) return MLA_ERR_CUDA;
+  if (mla::launch_decode_sm103(p, plan->lay, workspace, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (event_after_decode &&
       cudaEventRecord(static_cast<cudaEvent_t>(event_after_decode), s) != cudaSuccess)
     return MLA_ERR_CUDA;

@@ -31,7 +31,9 @@
 // MMA issuer and TMEM owner, warps 2-9 scores (two threads per row; the
 // warps on the peer's rows send, the warps on this CTA's rows run the
 // softmax), warps 10-13 O correction and epilogue (thread = V dim = TMEM
-// lane).  A warp reaches TMEM lanes 32 (w mod 4) .. + 31, so each group of
+// lane).  With an e4m3 cache two more warps (14-15) widen each staged e4m3
+// tile to bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and
+// the bf16 ring is 2 deep.  A warp reaches TMEM lanes 32 (w mod 4) .. + 31, so each group of
 // four consecutive warps covers all 128 lanes.
 // The running max is only raised, and O^T rescaled, when it grows by more
 // than 2^8.  Every wait is bounded; a timeout sets an error bit in the
@@ -54,8 +56,13 @@ constexpr int kRows = 128;        // query rows per work item
 constexpr int kHalfRows = 64;     // rows whose softmax each CTA owns
 constexpr int kTile = kKvTile;    // 64 KV rows per tile
 constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
-constexpr int kStages = 3;        // KV ring depth
-constexpr int kThreads = 448;
+// bf16 KV: a 3-deep ring of bf16 tiles.  e4m3 KV: a 2-deep ring of bf16
+// tiles fed by a 2-deep ring of e4m3 staging tiles (converted in smem).
+template <bool kFp8> struct Cfg {
+  static constexpr int kStages = kFp8 ? 2 : 3;
+  static constexpr int kThreads = kFp8 ? 512 : 448;  // + 2 converter warps
+};
+constexpr int kConvThreads = 64;
 constexpr uint32_t kWaitLimit = 1u << 26;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -70,7 +77,10 @@ constexpr uint32_t kStageBytes = kLatChunks * kChunkKV + kRopeKV;  // 36 KB
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_QROPE = OFF_Q + kLatChunks * kChunkQ;
 constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
-constexpr uint32_t OFF_P = OFF_KV + kStages * kStageBytes;
+constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 tile, 18 KB
+constexpr uint32_t OFF_STG = OFF_KV + 2 * kStageBytes;                // e4m3 staging (fp8 only)
+constexpr uint32_t OFF_P = OFF_KV + 3 * kStageBytes;
+static_assert(OFF_STG + 2 * kStgBytes == OFF_P, "e4m3 staging fills the third bf16 stage");
 constexpr uint32_t OFF_X = OFF_P + kRows * 128;        // peer's partial scores of my rows
 constexpr uint32_t OFF_BARS = OFF_X + kHalfRows * kTile * 4;
 constexpr uint32_t kSliceBytes = 144;                  // per warp: fac[16], l[16], flag[4]
@@ -91,7 +101,8 @@ constexpr uint32_t TM_S = 256;  // two 64-column S buffers
 enum Bar {
   Q_FULL, Q_FREE, KV_FULL0, KV_FULL1, KV_FULL2, KV_EMPTY0, KV_EMPTY1, KV_EMPTY2,
   S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, P_FREE, O_STABLE, CORR_DONE, CE_FREE, O_FINAL,
-  EPI_DONE, X_FULL, PEER_X_FREE, PEER_P_FREE, NUM_BARS
+  EPI_DONE, X_FULL, PEER_X_FREE, PEER_P_FREE, STG_FULL0, STG_FULL1, STG_EMPTY0, STG_EMPTY1,
+  NUM_BARS
 };
 
 // True if any of the eight 16-row groups (2 CTAs x 4 warps) asked for an O^T
@@ -158,12 +169,14 @@ __device__ __forceinline__ float* fac_of_row(unsigned char* sm, int b, int q) {
 
 }  // namespace
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                     const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_q_rope,
                     const __grid_constant__ CUtensorMap tm_kv,
                     const __grid_constant__ CUtensorMap tm_kv_rope) {
+  constexpr int kStages = Cfg<kFp8>::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -189,6 +202,10 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     counts[S_FREE0] = counts[S_FREE1] = 256;
     counts[P_FULL] = counts[PEER_X_FREE] = 2 * kHalfRows;
     counts[CORR_DONE] = counts[CE_FREE] = counts[EPI_DONE] = 128;
+    if (kFp8) {
+      for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kConvThreads;
+      counts[STG_EMPTY0] = counts[STG_EMPTY1] = kConvThreads;
+    }
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(&c.bars[i], counts[i]);
     *c.abort = 0;
     for (int b = 0; b < 2; ++b)
@@ -244,8 +261,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank, qrow, &c.bars[Q_FULL]);
         }
         for (int t = 0; t < nt; ++t, ++g) {
-          const int s = g % kStages;
-          const uint32_t use = g / kStages;
+          // bf16: load straight into the bf16 ring; e4m3: into the staging ring
+          const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
+          const uint32_t use = kFp8 ? (g >> 1) : g / kStages;
           // read the next tile's page ids while this tile's slot drains
           int next[2] = {-1, -1};
           if (t + 1 < nt)
@@ -253,7 +271,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               const int jr = it.kv_begin + (t + 1) * kTile + pg * ps;
               if (jr < it.kv_end) next[pg] = bt[jr / ps];
             }
-          if (!wait_bar(c, KV_EMPTY0 + s, (use & 1) ^ 1)) goto done_producer;
+          if (!wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1)) goto done_producer;
           const int j0 = it.kv_begin + t * kTile;
           uint32_t bytes = 0;
           for (int pg = 0; pg < npg; ++pg) {
@@ -266,18 +284,28 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               pages[pg] = -1;
               continue;
             }
-            bytes += ps * (kLatChunks * 128 + 64);
+            bytes += ps * (kLatChunks * 64 + 32) * (kFp8 ? 1 : 2);
           }
-          mbar_arrive_expect_tx(&c.bars[KV_FULL0 + s], bytes);
-          unsigned char* stage = sm + OFF_KV + s * kStageBytes;
+          uint64_t* full = &c.bars[kFp8 ? STG_FULL0 + s : KV_FULL0 + s];
+          mbar_arrive_expect_tx(full, bytes);
           for (int pg = 0; pg < npg; ++pg) {
             if (pages[pg] < 0) continue;
             const int y = pages[pg] * ps;
-            for (int lc = 0; lc < kLatChunks; ++lc)
-              tma_load_2d(stage + lc * kChunkKV + pg * ps * 128, &tm_kv, 256 * (int)rank + 64 * lc,
-                          y, &c.bars[KV_FULL0 + s]);
-            tma_load_2d(stage + kLatChunks * kChunkKV + pg * ps * 64, &tm_kv_rope,
-                        512 + 32 * (int)rank, y, &c.bars[KV_FULL0 + s]);
+            if (kFp8) {
+              unsigned char* stg = sm + OFF_STG + s * kStgBytes;
+              for (int lc = 0; lc < kLatChunks; ++lc)
+                tma_load_2d(stg + lc * kTile * 64 + pg * ps * 64, &tm_kv, 256 * (int)rank + 64 * lc,
+                            y, full);
+              tma_load_2d(stg + kLatChunks * kTile * 64 + pg * ps * 32, &tm_kv_rope,
+                          512 + 32 * (int)rank, y, full);
+            } else {
+              unsigned char* stage = sm + OFF_KV + s * kStageBytes;
+              for (int lc = 0; lc < kLatChunks; ++lc)
+                tma_load_2d(stage + lc * kChunkKV + pg * ps * 128, &tm_kv,
+                            256 * (int)rank + 64 * lc, y, full);
+              tma_load_2d(stage + kLatChunks * kChunkKV + pg * ps * 64, &tm_kv_rope,
+                          512 + 32 * (int)rank, y, full);
+            }
           }
           pages[0] = next[0];
           pages[1] = next[1];
@@ -595,7 +623,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       if (copy_pending && lane == 0) bulk_wait_read0();
     }
   done_scores:;
-  } else if (warp >= 10) {
+  } else if (warp >= 10 && warp < 14) {
     // ------------------------------------------------------------ correction + epilogue
     const int v = 32 * (warp & 3) + lane;  // V dim within each 128-wide O^T block == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -670,6 +698,64 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       ++n_item;
     }
   done_epi:;
+  } else if (kFp8 && warp >= 14) {
+    // ------------------------------------------------------------ e4m3 -> bf16
+    // Thread r converts KV row r of each tile from the staging ring (row-major
+    // bytes) into the bf16 ring in the swizzled layouts the MMAs read.
+    const int r = tid - 14 * 32;
+    uint32_t g = 0;
+    for (int idx = item_begin; idx < item_end; ++idx) {
+      const WorkItem it = items[idx];
+      const int nt = n_tiles_of(it);
+      if (nt <= 0) continue;
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int s = g & 1;  // staging slot == bf16 slot (both 2 deep)
+        if (!wait_bar(c, STG_FULL0 + s, (g >> 1) & 1)) goto done_conv;
+        if (!wait_bar(c, KV_EMPTY0 + s, ((g >> 1) & 1) ^ 1)) goto done_conv;
+        const unsigned char* src = sm + OFF_STG + s * kStgBytes;
+        unsigned char* dst = sm + OFF_KV + s * kStageBytes;
+#pragma unroll
+        for (int lc = 0; lc < kLatChunks; ++lc) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // 16 e4m3 values -> 2 x 16-byte bf16 units
+            const uint4 b = *reinterpret_cast<const uint4*>(src + lc * kTile * 64 + r * 64 + 16 * k);
+            const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              o[2 * e] = e4m3x2_to_bf16x2(w[e] & 0xFFFFu);
+              o[2 * e + 1] = e4m3x2_to_bf16x2(w[e] >> 16);
+            }
+            const int u0 = 2 * k, u1 = 2 * k + 1;  // 16-byte units of the 128-byte row
+            *reinterpret_cast<uint4*>(dst + lc * kChunkKV + r * 128 + ((u0 ^ (r & 7)) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + lc * kChunkKV + r * 128 + ((u1 ^ (r & 7)) << 4)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // RoPE half: 32 values -> four 16-byte units (64B swizzle)
+          const uint4 b = *reinterpret_cast<const uint4*>(src + kLatChunks * kTile * 64 + r * 32 + 16 * k);
+          const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o[2 * e] = e4m3x2_to_bf16x2(w[e] & 0xFFFFu);
+            o[2 * e + 1] = e4m3x2_to_bf16x2(w[e] >> 16);
+          }
+          const int sw = (r >> 1) & 3;
+          const int u0 = 2 * k, u1 = 2 * k + 1;
+          *reinterpret_cast<uint4*>(dst + kLatChunks * kChunkKV + r * 64 + ((u0 ^ sw) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(dst + kLatChunks * kChunkKV + r * 64 + ((u1 ^ sw) << 4)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&c.bars[KV_FULL0 + s]);
+        mbar_arrive(&c.bars[STG_EMPTY0 + s]);
+      }
+    }
+  done_conv:;
   }
 
   tc_fence_before();
@@ -698,28 +784,28 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_inner,
-               uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes,
+               uint64_t rows, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kQkDim, rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kQkDim * 2};
+  cuuint64_t strides[1] = {(cuuint64_t)kQkDim * elem_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-cudaError_t decode_sm103_setup(int sm_count, int* n_pairs) {
-  cudaError_t e = cudaFuncSetAttribute(decode_sm103_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+template <bool kFp8>
+cudaError_t setup_one(int sm_count, int* n_pairs) {
+  auto kernel = decode_sm103_kernel<kFp8>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Cfg<kFp8>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -729,11 +815,17 @@ cudaError_t decode_sm103_setup(int sm_count, int* n_pairs) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, decode_sm103_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
   if (e != cudaSuccess) return e;
   if (clusters <= 0) return cudaErrorInvalidConfiguration;
   *n_pairs = std::min(clusters, sm_count / 2);
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs) {
+  return kv_dtype == 1 ? setup_one<true>(sm_count, n_pairs) : setup_one<false>(sm_count, n_pairs);
 }
 
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
@@ -741,13 +833,30 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
   CUtensorMap tm_q, tm_q_rope, tm_kv, tm_kv_rope;
   const uint64_t q_rows = std::max<uint64_t>(1, (uint64_t)p.total_q * p.num_heads);
   const uint64_t kv_rows = (uint64_t)p.num_pages * p.page_size;
-  if (!encode_2d(&tm_q, p.query, q_rows, 64, kRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_q_rope, p.query, q_rows, 32, kRows, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_2d(&tm_kv, p.kv_cache, kv_rows, 64, p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_kv_rope, p.kv_cache, kv_rows, 32, p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
+  if (!encode_2d(&tm_q, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 64, kRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 32, kRows,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  decode_sm103_kernel<<<lay.n_ctas, kThreads, kSmemBytes, stream>>>(
-      p, lay, static_cast<char*>(ws), tm_q, tm_q_rope, tm_kv, tm_kv_rope);
+  const bool fp8 = p.kv_dtype == 1;
+  if (fp8) {
+    // e4m3 bytes land row-major in the staging ring; the converter swizzles
+    if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 64,
+                   p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 32,
+                   p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    decode_sm103_kernel<true><<<lay.n_ctas, Cfg<true>::kThreads, kSmemBytes, stream>>>(
+        p, lay, static_cast<char*>(ws), tm_q, tm_q_rope, tm_kv, tm_kv_rope);
+  } else {
+    if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64,
+                   p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 32,
+                   p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
+    decode_sm103_kernel<false><<<lay.n_ctas, Cfg<false>::kThreads, kSmemBytes, stream>>>(
+        p, lay, static_cast<char*>(ws), tm_q, tm_q_rope, tm_kv, tm_kv_rope);
+  }
   return cudaGetLastError();
 }
 

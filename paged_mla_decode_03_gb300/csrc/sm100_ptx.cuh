@@ -306,3 +306,26 @@ __device__ __forceinline__ void tmem_ld_16x32bx2_x32(uint32_t taddr, uint32_t (&
 
 }  // namespace ptx
 }  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+// Two e4m3 values (low byte first) -> two bf16 values, exactly: every e4m3
+// value (and NaN) is representable in f16, and every f16 produced here is
+// representable in bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
+  uint32_t h2;
+  asm("{\n .reg .b16 lo;\n mov.b32 {lo, _}, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}"
+      : "=r"(h2)
+      : "r"(two_bytes));
+  float a, b;
+  asm("{\n .reg .b16 x, y;\n mov.b32 {x, y}, %2;\n cvt.f32.f16 %0, x;\n cvt.f32.f16 %1, y;\n}"
+      : "=f"(a), "=f"(b)
+      : "r"(h2));
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+}  // namespace ptx
+}  // namespace mla
