@@ -339,11 +339,17 @@ def gpu_case(w, dev, steps, warmup, with_e2e):
 
 
 def load_traffic():
-    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary."""
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu summary,
+    or {} when the kernel source changed since that capture."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    src = os.path.join(ROOT, "paged_mla_decode_03_gb300", "csrc", "mla_decode_sm103.cu")
     try:
         with open(path) as f:
-            return json.load(f)
+            d = json.load(f)
+        with open(src, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        return d if d.get("kernel_source_sha256_16") == h else {}
     except Exception:
         return {}
 
@@ -358,7 +364,7 @@ def run_gpu(args):
     import paged_mla_decode_03_gb300 as mla
     mla.load_library()
 
-    w = make_workload(HEADLINE)
+    w = make_workload(args.workload)
     wm = work_model(w)
     with ClockSampler(local) as clk:
         r = gpu_case(w, dev, args.steps, args.warmup, with_e2e=True)
@@ -375,7 +381,7 @@ def run_gpu(args):
 
     per_config = []
     if not args.no_extra:
-        for name in ["tiny", "mtp", "ragged", "fp8_long"]:
+        for name in [n for n in mi.WORKLOADS if n != args.workload]:
             wx = make_workload(name)
             wmx = work_model(wx)
             rx = gpu_case(wx, dev, max(5, args.steps // 4), max(3, args.warmup), with_e2e=False)
@@ -403,7 +409,7 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "batch": w.batch, "num_heads": w.num_heads,
                        "q_len": int(w.q_lens[0]), "page_size": w.page_size,
-                       "seq_lens": "U[1024, 8192] seed 1002", "kv_dtype": w.kv_dtype,
+                       "seed": w.seed, "kv_dtype": w.kv_dtype,
                        "parallelism": f"replicas x{n}",
                        "l2": "inputs larger than L2 (KV pool > 129 MB), no flush"},
             "us_per_call": step_s * 1e6,
@@ -428,7 +434,7 @@ def run_reference(args):
     ws_, rank, _ = dist_env()
     if rank != 0:
         return
-    w = make_workload(HEADLINE)
+    w = make_workload(args.workload)
     per_step = []
     tf_last = None
     for k in range(args.warmup + args.steps):
@@ -460,6 +466,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=list(mi.WORKLOADS),
+                    help="workload timed for the JSON line (default: the B=64, H=128 decode)")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
