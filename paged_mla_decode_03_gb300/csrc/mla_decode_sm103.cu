@@ -17,27 +17,28 @@
 //    [256 r, 256 r + 256) and RoPE dims [512 + 32 r, 512 + 32 r + 32) of Q
 //    and of every KV tile (18 MMA K-steps of 16) and forms a partial
 //    S_r (M = 128 query rows, N = 64 KV rows, fp32 in TMEM);
-//  * the softmax is split by rows: CTA r owns query rows [64 r, 64 r + 64).
-//    Its "sender" warps push the partial scores of the peer's rows into the
-//    peer's shared memory with st.async (completing the peer's mbarrier
-//    transaction count); its softmax warps add the peer's partial for their
-//    own rows, normalise, write bf16 P rows and per-row rescale factors, and
-//    a bulk DSMEM copy hands those to the peer, so both CTAs hold all 128
-//    rows of P;
-//  * CTA r accumulates O^T for V dims [256 r, 256 r + 256), i.e. its latent
-//    chunks: O^T = V^T P^T with M = 128 V dims, N = 128 query rows, K = 64
-//    KV rows -- two 128 x 128 fp32 TMEM blocks.
+//  * as soon as QK lands, each row of partial scores is pushed into the peer's
+//    shared memory with st.async (completing the peer's mbarrier transaction
+//    count) as 16-bit fixed point with a per-row power-of-two scale (error
+//    <= 2^-14 of the row's largest partial score); the softmax threads add
+//    the peer's rows, so both CTAs hold S for all 128 rows and each runs the
+//    softmax on all of them (the two CTAs' S differ only by that rounding,
+//    so both derive the same P to within it; each uses its own for its V
+//    dims, and CTA 0's statistics give the LSE);
+//  * P (bf16) goes from registers straight into TMEM, where it is the A
+//    operand of O = P V: M = 128 query rows, N = 256 (CTA r's V dims
+//    [256 r, 256 r + 256), read MN-major from its latent chunks), K = 64 KV
+//    rows, into a 128 x 256 fp32 TMEM accumulator.
 // Warp roles (448 threads): warp 0 TMA producer (3-stage KV ring), warp 1
-// MMA issuer and TMEM owner, warps 2-9 scores (two threads per row; the
-// warps on the peer's rows send, the warps on this CTA's rows run the
-// softmax), warps 10-13 O correction and epilogue (thread = V dim = TMEM
-// lane).  With an e4m3 cache two more warps (14-15) widen each staged e4m3
-// tile to bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and
-// the bf16 ring is 2 deep.  A warp reaches TMEM lanes 32 (w mod 4) .. + 31, so each group of
-// four consecutive warps covers all 128 lanes.
-// The running max is only raised, and O^T rescaled, when it grows by more
-// than 2^8.  Every wait is bounded; a timeout sets an error bit in the
-// workspace status word and the kernel unwinds.
+// MMA issuer and TMEM owner (QK runs up to two tiles ahead of PV), warps 2-9
+// softmax (two threads per row: warp w covers TMEM lanes 32 (w mod 4) +
+// 16 grp .. + 15 with the 16x32bx2 access shapes), warps 10-13 score
+// senders, O correction and epilogue (thread = query row = TMEM lane).  With an e4m3 cache two
+// more warps (14-15) widen each staged e4m3 tile to bf16 in shared memory
+// (exact; the k_scale lives in bmm1/bmm2), and the bf16 ring is 2 deep.
+// The running max is only raised, and O rescaled, when it grows by more than
+// 2^8.  Every wait is bounded; a timeout sets an error bit in the workspace
+// status word and the kernel unwinds.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -53,9 +54,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kRows = 128;        // query rows per work item
-constexpr int kHalfRows = 64;     // rows whose softmax each CTA owns
 constexpr int kTile = kKvTile;    // 64 KV rows per tile
 constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
+constexpr int kSoftmaxThreads = 256;
 // bf16 KV: a 3-deep ring of bf16 tiles.  e4m3 KV: a 2-deep ring of bf16
 // tiles fed by a 2-deep ring of e4m3 staging tiles (converted in smem).
 template <bool kFp8> struct Cfg {
@@ -79,35 +80,36 @@ constexpr uint32_t OFF_QROPE = OFF_Q + kLatChunks * kChunkQ;
 constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
 constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 tile, 18 KB
 constexpr uint32_t OFF_STG = OFF_KV + 2 * kStageBytes;                // e4m3 staging (fp8 only)
-constexpr uint32_t OFF_P = OFF_KV + 3 * kStageBytes;
-static_assert(OFF_STG + 2 * kStgBytes == OFF_P, "e4m3 staging fills the third bf16 stage");
-constexpr uint32_t OFF_X = OFF_P + kRows * 128;        // peer's partial scores of my rows
-constexpr uint32_t OFF_BARS = OFF_X + kHalfRows * kTile * 4;
-constexpr uint32_t kSliceBytes = 144;                  // per warp: fac[16], l[16], flag[4]
-constexpr uint32_t kPartBytes = 4 * kSliceBytes;       // per rank: four warp slices
-constexpr uint32_t OFF_FAC = OFF_BARS + 512;           // [2 tile parities][2 ranks] parts
-constexpr uint32_t OFF_TMEM = OFF_FAC + 4 * kPartBytes;
+// peer's partial scores, 2 buffers of [128 rows][64] int16 + [128] fp32 row scales
+constexpr uint32_t kXRowBytes = kTile * 2;
+constexpr uint32_t kXBytes = kRows * kXRowBytes + kRows * 4;
+constexpr uint32_t OFF_X = OFF_KV + 3 * kStageBytes;
+static_assert(OFF_STG + 2 * kStgBytes == OFF_X, "e4m3 staging fills the third bf16 stage");
+constexpr uint32_t OFF_BARS = OFF_X + 2 * kXBytes;
+constexpr uint32_t OFF_FAC = OFF_BARS + 512;           // float fac[2][128]
+constexpr uint32_t OFF_L = OFF_FAC + 2 * kRows * 4;    // float l[2][128]
+constexpr uint32_t OFF_FLAG = OFF_L + 2 * kRows * 4;   // int flag[2][8] (per softmax warp)
+constexpr uint32_t OFF_TMEM = OFF_FLAG + 64;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
 constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0, "alignment");
+static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_STG % 1024 == 0, "alignment");
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_O = 0;    // two 128-column O^T blocks
-constexpr uint32_t TM_S = 256;  // two 64-column S buffers
+constexpr uint32_t TM_O = 0;    // O: 128 rows x 256 V dims (fp32)
+constexpr uint32_t TM_S = 256;  // two 64-column S buffers (fp32)
+constexpr uint32_t TM_P = 384;  // two 32-column P buffers (bf16 pairs)
 
 enum Bar {
   Q_FULL, Q_FREE, KV_FULL0, KV_FULL1, KV_FULL2, KV_EMPTY0, KV_EMPTY1, KV_EMPTY2,
-  S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL, P_FREE, O_STABLE, CORR_DONE, CE_FREE, O_FINAL,
-  EPI_DONE, X_FULL, PEER_X_FREE, PEER_P_FREE, STG_FULL0, STG_FULL1, STG_EMPTY0, STG_EMPTY1,
+  S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL0, P_FULL1, P_FREE0, P_FREE1, O_STABLE, CORR_DONE,
+  CE_FREE,
+  O_FINAL, EPI_DONE, X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1, STG_FULL0, STG_FULL1,
+  STG_EMPTY0, STG_EMPTY1,
   NUM_BARS
 };
-
-// True if any of the eight 16-row groups (2 CTAs x 4 warps) asked for an O^T
-// rescale at global tile g.
-__device__ __forceinline__ bool rescale_requested(unsigned char* sm, uint32_t g);
 
 struct Ctx {
   uint64_t* bars;
@@ -146,25 +148,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Pointer into the per-tile factor block: parity b, rank part k.
-__device__ __forceinline__ unsigned char* fac_part(unsigned char* sm, int b, int k) {
-  return sm + OFF_FAC + (2 * b + k) * kPartBytes;
-}
-
-__device__ __forceinline__ bool rescale_requested(unsigned char* sm, uint32_t g) {
+// True if any softmax warp asked for an O rescale at global tile g.
+__device__ __forceinline__ bool rescale_requested(const unsigned char* sm, uint32_t g) {
+  const volatile int* f = reinterpret_cast<const volatile int*>(sm + OFF_FLAG) + 8 * (g & 1);
   bool r = false;
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    r |= reinterpret_cast<volatile int*>(fac_part(sm, g & 1, k >> 2) + (k & 3) * kSliceBytes +
-                                         128)[0] == (int)g;
+  for (int k = 0; k < 8; ++k) r |= f[k] == (int)g;
   return r;
-}
-
-// Factor-block entry of query row q (0..127) for tile parity b: fac at +0,
-// running sum l at +64 bytes.
-__device__ __forceinline__ float* fac_of_row(unsigned char* sm, int b, int q) {
-  return reinterpret_cast<float*>(fac_part(sm, b, q >> 6) + ((q >> 4) & 3) * kSliceBytes) +
-         (q & 15);
 }
 
 }  // namespace
@@ -195,12 +185,16 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   c.abort = reinterpret_cast<volatile int*>(sm + OFF_ABORT);
   c.status = &hdr[kHdrStatus];
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
+  float* fac = reinterpret_cast<float*>(sm + OFF_FAC);
+  float* lrow = reinterpret_cast<float*>(sm + OFF_L);
+  volatile int* flags = reinterpret_cast<volatile int*>(sm + OFF_FLAG);
 
   if (tid == 0) {
     uint32_t counts[NUM_BARS];
     for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
-    counts[S_FREE0] = counts[S_FREE1] = 256;
-    counts[P_FULL] = counts[PEER_X_FREE] = 2 * kHalfRows;
+    counts[P_FULL0] = counts[P_FULL1] = kSoftmaxThreads;
+    counts[S_FREE0] = counts[S_FREE1] = kSoftmaxThreads + 128;  // softmax + senders
+    counts[PEER_X_FREE0] = counts[PEER_X_FREE1] = kSoftmaxThreads;
     counts[CORR_DONE] = counts[CE_FREE] = counts[EPI_DONE] = 128;
     if (kFp8) {
       for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kConvThreads;
@@ -208,13 +202,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     }
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(&c.bars[i], counts[i]);
     *c.abort = 0;
-    for (int b = 0; b < 2; ++b)
-      for (int k = 0; k < 2; ++k)
-        for (int w = 0; w < 4; ++w)
-          reinterpret_cast<int*>(fac_part(sm, b, k) + w * kSliceBytes + 128)[0] = -1;
+    for (int k = 0; k < 16; ++k) flags[k] = -1;
     fence_mbar_init();
-    // the first tile's peer scores may arrive as soon as the cluster is up
-    mbar_arrive_expect_tx(&c.bars[X_FULL], kHalfRows * kTile * 4);
+    // the first two tiles' peer scores may arrive as soon as the cluster is up
+    mbar_arrive_expect_tx(&c.bars[X_FULL0], kXBytes);
+    mbar_arrive_expect_tx(&c.bars[X_FULL1], kXBytes);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -264,14 +256,14 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           // bf16: load straight into the bf16 ring; e4m3: into the staging ring
           const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
           const uint32_t use = kFp8 ? (g >> 1) : g / kStages;
-          // read the next tile's page ids while this tile's slot drains
           int next[2] = {-1, -1};
           if (t + 1 < nt)
             for (int pg = 0; pg < npg; ++pg) {
               const int jr = it.kv_begin + (t + 1) * kTile + pg * ps;
               if (jr < it.kv_end) next[pg] = bt[jr / ps];
             }
-          if (!wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1)) goto done_producer;
+          if (!wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1))
+            goto done_producer;
           const int j0 = it.kv_begin + t * kTile;
           uint32_t bytes = 0;
           for (int pg = 0; pg < npg; ++pg) {
@@ -315,381 +307,369 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Within an item QK(g) is issued as soon as its KV tile and S buffer are
+    // ready (up to two tiles ahead of PV), PV(g) as soon as P(g) is in TMEM.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(128, 64, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(128, 128, true, false);
+      constexpr uint32_t idesc_pv = idesc_f16(128, 256, false, true);
       const uint32_t q_base = smem_u32(sm + OFF_Q);
       const uint32_t qr_base = smem_u32(sm + OFF_QROPE);
       const uint32_t kv_base = smem_u32(sm + OFF_KV);
-      const uint32_t p_base = smem_u32(sm + OFF_P);
-      uint32_t g = 0, n_rescale = 0;
+      uint32_t g0 = 0, n_rescale = 0;
       int n_item = 0;
-      bool ok = true;
-      auto issue_qk = [&](uint32_t gq) -> bool {
-        const int s = gq % kStages;
-        const int sb = gq & 1;
-        if (!wait_bar(c, KV_FULL0 + s, (gq / kStages) & 1)) return false;
-        if (!wait_bar(c, S_FREE0 + sb, ((gq >> 1) & 1) ^ 1)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + TM_S + 64 * sb;
-        const uint32_t stage = kv_base + s * kStageBytes;
-        for (int k = 0; k < 4 * kLatChunks; ++k) {
-          const int lc = k >> 2, ks = k & 3;
-          const uint64_t a = smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
-          const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
-          mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
-        }
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
-          const uint64_t b = smem_desc(stage + kLatChunks * kChunkKV + ks * 32, 16, 512,
-                                       kSwizzle64B);
-          mma_bf16_ss(d, a, b, idesc_qk, 1u);
-        }
-        mma_commit(&c.bars[S_FULL0 + sb]);
-        return true;
-      };
-      for (int idx = item_begin; idx < item_end && ok; ++idx) {
+      for (int idx = item_begin; idx < item_end; ++idx) {
         const WorkItem it = items[idx];
         const int nt = n_tiles_of(it);
         if (nt <= 0) continue;
-        if (!wait_bar(c, Q_FULL, n_item & 1)) break;
+        if (!wait_bar(c, Q_FULL, n_item & 1)) goto done_mma;
         ++n_item;
         tc_fence_after();
-        if (!issue_qk(g)) break;
-        for (int t = 0; t < nt; ++t, ++g) {
-          if (t + 1 < nt) {
-            if (!issue_qk(g + 1)) { ok = false; break; }
-          } else {
-            mma_commit(&c.bars[Q_FREE]);
-          }
-          if (!wait_bar(c, P_FULL, g & 1)) { ok = false; break; }
-          if (t > 0 && rescale_requested(sm, g)) {
-            // let the correction warps rescale O^T once the previous PV is done
-            mma_commit(&c.bars[O_STABLE]);
-            if (!wait_bar(c, CORR_DONE, n_rescale & 1)) { ok = false; break; }
-            ++n_rescale;
-          }
-          if (t == 0 && n_item > 1) {
-            // O^T of the previous item must have been read out before it is overwritten
-            if (!wait_bar(c, EPI_DONE, (n_item - 2) & 1)) { ok = false; break; }
-          }
-          tc_fence_after();
-          const int s = g % kStages;
-          const uint32_t stage = kv_base + s * kStageBytes;
-          for (int bb = 0; bb < 2; ++bb) {
-            for (int ks = 0; ks < kTile / 16; ++ks) {
-              const uint64_t a = smem_desc(stage + (2 * bb) * kChunkKV + ks * 16 * 128, 8192, 1024,
-                                           kSwizzle128B);
-              const uint64_t b = smem_desc(p_base + ks * 32, 16, 1024, kSwizzle128B);
-              mma_bf16_ss(tmem + TM_O + 128 * bb, a, b, idesc_pv, (t == 0 && ks == 0) ? 0u : 1u);
+        int qk = 0, pv = 0, pv_state = 0;
+        uint32_t idle = 0;
+        while (pv < nt) {
+          bool progressed = false;
+          if (qk < nt && qk <= pv + 2) {
+            const uint32_t gq = g0 + qk;
+            const int s = gq % kStages, sb = gq & 1;
+            if (mbar_test_wait(&c.bars[KV_FULL0 + s], (gq / kStages) & 1) &&
+                mbar_test_wait(&c.bars[S_FREE0 + sb], ((gq >> 1) & 1) ^ 1)) {
+              tc_fence_after();
+              const uint32_t d = tmem + TM_S + 64 * sb;
+              const uint32_t stage = kv_base + s * kStageBytes;
+              for (int k = 0; k < 4 * kLatChunks; ++k) {
+                const int lc = k >> 2, ks = k & 3;
+                const uint64_t a = smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
+                const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
+                mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
+              }
+              for (int ks = 0; ks < 2; ++ks) {
+                const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
+                const uint64_t b = smem_desc(stage + kLatChunks * kChunkKV + ks * 32, 16, 512,
+                                             kSwizzle64B);
+                mma_bf16_ss(d, a, b, idesc_qk, 1u);
+              }
+              mma_commit(&c.bars[S_FULL0 + sb]);
+              if (++qk == nt) mma_commit(&c.bars[Q_FREE]);
+              progressed = true;
             }
           }
-          mma_commit(&c.bars[KV_EMPTY0 + s]);
-          mma_commit(&c.bars[P_FREE]);
-          if (t + 1 == nt) mma_commit(&c.bars[O_FINAL]);
+          if (!progressed && pv < qk) {
+            // PV(pv): wait (without blocking QK issue) for P in TMEM, for an O
+            // rescale if one was asked for, and for the previous item's epilogue.
+            const uint32_t gp = g0 + pv;
+            const int pb = gp & 1;
+            if (pv_state == 0 && mbar_test_wait(&c.bars[P_FULL0 + pb], (gp >> 1) & 1)) {
+              if (pv > 0 && rescale_requested(sm, gp)) {
+                mma_commit(&c.bars[O_STABLE]);  // the correction warps start after PV(pv - 1)
+                pv_state = 1;
+              } else {
+                pv_state = 2;
+              }
+              progressed = true;
+            }
+            if (pv_state == 1 && mbar_test_wait(&c.bars[CORR_DONE], n_rescale & 1)) {
+              ++n_rescale;
+              pv_state = 2;
+              progressed = true;
+            }
+            if (pv_state == 2 &&
+                (pv != 0 || n_item <= 1 || mbar_test_wait(&c.bars[EPI_DONE], (n_item - 2) & 1))) {
+              tc_fence_after();
+              const int s = gp % kStages;
+              const uint32_t stage = kv_base + s * kStageBytes;
+              for (int ks = 0; ks < kTile / 16; ++ks) {
+                const uint64_t b = smem_desc(stage + ks * 16 * 128, 8192, 1024, kSwizzle128B);
+                mma_bf16_ts(tmem + TM_O, tmem + TM_P + 32 * pb + 8 * ks, b, idesc_pv,
+                            (pv == 0 && ks == 0) ? 0u : 1u);
+              }
+              mma_commit(&c.bars[KV_EMPTY0 + s]);
+              mma_commit(&c.bars[P_FREE0 + pb]);
+              if (pv + 1 == nt) mma_commit(&c.bars[O_FINAL]);
+              ++pv;
+              pv_state = 0;
+              progressed = true;
+            }
+          }
+          if (progressed) {
+            idle = 0;
+          } else if (++idle > kWaitLimit || ((idle & 1023) == 0 && *c.abort)) {
+            if (idle > kWaitLimit) {
+              *c.abort = 1;
+              atomicOr(c.status, 32);
+            }
+            goto done_mma;
+          }
         }
+        g0 += nt;
       }
+    done_mma:;
     }
   } else if (warp >= 2 && warp < 10) {
-    // ------------------------------------------------------------ scores
-    // Warp w reads TMEM lanes 32 (w mod 4) + 16 grp + 0..15 (grp = 0 for
-    // warps 2-5, 1 for warps 6-9) with two threads per row: thread t handles
-    // row (t mod 16) of its 16 and columns [32 h, 32 h + 32), h = t / 16.
+    // ------------------------------------------------------------ softmax
+    // Two threads per row: thread t of warp w handles row 32 (w mod 4) +
+    // 16 grp + (t mod 16), columns [32 h, 32 h + 32), h = t / 16.
     const int sp = warp & 3, grp = (warp - 2) >> 2;
     const int half = lane >> 4;
     const int q = 32 * sp + 16 * grp + (lane & 15);  // query row == TMEM lane
-    const bool mine = (q >> 6) == (int)rank;
     const uint32_t lane_addr = (uint32_t)(32 * sp + 16 * grp) << 16;
+    const bool designated = warp == 2 && lane == 0;
+    const float scale = p.bmm1_scale * kLog2e;
+    const uint32_t xfree_peer0 = map_to_rank(smem_u32(&c.bars[PEER_X_FREE0]), peer);
     uint32_t g = 0;
-    if (!mine) {
-      // sender: my half of the partial scores of a peer row -> peer's X buffer
-      const int pr = q & 63;  // row index inside the peer's buffer
-      const uint32_t x_peer = map_to_rank(smem_u32(sm + OFF_X + pr * 256), peer);
-      const uint32_t xfull_peer = map_to_rank(smem_u32(&c.bars[X_FULL]), peer);
-      for (int idx = item_begin; idx < item_end; ++idx) {
-        const WorkItem it = items[idx];
-        const int nt = n_tiles_of(it);
-        if (nt <= 0) continue;
-        for (int t = 0; t < nt; ++t, ++g) {
-          const int sb = g & 1;
-          if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_scores;
-          tc_fence_after();
+    for (int idx = item_begin; idx < item_end; ++idx) {
+      const WorkItem it = items[idx];
+      const int nt = n_tiles_of(it);
+      if (nt <= 0) continue;
+      const int rows_total = it.q_len * H;
+      const int row0 = it.g * kRows;
+      const bool row_ok = q < rows_total - row0;
+      const int qi = (row0 + q) / H;
+      const int last = p.causal ? it.seq_len - it.q_len + qi : it.seq_len - 1;
+      // tiles ending at or before `clean_end` need no mask for any valid row
+      const int first_qi = row0 / H;
+      const int clean_end =
+          min(it.kv_end, p.causal ? it.seq_len - it.q_len + first_qi + 1 : it.seq_len);
+      float m_ref = -INFINITY, l_half = 0.f;  // l_half: this thread's columns only
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int sb = g & 1;
+        float sv[32];
+        if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
+        tc_fence_after();
+        {
           uint32_t v[32];
           tmem_ld_16x32bx2_x32(tmem + lane_addr + TM_S + 64 * sb, v);
           tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(&c.bars[S_FREE0 + sb]);
-          if (!wait_bar_cluster(c, PEER_X_FREE, (g & 1) ^ 1)) goto done_scores;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int chunk = 8 * half + k;
-            st_async_v4(x_peer + (uint32_t)((chunk ^ (pr & 7)) << 4),
-                        make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                    __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])),
-                        xfull_peer);
+          for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]);
+        }
+        tc_fence_before();
+        mbar_arrive(&c.bars[S_FREE0 + sb]);
+        // add the peer's partial scores (pushed by the peer's sender warps as
+        // 16-bit fixed point with a per-row power-of-two scale)
+        if (!wait_bar(c, X_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
+        {
+          const unsigned char* xb = sm + OFF_X + sb * kXBytes;
+          const float inv = 1.f / reinterpret_cast<const float*>(xb + kRows * kXRowBytes)[q];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 x = *reinterpret_cast<const uint4*>(
+                xb + q * kXRowBytes + (((4 * half + k) ^ (q & 7)) << 4));
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f2 = unpack_fix16x2(w[e]);
+              sv[8 * k + 2 * e] += f2.x * inv;
+              sv[8 * k + 2 * e + 1] += f2.y * inv;
+            }
           }
         }
-      }
-    } else {
-      // softmax of my 64 rows: 4 warps x 16 rows x 2 threads per row.  Each
-      // tile ends with its hand-off: bf16 P rows and rescale factors are
-      // written locally and copied to the peer, then P_FULL is signalled.
-      const int mr = q & 63;                  // my row index (0..63)
-      const int wslice = mr >> 4;             // this warp's 16-row slice (0..3)
-      const bool leader = mr == 0 && half == 0;
-      const float scale = p.bmm1_scale * kLog2e;
-      const uint32_t pfree_peer = map_to_rank(smem_u32(&c.bars[PEER_P_FREE]), peer);
-      const uint32_t xfree_peer = map_to_rank(smem_u32(&c.bars[PEER_X_FREE]), peer);
-      const uint32_t pfull_peer = map_to_rank(smem_u32(&c.bars[P_FULL]), peer);
-      const uint32_t p_rows_off = OFF_P + (uint32_t)(32 * sp + 16 * grp) * 128;
-      const uint32_t p_peer = map_to_rank(smem_u32(sm + p_rows_off), peer);
-      const float4* xs = reinterpret_cast<const float4*>(sm + OFF_X + mr * 256);
-      // state of the tile whose hand-off is pending
-      float pv[32];
-      float pf = 1.f, pl = 0.f, plse = 0.f;
-      bool pneed = false, pending = false, plse_valid = false, copy_pending = false;
-      int pslot = 0;
-      size_t plse_idx = 0;
-      uint32_t pg = 0;
-      // hand-off of tile `pg`: P rows, factor slice, copies to the peer, P_FULL
-      auto handoff = [&]() -> bool {
-        if (!wait_bar(c, P_FREE, (pg & 1) ^ 1)) return false;
-        if (!wait_bar(c, CE_FREE, (pg & 1) ^ 1)) return false;
-        if (copy_pending) {  // the previous copy has finished reading my P rows
-          if (lane == 0) bulk_wait_read0();
-          __syncwarp();
-          copy_pending = false;
-        }
-        if (leader) {
-          // expect the peer's P rows and factor slices, then let the peer send them
-          mbar_expect_tx(&c.bars[P_FULL], kHalfRows * 128 + kPartBytes);
-          mbar_arrive_cluster_relaxed(pfree_peer);
-        }
-        unsigned char* prow = sm + OFF_P + q * 128;
+        if (designated) mbar_arrive_expect_tx(&c.bars[X_FULL0 + sb], kXBytes);  // tile g + 2
+        mbar_arrive_cluster_relaxed(xfree_peer0 + 8u * sb);
+        // mask, online softmax (scale folded into the exponent)
+        const int j0 = it.kv_begin + t * kTile;
+        const int c0 = j0 + 32 * half;  // KV index of sv[0]
+        float f = 1.f;
+        bool need = false;
+        float tmax = -INFINITY;
+        if (row_ok) {
+          if (j0 + kTile <= clean_end) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint4 w;
-          w.x = pack_bf16(pv[8 * k + 0], pv[8 * k + 1]);
-          w.y = pack_bf16(pv[8 * k + 2], pv[8 * k + 3]);
-          w.z = pack_bf16(pv[8 * k + 4], pv[8 * k + 5]);
-          w.w = pack_bf16(pv[8 * k + 6], pv[8 * k + 7]);
-          *reinterpret_cast<uint4*>(prow + (((4 * half + k) ^ (q & 7)) << 4)) = w;
-        }
-        unsigned char* slice = fac_part(sm, pg & 1, rank) + wslice * kSliceBytes;
-        if (half == 0) {
-          reinterpret_cast<float*>(slice)[lane] = pf;
-          reinterpret_cast<float*>(slice + 64)[lane] = pl;
-        }
-        const bool any = __any_sync(0xffffffffu, pneed);
-        if (lane == 0 && any) reinterpret_cast<volatile int*>(slice + 128)[0] = (int)pg;
-        fence_proxy_async_smem();
-        __syncwarp();
-        bool ok = true;
-        if (lane == 0) {
-          ok = wait_bar_cluster(c, PEER_P_FREE, pg & 1);
-          if (ok) {
-            bulk_copy_to_peer(p_peer, sm + p_rows_off, 16 * 128, pfull_peer);
-            bulk_copy_to_peer(map_to_rank(smem_u32(slice), peer), slice, kSliceBytes, pfull_peer);
-            bulk_commit();
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) return false;
-        copy_pending = true;
-        mbar_arrive(&c.bars[P_FULL]);
-        if (plse_valid) {
-          if (pslot < 0) {
-            if (p.return_lse) p.lse[plse_idx] = plse;
+            for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, sv[j]);
           } else {
-            part_lse[plse_idx] = plse;
-          }
-        }
-        pending = false;
-        return true;
-      };
-      for (int idx = item_begin; idx < item_end; ++idx) {
-        const WorkItem it = items[idx];
-        const int nt = n_tiles_of(it);
-        if (nt <= 0) continue;
-        const int rows_total = it.q_len * H;
-        const int row0 = it.g * kRows;
-        const bool row_ok = q < rows_total - row0;
-        const int qi = (row0 + q) / H;
-        const int last = p.causal ? it.seq_len - it.q_len + qi : it.seq_len - 1;
-        // tiles ending at or before `clean_end` need no mask for any valid row
-        const int first_qi = row0 / H;
-        const int clean_end =
-            min(it.kv_end, p.causal ? it.seq_len - it.q_len + first_qi + 1 : it.seq_len);
-        float m_ref = -INFINITY, l_half = 0.f;  // l_half: this thread's columns only
-        for (int t = 0; t < nt; ++t, ++g) {
-          const int sb = g & 1;
-          float sv[32];
-          if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_scores;
-          tc_fence_after();
-          {
-            uint32_t v[32];
-            tmem_ld_16x32bx2_x32(tmem + lane_addr + TM_S + 64 * sb, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]);
-          }
-          tc_fence_before();
-          mbar_arrive(&c.bars[S_FREE0 + sb]);
-          // add the peer's partial for my half row, then release it to the peer
-          if (!wait_bar(c, X_FULL, g & 1)) goto done_scores;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 x = xs[(8 * half + k) ^ (mr & 7)];
-            sv[4 * k] += x.x;
-            sv[4 * k + 1] += x.y;
-            sv[4 * k + 2] += x.z;
-            sv[4 * k + 3] += x.w;
-          }
-          if (leader) mbar_arrive_expect_tx(&c.bars[X_FULL], kHalfRows * kTile * 4);  // next tile
-          mbar_arrive_cluster_relaxed(xfree_peer);
-          // mask, online softmax (scale folded into the exponent)
-          const int j0 = it.kv_begin + t * kTile;
-          const int c0 = j0 + 32 * half;  // KV index of sv[0]
-          float f = 1.f;
-          bool need = false;
-          float tmax = -INFINITY;
-          if (row_ok) {
-            if (j0 + kTile <= clean_end) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, sv[j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int col = c0 + j;
-                sv[j] = (col <= last && col < it.kv_end) ? sv[j] : -INFINITY;
-                tmax = fmaxf(tmax, sv[j]);
-              }
-            }
-          }
-          // both threads of a row live in the same warp (lanes t and t + 16)
-          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-          if (row_ok) {
-            const float m_new = fmaxf(m_ref, tmax * scale);
-            if (t == 0) {
-              m_ref = m_new;
-            } else if (m_new > m_ref + kRescaleThreshold) {
-              f = ex2(m_ref - m_new);  // m_ref = -inf gives 0
-              need = true;
-              l_half *= f;
-              m_ref = m_new;
-            }
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float rs = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              sv[j] = ex2(fmaf(sv[j], scale, -m_use));
-              rs += sv[j];
+              const int col = c0 + j;
+              sv[j] = (col <= last && col < it.kv_end) ? sv[j] : -INFINITY;
+              tmax = fmaxf(tmax, sv[j]);
             }
-            l_half += rs;
+          }
+        }
+        // both threads of a row live in the same warp (lanes t and t + 16)
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        if (row_ok) {
+          const float m_new = fmaxf(m_ref, tmax * scale);
+          if (t == 0) {
+            m_ref = m_new;
+          } else if (m_new > m_ref + kRescaleThreshold) {
+            f = ex2(m_ref - m_new);  // m_ref = -inf gives 0
+            need = true;
+            l_half *= f;
+            m_ref = m_new;
+          }
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          float rs = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            sv[j] = ex2(fmaf(sv[j], scale, -m_use));
+            rs += sv[j];
+          }
+          l_half += rs;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sv[j] = 0.f;
+        }
+        const float l_row = l_half + __shfl_xor_sync(0xffffffffu, l_half, 16);
+        // zero V rows past the end of the KV range (last tile of the item)
+        const int valid = it.kv_end - j0;
+        if (valid < kTile) {
+          unsigned char* stage = sm + OFF_KV + (g % kStages) * kStageBytes;
+          const int nz = (kTile - valid) * kLatChunks * 8;  // 16-byte units
+          for (int e = 2 * q + half; e < nz; e += kSoftmaxThreads) {
+            const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
+            *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        // P (bf16) into TMEM once the PV that last read this buffer is done
+        if (!wait_bar(c, P_FREE0 + sb, ((g >> 1) & 1) ^ 1)) goto done_softmax;
+        {
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) w[k] = pack_bf16(sv[2 * k], sv[2 * k + 1]);
+          tmem_st_16x32bx2_x16(tmem + lane_addr + TM_P + 32 * sb, w);
+          tmem_wait_st();
+        }
+        // the factor slot of this parity was read by the correction warps (tile g - 2)
+        if (!wait_bar(c, CE_FREE, (g & 1) ^ 1)) goto done_softmax;
+        if (half == 0) {
+          fac[sb * kRows + q] = f;
+          lrow[sb * kRows + q] = l_row;
+        }
+        const bool any = __any_sync(0xffffffffu, need);
+        if (lane == 0 && any) flags[8 * sb + (warp - 2)] = (int)g;
+        tc_fence_before();
+        mbar_arrive(&c.bars[P_FULL0 + sb]);
+        if (t + 1 == nt && rank == 0 && row_ok && half == 0) {
+          const float lse = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
+          const size_t grow = (size_t)it.q_start * H + row0 + q;
+          if (it.slot < 0) {
+            if (p.return_lse) p.lse[grow] = lse;
           } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) sv[j] = 0.f;
+            part_lse[(size_t)it.slot * kRows + q] = lse;
           }
-          const float l_row = l_half + __shfl_xor_sync(0xffffffffu, l_half, 16);
-          // zero V rows past the end of the KV range (last tile of the item)
-          const int valid = it.kv_end - j0;
-          if (valid < kTile) {
-            unsigned char* stage = sm + OFF_KV + (g % kStages) * kStageBytes;
-            const int nz = (kTile - valid) * kLatChunks * 8;  // 16-byte units
-            for (int e = 2 * mr + half; e < nz; e += 2 * kHalfRows) {
-              const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
-              *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-          }
-          // hand-off of this tile
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pv[j] = sv[j];
-          pf = f;
-          pl = l_row;
-          pneed = need;
-          pg = g;
-          pending = true;
-          plse_valid = (t + 1 == nt) && row_ok && half == 0;
-          if (plse_valid) {
-            plse = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
-            pslot = it.slot;
-            const size_t grow = (size_t)it.q_start * H + row0 + q;
-            plse_idx = it.slot < 0 ? grow : (size_t)it.slot * kRows + q;
-          }
-          if (!handoff()) goto done_scores;
         }
       }
-      if (copy_pending && lane == 0) bulk_wait_read0();
     }
-  done_scores:;
+  done_softmax:;
   } else if (warp >= 10 && warp < 14) {
-    // ------------------------------------------------------------ correction + epilogue
-    const int v = 32 * (warp & 3) + lane;  // V dim within each 128-wide O^T block == TMEM lane
+    // ------------------------------------------------------------ send + correction + epilogue
+    // Thread q (TMEM lane q) pushes row q of each partial-score tile to the
+    // peer as soon as QK lands, then, one tile behind, applies any O rescale
+    // the softmax asked for; at the end of an item it writes O / l.
+    const int q = 32 * (warp & 3) + lane;  // query row == TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t x_peer0 = map_to_rank(smem_u32(sm + OFF_X), peer);
+    const uint32_t xfull_peer0 = map_to_rank(smem_u32(&c.bars[X_FULL0]), peer);
     uint32_t g = 0, n_rescale = 0;
     int n_item = 0;
+    // `valid`: KV rows of the tile inside the item's range; the others may hold
+    // stale shared memory (an unloaded page) and are masked by the softmax
+    auto send = [&](uint32_t gs, int valid) -> bool {
+      const int sb = gs & 1;
+      if (!wait_bar(c, S_FULL0 + sb, (gs >> 1) & 1)) return false;
+      tc_fence_after();
+      uint32_t v[4][16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * sb + 16 * k, v[k]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&c.bars[S_FREE0 + sb]);
+      // 16-bit fixed point with a power-of-two scale that puts the row's largest
+      // magnitude in [2^13, 2^14): absolute error <= 2^-14 of that magnitude,
+      // i.e. the softmax's dominant scores keep ~14 bits (finer than the bf16
+      // rounding of P)
+      float amax = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        if (j >= valid) v[j >> 4][j & 15] = 0u;
+        amax = fmaxf(amax, fabsf(__uint_as_float(v[j >> 4][j & 15])));
+      }
+      const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+      const int k2 = (e == 0) ? 0 : min(max(140 - e, -126), 127);
+      const float scale = __uint_as_float((uint32_t)(k2 + 127) << 23);
+      uint32_t h[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        h[j] = pack_fix16x2(__uint_as_float(v[(2 * j) >> 4][(2 * j) & 15]) * scale,
+                          __uint_as_float(v[(2 * j + 1) >> 4][(2 * j + 1) & 15]) * scale);
+      if (!wait_bar_cluster(c, PEER_X_FREE0 + sb, ((gs >> 1) & 1) ^ 1)) return false;
+      const uint32_t xb = x_peer0 + (uint32_t)sb * kXBytes;
+      const uint32_t bar = xfull_peer0 + 8u * sb;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        st_async_v4_b32(xb + q * kXRowBytes + (uint32_t)((k ^ (q & 7)) << 4),
+                        make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]), bar);
+      st_async_b32(xb + kRows * kXRowBytes + 4 * q, __float_as_uint(scale), bar);
+      return true;
+    };
+    auto correct = [&](uint32_t gc, bool first) -> bool {
+      if (!wait_bar(c, P_FULL0 + (gc & 1), (gc >> 1) & 1)) return false;
+      if (!first && rescale_requested(sm, gc)) {
+        if (!wait_bar(c, O_STABLE, n_rescale & 1)) return false;
+        ++n_rescale;
+        tc_fence_after();
+        const float f = fac[(gc & 1) * kRows + q];
+#pragma unroll 1
+        for (int c16 = 0; c16 < 16; ++c16) {
+          uint32_t x[16];
+          const uint32_t addr = tmem + lane_base + TM_O + 16 * c16;
+          tmem_ld_32x32b_x16(addr, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * f);
+          tmem_st_32x32b_x16(addr, x);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&c.bars[CORR_DONE]);
+      }
+      mbar_arrive(&c.bars[CE_FREE]);
+      return true;
+    };
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
       const int nt = n_tiles_of(it);
       if (nt <= 0) continue;
       for (int t = 0; t < nt; ++t, ++g) {
-        if (!wait_bar(c, P_FULL, g & 1)) goto done_epi;
-        if (t > 0 && rescale_requested(sm, g)) {
-          if (!wait_bar(c, O_STABLE, n_rescale & 1)) goto done_epi;
-          ++n_rescale;
-          tc_fence_after();
-          for (int bb = 0; bb < 2; ++bb) {
-#pragma unroll 1
-            for (int q16 = 0; q16 < kRows / 16; ++q16) {
-              const float* f = fac_of_row(sm, g & 1, 16 * q16);
-              uint32_t x[16];
-              const uint32_t addr = tmem + lane_base + TM_O + 128 * bb + 16 * q16;
-              tmem_ld_32x32b_x16(addr, x);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) x[j] = __float_as_uint(__uint_as_float(x[j]) * f[j]);
-              tmem_st_32x32b_x16(addr, x);
-            }
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(&c.bars[CORR_DONE]);
-        }
-        mbar_arrive(&c.bars[CE_FREE]);
+        if (!send(g, it.kv_end - (it.kv_begin + t * kTile))) goto done_epi;
+        if (t > 0 && !correct(g - 1, t == 1)) goto done_epi;
       }
-      // epilogue: O = O^T(transposed) / l, from the last tile's factor block
+      if (!correct(g - 1, nt == 1)) goto done_epi;
+      // epilogue: O / l for my V dims, from the last tile's statistics
       if (!wait_bar(c, O_FINAL, n_item & 1)) goto done_epi;
       tc_fence_after();
       {
         const int rows_total = it.q_len * H;
         const int row0 = it.g * kRows;
-        const int n_rows = min(kRows, rows_total - row0);
-        const size_t grow0 = (size_t)it.q_start * H + row0;
-        const int lb = (g - 1) & 1;
-        for (int bb = 0; bb < 2; ++bb) {
-          const int vd = 256 * (int)rank + 128 * bb + v;  // output V dim
+        const bool row_ok = q < min(kRows, rows_total - row0);
+        const float l = lrow[((g - 1) & 1) * kRows + q];
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t grow = (size_t)it.q_start * H + row0 + q;
 #pragma unroll 1
-          for (int q16 = 0; q16 < kRows / 16; ++q16) {
-            if (16 * q16 >= n_rows) break;
-            const float* lrow = fac_of_row(sm, lb, 16 * q16) + 16;
-            uint32_t x[16];
-            tmem_ld_32x32b_x16(tmem + lane_base + TM_O + 128 * bb + 16 * q16, x);
-            tmem_wait_ld();
+        for (int c16 = 0; c16 < 16; ++c16) {
+          uint32_t x[16];
+          tmem_ld_32x32b_x16(tmem + lane_base + TM_O + 16 * c16, x);
+          tmem_wait_ld();
+          if (!row_ok) continue;
+          const int vd = 256 * (int)rank + 16 * c16;  // first output V dim of this chunk
+          if (it.slot < 0) {
+            const float s2 = inv * p.bmm2_scale;
+            uint32_t o[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int qq = 16 * q16 + j;
-              if (qq >= n_rows) break;
-              const float l = lrow[j];
-              const float inv = l > 0.f ? 1.f / l : 0.f;
-              const float o = __uint_as_float(x[j]) * inv;
-              if (it.slot < 0) {
-                reinterpret_cast<__nv_bfloat16*>(p.out)[(grow0 + qq) * kVDim + vd] =
-                    __float2bfloat16_rn(o * p.bmm2_scale);
-              } else {
-                part_o[((size_t)it.slot * kRows + qq) * kVDim + vd] = o;
-              }
-            }
+            for (int k = 0; k < 8; ++k)
+              o[k] = pack_bf16(__uint_as_float(x[2 * k]) * s2, __uint_as_float(x[2 * k + 1]) * s2);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                                  grow * kVDim + vd);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          } else {
+            float4* dst = reinterpret_cast<float4*>(part_o + ((size_t)it.slot * kRows + q) * kVDim + vd);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[k] = make_float4(__uint_as_float(x[4 * k]) * inv, __uint_as_float(x[4 * k + 1]) * inv,
+                                   __uint_as_float(x[4 * k + 2]) * inv, __uint_as_float(x[4 * k + 3]) * inv);
           }
         }
       }
@@ -735,7 +715,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
 #pragma unroll
         for (int k = 0; k < 2; ++k) {  // RoPE half: 32 values -> four 16-byte units (64B swizzle)
-          const uint4 b = *reinterpret_cast<const uint4*>(src + kLatChunks * kTile * 64 + r * 32 + 16 * k);
+          const uint4 b =
+              *reinterpret_cast<const uint4*>(src + kLatChunks * kTile * 64 + r * 32 + 16 * k);
           const uint32_t w[4] = {b.x, b.y, b.z, b.w};
           uint32_t o[8];
 #pragma unroll

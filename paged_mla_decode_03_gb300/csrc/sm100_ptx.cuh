@@ -44,6 +44,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait: returns false (and leaves the barrier alone) if the phase did
 // not complete within `max_iters` polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iters) {
@@ -325,6 +337,90 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
   return r;
+}
+
+}  // namespace ptx
+}  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+// MMA with the A operand in tensor memory (K-major, one row per lane, two
+// 16-bit elements per 32-bit column) and B in shared memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 16 lanes x 32 bit, two column halves, 16 repetitions: threads 0-15 write
+// lanes 0-15 of the address at columns [col, col + 16), threads 16-31 the
+// same lanes at columns [col + 16, col + 32).
+__device__ __forceinline__ void tmem_st_16x32bx2_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+}  // namespace ptx
+}  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+__device__ __forceinline__ void st_async_v4_b32(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(remote_addr),
+      "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+      "r"(v), "r"(remote_bar)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  float a, b;
+  asm("{\n .reg .b16 x, y;\n mov.b32 {x, y}, %2;\n cvt.f32.f16 %0, x;\n cvt.f32.f16 %1, y;\n}"
+      : "=f"(a), "=f"(b)
+      : "r"(v));
+  return make_float2(a, b);
+}
+
+}  // namespace ptx
+}  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+// 16-bit fixed point through the float pipe.  For |x| < 2^15, adding
+// 1.5 * 2^23 + 2^15 rounds x to the nearest integer (ties to even) and leaves
+// x + 2^15 in the low 16 mantissa bits; OR-ing 16 such bits back under the
+// exponent of 1.5 * 2^23 and subtracting the same constant recovers x.
+constexpr float kFixBias = 12615680.0f;  // 1.5 * 2^23 + 2^15
+__device__ __forceinline__ uint32_t pack_fix16x2(float lo, float hi) {
+  const uint32_t a = __float_as_uint(lo + kFixBias), b = __float_as_uint(hi + kFixBias);
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_fix16x2(uint32_t v) {
+  const float lo = __uint_as_float((v & 0xFFFFu) | 0x4B400000u) - kFixBias;
+  const float hi = __uint_as_float((v >> 16) | 0x4B400000u) - kFixBias;
+  return make_float2(lo, hi);
 }
 
 }  // namespace ptx
