@@ -328,32 +328,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         uint32_t idle = 0;
         while (pv < nt) {
           bool progressed = false;
-          if (qk < nt && qk <= pv + 2) {
-            const uint32_t gq = g0 + qk;
-            const int s = gq % kStages, sb = gq & 1;
-            if (mbar_test_wait(&c.bars[KV_FULL0 + s], (gq / kStages) & 1) &&
-                mbar_test_wait(&c.bars[S_FREE0 + sb], ((gq >> 1) & 1) ^ 1)) {
-              tc_fence_after();
-              const uint32_t d = tmem + TM_S + 64 * sb;
-              const uint32_t stage = kv_base + s * kStageBytes;
-              for (int k = 0; k < 4 * kLatChunks; ++k) {
-                const int lc = k >> 2, ks = k & 3;
-                const uint64_t a = smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
-                const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
-                mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
-              }
-              for (int ks = 0; ks < 2; ++ks) {
-                const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
-                const uint64_t b = smem_desc(stage + kLatChunks * kChunkKV + ks * 32, 16, 512,
-                                             kSwizzle64B);
-                mma_bf16_ss(d, a, b, idesc_qk, 1u);
-              }
-              mma_commit(&c.bars[S_FULL0 + sb]);
-              if (++qk == nt) mma_commit(&c.bars[Q_FREE]);
-              progressed = true;
-            }
-          }
-          if (!progressed && pv < qk) {
+          // PV first: it frees a KV stage (and the next load) as early as possible
+          if (pv < qk) {
             // PV(pv): wait (without blocking QK issue) for P in TMEM, for an O
             // rescale if one was asked for, and for the previous item's epilogue.
             const uint32_t gp = g0 + pv;
@@ -387,6 +363,31 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               if (pv + 1 == nt) mma_commit(&c.bars[O_FINAL]);
               ++pv;
               pv_state = 0;
+              progressed = true;
+            }
+          }
+          if (!progressed && qk < nt && qk <= pv + 2) {
+            const uint32_t gq = g0 + qk;
+            const int s = gq % kStages, sb = gq & 1;
+            if (mbar_test_wait(&c.bars[KV_FULL0 + s], (gq / kStages) & 1) &&
+                mbar_test_wait(&c.bars[S_FREE0 + sb], ((gq >> 1) & 1) ^ 1)) {
+              tc_fence_after();
+              const uint32_t d = tmem + TM_S + 64 * sb;
+              const uint32_t stage = kv_base + s * kStageBytes;
+              for (int k = 0; k < 4 * kLatChunks; ++k) {
+                const int lc = k >> 2, ks = k & 3;
+                const uint64_t a = smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
+                const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
+                mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
+              }
+              for (int ks = 0; ks < 2; ++ks) {
+                const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
+                const uint64_t b = smem_desc(stage + kLatChunks * kChunkKV + ks * 32, 16, 512,
+                                             kSwizzle64B);
+                mma_bf16_ss(d, a, b, idesc_qk, 1u);
+              }
+              mma_commit(&c.bars[S_FULL0 + sb]);
+              if (++qk == nt) mma_commit(&c.bars[Q_FREE]);
               progressed = true;
             }
           }
