@@ -107,7 +107,8 @@ int mla_decode_plan(const mla_decode_params *params, mla_plan_t **plan,
  *              fixed: must be NULL.
  * total_q      packed: query.shape[0] (<= max_total_q); fixed: ignored.
  * bmm1_scale   multiplies the 576-dim dot products (softmax scale and any
- *              q/k dequantisation scales already folded in by the caller).
+ *              q/k dequantisation scales already folded in by the caller);
+ *              finite and >= 0, else MLA_ERR_INVALID_ARG.
  * bmm2_scale   multiplies the normalised output (v/o scales folded in).
  * out          bf16, [B, SQ, H, 512] or [total_q, H, 512]; required.
  * lse          fp32, [B * SQ or total_q, H]; required iff params.return_lse.

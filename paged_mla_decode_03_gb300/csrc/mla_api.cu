@@ -140,6 +140,8 @@ int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const voi
   if (!query || !kv_cache || !block_tables || !seq_lens || !out || !workspace)
     return MLA_ERR_INVALID_ARG;
   if (prm.return_lse && !lse) return MLA_ERR_INVALID_ARG;
+  // the kernel takes the running max of raw scores and scales it afterwards
+  if (!(bmm1_scale >= 0.f) || bmm1_scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
   if (prm.packed) {
     if (!qo_indptr || total_q < 0 || total_q > prm.max_total_q) return MLA_ERR_INVALID_ARG;
   } else if (qo_indptr) {

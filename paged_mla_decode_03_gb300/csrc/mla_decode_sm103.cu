@@ -16,7 +16,10 @@
 //  * the QK contraction is split along its 576 dims: CTA r holds latent dims
 //    [256 r, 256 r + 256) and RoPE dims [512 + 32 r, 512 + 32 r + 32) of Q
 //    and of every KV tile (18 MMA K-steps of 16) and forms a partial
-//    S_r (M = 128 query rows, N = 64 KV rows, fp32 in TMEM);
+//    S_r (M = 128 query rows, N = 64 KV rows, fp32 in TMEM).  Q's first 128
+//    latent dims and its RoPE dims sit in shared memory; its other 128 latent
+//    dims sit in the 64 TMEM columns that O, S and P leave free (A operand
+//    of the ts MMAs), which makes room for a 4-deep KV ring;
 //  * as soon as QK lands, each row of partial scores is pushed into the peer's
 //    shared memory with st.async (completing the peer's mbarrier transaction
 //    count) as 16-bit fixed point with a per-row power-of-two scale (error
@@ -29,13 +32,14 @@
 //    operand of O = P V: M = 128 query rows, N = 256 (CTA r's V dims
 //    [256 r, 256 r + 256), read MN-major from its latent chunks), K = 64 KV
 //    rows, into a 128 x 256 fp32 TMEM accumulator.
-// Warp roles (448 threads): warp 0 TMA producer (3-stage KV ring), warp 1
+// Warp roles (448 threads): warp 0 TMA producer (4-stage KV ring), warp 1
 // MMA issuer and TMEM owner (QK runs up to two tiles ahead of PV), warps 2-9
 // softmax (two threads per row: warp w covers TMEM lanes 32 (w mod 4) +
 // 16 grp .. + 15 with the 16x32bx2 access shapes), warps 10-13 score
-// senders, O correction and epilogue (thread = query row = TMEM lane).  With an e4m3 cache two
-// more warps (14-15) widen each staged e4m3 tile to bf16 in shared memory
-// (exact; the k_scale lives in bmm1/bmm2), and the bf16 ring is 2 deep.
+// senders, O correction, epilogue and the TMEM half of Q (thread = query row
+// = TMEM lane).  With an e4m3 cache two more warps (14-15) widen each staged
+// e4m3 tile to bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2),
+// and the bf16 ring is 3 deep.
 // The running max is only raised, and O rescaled, when it grows by more than
 // 2^8.  Every wait is bounded; a timeout sets an error bit in the workspace
 // status word and the kernel unwinds.
@@ -57,10 +61,11 @@ constexpr int kRows = 128;        // query rows per work item
 constexpr int kTile = kKvTile;    // 64 KV rows per tile
 constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
 constexpr int kSoftmaxThreads = 256;
-// bf16 KV: a 3-deep ring of bf16 tiles.  e4m3 KV: a 2-deep ring of bf16
+// bf16 KV: a 4-deep ring of bf16 tiles.  e4m3 KV: a 3-deep ring of bf16
 // tiles fed by a 2-deep ring of e4m3 staging tiles (converted in smem).
+constexpr int kMaxStages = 4;
 template <bool kFp8> struct Cfg {
-  static constexpr int kStages = kFp8 ? 2 : 3;
+  static constexpr int kStages = kFp8 ? 3 : 4;
   static constexpr int kThreads = kFp8 ? 512 : 448;  // + 2 converter warps
 };
 constexpr int kConvThreads = 64;
@@ -69,6 +74,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// Q's latent dims of this CTA: chunks 0-1 in shared memory (A of the ss
+// MMAs), chunks 2-3 in TMEM (A of the ts MMAs)
+constexpr int kQSmemChunks = 2;
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t kChunkQ = kRows * 128;   // 64-dim chunk of Q, 128B-swizzled rows
 constexpr uint32_t kRopeQ = kRows * 64;     // 32-dim RoPE half of Q, 64B-swizzled rows
@@ -76,15 +84,15 @@ constexpr uint32_t kChunkKV = kTile * 128;  // 64-dim chunk of a KV tile
 constexpr uint32_t kRopeKV = kTile * 64;    // 32-dim RoPE half of a KV tile
 constexpr uint32_t kStageBytes = kLatChunks * kChunkKV + kRopeKV;  // 36 KB
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_QROPE = OFF_Q + kLatChunks * kChunkQ;
+constexpr uint32_t OFF_QROPE = OFF_Q + kQSmemChunks * kChunkQ;
 constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
 constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 tile, 18 KB
-constexpr uint32_t OFF_STG = OFF_KV + 2 * kStageBytes;                // e4m3 staging (fp8 only)
+constexpr uint32_t OFF_STG = OFF_KV + 3 * kStageBytes;                // e4m3 staging (fp8 only)
 // peer's partial scores, 2 buffers of [128 rows][64] int16 + [128] fp32 row scales
 constexpr uint32_t kXRowBytes = kTile * 2;
 constexpr uint32_t kXBytes = kRows * kXRowBytes + kRows * 4;
-constexpr uint32_t OFF_X = OFF_KV + 3 * kStageBytes;
-static_assert(OFF_STG + 2 * kStgBytes == OFF_X, "e4m3 staging fills the third bf16 stage");
+constexpr uint32_t OFF_X = OFF_KV + kMaxStages * kStageBytes;
+static_assert(OFF_STG + 2 * kStgBytes == OFF_X, "e4m3 staging fills the last bf16 stage");
 constexpr uint32_t OFF_BARS = OFF_X + 2 * kXBytes;
 constexpr uint32_t OFF_FAC = OFF_BARS + 512;           // float fac[2][128]
 constexpr uint32_t OFF_L = OFF_FAC + 2 * kRows * 4;    // float l[2][128]
@@ -101,9 +109,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0;    // O: 128 rows x 256 V dims (fp32)
 constexpr uint32_t TM_S = 256;  // two 64-column S buffers (fp32)
 constexpr uint32_t TM_P = 384;  // two 32-column P buffers (bf16 pairs)
+constexpr uint32_t TM_Q = 448;  // Q latent chunks 2-3: 128 rows x 128 dims (bf16 pairs)
 
 enum Bar {
-  Q_FULL, Q_FREE, KV_FULL0, KV_FULL1, KV_FULL2, KV_EMPTY0, KV_EMPTY1, KV_EMPTY2,
+  Q_FULL, Q_FREE, QT_FULL, KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3, KV_EMPTY0, KV_EMPTY1,
+  KV_EMPTY2, KV_EMPTY3,
   S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL0, P_FULL1, P_FREE0, P_FREE1, O_STABLE, CORR_DONE,
   CE_FREE,
   O_FINAL, EPI_DONE, X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1, STG_FULL0, STG_FULL1,
@@ -192,13 +202,16 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   if (tid == 0) {
     uint32_t counts[NUM_BARS];
     for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
-    counts[P_FULL0] = counts[P_FULL1] = kSoftmaxThreads;
-    counts[S_FREE0] = counts[S_FREE1] = kSoftmaxThreads + 128;  // softmax + senders
-    counts[PEER_X_FREE0] = counts[PEER_X_FREE1] = kSoftmaxThreads;
-    counts[CORR_DONE] = counts[CE_FREE] = counts[EPI_DONE] = 128;
+    // thread groups arrive once per warp (lane 0, after __syncwarp): 256
+    // single-thread arrives on one barrier serialise for several hundred ns
+    constexpr uint32_t kSoftmaxWarps = kSoftmaxThreads / 32, kCeWarps = 4;
+    counts[P_FULL0] = counts[P_FULL1] = kSoftmaxWarps;
+    counts[S_FREE0] = counts[S_FREE1] = kSoftmaxWarps + kCeWarps;  // softmax + senders
+    counts[PEER_X_FREE0] = counts[PEER_X_FREE1] = kSoftmaxWarps;
+    counts[CORR_DONE] = counts[CE_FREE] = counts[EPI_DONE] = counts[QT_FULL] = kCeWarps;
     if (kFp8) {
-      for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kConvThreads;
-      counts[STG_EMPTY0] = counts[STG_EMPTY1] = kConvThreads;
+      for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kConvThreads / 32;
+      counts[STG_EMPTY0] = counts[STG_EMPTY1] = kConvThreads / 32;
     }
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(&c.bars[i], counts[i]);
     *c.abort = 0;
@@ -245,9 +258,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         if (!wait_bar(c, Q_FREE, (n_item & 1) ^ 1)) goto done_producer;
         ++n_item;
         {
-          mbar_arrive_expect_tx(&c.bars[Q_FULL], kLatChunks * kChunkQ + kRopeQ);
+          mbar_arrive_expect_tx(&c.bars[Q_FULL], kQSmemChunks * kChunkQ + kRopeQ);
           const int qrow = it.q_start * H + it.g * kRows;
-          for (int lc = 0; lc < kLatChunks; ++lc)
+          for (int lc = 0; lc < kQSmemChunks; ++lc)
             tma_load_2d(sm + OFF_Q + lc * kChunkQ, &tm_q, 256 * (int)rank + 64 * lc, qrow,
                         &c.bars[Q_FULL]);
           tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank, qrow, &c.bars[Q_FULL]);
@@ -321,7 +334,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         const WorkItem it = items[idx];
         const int nt = n_tiles_of(it);
         if (nt <= 0) continue;
-        if (!wait_bar(c, Q_FULL, n_item & 1)) goto done_mma;
+        if (!wait_bar(c, Q_FULL, n_item & 1) || !wait_bar(c, QT_FULL, n_item & 1)) goto done_mma;
         ++n_item;
         tc_fence_after();
         int qk = 0, pv = 0, pv_state = 0;
@@ -376,9 +389,15 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               const uint32_t stage = kv_base + s * kStageBytes;
               for (int k = 0; k < 4 * kLatChunks; ++k) {
                 const int lc = k >> 2, ks = k & 3;
-                const uint64_t a = smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
                 const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
-                mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
+                if (lc < kQSmemChunks) {
+                  const uint64_t a =
+                      smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
+                  mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
+                } else {
+                  // 16 dims = 8 TMEM columns of bf16 pairs
+                  mma_bf16_ts(d, tmem + TM_Q + 32 * (lc - kQSmemChunks) + 8 * ks, b, idesc_qk, 1u);
+                }
               }
               for (int ks = 0; ks < 2; ++ks) {
                 const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
@@ -444,7 +463,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]);
         }
         tc_fence_before();
-        mbar_arrive(&c.bars[S_FREE0 + sb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.bars[S_FREE0 + sb]);
         // add the peer's partial scores (pushed by the peer's sender warps as
         // 16-bit fixed point with a per-row power-of-two scale)
         if (!wait_bar(c, X_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
@@ -465,26 +485,30 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           }
         }
         if (designated) mbar_arrive_expect_tx(&c.bars[X_FULL0 + sb], kXBytes);  // tile g + 2
-        mbar_arrive_cluster_relaxed(xfree_peer0 + 8u * sb);
+        // relaxed: the warp's reads of the buffer have returned their values
+        // (release at cluster scope would cost a cluster-wide fence per tile)
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer0 + 8u * sb);
         // mask, online softmax (scale folded into the exponent)
         const int j0 = it.kv_begin + t * kTile;
         const int c0 = j0 + 32 * half;  // KV index of sv[0]
         float f = 1.f;
         bool need = false;
-        float tmax = -INFINITY;
+        float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 chains for ILP
         if (row_ok) {
           if (j0 + kTile <= clean_end) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) tmax = fmaxf(tmax, sv[j]);
+            for (int j = 0; j < 32; ++j) tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int col = c0 + j;
               sv[j] = (col <= last && col < it.kv_end) ? sv[j] : -INFINITY;
-              tmax = fmaxf(tmax, sv[j]);
+              tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
             }
           }
         }
+        float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
         // both threads of a row live in the same warp (lanes t and t + 16)
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
         if (row_ok) {
@@ -498,13 +522,13 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
             m_ref = m_new;
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-          float rs = 0.f;
+          float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             sv[j] = ex2(fmaf(sv[j], scale, -m_use));
-            rs += sv[j];
+            rs[j & 3] += sv[j];
           }
-          l_half += rs;
+          l_half += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) sv[j] = 0.f;
@@ -540,7 +564,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         const bool any = __any_sync(0xffffffffu, need);
         if (lane == 0 && any) flags[8 * sb + (warp - 2)] = (int)g;
         tc_fence_before();
-        mbar_arrive(&c.bars[P_FULL0 + sb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.bars[P_FULL0 + sb]);
         if (t + 1 == nt && rank == 0 && row_ok && half == 0) {
           const float lse = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
           const size_t grow = (size_t)it.q_start * H + row0 + q;
@@ -576,17 +601,19 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * sb + 16 * k, v[k]);
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&c.bars[S_FREE0 + sb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.bars[S_FREE0 + sb]);
       // 16-bit fixed point with a power-of-two scale that puts the row's largest
       // magnitude in [2^13, 2^14): absolute error <= 2^-14 of that magnitude,
       // i.e. the softmax's dominant scores keep ~14 bits (finer than the bf16
       // rounding of P)
-      float amax = 0.f;
+      float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         if (j >= valid) v[j >> 4][j & 15] = 0u;
-        amax = fmaxf(amax, fabsf(__uint_as_float(v[j >> 4][j & 15])));
+        am[j & 3] = fmaxf(am[j & 3], fabsf(__uint_as_float(v[j >> 4][j & 15])));
       }
+      const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
       const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF);
       const int k2 = (e == 0) ? 0 : min(max(140 - e, -126), 127);
       const float scale = __uint_as_float((uint32_t)(k2 + 127) << 23);
@@ -604,6 +631,38 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                         make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]), bar);
       st_async_b32(xb + kRows * kXRowBytes + 4 * q, __float_as_uint(scale), bar);
       return true;
+    };
+    // Row q of the item's Q latent chunks 2-3 (this CTA's dims
+    // [256 r + 128, 256 r + 256)) into TMEM, where they are the A operand of
+    // the ts QK MMAs.  Called only when no QK of an earlier item is pending.
+    const long long q_rows = p.total_q * H;
+    auto write_q = [&](const WorkItem& it) {
+      const long long qrow = (long long)it.q_start * H + (long long)it.g * kRows + q;
+      uint32_t w[64];
+      if (qrow < q_rows) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(p.query) + qrow * kQkDim + 256 * (int)rank +
+            64 * kQSmemChunks);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint4 x = __ldg(src + k);
+          w[4 * k] = x.x;
+          w[4 * k + 1] = x.y;
+          w[4 * k + 2] = x.z;
+          w[4 * k + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) w[k] = 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tmem_st_32x32b_x16(tmem + lane_base + TM_Q + 16 * j,
+                           *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.bars[QT_FULL]);
     };
     auto correct = [&](uint32_t gc, bool first) -> bool {
       if (!wait_bar(c, P_FULL0 + (gc & 1), (gc >> 1) & 1)) return false;
@@ -624,18 +683,30 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&c.bars[CORR_DONE]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.bars[CORR_DONE]);
       }
-      mbar_arrive(&c.bars[CE_FREE]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.bars[CE_FREE]);
       return true;
     };
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
       const int nt = n_tiles_of(it);
       if (nt <= 0) continue;
+      if (n_item == 0) write_q(it);
       for (int t = 0; t < nt; ++t, ++g) {
         if (!send(g, it.kv_end - (it.kv_begin + t * kTile))) goto done_epi;
         if (t > 0 && !correct(g - 1, t == 1)) goto done_epi;
+      }
+      // every QK of this item has completed (send saw the last S_FULL): the
+      // next item's Q may replace this one in TMEM
+      for (int nx = idx + 1; nx < item_end; ++nx) {
+        const WorkItem itn = items[nx];
+        if (n_tiles_of(itn) > 0) {
+          write_q(itn);
+          break;
+        }
       }
       if (!correct(g - 1, nt == 1)) goto done_epi;
       // epilogue: O / l for my V dims, from the last tile's statistics
@@ -675,7 +746,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
       }
       tc_fence_before();
-      mbar_arrive(&c.bars[EPI_DONE]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.bars[EPI_DONE]);
       ++n_item;
     }
   done_epi:;
@@ -690,10 +762,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const int nt = n_tiles_of(it);
       if (nt <= 0) continue;
       for (int t = 0; t < nt; ++t, ++g) {
-        const int s = g & 1;  // staging slot == bf16 slot (both 2 deep)
-        if (!wait_bar(c, STG_FULL0 + s, (g >> 1) & 1)) goto done_conv;
-        if (!wait_bar(c, KV_EMPTY0 + s, ((g >> 1) & 1) ^ 1)) goto done_conv;
-        const unsigned char* src = sm + OFF_STG + s * kStgBytes;
+        const int ss = g & 1;        // staging slot (2 deep)
+        const int s = g % kStages;   // bf16 slot
+        if (!wait_bar(c, STG_FULL0 + ss, (g >> 1) & 1)) goto done_conv;
+        if (!wait_bar(c, KV_EMPTY0 + s, ((g / kStages) & 1) ^ 1)) goto done_conv;
+        const unsigned char* src = sm + OFF_STG + ss * kStgBytes;
         unsigned char* dst = sm + OFF_KV + s * kStageBytes;
 #pragma unroll
         for (int lc = 0; lc < kLatChunks; ++lc) {
@@ -733,8 +806,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               make_uint4(o[4], o[5], o[6], o[7]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&c.bars[KV_FULL0 + s]);
-        mbar_arrive(&c.bars[STG_EMPTY0 + s]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&c.bars[KV_FULL0 + s]);
+          mbar_arrive(&c.bars[STG_EMPTY0 + ss]);
+        }
       }
     }
   done_conv:;

@@ -235,3 +235,8 @@ def test_host_side_errors():
         d.plan.run(d.query.view(-1)[1:], d.kv_cache, d.block_tables, d.seq_lens, d.out,
                    lse=d.lse, workspace=d.workspace)
     assert e.value.status == -4
+    for bad in (-0.5, float("nan"), float("inf")):
+        with pytest.raises(mla.MlaDecodeError) as e:
+            d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=d.lse,
+                       workspace=d.workspace, bmm1_scale=bad)
+        assert e.value.status == -1
