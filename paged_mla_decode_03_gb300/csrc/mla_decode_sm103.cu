@@ -11,35 +11,34 @@
 // streaming the KV range in 64-row tiles with an online (running-max) softmax.
 //
 // GB300 mapping.  A 128 x 512 fp32 accumulator fills a whole SM's TMEM and a
-// 128 x 576 bf16 query tile needs 144 KB of shared memory, so one work item
-// is shared by the two CTAs of a cluster:
-//  * the QK contraction is split along its 576 dims: CTA r holds latent dims
-//    [256 r, 256 r + 256) and RoPE dims [512 + 32 r, 512 + 32 r + 32) of Q
-//    and of every KV tile (18 MMA K-steps of 16) and forms a partial
-//    S_r (M = 128 query rows, N = 64 KV rows, fp32 in TMEM).  Q's first 128
-//    latent dims and its RoPE dims sit in shared memory; its other 128 latent
-//    dims sit in the 64 TMEM columns that O, S and P leave free (A operand
-//    of the ts MMAs), which makes room for a 4-deep KV ring;
-//  * as soon as QK lands, each row of partial scores is pushed into the peer's
-//    shared memory with st.async (completing the peer's mbarrier transaction
-//    count) as 16-bit fixed point with a per-row power-of-two scale (error
-//    <= 2^-14 of the row's largest partial score); the softmax threads add
-//    the peer's rows, so both CTAs hold S for all 128 rows and each runs the
-//    softmax on all of them (the two CTAs' S differ only by that rounding,
-//    so both derive the same P to within it; each uses its own for its V
-//    dims, and CTA 0's statistics give the LSE);
-//  * P (bf16) goes from registers straight into TMEM, where it is the A
-//    operand of O = P V: M = 128 query rows, N = 256 (CTA r's V dims
-//    [256 r, 256 r + 256), read MN-major from its latent chunks), K = 64 KV
-//    rows, into a 128 x 256 fp32 TMEM accumulator.
+// 128 x 576 bf16 query tile needs 144 KB, so one work item is shared by the
+// two CTAs of a cluster, split along the head dims:
+//  * CTA r holds latent dims [256 r, 256 r + 256) and RoPE dims
+//    [512 + 32 r, 512 + 32 r + 32) of Q and of every KV tile.  Its Q latent
+//    dims live in TMEM (A operand of 16 ts MMAs), its Q RoPE dims in shared
+//    memory (2 ss MMAs); QK yields a partial S_r (M = 128 query rows,
+//    N = 64 KV rows, fp32 in TMEM);
+//  * each query row (TMEM lane l) has an owner CTA, (l / 16) mod 2.  The
+//    owner runs that row's softmax: the other CTA pushes its partial scores of
+//    the row into the owner's shared memory with st.async (16-bit fixed point
+//    with a per-row power-of-two scale: error <= 2^-14 of the row's largest
+//    partial score), the owner adds them to its own and forms P (bf16), which
+//    it writes into the P tile of both CTAs (its own with st.shared, the
+//    peer's with st.async), together with the row's rescale factor;
+//  * O = P V with P from shared memory: M = 128 query rows, N = 256 (CTA r's
+//    V dims, read MN-major from its latent chunks), K = 64 KV rows, into a
+//    128 x 256 fp32 TMEM accumulator.  The PV commit is multicast to both CTAs,
+//    so a P buffer is reused only after both CTAs' PV read it.
 // Warp roles (448 threads): warp 0 TMA producer (4-stage KV ring), warp 1
 // MMA issuer and TMEM owner (QK runs up to two tiles ahead of PV), warps 2-9
-// softmax (two threads per row: warp w covers TMEM lanes 32 (w mod 4) +
-// 16 grp .. + 15 with the 16x32bx2 access shapes), warps 10-13 score
-// senders, O correction, epilogue and the TMEM half of Q (thread = query row
-// = TMEM lane).  With an e4m3 cache two more warps (14-15) widen each staged
-// e4m3 tile to bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2),
-// and the bf16 ring is 3 deep.
+// softmax of the 64 owned rows (four threads per row, 16 KV columns each:
+// warp w covers the owned lanes 32 (w mod 4) + 16 r .. + 15, columns
+// [32 h, 32 h + 32), h = (w - 2) / 4, with the 16x32bx2 access shape),
+// warps 10-13 partial-score senders (the peer-owned lanes), O correction,
+// epilogue and the Q latent load into TMEM (thread = query row = TMEM lane).
+// With an e4m3 cache two more warps (14-15) widen each staged e4m3 tile to
+// bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and the
+// bf16 ring is 3 deep.
 // The running max is only raised, and O rescaled, when it grows by more than
 // 2^8.  Every wait is bounded; a timeout sets an error bit in the workspace
 // status word and the kernel unwinds.
@@ -58,9 +57,11 @@ namespace {
 using namespace ptx;
 
 constexpr int kRows = 128;        // query rows per work item
+constexpr int kOwnRows = 64;      // rows whose softmax this CTA runs
 constexpr int kTile = kKvTile;    // 64 KV rows per tile
 constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
-constexpr int kSoftmaxThreads = 256;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kCeWarps = 4;       // senders / correction / epilogue
 // bf16 KV: a 4-deep ring of bf16 tiles.  e4m3 KV: a 3-deep ring of bf16
 // tiles fed by a 2-deep ring of e4m3 staging tiles (converted in smem).
 constexpr int kMaxStages = 4;
@@ -74,52 +75,61 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// Q's latent dims of this CTA: chunks 0-1 in shared memory (A of the ss
-// MMAs), chunks 2-3 in TMEM (A of the ts MMAs)
-constexpr int kQSmemChunks = 2;
 // shared-memory layout (bytes from a 1024-aligned base)
-constexpr uint32_t kChunkQ = kRows * 128;   // 64-dim chunk of Q, 128B-swizzled rows
 constexpr uint32_t kRopeQ = kRows * 64;     // 32-dim RoPE half of Q, 64B-swizzled rows
 constexpr uint32_t kChunkKV = kTile * 128;  // 64-dim chunk of a KV tile
 constexpr uint32_t kRopeKV = kTile * 64;    // 32-dim RoPE half of a KV tile
 constexpr uint32_t kStageBytes = kLatChunks * kChunkKV + kRopeKV;  // 36 KB
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_QROPE = OFF_Q + kQSmemChunks * kChunkQ;
-constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
+constexpr uint32_t kPBytes = kRows * 128;   // P: 128 rows x 64 KV rows bf16, 128B-swizzled
 constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 tile, 18 KB
-constexpr uint32_t OFF_STG = OFF_KV + 3 * kStageBytes;                // e4m3 staging (fp8 only)
-// peer's partial scores, 2 buffers of [128 rows][64] int16 + [128] fp32 row scales
+// peer's partial scores of the owned rows: [64 rows][64] int16 + [64] fp32 scales
 constexpr uint32_t kXRowBytes = kTile * 2;
-constexpr uint32_t kXBytes = kRows * kXRowBytes + kRows * 4;
-constexpr uint32_t OFF_X = OFF_KV + kMaxStages * kStageBytes;
-static_assert(OFF_STG + 2 * kStgBytes == OFF_X, "e4m3 staging fills the last bf16 stage");
+constexpr uint32_t kXBytes = kOwnRows * kXRowBytes + kOwnRows * 4;
+constexpr uint32_t OFF_QROPE = 0;
+constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
+constexpr uint32_t OFF_STG = OFF_KV + 3 * kStageBytes;  // e4m3 staging (fp8 only)
+constexpr uint32_t OFF_P = OFF_KV + kMaxStages * kStageBytes;
+constexpr uint32_t OFF_X = OFF_P + 2 * kPBytes;
 constexpr uint32_t OFF_BARS = OFF_X + 2 * kXBytes;
-constexpr uint32_t OFF_FAC = OFF_BARS + 512;           // float fac[2][128]
-constexpr uint32_t OFF_L = OFF_FAC + 2 * kRows * 4;    // float l[2][128]
-constexpr uint32_t OFF_FLAG = OFF_L + 2 * kRows * 4;   // int flag[2][8] (per softmax warp)
-constexpr uint32_t OFF_TMEM = OFF_FLAG + 64;
+constexpr uint32_t OFF_FAC = OFF_BARS + 512;        // float fac[2][128]: rescale factor per row
+constexpr uint32_t OFF_LROW = OFF_FAC + 2 * kRows * 4;  // float l[128]: row sums, last tile
+constexpr uint32_t OFF_FLAG = OFF_LROW + kRows * 4;     // int flag[2][16]: 8 own + 8 peer warps
+constexpr uint32_t OFF_MX = OFF_FLAG + 2 * 16 * 4;      // float [2][2][128]: half-row maxima
+constexpr uint32_t OFF_LX = OFF_MX + 2 * 2 * kRows * 4;  // float [2][128]: half-row sums
+constexpr uint32_t OFF_TMEM = OFF_LX + 2 * kRows * 4;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
 constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_STG % 1024 == 0, "alignment");
+static_assert(OFF_STG + 2 * kStgBytes == OFF_P, "e4m3 staging fills the last bf16 stage");
+static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_STG % 1024 == 0 &&
+                  OFF_P % 1024 == 0 && OFF_X % 16 == 0,
+              "alignment");
+// bytes the peer pushes into this CTA's P tile per KV tile (P rows, factors,
+// flags), plus the row sums on an item's last tile
+constexpr uint32_t kPeerPBytes = kOwnRows * 128 + kOwnRows * 4 + kSoftmaxWarps * 4;
+constexpr uint32_t kPeerLBytes = kOwnRows * 4;
 
 // TMEM columns
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t TM_O = 0;    // O: 128 rows x 256 V dims (fp32)
 constexpr uint32_t TM_S = 256;  // two 64-column S buffers (fp32)
-constexpr uint32_t TM_P = 384;  // two 32-column P buffers (bf16 pairs)
-constexpr uint32_t TM_Q = 448;  // Q latent chunks 2-3: 128 rows x 128 dims (bf16 pairs)
+constexpr uint32_t TM_Q = 384;  // Q latent: 128 rows x 256 dims (bf16 pairs)
 
 enum Bar {
-  Q_FULL, Q_FREE, QT_FULL, KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3, KV_EMPTY0, KV_EMPTY1,
-  KV_EMPTY2, KV_EMPTY3,
-  S_FULL0, S_FULL1, S_FREE0, S_FREE1, P_FULL0, P_FULL1, P_FREE0, P_FREE1, O_STABLE, CORR_DONE,
-  CE_FREE,
-  O_FINAL, EPI_DONE, X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1, STG_FULL0, STG_FULL1,
-  STG_EMPTY0, STG_EMPTY1,
+  Q_FULL, Q_FREE, QT_FULL,
+  KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3, KV_EMPTY0, KV_EMPTY1, KV_EMPTY2, KV_EMPTY3,
+  S_FULL0, S_FULL1, S_FREE0, S_FREE1,
+  X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1,
+  P_FULL0, P_FULL1, P_FREE0, P_FREE1,
+  MX_FULL0,                    // 8: [subpartition][tile parity]
+  LX_FULL0 = MX_FULL0 + 8,     // 4: [subpartition]
+  LROW_FREE = LX_FULL0 + 4,
+  O_STABLE, CORR_DONE, O_FINAL, EPI_DONE,
+  STG_FULL0, STG_FULL1, STG_EMPTY0, STG_EMPTY1,
   NUM_BARS
 };
+static_assert(NUM_BARS * 8 <= 512, "barrier area");
 
 struct Ctx {
   uint64_t* bars;
@@ -158,12 +168,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// True if any softmax warp asked for an O rescale at global tile g.
+// True if any softmax warp of either CTA asked for an O rescale at global tile g.
 __device__ __forceinline__ bool rescale_requested(const unsigned char* sm, uint32_t g) {
-  const volatile int* f = reinterpret_cast<const volatile int*>(sm + OFF_FLAG) + 8 * (g & 1);
+  const volatile int* f = reinterpret_cast<const volatile int*>(sm + OFF_FLAG) + 16 * (g & 1);
   bool r = false;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) r |= f[k] == (int)g;
+  for (int k = 0; k < 16; ++k) r |= f[k] == (int)g;
   return r;
 }
 
@@ -172,7 +182,6 @@ __device__ __forceinline__ bool rescale_requested(const unsigned char* sm, uint3
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
-                    const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_q_rope,
                     const __grid_constant__ CUtensorMap tm_kv,
                     const __grid_constant__ CUtensorMap tm_kv_rope) {
@@ -196,26 +205,28 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   c.status = &hdr[kHdrStatus];
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
   float* fac = reinterpret_cast<float*>(sm + OFF_FAC);
-  float* lrow = reinterpret_cast<float*>(sm + OFF_L);
+  float* lrow = reinterpret_cast<float*>(sm + OFF_LROW);
   volatile int* flags = reinterpret_cast<volatile int*>(sm + OFF_FLAG);
 
   if (tid == 0) {
     uint32_t counts[NUM_BARS];
     for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
-    // thread groups arrive once per warp (lane 0, after __syncwarp): 256
-    // single-thread arrives on one barrier serialise for several hundred ns
-    constexpr uint32_t kSoftmaxWarps = kSoftmaxThreads / 32, kCeWarps = 4;
-    counts[P_FULL0] = counts[P_FULL1] = kSoftmaxWarps;
-    counts[S_FREE0] = counts[S_FREE1] = kSoftmaxWarps + kCeWarps;  // softmax + senders
-    counts[PEER_X_FREE0] = counts[PEER_X_FREE1] = kSoftmaxWarps;
-    counts[CORR_DONE] = counts[CE_FREE] = counts[EPI_DONE] = counts[QT_FULL] = kCeWarps;
+    // thread groups arrive once per warp (lane 0, after __syncwarp)
+    counts[S_FREE0] = counts[S_FREE1] = kSoftmaxWarps + kCeWarps;
+    counts[PEER_X_FREE0] = counts[PEER_X_FREE1] = kSoftmaxWarps;  // the peer's softmax warps
+    counts[P_FULL0] = counts[P_FULL1] = kSoftmaxWarps;            // + the peer's bytes
+    counts[P_FREE0] = counts[P_FREE1] = 2;                        // both CTAs' PV
+    for (int i = 0; i < 8; ++i) counts[MX_FULL0 + i] = 2;
+    for (int i = 0; i < 4; ++i) counts[LX_FULL0 + i] = 2;
+    counts[LROW_FREE] = 2 * kCeWarps;                             // both CTAs' epilogues
+    counts[CORR_DONE] = counts[EPI_DONE] = counts[QT_FULL] = kCeWarps;
     if (kFp8) {
       for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kConvThreads / 32;
       counts[STG_EMPTY0] = counts[STG_EMPTY1] = kConvThreads / 32;
     }
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(&c.bars[i], counts[i]);
     *c.abort = 0;
-    for (int k = 0; k < 16; ++k) flags[k] = -1;
+    for (int k = 0; k < 32; ++k) flags[k] = -1;
     fence_mbar_init();
     // the first two tiles' peer scores may arrive as soon as the cluster is up
     mbar_arrive_expect_tx(&c.bars[X_FULL0], kXBytes);
@@ -236,7 +247,6 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_q_rope);
       tma_prefetch_desc(&tm_kv);
       tma_prefetch_desc(&tm_kv_rope);
@@ -257,14 +267,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
         if (!wait_bar(c, Q_FREE, (n_item & 1) ^ 1)) goto done_producer;
         ++n_item;
-        {
-          mbar_arrive_expect_tx(&c.bars[Q_FULL], kQSmemChunks * kChunkQ + kRopeQ);
-          const int qrow = it.q_start * H + it.g * kRows;
-          for (int lc = 0; lc < kQSmemChunks; ++lc)
-            tma_load_2d(sm + OFF_Q + lc * kChunkQ, &tm_q, 256 * (int)rank + 64 * lc, qrow,
-                        &c.bars[Q_FULL]);
-          tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank, qrow, &c.bars[Q_FULL]);
-        }
+        mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
+        tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank, it.q_start * H + it.g * kRows,
+                    &c.bars[Q_FULL]);
         for (int t = 0; t < nt; ++t, ++g) {
           // bf16: load straight into the bf16 ring; e4m3: into the staging ring
           const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
@@ -321,13 +326,13 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Within an item QK(g) is issued as soon as its KV tile and S buffer are
-    // ready (up to two tiles ahead of PV), PV(g) as soon as P(g) is in TMEM.
+    // ready (up to two tiles ahead of PV), PV(g) as soon as P(g) is complete.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(128, 64, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(128, 256, false, true);
-      const uint32_t q_base = smem_u32(sm + OFF_Q);
       const uint32_t qr_base = smem_u32(sm + OFF_QROPE);
       const uint32_t kv_base = smem_u32(sm + OFF_KV);
+      const uint32_t p_base = smem_u32(sm + OFF_P);
       uint32_t g0 = 0, n_rescale = 0;
       int n_item = 0;
       for (int idx = item_begin; idx < item_end; ++idx) {
@@ -343,8 +348,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           bool progressed = false;
           // PV first: it frees a KV stage (and the next load) as early as possible
           if (pv < qk) {
-            // PV(pv): wait (without blocking QK issue) for P in TMEM, for an O
-            // rescale if one was asked for, and for the previous item's epilogue.
+            // PV(pv): wait (without blocking QK issue) for P, for an O rescale
+            // if one was asked for, and for the previous item's epilogue.
             const uint32_t gp = g0 + pv;
             const int pb = gp & 1;
             if (pv_state == 0 && mbar_test_wait(&c.bars[P_FULL0 + pb], (gp >> 1) & 1)) {
@@ -367,12 +372,12 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               const int s = gp % kStages;
               const uint32_t stage = kv_base + s * kStageBytes;
               for (int ks = 0; ks < kTile / 16; ++ks) {
+                const uint64_t a = smem_desc(p_base + pb * kPBytes + ks * 32, 16, 1024, kSwizzle128B);
                 const uint64_t b = smem_desc(stage + ks * 16 * 128, 8192, 1024, kSwizzle128B);
-                mma_bf16_ts(tmem + TM_O, tmem + TM_P + 32 * pb + 8 * ks, b, idesc_pv,
-                            (pv == 0 && ks == 0) ? 0u : 1u);
+                mma_bf16_ss(tmem + TM_O, a, b, idesc_pv, (pv == 0 && ks == 0) ? 0u : 1u);
               }
               mma_commit(&c.bars[KV_EMPTY0 + s]);
-              mma_commit(&c.bars[P_FREE0 + pb]);
+              mma_commit_multicast(&c.bars[P_FREE0 + pb], 0x3);  // both CTAs' P buffer pb
               if (pv + 1 == nt) mma_commit(&c.bars[O_FINAL]);
               ++pv;
               pv_state = 0;
@@ -390,14 +395,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               for (int k = 0; k < 4 * kLatChunks; ++k) {
                 const int lc = k >> 2, ks = k & 3;
                 const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
-                if (lc < kQSmemChunks) {
-                  const uint64_t a =
-                      smem_desc(q_base + lc * kChunkQ + ks * 32, 16, 1024, kSwizzle128B);
-                  mma_bf16_ss(d, a, b, idesc_qk, k > 0 ? 1u : 0u);
-                } else {
-                  // 16 dims = 8 TMEM columns of bf16 pairs
-                  mma_bf16_ts(d, tmem + TM_Q + 32 * (lc - kQSmemChunks) + 8 * ks, b, idesc_qk, 1u);
-                }
+                // 16 dims = 8 TMEM columns of bf16 pairs
+                mma_bf16_ts(d, tmem + TM_Q + 32 * lc + 8 * ks, b, idesc_qk, k > 0 ? 1u : 0u);
               }
               for (int ks = 0; ks < 2; ++ks) {
                 const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
@@ -424,18 +423,31 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       }
     done_mma:;
     }
-  } else if (warp >= 2 && warp < 10) {
-    // ------------------------------------------------------------ softmax
-    // Two threads per row: thread t of warp w handles row 32 (w mod 4) +
-    // 16 grp + (t mod 16), columns [32 h, 32 h + 32), h = t / 16.
-    const int sp = warp & 3, grp = (warp - 2) >> 2;
-    const int half = lane >> 4;
-    const int q = 32 * sp + 16 * grp + (lane & 15);  // query row == TMEM lane
-    const uint32_t lane_addr = (uint32_t)(32 * sp + 16 * grp) << 16;
+  } else if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
+    // ------------------------------------------------------------ softmax (owned rows)
+    // Warp w covers the 16 owned lanes of subpartition sp = w mod 4 and KV
+    // columns [32 hw, 32 hw + 32), hw = (w - 2) / 4; its thread t takes lane
+    // 32 sp + 16 r + (t mod 16), columns 32 hw + 16 (t / 16) + [0, 16).  The
+    // two warps of a subpartition combine their row maxima (and, on an item's
+    // last tile, row sums) through shared memory.
+    const int sp = warp & 3, hw = (warp - 2) >> 2, hh = lane >> 4;
+    const int kq = 2 * hw + hh;                           // column quarter
+    const int k = 16 * sp + (lane & 15);                  // owned-row index
+    const int q = 32 * sp + 16 * (int)rank + (lane & 15);  // query row == TMEM lane
+    const uint32_t lane_addr = (uint32_t)(32 * sp + 16 * (int)rank) << 16;
     const bool designated = warp == 2 && lane == 0;
+    const int sm_tid = (warp - 2) * 32 + lane;
     const float scale = p.bmm1_scale * kLog2e;
+    float* mx = reinterpret_cast<float*>(sm + OFF_MX);  // [parity][hw][lane]
+    float* lx = reinterpret_cast<float*>(sm + OFF_LX);  // [hw][lane]
     const uint32_t xfree_peer0 = map_to_rank(smem_u32(&c.bars[PEER_X_FREE0]), peer);
+    const uint32_t pfull_peer0 = map_to_rank(smem_u32(&c.bars[P_FULL0]), peer);
+    const uint32_t p_peer0 = map_to_rank(smem_u32(sm + OFF_P), peer);
+    const uint32_t fac_peer0 = map_to_rank(smem_u32(sm + OFF_FAC), peer);
+    const uint32_t flag_peer0 = map_to_rank(smem_u32(sm + OFF_FLAG), peer);
+    const uint32_t lrow_peer = map_to_rank(smem_u32(sm + OFF_LROW), peer);
     uint32_t g = 0;
+    int n_item = 0;
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
       const int nt = n_tiles_of(it);
@@ -449,38 +461,39 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const int first_qi = row0 / H;
       const int clean_end =
           min(it.kv_end, p.causal ? it.seq_len - it.q_len + first_qi + 1 : it.seq_len);
-      float m_ref = -INFINITY, l_half = 0.f;  // l_half: this thread's columns only
+      float m_ref = -INFINITY, l_part = 0.f;  // l_part: this thread's 16 columns only
       for (int t = 0; t < nt; ++t, ++g) {
         const int sb = g & 1;
-        float sv[32];
+        const bool last_tile = t + 1 == nt;
+        float sv[16];
         if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
         tc_fence_after();
         {
-          uint32_t v[32];
-          tmem_ld_16x32bx2_x32(tmem + lane_addr + TM_S + 64 * sb, v);
+          uint32_t v[16];
+          tmem_ld_16x32bx2_x16_s16(tmem + lane_addr + TM_S + 64 * sb + 32 * hw, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]);
+          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(v[j]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.bars[S_FREE0 + sb]);
-        // add the peer's partial scores (pushed by the peer's sender warps as
-        // 16-bit fixed point with a per-row power-of-two scale)
+        // add the peer's partial scores of this row (16-bit fixed point with a
+        // per-row power-of-two scale)
         if (!wait_bar(c, X_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
         {
           const unsigned char* xb = sm + OFF_X + sb * kXBytes;
-          const float inv = 1.f / reinterpret_cast<const float*>(xb + kRows * kXRowBytes)[q];
+          const float inv = 1.f / reinterpret_cast<const float*>(xb + kOwnRows * kXRowBytes)[k];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 x = *reinterpret_cast<const uint4*>(
-                xb + q * kXRowBytes + (((4 * half + k) ^ (q & 7)) << 4));
+          for (int u = 0; u < 2; ++u) {
+            const uint4 x =
+                *reinterpret_cast<const uint4*>(xb + k * kXRowBytes + (((2 * kq + u) ^ (k & 7)) << 4));
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 f2 = unpack_fix16x2(w[e]);
-              sv[8 * k + 2 * e] += f2.x * inv;
-              sv[8 * k + 2 * e + 1] += f2.y * inv;
+              sv[8 * u + 2 * e] += f2.x * inv;
+              sv[8 * u + 2 * e + 1] += f2.y * inv;
             }
           }
         }
@@ -491,17 +504,17 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer0 + 8u * sb);
         // mask, online softmax (scale folded into the exponent)
         const int j0 = it.kv_begin + t * kTile;
-        const int c0 = j0 + 32 * half;  // KV index of sv[0]
+        const int c0 = j0 + 16 * kq;  // KV index of sv[0]
         float f = 1.f;
         bool need = false;
         float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 chains for ILP
         if (row_ok) {
           if (j0 + kTile <= clean_end) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
+            for (int j = 0; j < 16; ++j) tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
               const int col = c0 + j;
               sv[j] = (col <= last && col < it.kv_end) ? sv[j] : -INFINITY;
               tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
@@ -509,8 +522,18 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           }
         }
         float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
-        // both threads of a row live in the same warp (lanes t and t + 16)
+        // the row's four threads: lanes t and t + 16 of this warp and of the
+        // partner warp (same subpartition, other column half)
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        {
+          float* slot = mx + sb * 2 * kRows;
+          if (hh == 0) slot[hw * kRows + q] = tmax;
+          __syncwarp();
+          const int bar = MX_FULL0 + 2 * sp + sb;
+          if (lane == 0) mbar_arrive(&c.bars[bar]);
+          if (!wait_bar(c, bar, (g >> 1) & 1)) goto done_softmax;
+          tmax = fmaxf(tmax, slot[(hw ^ 1) * kRows + q]);
+        }
         if (row_ok) {
           const float m_new = fmaxf(m_ref, tmax * scale);
           if (t == 0) {
@@ -518,75 +541,109 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           } else if (m_new > m_ref + kRescaleThreshold) {
             f = ex2(m_ref - m_new);  // m_ref = -inf gives 0
             need = true;
-            l_half *= f;
+            l_part *= f;
             m_ref = m_new;
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 16; ++j) {
             sv[j] = ex2(fmaf(sv[j], scale, -m_use));
             rs[j & 3] += sv[j];
           }
-          l_half += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+          l_part += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sv[j] = 0.f;
+          for (int j = 0; j < 16; ++j) sv[j] = 0.f;
         }
-        const float l_row = l_half + __shfl_xor_sync(0xffffffffu, l_half, 16);
         // zero V rows past the end of the KV range (last tile of the item)
         const int valid = it.kv_end - j0;
         if (valid < kTile) {
           unsigned char* stage = sm + OFF_KV + (g % kStages) * kStageBytes;
           const int nz = (kTile - valid) * kLatChunks * 8;  // 16-byte units
-          for (int e = 2 * q + half; e < nz; e += kSoftmaxThreads) {
+          for (int e = sm_tid; e < nz; e += kSoftmaxWarps * 32) {
             const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
             *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
                 make_uint4(0, 0, 0, 0);
           }
-          fence_proxy_async_smem();
         }
-        // P (bf16) into TMEM once the PV that last read this buffer is done
+        // P (bf16) of this row into both CTAs' P tiles once both PVs that last
+        // read them are done
         if (!wait_bar(c, P_FREE0 + sb, ((g >> 1) & 1) ^ 1)) goto done_softmax;
         {
-          uint32_t w[16];
+          uint32_t w[8];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) w[k] = pack_bf16(sv[2 * k], sv[2 * k + 1]);
-          tmem_st_16x32bx2_x16(tmem + lane_addr + TM_P + 32 * sb, w);
-          tmem_wait_st();
-        }
-        // the factor slot of this parity was read by the correction warps (tile g - 2)
-        if (!wait_bar(c, CE_FREE, (g & 1) ^ 1)) goto done_softmax;
-        if (half == 0) {
-          fac[sb * kRows + q] = f;
-          lrow[sb * kRows + q] = l_row;
-        }
-        const bool any = __any_sync(0xffffffffu, need);
-        if (lane == 0 && any) flags[8 * sb + (warp - 2)] = (int)g;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c.bars[P_FULL0 + sb]);
-        if (t + 1 == nt && rank == 0 && row_ok && half == 0) {
-          const float lse = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
-          const size_t grow = (size_t)it.q_start * H + row0 + q;
-          if (it.slot < 0) {
-            if (p.return_lse) p.lse[grow] = lse;
-          } else {
-            part_lse[(size_t)it.slot * kRows + q] = lse;
+          for (int e = 0; e < 8; ++e) w[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
+          const uint32_t pbar = pfull_peer0 + 8u * sb;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t off = sb * kPBytes + q * 128 + (((2 * kq + u) ^ (q & 7)) << 4);
+            const uint4 val = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            *reinterpret_cast<uint4*>(sm + OFF_P + off) = val;
+            st_async_v4_b32(p_peer0 + off, val, pbar);
+          }
+          if (kq == 0) {
+            fac[sb * kRows + q] = f;
+            st_async_b32(fac_peer0 + 4u * (sb * kRows + q), __float_as_uint(f), pbar);
+          }
+          const bool any = __any_sync(0xffffffffu, need);
+          if (lane == 0) {
+            const int fv = any ? (int)g : -1;
+            flags[16 * sb + (warp - 2)] = fv;
+            st_async_b32(flag_peer0 + 4u * (16 * sb + 8 + (warp - 2)), (uint32_t)fv, pbar);
           }
         }
+        if (last_tile) {
+          // row sum over the row's four threads -> both CTAs' l (epilogue) and the LSE
+          float l_pair = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+          if (hh == 0) lx[hw * kRows + q] = l_pair;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c.bars[LX_FULL0 + sp]);
+          if (!wait_bar(c, LX_FULL0 + sp, n_item & 1)) goto done_softmax;
+          const float l_row = l_pair + lx[(hw ^ 1) * kRows + q];
+          if (kq == 0) {
+            // the previous item's epilogues (both CTAs) have read l
+            if (n_item > 0 && !wait_bar_cluster(c, LROW_FREE, (n_item - 1) & 1)) goto done_softmax;
+            lrow[q] = l_row;
+            st_async_b32(lrow_peer + 4u * q, __float_as_uint(l_row), pfull_peer0 + 8u * sb);
+            if (row_ok) {
+              const float lse = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
+              const size_t grow = (size_t)it.q_start * H + row0 + q;
+              if (it.slot < 0) {
+                if (p.return_lse) p.lse[grow] = lse;
+              } else {
+                part_lse[(size_t)it.slot * kRows + q] = lse;
+              }
+            }
+          }
+        }
+        fence_proxy_async_smem();  // P and zeroed V rows are read by the MMA
+        __syncwarp();
+        if (lane == 0) {
+          if (warp == 2)
+            mbar_arrive_expect_tx(&c.bars[P_FULL0 + sb],
+                                  kPeerPBytes + (last_tile ? kPeerLBytes : 0u));
+          else
+            mbar_arrive(&c.bars[P_FULL0 + sb]);
+        }
       }
+      ++n_item;
     }
   done_softmax:;
-  } else if (warp >= 10 && warp < 14) {
+  } else if (warp >= 2 + kSoftmaxWarps && warp < 2 + kSoftmaxWarps + kCeWarps) {
     // ------------------------------------------------------------ send + correction + epilogue
-    // Thread q (TMEM lane q) pushes row q of each partial-score tile to the
-    // peer as soon as QK lands, then, one tile behind, applies any O rescale
-    // the softmax asked for; at the end of an item it writes O / l.
-    const int q = 32 * (warp & 3) + lane;  // query row == TMEM lane
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    // Threads t and t + 16 of warp w push the peer-owned row at lane
+    // 32 (w mod 4) + 16 (1 - r) + (t mod 16) of each partial-score tile to the
+    // peer as soon as QK lands (columns [32 (t / 16), + 32)).  For correction,
+    // the epilogue and the Q load, thread q = 32 (w mod 4) + t covers TMEM lane q.
+    const int sp = warp & 3, hh = lane >> 4;
+    const int q = 32 * sp + lane;  // query row == TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
+    const uint32_t peer_lanes = (uint32_t)(32 * sp + 16 * (int)peer) << 16;
+    const int kp = 16 * sp + (lane & 15);  // the peer's owned-row index of my send row
     const uint32_t x_peer0 = map_to_rank(smem_u32(sm + OFF_X), peer);
     const uint32_t xfull_peer0 = map_to_rank(smem_u32(&c.bars[X_FULL0]), peer);
+    const uint32_t lfree_peer = map_to_rank(smem_u32(&c.bars[LROW_FREE]), peer);
     uint32_t g = 0, n_rescale = 0;
     int n_item = 0;
     // `valid`: KV rows of the tile inside the item's range; the others may hold
@@ -595,10 +652,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const int sb = gs & 1;
       if (!wait_bar(c, S_FULL0 + sb, (gs >> 1) & 1)) return false;
       tc_fence_after();
-      uint32_t v[4][16];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tmem_ld_32x32b_x16(tmem + lane_base + TM_S + 64 * sb + 16 * k, v[k]);
+      uint32_t v[32];
+      tmem_ld_16x32bx2_x32(tmem + peer_lanes + TM_S + 64 * sb, v);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -609,56 +664,56 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       // rounding of P)
       float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        if (j >= valid) v[j >> 4][j & 15] = 0u;
-        am[j & 3] = fmaxf(am[j & 3], fabsf(__uint_as_float(v[j >> 4][j & 15])));
+      for (int j = 0; j < 32; ++j) {
+        if (32 * hh + j >= valid) v[j] = 0u;
+        am[j & 3] = fmaxf(am[j & 3], fabsf(__uint_as_float(v[j])));
       }
-      const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+      float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
       const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF);
       const int k2 = (e == 0) ? 0 : min(max(140 - e, -126), 127);
-      const float scale = __uint_as_float((uint32_t)(k2 + 127) << 23);
-      uint32_t h[32];
+      const float fscale = __uint_as_float((uint32_t)(k2 + 127) << 23);
+      uint32_t h[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        h[j] = pack_fix16x2(__uint_as_float(v[(2 * j) >> 4][(2 * j) & 15]) * scale,
-                          __uint_as_float(v[(2 * j + 1) >> 4][(2 * j + 1) & 15]) * scale);
+      for (int j = 0; j < 16; ++j)
+        h[j] = pack_fix16x2(__uint_as_float(v[2 * j]) * fscale,
+                            __uint_as_float(v[2 * j + 1]) * fscale);
       if (!wait_bar_cluster(c, PEER_X_FREE0 + sb, ((gs >> 1) & 1) ^ 1)) return false;
       const uint32_t xb = x_peer0 + (uint32_t)sb * kXBytes;
       const uint32_t bar = xfull_peer0 + 8u * sb;
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        st_async_v4_b32(xb + q * kXRowBytes + (uint32_t)((k ^ (q & 7)) << 4),
-                        make_uint4(h[4 * k], h[4 * k + 1], h[4 * k + 2], h[4 * k + 3]), bar);
-      st_async_b32(xb + kRows * kXRowBytes + 4 * q, __float_as_uint(scale), bar);
+      for (int u = 0; u < 4; ++u)
+        st_async_v4_b32(xb + kp * kXRowBytes + (uint32_t)(((4 * hh + u) ^ (kp & 7)) << 4),
+                        make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]), bar);
+      if (hh == 0) st_async_b32(xb + kOwnRows * kXRowBytes + 4 * kp, __float_as_uint(fscale), bar);
       return true;
     };
-    // Row q of the item's Q latent chunks 2-3 (this CTA's dims
-    // [256 r + 128, 256 r + 256)) into TMEM, where they are the A operand of
-    // the ts QK MMAs.  Called only when no QK of an earlier item is pending.
+    // Row q of the item's Q latent dims of this CTA ([256 r, 256 r + 256)) into
+    // TMEM, where they are the A operand of the ts QK MMAs.  Called only when
+    // no QK of an earlier item is pending.
     const long long q_rows = p.total_q * H;
     auto write_q = [&](const WorkItem& it) {
       const long long qrow = (long long)it.q_start * H + (long long)it.g * kRows + q;
-      uint32_t w[64];
-      if (qrow < q_rows) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const __nv_bfloat16*>(p.query) + qrow * kQkDim + 256 * (int)rank +
-            64 * kQSmemChunks);
+      const bool in = qrow < q_rows;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim +
+          256 * (int)rank);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint4 x = __ldg(src + k);
-          w[4 * k] = x.x;
-          w[4 * k + 1] = x.y;
-          w[4 * k + 2] = x.z;
-          w[4 * k + 3] = x.w;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[64];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint4 x = in ? __ldg(src + 16 * half + u) : make_uint4(0, 0, 0, 0);
+          w[4 * u] = x.x;
+          w[4 * u + 1] = x.y;
+          w[4 * u + 2] = x.z;
+          w[4 * u + 3] = x.w;
         }
-      } else {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) w[k] = 0u;
+        for (int j = 0; j < 4; ++j)
+          tmem_st_32x32b_x16(tmem + lane_base + TM_Q + 64 * half + 16 * j,
+                             *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        tmem_st_32x32b_x16(tmem + lane_base + TM_Q + 16 * j,
-                           *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -686,8 +741,6 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.bars[CORR_DONE]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.bars[CE_FREE]);
       return true;
     };
     for (int idx = item_begin; idx < item_end; ++idx) {
@@ -709,14 +762,19 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
       }
       if (!correct(g - 1, nt == 1)) goto done_epi;
-      // epilogue: O / l for my V dims, from the last tile's statistics
+      // epilogue: O / l for my V dims (l of every row arrived with the last P)
       if (!wait_bar(c, O_FINAL, n_item & 1)) goto done_epi;
       tc_fence_after();
       {
         const int rows_total = it.q_len * H;
         const int row0 = it.g * kRows;
         const bool row_ok = q < min(kRows, rows_total - row0);
-        const float l = lrow[((g - 1) & 1) * kRows + q];
+        const float l = lrow[q];
+        __syncwarp();
+        if (lane == 0) {  // both CTAs' softmax may overwrite l for the next item
+          mbar_arrive(&c.bars[LROW_FREE]);
+          mbar_arrive_cluster_relaxed(lfree_peer);
+        }
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const size_t grow = (size_t)it.q_start * H + row0 + q;
 #pragma unroll 1
@@ -751,11 +809,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       ++n_item;
     }
   done_epi:;
-  } else if (kFp8 && warp >= 14) {
+  } else if (kFp8 && warp >= 2 + kSoftmaxWarps + kCeWarps) {
     // ------------------------------------------------------------ e4m3 -> bf16
     // Thread r converts KV row r of each tile from the staging ring (row-major
     // bytes) into the bf16 ring in the swizzled layouts the MMAs read.
-    const int r = tid - 14 * 32;
+    const int r = tid - (2 + kSoftmaxWarps + kCeWarps) * 32;
     uint32_t g = 0;
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
@@ -888,12 +946,10 @@ cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs) {
 
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                                 cudaStream_t stream) {
-  CUtensorMap tm_q, tm_q_rope, tm_kv, tm_kv_rope;
+  CUtensorMap tm_q_rope, tm_kv, tm_kv_rope;
   const uint64_t q_rows = std::max<uint64_t>(1, (uint64_t)p.total_q * p.num_heads);
   const uint64_t kv_rows = (uint64_t)p.num_pages * p.page_size;
-  if (!encode_2d(&tm_q, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 64, kRows,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 32, kRows,
+  if (!encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 32, kRows,
                  CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   const bool fp8 = p.kv_dtype == 1;
@@ -905,7 +961,7 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     decode_sm103_kernel<true><<<lay.n_ctas, Cfg<true>::kThreads, kSmemBytes, stream>>>(
-        p, lay, static_cast<char*>(ws), tm_q, tm_q_rope, tm_kv, tm_kv_rope);
+        p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
   } else {
     if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -913,7 +969,7 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
     decode_sm103_kernel<false><<<lay.n_ctas, Cfg<false>::kThreads, kSmemBytes, stream>>>(
-        p, lay, static_cast<char*>(ws), tm_q, tm_q_rope, tm_kv, tm_kv_rope);
+        p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
   }
   return cudaGetLastError();
 }

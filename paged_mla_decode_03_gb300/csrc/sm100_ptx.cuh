@@ -425,3 +425,31 @@ __device__ __forceinline__ float2 unpack_fix16x2(uint32_t v) {
 
 }  // namespace ptx
 }  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+// Arrive on the mbarrier at the same shared-memory offset in every CTA of
+// `cta_mask` once every MMA previously issued by this thread completes.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+// 16 lanes x 32 bit, two column halves, 16 repetitions: threads 0-15 read
+// lanes 0-15 of the address at columns [col, col + 16), threads 16-31 the same
+// lanes at columns [col + 16, col + 32) (half split offset 16 columns).
+__device__ __forceinline__ void tmem_ld_16x32bx2_x16_s16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16], 16;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+}  // namespace ptx
+}  // namespace mla
