@@ -16,6 +16,7 @@
 
 namespace mla {
 cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cudaStream_t stream);
+cudaError_t partition_setup();
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream);
 cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs);
@@ -67,11 +68,16 @@ int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int row
   lay->worker_ranges = off;
   off = align_up(off + sizeof(int) * (n_workers + 1), 256);
   lay->req_scratch = off;
-  off = align_up(off + sizeof(int) * 4 * std::max(B, 1LL), 256);
+  const size_t req_bytes = align_up(sizeof(int) * 4 * std::max(B, 1LL), 256);
+  off += req_bytes;
   lay->group_scratch = off;
-  off = align_up(off + sizeof(long long) * lay->max_groups + sizeof(int) * 5 * lay->max_groups +
-                     sizeof(int) * lay->max_items,
-                 256);
+  const size_t grp_bytes = align_up(sizeof(long long) * lay->max_groups +
+                                        sizeof(int) * 5 * lay->max_groups +
+                                        sizeof(int) * lay->max_items,
+                                    256);
+  off += grp_bytes;
+  lay->scratch_bytes = req_bytes + grp_bytes;
+  lay->scratch_in_smem = lay->scratch_bytes <= kPartitionSmemMax ? 1 : 0;
   lay->part_o = off;
   off = align_up(off + sizeof(float) * R * kVDim * (size_t)lay->max_partials, 256);
   lay->part_lse = off;
@@ -109,6 +115,7 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   int sms = 0, n_pairs = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
   if (e == cudaSuccess) e = mla::decode_sm103_setup(p.kv_dtype, sms, &n_pairs);
+  if (e == cudaSuccess) e = mla::partition_setup();
   cudaSetDevice(prev);
   if (e != cudaSuccess || sms <= 0) return MLA_ERR_CUDA;
 

@@ -8,24 +8,28 @@
 // the vLLM "FlashInferMLAImpl" page uses to merge partial attention across
 // decode-context-parallel shards; here the shards are KV chunks of one GPU.
 //
-// Grid: (row blocks of 4 rows) x (combine entries), 256 threads; 64 threads
-// per row, 8 output dims per thread, all chunk loads of a thread issued
-// together.  Blocks past the live number of entries exit at once, so the
-// grid depends only on plan-time bounds.
+// Grid: (row blocks of 8 rows) x (combine entries), 256 threads; 32 threads
+// per row, 16 output dims per thread.  Every load of a thread (the LSEs and
+// the 16-dim slices of up to kBatch chunks) is issued before any is used, so
+// a row costs one memory round trip per kBatch chunks, and the grid fits one
+// wave.  Blocks past the live number of entries exit at once, so the grid
+// depends only on plan-time bounds.
 #include <cuda_bf16.h>
 
 #include "mla_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 
 namespace {
 constexpr int kThreads = 256;
-constexpr int kRowsPerBlock = 4;
-constexpr int kUnroll = 8;
+constexpr int kRowsPerBlock = 8;
+constexpr int kBatch = 4;  // chunks loaded per round trip
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
+  ptx::pdl_wait();  // the decode kernel's partials are complete and visible
   const int* hdr = reinterpret_cast<const int*>(ws);
   const CombineItem* comb = reinterpret_cast<const CombineItem*>(ws + lay.combine);
   const float* part_o = reinterpret_cast<const float*>(ws + lay.part_o);
@@ -33,58 +37,65 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   const int n_combine = hdr[kHdrNumCombine];
   const int H = p.num_heads;
   const int R = lay.rows_per_group;
-  const int row_in_block = threadIdx.x >> 6;  // 0..3
-  const int t = threadIdx.x & 63;             // output dims [8 t, 8 t + 8)
+  const int row_in_block = threadIdx.x >> 5;  // 0..7
+  const int t = threadIdx.x & 31;             // output dims [16 t, 16 t + 16)
 
   for (int ci = blockIdx.y; ci < n_combine; ci += gridDim.y) {
     const CombineItem c = comb[ci];
     const int rows = min(R, c.q_len * H - c.g * R);
     const int r = blockIdx.x * kRowsPerBlock + row_in_block;
     if (r >= rows) continue;
-    float m = -INFINITY;
-    for (int k = 0; k < c.n_chunks; ++k)
-      m = fmaxf(m, part_lse[(size_t)(c.first_slot + k * c.stride) * R + r]);
-    const float m_use = (m == -INFINITY) ? 0.f : m;
-    float sum = 0.f;
-    float acc[8];
+    // running merge over batches of chunks: (m, sum, acc) rescaled per batch
+    float m = -INFINITY, sum = 0.f;
+    float acc[16];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (int k0 = 0; k0 < c.n_chunks; k0 += kUnroll) {
-      float4 x[kUnroll][2];
-      float w[kUnroll];
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int k0 = 0; k0 < c.n_chunks; k0 += kBatch) {
+      float4 x[kBatch][4];
+      float l[kBatch];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        w[u] = 0.f;
-        x[u][0] = x[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kBatch; ++u) {
+        l[u] = -INFINITY;
         if (k0 + u < c.n_chunks) {
           const size_t slot = (size_t)(c.first_slot + (k0 + u) * c.stride);
           const float4* src =
-              reinterpret_cast<const float4*>(part_o + (slot * R + r) * kVDim) + 2 * t;
-          x[u][0] = src[0];
-          x[u][1] = src[1];
-          w[u] = expf(part_lse[slot * R + r] - m_use);
+              reinterpret_cast<const float4*>(part_o + (slot * R + r) * kVDim) + 4 * t;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) x[u][v] = src[v];
+          l[u] = part_lse[slot * R + r];
+        } else {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+      float m_new = m;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        sum += w[u];
-        acc[0] += w[u] * x[u][0].x;
-        acc[1] += w[u] * x[u][0].y;
-        acc[2] += w[u] * x[u][0].z;
-        acc[3] += w[u] * x[u][0].w;
-        acc[4] += w[u] * x[u][1].x;
-        acc[5] += w[u] * x[u][1].y;
-        acc[6] += w[u] * x[u][1].z;
-        acc[7] += w[u] * x[u][1].w;
+      for (int u = 0; u < kBatch; ++u) m_new = fmaxf(m_new, l[u]);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float f = expf(m - m_use);  // m = -inf: 0
+      sum *= f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) acc[e] *= f;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float w = expf(l[u] - m_use);  // absent chunks: l = -inf, w = 0
+        sum += w;
+        const float* xv = reinterpret_cast<const float*>(x[u]);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] += w * xv[e];
       }
+      m = m_new;
     }
     const float s2 = sum > 0.f ? p.bmm2_scale / sum : 0.f;
     const size_t grow = (size_t)c.q_start * H + (size_t)c.g * R + r;
-    __nv_bfloat162 o[4];
+    __nv_bfloat162 o[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
-    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kVDim + 8 * t) =
-        *reinterpret_cast<uint4*>(o);
+    for (int e = 0; e < 8; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kVDim +
+                                          16 * t);
+    dst[0] = *reinterpret_cast<uint4*>(o);
+    dst[1] = *reinterpret_cast<uint4*>(o + 4);
+    const float m_use = (m == -INFINITY) ? 0.f : m;
     if (p.return_lse && t == 0) p.lse[grow] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
   }
 }
@@ -92,9 +103,16 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
-  const dim3 g((lay.rows_per_group + kRowsPerBlock - 1) / kRowsPerBlock, grid, 1);
-  combine_kernel<<<g, kThreads, 0, stream>>>(p, lay, static_cast<char*>(ws));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((lay.rows_per_group + kRowsPerBlock - 1) / kRowsPerBlock, grid, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, p, lay, static_cast<char*>(ws));
 }
 
 }  // namespace mla

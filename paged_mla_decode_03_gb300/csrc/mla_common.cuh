@@ -14,6 +14,9 @@ constexpr int kVDim = 512;        // V = the latent part of each cache row
 constexpr int kKvTile = 64;       // KV rows per pipeline tile
 
 // Problem record: static plan parameters plus the per-run pointers/scales.
+// Largest partitioner scratch kept in shared memory (else in the workspace).
+constexpr size_t kPartitionSmemMax = 160 * 1024;
+
 struct Problem {
   int batch, num_heads, max_q, max_seq_len, page_size, max_pages;
   int packed, kv_dtype, causal, return_lse;
@@ -63,6 +66,8 @@ struct Layout {
   size_t worker_ranges;  // int[n_workers + 1]: worker w owns items [r[w], r[w+1])
   size_t req_scratch;    // int[4 * batch]: partitioner scratch
   size_t group_scratch;  // partitioner scratch per row group / item
+  size_t scratch_bytes;  // bytes of the two scratch areas
+  int scratch_in_smem;   // 1: the partitioner keeps its scratch in shared memory
   size_t part_o;         // float[max_partials][rows_per_group][512]
   size_t part_lse;       // float[max_partials][rows_per_group]
   size_t total;

@@ -240,6 +240,10 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote access
+  // the work list comes from the partition kernel; the combine kernel may be
+  // scheduled as soon as SMs free up (it waits for this grid to complete)
+  pdl_wait();
+  pdl_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   const int item_begin = worker_begin[worker], item_end = worker_begin[worker + 1];
   const int H = p.num_heads;
@@ -369,6 +373,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
             if (pv_state == 2 &&
                 (pv != 0 || n_item <= 1 || mbar_test_wait(&c.bars[EPI_DONE], (n_item - 2) & 1))) {
               tc_fence_after();
+              // the peer's P rows arrived through st.async (generic proxy); order
+              // them before this thread's MMA reads (async proxy)
+              fence_proxy_async_smem();
               const int s = gp % kStages;
               const uint32_t stage = kv_base + s * kStageBytes;
               for (int ks = 0; ks < kTile / 16; ++ks) {
@@ -938,6 +945,24 @@ cudaError_t setup_one(int sm_count, int* n_pairs) {
   return cudaSuccess;
 }
 
+// Launch as a programmatic dependent of the previous kernel in the stream.
+template <typename Kernel>
+cudaError_t launch_pdl(Kernel kernel, int grid, int threads, cudaStream_t stream, const Problem& p,
+                       const Layout& lay, char* ws, const CUtensorMap& a, const CUtensorMap& b,
+                       const CUtensorMap& c) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p, lay, ws, a, b, c);
+}
+
 }  // namespace
 
 cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs) {
@@ -960,18 +985,17 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
         !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 32,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    decode_sm103_kernel<true><<<lay.n_ctas, Cfg<true>::kThreads, kSmemBytes, stream>>>(
-        p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
+    return launch_pdl(decode_sm103_kernel<true>, lay.n_ctas, Cfg<true>::kThreads, stream, p, lay,
+                      static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
   } else {
     if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 32,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
-    decode_sm103_kernel<false><<<lay.n_ctas, Cfg<false>::kThreads, kSmemBytes, stream>>>(
-        p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
+    return launch_pdl(decode_sm103_kernel<false>, lay.n_ctas, Cfg<false>::kThreads, stream, p, lay,
+                      static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mla

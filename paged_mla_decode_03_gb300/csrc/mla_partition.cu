@@ -17,6 +17,7 @@
 // workers are balanced to within one tile plus one overhead, and there are at
 // most n + #groups items and n - 1 cut points.  One CTA of 1024 threads.
 #include "mla_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 
@@ -104,6 +105,9 @@ __device__ int owner_of(long long x, long long W, long long n) {
 __global__ void __launch_bounds__(kThreads, 1)
 partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   __shared__ Shared sh;
+  // the decode kernel may set up its barriers and TMEM meanwhile; it reads
+  // nothing written here before its grid-dependency wait
+  ptx::pdl_launch_dependents();
   int* hdr = reinterpret_cast<int*>(ws);
   WorkItem* items = reinterpret_cast<WorkItem*>(ws + lay.items);
   CombineItem* comb = reinterpret_cast<CombineItem*>(ws + lay.combine);
@@ -111,13 +115,19 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   const int B = p.batch;
   const int R = lay.rows_per_group;
   const int H = p.num_heads;
-  // per-request scratch
-  int* r_qlen = reinterpret_cast<int*>(ws + lay.req_scratch);
+  // per-request and per-group scratch: in shared memory when it fits (no
+  // memory round trip between the phases below), else in the workspace
+  extern __shared__ __align__(16) unsigned char scratch_smem[];
+  char* req_base = lay.scratch_in_smem ? reinterpret_cast<char*>(scratch_smem) : ws + lay.req_scratch;
+  char* grp_base = lay.scratch_in_smem
+                       ? reinterpret_cast<char*>(scratch_smem) + (lay.group_scratch - lay.req_scratch)
+                       : ws + lay.group_scratch;
+  int* r_qlen = reinterpret_cast<int*>(req_base);
   int* r_qstart = r_qlen + B;
   int* r_len = r_qstart + B;
   int* r_gbase = r_len + B;  // first group index of the request
   // per-group scratch
-  long long* g_start = reinterpret_cast<long long*>(ws + lay.group_scratch);  // unit offset
+  long long* g_start = reinterpret_cast<long long*>(grp_base);  // unit offset
   int* g_items = reinterpret_cast<int*>(g_start + lay.max_groups);              // -> item base
   int* g_req = g_items + lay.max_groups;
   int* g_nch = g_req + lay.max_groups;
@@ -279,8 +289,14 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
 }
 
 cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cudaStream_t stream) {
-  partition_kernel<<<1, kThreads, 0, stream>>>(p, lay, static_cast<char*>(ws));
+  const size_t smem = lay.scratch_in_smem ? lay.scratch_bytes : 0;
+  partition_kernel<<<1, kThreads, smem, stream>>>(p, lay, static_cast<char*>(ws));
   return cudaGetLastError();
+}
+
+cudaError_t partition_setup() {
+  return cudaFuncSetAttribute(partition_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kPartitionSmemMax);
 }
 
 }  // namespace mla

@@ -453,3 +453,18 @@ __device__ __forceinline__ void tmem_ld_16x32bx2_x16_s16(uint32_t taddr, uint32_
 
 }  // namespace ptx
 }  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+// Programmatic dependent launch: let the next kernel of the stream start its
+// prologue now / wait until the previous kernel of the stream has completed
+// and its memory is visible (returns at once if it was not launched as a
+// programmatic dependent).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+}  // namespace ptx
+}  // namespace mla
