@@ -130,7 +130,9 @@ int mla_decode_run(const mla_plan_t *plan, const void *query, const void *kv_cac
  * mla_decode_run, plus two CUDA events (cudaEvent_t, may be NULL) recorded on
  * `stream` immediately before and after the decode kernel, so that a caller
  * can time that kernel alone with cudaEventElapsedTime.  Same arguments,
- * errors and capture rules as mla_decode_run.
+ * errors and capture rules as mla_decode_run; while the stream is being
+ * captured into a CUDA graph the two records become event-record nodes
+ * (cudaEventRecordExternal), so every replay re-times the kernel.
  */
 int mla_decode_run_profiled(const mla_plan_t *plan, const void *query, const void *kv_cache,
                             const int32_t *block_tables, const int32_t *seq_lens,

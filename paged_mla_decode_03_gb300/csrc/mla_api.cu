@@ -184,13 +184,23 @@ int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const voi
   p.lse = prm.return_lse ? lse : nullptr;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // while the stream is being captured into a graph, the events become
+  // event-record nodes of the graph (timed at every replay)
+  unsigned int ev_flags = cudaEventRecordDefault;
+  if (event_before_decode || event_after_decode) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+  }
   if (mla::launch_partition(p, plan->lay, workspace, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (event_before_decode &&
-      cudaEventRecord(static_cast<cudaEvent_t>(event_before_decode), s) != cudaSuccess)
+      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(event_before_decode), s, ev_flags) !=
+          cudaSuccess)
     return MLA_ERR_CUDA;
   if (mla::launch_decode_sm103(p, plan->lay, workspace, s) != cudaSuccess) return MLA_ERR_CUDA;
   if (event_after_decode &&
-      cudaEventRecord(static_cast<cudaEvent_t>(event_after_decode), s) != cudaSuccess)
+      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(event_after_decode), s, ev_flags) !=
+          cudaSuccess)
     return MLA_ERR_CUDA;
   if (mla::launch_combine(p, plan->lay, workspace, plan->combine_grid, s) != cudaSuccess)
     return MLA_ERR_CUDA;
