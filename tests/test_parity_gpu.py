@@ -240,3 +240,38 @@ def test_host_side_errors():
             d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=d.lse,
                        workspace=d.workspace, bmm1_scale=bad)
         assert e.value.status == -1
+
+
+def test_e4m3_widening_is_exact_for_every_code():
+    """The kernel widens e4m3 KV to bf16 in shared memory.  With Q = 0 and a
+    single KV row, P = 1 exactly and O is that row's V, so every output
+    element must be the bf16 value of its e4m3 code, bit for bit, for all
+    254 non-NaN codes (subnormals included).  The sign of a zero does not
+    survive the fp32 accumulation of P V (1 * -0 + 0 * v = +0), so zeros are
+    compared by value.  A NaN code would turn the scores NaN, so it cannot be
+    read back this way."""
+    import paged_mla_decode_03_gb300 as mla
+    dev = torch.device("cuda", 0)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)  # 254
+    row = np.zeros(576, dtype=np.uint8)
+    row[:254] = codes
+    row[254:508] = codes[::-1]
+    kv = np.zeros((1, 64, 576), dtype=np.uint8)
+    kv[0, 0] = row
+    H = 16
+    kv_t = torch.from_numpy(kv).to(dev).view(torch.float8_e4m3fn)
+    q = torch.zeros((1, H, 576), dtype=torch.bfloat16, device=dev)
+    bt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+    sl = torch.ones(1, dtype=torch.int32, device=dev)
+    plan = mla.Plan(batch=1, num_heads=H, max_seq_len_q=1, max_seq_len=1, page_size=64,
+                    max_pages_per_req=1, num_pages=1, packed=False, kv_dtype="e4m3")
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    out = torch.full((1, H, 512), float("nan"), dtype=torch.bfloat16, device=dev)
+    plan.run(q, kv_t, bt, sl, out, workspace=ws)
+    torch.cuda.synchronize()
+    want = torch.from_numpy(row[:512].copy()).view(torch.float8_e4m3fn).to(torch.bfloat16)
+    got = out.cpu()
+    nz = want != 0
+    for h in range(H):
+        assert torch.equal(got[0, h].float(), want.float()), h
+        assert torch.equal(got[0, h][nz].view(torch.int16), want[nz].view(torch.int16)), h
