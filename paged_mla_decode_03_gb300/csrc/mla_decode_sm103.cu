@@ -29,14 +29,14 @@
 //    V dims, read MN-major from its latent chunks), K = 64 KV rows, into a
 //    128 x 256 fp32 TMEM accumulator.  The PV commit is multicast to both CTAs,
 //    so a P buffer is reused only after both CTAs' PV read it.
-// Warp roles (448 threads): warp 0 TMA producer (4-stage KV ring), warp 1
+// Warp roles (448 threads, 704 with e4m3): warp 0 TMA producer (4-stage KV ring), warp 1
 // MMA issuer and TMEM owner (QK runs up to two tiles ahead of PV), warps 2-9
 // softmax of the 64 owned rows (four threads per row, 16 KV columns each:
 // warp w covers the owned lanes 32 (w mod 4) + 16 r .. + 15, columns
 // [32 h, 32 h + 32), h = (w - 2) / 4, with the 16x32bx2 access shape),
 // warps 10-13 partial-score senders (the peer-owned lanes), O correction,
 // epilogue and the Q latent load into TMEM (thread = query row = TMEM lane).
-// With an e4m3 cache two more warps (14-15) widen each staged e4m3 tile to
+// With an e4m3 cache eight more warps (14-21) widen each staged e4m3 tile to
 // bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and the
 // bf16 ring is 3 deep.
 // The running max is only raised, and O rescaled, when it grows by more than
@@ -67,9 +67,9 @@ constexpr int kCeWarps = 4;       // senders / correction / epilogue
 constexpr int kMaxStages = 4;
 template <bool kFp8> struct Cfg {
   static constexpr int kStages = kFp8 ? 3 : 4;
-  static constexpr int kThreads = kFp8 ? 512 : 448;  // + 2 converter warps
+  static constexpr int kThreads = kFp8 ? 704 : 448;  // + 8 converter warps
 };
-constexpr int kConvThreads = 64;
+constexpr int kConvThreads = 256;  // four per KV row of a tile
 constexpr uint32_t kWaitLimit = 1u << 26;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -818,9 +818,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   done_epi:;
   } else if (kFp8 && warp >= 2 + kSoftmaxWarps + kCeWarps) {
     // ------------------------------------------------------------ e4m3 -> bf16
-    // Thread r converts KV row r of each tile from the staging ring (row-major
-    // bytes) into the bf16 ring in the swizzled layouts the MMAs read.
-    const int r = tid - (2 + kSoftmaxWarps + kCeWarps) * 32;
+    // Threads r + 64 p (p = 0..3) convert KV row r of each tile from the
+    // staging ring (row-major bytes) into the bf16 ring in the swizzled layouts
+    // the MMAs read: latent chunk p, and for p < 2 half p of the RoPE dims.
+    const int ct = tid - (2 + kSoftmaxWarps + kCeWarps) * 32;
+    const int r = ct & (kTile - 1), part = ct / kTile;
     uint32_t g = 0;
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
@@ -833,8 +835,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         if (!wait_bar(c, KV_EMPTY0 + s, ((g / kStages) & 1) ^ 1)) goto done_conv;
         const unsigned char* src = sm + OFF_STG + ss * kStgBytes;
         unsigned char* dst = sm + OFF_KV + s * kStageBytes;
-#pragma unroll
-        for (int lc = 0; lc < kLatChunks; ++lc) {
+        {
+          const int lc = part;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // 16 e4m3 values -> 2 x 16-byte bf16 units
             const uint4 b = *reinterpret_cast<const uint4*>(src + lc * kTile * 64 + r * 64 + 16 * k);
@@ -852,8 +854,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                 make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {  // RoPE half: 32 values -> four 16-byte units (64B swizzle)
+        if (part < 2) {  // RoPE: 16 of its 32 values -> two 16-byte units (64B swizzle)
+          const int k = part;
           const uint4 b =
               *reinterpret_cast<const uint4*>(src + kLatChunks * kTile * 64 + r * 32 + 16 * k);
           const uint32_t w[4] = {b.x, b.y, b.z, b.w};
