@@ -72,7 +72,7 @@ int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int row
   off += req_bytes;
   lay->group_scratch = off;
   const size_t grp_bytes = align_up(sizeof(long long) * lay->max_groups +
-                                        sizeof(int) * 5 * lay->max_groups +
+                                        sizeof(int) * 6 * lay->max_groups +
                                         sizeof(int) * lay->max_items,
                                     256);
   off += grp_bytes;

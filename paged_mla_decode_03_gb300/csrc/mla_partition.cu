@@ -45,6 +45,22 @@ __device__ int block_or(int v, Shared& sh) {
   return t;
 }
 
+__device__ int block_min(int v, Shared& sh) {
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) sh.warp_i[warp] = v;
+  __syncthreads();
+  int t = sh.warp_i[0];
+  for (int w = 1; w < kThreads / 32; ++w) t = min(t, sh.warp_i[w]);
+  __syncthreads();
+  return t;
+}
+
+__device__ int block_max(int v, Shared& sh) {
+  return -block_min(-v, sh);
+}
+
 // In-place exclusive prefix sum of data[0, n); returns the total.
 template <typename T>
 __device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
@@ -80,24 +96,34 @@ __device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
   return (T)sh.carry_ll;
 }
 
-// Start unit of worker p's range: floor(p * W / n).
-__device__ __forceinline__ long long boundary(long long p, long long W, long long n) {
-  return (p * W) / n;
-}
+// Worker ranges.  The workers form `lanes` lanes of nl workers (leftover
+// workers get empty ranges); lane k owns units [k WL, (k + 1) WL) and its
+// worker i the units [k WL + floor(i WL / nl), k WL + floor((i + 1) WL / nl)).
+// With one lane this is the plain split of [0, W) into n near-equal ranges.
+struct Bounds {
+  long long W, n, lanes, nl, WL;
+  // start unit of worker p's range
+  __device__ long long boundary(long long p) const {
+    if (p >= lanes * nl) return W;
+    const long long k = p / nl, i = p - k * nl;
+    return k * WL + (i * WL) / nl;
+  }
+  // first worker p whose range starts after unit x (0 <= x < W)
+  __device__ long long first_above(long long x) const {
+    const long long k = x / WL, r = x - k * WL;
+    const long long i = ((r + 1) * nl + WL - 1) / WL;
+    return i >= nl ? (k + 1) * nl : k * nl + i;
+  }
+  // worker that owns unit x (0 <= x < W): the largest p with boundary(p) <= x
+  __device__ long long owner_of(long long x) const {
+    return min(first_above(x) - 1, n - 1);
+  }
+};
 
 // Tile cut position of range boundary p inside a group starting at unit S.
-__device__ __forceinline__ int cut_tile(long long p, long long W, long long n, long long S,
-                                        int T) {
-  const long long t = boundary(p, W, n) - S - kOverheadTiles;
+__device__ __forceinline__ int cut_tile(const Bounds& bd, long long p, long long S, int T) {
+  const long long t = bd.boundary(p) - S - kOverheadTiles;
   return (int)min(max(t, 0LL), (long long)T);
-}
-
-// Worker that owns unit x: the largest p with boundary(p) <= x.
-__device__ int owner_of(long long x, long long W, long long n) {
-  long long p = W > 0 ? min((x * n) / W, n - 1) : 0;
-  while (p + 1 < n && boundary(p + 1, W, n) <= x) ++p;
-  while (p > 0 && boundary(p, W, n) > x) --p;
-  return (int)p;
 }
 
 }  // namespace
@@ -133,7 +159,8 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   int* g_nch = g_req + lay.max_groups;
   int* g_slot = g_nch + lay.max_groups;  // partial-slot base
   int* g_comb = g_slot + lay.max_groups;  // combine-entry base
-  int* it_owner = g_comb + lay.max_groups;  // per item: owning worker
+  int* g_k = g_comb + lay.max_groups;     // row group within its request
+  int* it_owner = g_k + lay.max_groups;   // per item: owning worker
 
   // 1. Per-request lengths, clamped so that nothing downstream leaves the
   //    caller's buffers; contract violations are flagged in the status word.
@@ -162,6 +189,15 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     r_gbase[b] = (L > 0) ? (q * H + R - 1) / R : 0;
   }
   status = __syncthreads_or(status) ? block_or(status, sh) : 0;
+  // do all requests that have row groups have the same number of them?
+  int g_min = 1 << 30, g_max = 0;
+  for (int b = threadIdx.x; b < B; b += kThreads)
+    if (r_gbase[b] > 0) {
+      g_min = min(g_min, r_gbase[b]);
+      g_max = max(g_max, r_gbase[b]);
+    }
+  g_min = block_min(g_min, sh);
+  g_max = block_max(g_max, sh);
   __syncthreads();
   int n_groups = block_exclusive_scan(r_gbase, B, sh);
   if (n_groups > lay.max_groups) {  // unreachable within the contract
@@ -169,19 +205,37 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     n_groups = 0;
   }
 
-  // 2. Groups in request order with their unit costs.
+  // 2. Groups with their unit costs.  When every request that has row
+  //    groups has the same number G >= 2 of them (a uniform q_len) and the
+  //    workers can be split into G lanes of at least two, group k of every
+  //    request goes to lane k (order lane-major), so lane k's worker i walks
+  //    the same KV ranges as every other lane's worker i at the same time: a
+  //    page comes from DRAM once and from L2 for the other lanes.  Otherwise
+  //    groups are laid out in request order on one lane.
+  const long long n = lay.n_workers;
+  const int G = g_max;
+  const int lanes = (g_min == g_max && G >= 2 && n / G >= 2) ? G : 1;
+  const int n_req_groups = lanes > 1 ? n_groups / G : 0;  // requests that have groups
   for (int b = threadIdx.x; b < B; b += kThreads) {
     const int gb = r_gbase[b];
     const int ge = (b + 1 < B) ? r_gbase[b + 1] : n_groups;
     const int T = (r_len[b] + kKvTile - 1) / kKvTile;
     for (int g = gb; g < ge && g < n_groups; ++g) {
-      g_req[g] = b;
-      g_start[g] = kOverheadTiles + T;  // cost; scanned into the start unit below
+      const int k = g - gb;
+      const int slot = lanes > 1 ? k * n_req_groups + gb / G : g;
+      g_req[slot] = b;
+      g_k[slot] = k;
+      g_start[slot] = kOverheadTiles + T;  // cost; scanned into the start unit below
     }
   }
   __syncthreads();
   const long long W = block_exclusive_scan(g_start, n_groups, sh);
-  const long long n = lay.n_workers;
+  Bounds bd;
+  bd.W = W;
+  bd.n = n;
+  bd.lanes = lanes;
+  bd.nl = n / lanes;
+  bd.WL = W / lanes;  // every lane has the same cost
 
   // 3. Cut points inside each group -> chunk counts.
   for (int g = threadIdx.x; g < n_groups; g += kThreads) {
@@ -190,11 +244,11 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     const long long S = g_start[g], c = kOverheadTiles + T;
     int nch = 1;
     if (W > 0) {
-      const long long p_lo = ((S + 1) * n + W - 1) / W;
-      const long long p_hi = ((S + c) * n + W - 1) / W - 1;
+      const long long p_lo = bd.first_above(S);           // boundaries after the group start
+      const long long p_hi = bd.first_above(S + c - 1) - 1;  // ... and before its end
       int prev = 0;
       for (long long q = max(p_lo, 1LL); q <= min(p_hi, n - 1); ++q) {
-        const int t = cut_tile(q, W, n, S, T);
+        const int t = cut_tile(bd, q, S, T);
         if (t > prev && t < T) {
           ++nch;
           prev = t;
@@ -223,7 +277,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
       const int T = (L + kKvTile - 1) / kKvTile;
       const long long S = g_start[g], c = kOverheadTiles + T;
       const int nch = g_nch[g];
-      const int g_local = g - r_gbase[b];
+      const int g_local = g_k[g];
       int k = 0, prev = 0;
       // an item belongs to the worker whose range holds its first KV tile
       long long start_unit = S + kOverheadTiles;
@@ -238,14 +292,14 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
         it.seq_len = L;
         it.q_start = r_qstart[b];
         items[g_items[g] + k] = it;
-        it_owner[g_items[g] + k] = owner_of(unit, W, n);
+        it_owner[g_items[g] + k] = (int)bd.owner_of(unit);
         ++k;
       };
       if (nch > 1 && W > 0) {
-        const long long p_lo = ((S + 1) * n + W - 1) / W;
-        const long long p_hi = ((S + c) * n + W - 1) / W - 1;
+        const long long p_lo = bd.first_above(S);
+        const long long p_hi = bd.first_above(S + c - 1) - 1;
         for (long long q = max(p_lo, 1LL); q <= min(p_hi, n - 1); ++q) {
-          const int t = cut_tile(q, W, n, S, T);
+          const int t = cut_tile(bd, q, S, T);
           if (t > prev && t < T) {
             emit(prev, t, start_unit);
             start_unit = S + kOverheadTiles + t;
