@@ -275,3 +275,80 @@ def test_e4m3_widening_is_exact_for_every_code():
     for h in range(H):
         assert torch.equal(got[0, h].float(), want.float()), h
         assert torch.equal(got[0, h][nz].view(torch.int16), want[nz].view(torch.int16)), h
+
+
+def _index_encoded(w):
+    """Q = 0 and every visible cache row j of request b one-hot at dim j mod 512
+    (RoPE dims 0): all scores are 0, so row (b, i, h) must return
+    O[d] = #{visible j : j mod 512 = d} / n and lse = ln n, n = its visible count."""
+    w.query[...] = 0
+    ps = w.page_size
+    one = mi.bf16_bits(np.ones(1, dtype=np.float32))[0]
+    for b in range(w.batch):
+        for j in range(int(w.seq_lens[b])):
+            page = int(w.block_tables[b, j // ps])
+            w.kv_cache[page, j % ps, :] = 0
+            w.kv_cache[page, j % ps, j % 512] = one
+    return w
+
+
+@pytest.mark.parametrize("page_size,causal,q_len", [(64, True, 3), (32, True, 5), (64, False, 2)])
+def test_mask_decisions_are_exact_with_index_encoded_values(page_size, causal, q_len):
+    """Every mask decision of every row, read back as exact counts: lengths on
+    both sides of tile and page boundaries, long rows that are split across
+    workers, causal q_len > 1 and dense."""
+    lens = [q_len, q_len + 1, 63, 64, 65, 66, 127, 128, 129, 191, 200, 513, 700, 1000, 2500]
+    w = mi.build("mask_index", 4242, num_heads=16, page_size=page_size, seq_lens=lens,
+                 q_lens=[q_len] * len(lens), packed=False, causal=causal, return_lse=True,
+                 bmm1_scale=0.5, bmm2_scale=1.0)
+    w = _index_encoded(w)
+    d = to_device(w)
+    run(w, d)
+    out, lse = results(d)
+    out = out.reshape(len(lens), q_len, 16, 512)
+    lse = lse.reshape(len(lens), q_len, 16)
+    assert device_status(d) == 0
+    for b, L in enumerate(lens):
+        for i in range(q_len):
+            n = L - q_len + i + 1 if causal else L
+            count = np.bincount(np.arange(n) % 512, minlength=512).astype(np.float64)
+            got = out[b, i] * n  # [16, 512]
+            assert np.abs(got - count[None, :]).max() < 0.25, (b, L, i)
+            assert np.abs(lse[b, i] - np.log(n)).max() < 2e-3, (b, L, i)
+
+
+def test_ragged_request_equals_its_own_single_request_launch():
+    """Each request of a packed ragged batch equals a separate fixed-shape B=1
+    launch of the same request (same pages, same query rows)."""
+    w = REDUCED["ragged"]()
+    d = to_device(w)
+    run(w, d)
+    out, lse = results(d)
+    import paged_mla_decode_03_gb300 as mla
+    dev = torch.device("cuda", 0)
+    H = w.num_heads
+    qs = w.q_start()
+    kv = d.kv_cache
+    for b in [0, 3, 7, w.batch - 1]:
+        q_b = int(w.q_lens[b])
+        rows = w.query_rows()[qs[b]:qs[b + 1]]
+        q = torch.from_numpy(rows.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+        bt = torch.from_numpy(w.block_tables[b:b + 1].copy()).to(dev)
+        sl = torch.from_numpy(w.seq_lens[b:b + 1].copy()).to(dev)
+        plan = mla.Plan(batch=1, num_heads=H, max_seq_len_q=q_b, max_seq_len=int(w.seq_lens[b]),
+                        page_size=w.page_size, max_pages_per_req=w.block_tables.shape[1],
+                        num_pages=w.num_pages, packed=False, kv_dtype=w.kv_dtype,
+                        causal=w.causal, return_lse=True)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+        o1 = torch.full((q_b, H, 512), float("nan"), dtype=torch.bfloat16, device=dev)
+        l1 = torch.full((q_b, H), float("nan"), dtype=torch.float32, device=dev)
+        plan.run(q, kv, bt, sl, o1, lse=l1, workspace=ws, bmm1_scale=w.bmm1_scale,
+                 bmm2_scale=w.bmm2_scale)
+        torch.cuda.synchronize()
+        o1 = o1.float().cpu().numpy()
+        l1 = l1.cpu().numpy()
+        ob = out[qs[b]:qs[b + 1]]
+        lb = lse[qs[b]:qs[b + 1]]
+        # the two launches may cut the KV range differently: equal to rounding
+        assert np.abs(o1 - ob).max() <= 4e-3 + 1e-2 * np.abs(ob).max(), b
+        assert np.abs(l1 - lb).max() <= 1e-3, b
