@@ -142,6 +142,30 @@ int mla_decode_run_profiled(const mla_plan_t *plan, const void *query, const voi
                             void *event_after_decode);
 
 /*
+ * mla_decode_run with bmm1_scale and bmm2_scale read from device memory by
+ * the kernels when they run, instead of passed by value.  This is the form a
+ * captured CUDA graph needs when the scales change between replays, e.g.
+ * when the caller folds per-step q/k/v quantisation scales into them (the
+ * FlashInfer pull request "dynamic scale factor interface and one-copy
+ * kvcache on trtllm-gen mla", its summary of the device-tensor scale
+ * interface).
+ *
+ * bmm1_scale, bmm2_scale  device pointers to one fp32 each, 4-byte aligned,
+ *              non-NULL; written by earlier work on `stream` or before the
+ *              launch.  The same meaning as the by-value scales.  bmm1 must
+ *              be finite and >= 0: the host cannot check it, so a violation
+ *              sets status bit 64 (mla_decode_status_offset) and bmm1 reads
+ *              as 0.
+ * All other arguments, errors and capture rules as mla_decode_run.
+ */
+int mla_decode_run_device_scales(const mla_plan_t *plan, const void *query, const void *kv_cache,
+                                 const int32_t *block_tables, const int32_t *seq_lens,
+                                 const int32_t *qo_indptr, int64_t total_q,
+                                 const float *bmm1_scale, const float *bmm2_scale, void *out,
+                                 float *lse, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/*
  * Size of the library-owned scratch array used by
  * mla_decode_run_static_workspace (48 MiB on every GPU that loads the
  * library, held until the process exits).
@@ -181,10 +205,17 @@ size_t mla_decode_workspace_size(const mla_plan_t *plan);
 
 /*
  * Byte offset, inside the workspace, of the int32 device status word the last
- * run left behind (0 = every length and offset was within the contract; bit 0:
- * a seq_len out of [1, max_seq_len]; bit 1: a q_len out of [1, max_seq_len_q]
- * or a qo_indptr offset out of range; bit 2: causal q_len > seq_len).  Reading
- * it is the caller's choice (a device-to-host copy after the stream syncs).
+ * run left behind.  0: every device-side value was within the contract.
+ * Bits (values are clamped and never read out of bounds):
+ *   1  a seq_len out of [1, max_seq_len]
+ *   2  a q_len out of [1, max_seq_len_q], or a qo_indptr offset out of range
+ *   4  causal masking with q_len > seq_len
+ *   8  a workspace capacity exceeded (unreachable within the contract)
+ *  16  a block_tables entry of a visible page out of [0, num_pages)
+ *  32  an internal wait timed out (the run unwound; results are invalid)
+ *  64  a device bmm1 scale negative or not finite (read as 0)
+ * Reading it is the caller's choice (a device-to-host copy after the stream
+ * syncs).
  */
 size_t mla_decode_status_offset(void);
 

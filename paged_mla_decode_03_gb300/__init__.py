@@ -86,6 +86,9 @@ def load_library():
     lib.mla_decode_run.restype = ctypes.c_int
     lib.mla_decode_run_profiled.argtypes = lib.mla_decode_run.argtypes + [vp, vp]
     lib.mla_decode_run_profiled.restype = ctypes.c_int
+    lib.mla_decode_run_device_scales.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp,
+                                                 sz, vp]
+    lib.mla_decode_run_device_scales.restype = ctypes.c_int
     lib.mla_decode_destroy.argtypes = [vp]
     lib.mla_decode_destroy.restype = None
     lib.mla_decode_workspace_size.argtypes = [vp]
@@ -159,6 +162,31 @@ def mla_decode_run(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr
         raise MlaDecodeError(rc, "mla_decode_run")
 
 
+def mla_decode_run_device_scales(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr,
+                                 total_q: int, bmm1_scale, bmm2_scale, out, lse, workspace,
+                                 workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """``mla_decode_run`` with the two scales read from device memory at run
+    time (``bmm1_scale`` / ``bmm2_scale``: one-element fp32 CUDA tensors or
+    raw device pointers), so a captured graph sees new values at every replay."""
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    for t in (bmm1_scale, bmm2_scale):
+        if isinstance(t, torch.Tensor) and (t.dtype != torch.float32 or not t.is_cuda
+                                            or t.numel() != 1):
+            raise TypeError("device scales must be one-element fp32 CUDA tensors")
+    rc = lib.mla_decode_run_device_scales(
+        ctypes.c_void_p(plan), _ptr(query), _ptr(kv_cache), _ptr(block_tables), _ptr(seq_lens),
+        _ptr(qo_indptr), int(total_q), _ptr(bmm1_scale), _ptr(bmm2_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), int(workspace_bytes), stream)
+    if rc != 0:
+        raise MlaDecodeError(rc, "mla_decode_run_device_scales")
+
+
 def mla_decode_run_profiled(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr,
                             total_q: int, bmm1_scale: float, bmm2_scale: float, out, lse,
                             workspace, workspace_bytes: Optional[int] = None, stream=None,
@@ -205,6 +233,13 @@ class Plan:
 
     def run(self, query, kv_cache, block_tables, seq_lens, out, *, qo_indptr=None, total_q=0,
             lse=None, workspace=None, bmm1_scale=1.0, bmm2_scale=1.0, stream=None):
+        """Scales are Python floats, or one-element fp32 CUDA tensors (then both
+        must be, and the kernels read them when they run)."""
+        if isinstance(bmm1_scale, torch.Tensor) or isinstance(bmm2_scale, torch.Tensor):
+            mla_decode_run_device_scales(self.handle, query, kv_cache, block_tables, seq_lens,
+                                         qo_indptr, total_q, bmm1_scale, bmm2_scale, out, lse,
+                                         workspace, None, stream)
+            return
         mla_decode_run(self.handle, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q,
                        bmm1_scale, bmm2_scale, out, lse, workspace, None, stream)
 
@@ -227,7 +262,7 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
            block_tables: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, *,
            qo_indptr: Optional[torch.Tensor] = None, max_seq_len_q: Optional[int] = None,
            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-           bmm1_scale: float = 1.0, bmm2_scale: float = 1.0, mask_type: str = "causal",
+           bmm1_scale=1.0, bmm2_scale=1.0, mask_type: str = "causal",
            return_lse: bool = False):
     """Paged MLA decode.  Returns ``out`` (and ``lse`` when ``return_lse``).
 
@@ -235,6 +270,8 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
     ``kv_cache``: bf16 or float8_e4m3fn, ``[pages, page_size, 576]`` or
     ``[pages, 1, page_size, 576]``.  ``workspace_buffer`` must hold at least
     the plan's workspace bytes (see ``Plan``).  Plans are cached per static key.
+    ``bmm1_scale`` / ``bmm2_scale``: floats, or one-element fp32 CUDA tensors the
+    kernels read at run time (for scales that change between graph replays).
     """
     if query.dtype != torch.bfloat16 or not query.is_cuda:
         raise ValueError("query must be a bf16 CUDA tensor")

@@ -135,12 +135,18 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   return MLA_OK;
 }
 
-int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const void* kv_cache,
-                            const int32_t* block_tables, const int32_t* seq_lens,
-                            const int32_t* qo_indptr, int64_t total_q, float bmm1_scale,
-                            float bmm2_scale, void* out, float* lse, void* workspace,
-                            size_t workspace_bytes, void* stream, void* event_before_decode,
-                            void* event_after_decode) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the run entry points.  Device scales (bmm1_dev / bmm2_dev
+// non-null) replace the host values and are read by the kernels.
+int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
+             const int32_t* block_tables, const int32_t* seq_lens, const int32_t* qo_indptr,
+             int64_t total_q, float bmm1_scale, float bmm2_scale, const float* bmm1_dev,
+             const float* bmm2_dev, void* out, float* lse, void* workspace,
+             size_t workspace_bytes, void* stream, void* event_before_decode,
+             void* event_after_decode) {
   if (!plan) return MLA_ERR_INVALID_ARG;
   const mla_decode_params& prm = plan->prm;
   if (prm.batch == 0) return MLA_OK;
@@ -148,7 +154,9 @@ int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const voi
     return MLA_ERR_INVALID_ARG;
   if (prm.return_lse && !lse) return MLA_ERR_INVALID_ARG;
   // the kernel takes the running max of raw scores and scales it afterwards
-  if (!(bmm1_scale >= 0.f) || bmm1_scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
+  if (!bmm1_dev && (!(bmm1_scale >= 0.f) || bmm1_scale > 3.0e38f)) return MLA_ERR_INVALID_ARG;
+  if ((bmm1_dev && !aligned(bmm1_dev, 4)) || (bmm2_dev && !aligned(bmm2_dev, 4)))
+    return MLA_ERR_ALIGNMENT;
   if (prm.packed) {
     if (!qo_indptr || total_q < 0 || total_q > prm.max_total_q) return MLA_ERR_INVALID_ARG;
   } else if (qo_indptr) {
@@ -175,6 +183,8 @@ int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const voi
   p.total_q = prm.packed ? total_q : (long long)prm.batch * prm.max_seq_len_q;
   p.bmm1_scale = bmm1_scale;
   p.bmm2_scale = bmm2_scale;
+  p.bmm1_dev = bmm1_dev;
+  p.bmm2_dev = bmm2_dev;
   p.query = query;
   p.kv_cache = kv_cache;
   p.block_tables = block_tables;
@@ -205,6 +215,33 @@ int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const voi
   if (mla::launch_combine(p, plan->lay, workspace, plan->combine_grid, s) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const void* kv_cache,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* qo_indptr, int64_t total_q, float bmm1_scale,
+                            float bmm2_scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream, void* event_before_decode,
+                            void* event_after_decode) {
+  return run_impl(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q, bmm1_scale,
+                  bmm2_scale, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream,
+                  event_before_decode, event_after_decode);
+}
+
+int mla_decode_run_device_scales(const mla_plan_t* plan, const void* query, const void* kv_cache,
+                                 const int32_t* block_tables, const int32_t* seq_lens,
+                                 const int32_t* qo_indptr, int64_t total_q,
+                                 const float* bmm1_scale, const float* bmm2_scale, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (!bmm1_scale || !bmm2_scale) return MLA_ERR_INVALID_ARG;
+  return run_impl(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q, 0.f, 0.f,
+                  bmm1_scale, bmm2_scale, out, lse, workspace, workspace_bytes, stream, nullptr,
+                  nullptr);
 }
 
 int mla_decode_run(const mla_plan_t* plan, const void* query, const void* kv_cache,

@@ -86,7 +86,7 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
       }
       m = m_new;
     }
-    const float s2 = sum > 0.f ? p.bmm2_scale / sum : 0.f;
+    const float s2 = sum > 0.f ? run_bmm2(p) / sum : 0.f;
     const size_t grow = (size_t)c.q_start * H + (size_t)c.g * R + r;
     __nv_bfloat162 o[8];
 #pragma unroll

@@ -17,11 +17,17 @@ constexpr int kKvTile = 64;       // KV rows per pipeline tile
 // Largest partitioner scratch kept in shared memory (else in the workspace).
 constexpr size_t kPartitionSmemMax = 160 * 1024;
 
+// Status word bits (workspace header word kHdrStatus).
+constexpr int kStatusSeqLen = 1, kStatusQLen = 2, kStatusCausal = 4, kStatusCapacity = 8,
+              kStatusPage = 16, kStatusTimeout = 32, kStatusScale = 64;
+
 struct Problem {
   int batch, num_heads, max_q, max_seq_len, page_size, max_pages;
   int packed, kv_dtype, causal, return_lse;
   long long num_pages, total_q;  // total_q: rows of the query tensor (tokens)
   float bmm1_scale, bmm2_scale;
+  const float* bmm1_dev;         // non-null: read bmm1 from device memory at run time
+  const float* bmm2_dev;         // non-null: read bmm2 from device memory at run time
   const void* query;             // bf16 [tokens, H, 576]
   const void* kv_cache;          // bf16 or e4m3 [num_pages, page_size, 576]
   const int* block_tables;       // [B, max_pages]
@@ -30,6 +36,19 @@ struct Problem {
   void* out;                     // bf16 [tokens, H, 512]
   float* lse;                    // fp32 [tokens, H] or nullptr
 };
+
+// bmm1 of this run: the host value, or the device value when one was given.
+// A negative or non-finite device value sets kStatusScale and reads as 0.
+__device__ __forceinline__ float run_bmm1(const Problem& p, int* status) {
+  if (!p.bmm1_dev) return p.bmm1_scale;
+  const float v = *p.bmm1_dev;
+  if (v >= 0.f && v <= 3.0e38f) return v;
+  atomicOr(status, kStatusScale);
+  return 0.f;
+}
+__device__ __forceinline__ float run_bmm2(const Problem& p) {
+  return p.bmm2_dev ? *p.bmm2_dev : p.bmm2_scale;
+}
 
 // One unit of work of the decode kernel: query rows [R g, R g + R) of request
 // b (R = Layout::rows_per_group, clipped to its q_len * H rows) against KV rows

@@ -144,7 +144,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int bar, uint32_t parity)
     if ((i & 1023) == 1023 && *c.abort) return false;
   }
   *c.abort = 1;
-  atomicOr(c.status, 32);
+  atomicOr(c.status, kStatusTimeout);
   return false;
 }
 
@@ -155,7 +155,7 @@ __device__ __forceinline__ bool wait_bar_cluster(const Ctx& c, int bar, uint32_t
     if ((i & 1023) == 1023 && *c.abort) return false;
   }
   *c.abort = 1;
-  atomicOr(c.status, 32);
+  atomicOr(c.status, kStatusTimeout);
   return false;
 }
 
@@ -294,7 +294,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               continue;
             }
             if (pages[pg] < 0 || (long long)pages[pg] >= p.num_pages) {
-              atomicOr(c.status, 16);
+              atomicOr(c.status, kStatusPage);
               pages[pg] = -1;
               continue;
             }
@@ -421,7 +421,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           } else if (++idle > kWaitLimit || ((idle & 1023) == 0 && *c.abort)) {
             if (idle > kWaitLimit) {
               *c.abort = 1;
-              atomicOr(c.status, 32);
+              atomicOr(c.status, kStatusTimeout);
             }
             goto done_mma;
           }
@@ -444,7 +444,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const uint32_t lane_addr = (uint32_t)(32 * sp + 16 * (int)rank) << 16;
     const bool designated = warp == 2 && lane == 0;
     const int sm_tid = (warp - 2) * 32 + lane;
-    const float scale = p.bmm1_scale * kLog2e;
+    const float scale = run_bmm1(p, c.status) * kLog2e;
     float* mx = reinterpret_cast<float*>(sm + OFF_MX);  // [parity][hw][lane]
     float* lx = reinterpret_cast<float*>(sm + OFF_LX);  // [hw][lane]
     const uint32_t xfree_peer0 = map_to_rank(smem_u32(&c.bars[PEER_X_FREE0]), peer);
@@ -515,15 +515,18 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         float f = 1.f;
         bool need = false;
         float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 chains for ILP
+        // tiles with masked columns are scaled before the -inf mask goes in,
+        // so that bmm1 = 0 never multiplies -inf (the same for the whole tile)
+        const bool pre_scaled = j0 + kTile > clean_end;
         if (row_ok) {
-          if (j0 + kTile <= clean_end) {
+          if (!pre_scaled) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const int col = c0 + j;
-              sv[j] = (col <= last && col < it.kv_end) ? sv[j] : -INFINITY;
+              sv[j] = (col <= last && col < it.kv_end) ? sv[j] * scale : -INFINITY;
               tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
             }
           }
@@ -542,7 +545,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           tmax = fmaxf(tmax, slot[(hw ^ 1) * kRows + q]);
         }
         if (row_ok) {
-          const float m_new = fmaxf(m_ref, tmax * scale);
+          const float sc = pre_scaled ? 1.f : scale;  // what the scores still need
+          const float m_new = fmaxf(m_ref, tmax * sc);
           if (t == 0) {
             m_ref = m_new;
           } else if (m_new > m_ref + kRescaleThreshold) {
@@ -555,7 +559,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            sv[j] = ex2(fmaf(sv[j], scale, -m_use));
+            sv[j] = ex2(fmaf(sv[j], sc, -m_use));
             rs[j & 3] += sv[j];
           }
           l_part += (rs[0] + rs[1]) + (rs[2] + rs[3]);
@@ -699,6 +703,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     // TMEM, where they are the A operand of the ts QK MMAs.  Called only when
     // no QK of an earlier item is pending.
     const long long q_rows = p.total_q * H;
+    const float bmm2 = run_bmm2(p);
     auto write_q = [&](const WorkItem& it) {
       const long long qrow = (long long)it.q_start * H + (long long)it.g * kRows + q;
       const bool in = qrow < q_rows;
@@ -792,7 +797,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           if (!row_ok) continue;
           const int vd = 256 * (int)rank + 16 * c16;  // first output V dim of this chunk
           if (it.slot < 0) {
-            const float s2 = inv * p.bmm2_scale;
+            const float s2 = inv * bmm2;
             uint32_t o[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k)

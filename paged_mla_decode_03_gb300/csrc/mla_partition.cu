@@ -170,7 +170,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     if (p.packed) {
       int lo = p.qo_indptr[b], hi = p.qo_indptr[b + 1];
       const int tq = (int)p.total_q;
-      if (lo < 0 || hi > tq || hi - lo < 1 || hi - lo > p.max_q) status |= 2;
+      if (lo < 0 || hi > tq || hi - lo < 1 || hi - lo > p.max_q) status |= kStatusQLen;
       lo = min(max(lo, 0), tq);
       hi = min(max(hi, lo), tq);
       q = min(hi - lo, p.max_q);
@@ -180,9 +180,9 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
       qs = b * p.max_q;
     }
     int L = p.seq_lens[b];
-    if (L < 1 || L > p.max_seq_len) status |= 1;
+    if (L < 1 || L > p.max_seq_len) status |= kStatusSeqLen;
     L = min(max(L, 0), p.max_seq_len);
-    if (p.causal && q > L) status |= 4;
+    if (p.causal && q > L) status |= kStatusCausal;
     r_qlen[b] = q;
     r_qstart[b] = qs;
     r_len[b] = L;
@@ -201,7 +201,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   __syncthreads();
   int n_groups = block_exclusive_scan(r_gbase, B, sh);
   if (n_groups > lay.max_groups) {  // unreachable within the contract
-    status |= 8;
+    status |= kStatusCapacity;
     n_groups = 0;
   }
 
@@ -265,7 +265,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   const int n_partials = block_exclusive_scan(g_slot, n_groups, sh);
   const int n_combine = block_exclusive_scan(g_comb, n_groups, sh);
   if (n_items > lay.max_items || n_partials > lay.max_partials || n_combine > lay.max_combine) {
-    status |= 8;  // unreachable within the contract
+    status |= kStatusCapacity;  // unreachable within the contract
     n_items = 0;
   }
 

@@ -90,6 +90,8 @@ def test_null_arguments_are_rejected(lib):
     assert lib.mla_decode_plan(None, None, None) == -1
     assert lib.mla_decode_run(None, None, None, None, None, None, 0, 1.0, 1.0, None, None, None,
                               0, None) == -1
+    assert lib.mla_decode_run_device_scales(None, None, None, None, None, None, 0, None, None,
+                                            None, None, None, 0, None) == -1
     lib.mla_decode_destroy(None)
     assert lib.mla_decode_workspace_size(None) == 0
 

@@ -352,3 +352,68 @@ def test_ragged_request_equals_its_own_single_request_launch():
         # the two launches may cut the KV range differently: equal to rounding
         assert np.abs(o1 - ob).max() <= 4e-3 + 1e-2 * np.abs(ob).max(), b
         assert np.abs(l1 - lb).max() <= 1e-3, b
+
+
+def test_device_scales_equal_host_scales_and_follow_graph_replays():
+    """mla_decode_run_device_scales reads bmm1/bmm2 from device memory when the
+    kernels run: with the same values it is bitwise equal to the by-value
+    run, and a captured graph picks up new values at every replay."""
+    w = REDUCED["deepseek_v3"]()
+    w.return_lse = True
+    d = to_device(w)
+    dev = torch.device("cuda", 0)
+
+    def host_run(b1, b2):
+        d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=d.lse,
+                   workspace=d.workspace, bmm1_scale=b1, bmm2_scale=b2)
+        torch.cuda.synchronize()
+        return d.out.clone(), d.lse.clone()
+
+    s1 = torch.tensor([w.bmm1_scale], dtype=torch.float32, device=dev)
+    s2 = torch.tensor([w.bmm2_scale], dtype=torch.float32, device=dev)
+    o_ref, l_ref = host_run(w.bmm1_scale, w.bmm2_scale)
+    d.out.fill_(float("nan"))
+    d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=d.lse,
+               workspace=d.workspace, bmm1_scale=s1, bmm2_scale=s2)
+    torch.cuda.synchronize()
+    assert torch.equal(d.out.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(d.lse, l_ref)
+    assert device_status(d) == 0
+
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=d.lse,
+                   workspace=d.workspace, bmm1_scale=s1, bmm2_scale=s2, stream=stream)
+    for b1, b2 in [(0.03125, 2.0), (0.1, 0.5), (0.0, 1.0)]:
+        s1.fill_(b1)
+        s2.fill_(b2)
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        o_g, l_g = d.out.clone(), d.lse.clone()
+        o_h, l_h = host_run(b1, b2)
+        assert torch.equal(o_g.view(torch.int16), o_h.view(torch.int16)), (b1, b2)
+        assert torch.equal(l_g, l_h), (b1, b2)
+
+
+def test_invalid_device_bmm1_sets_status_bit_without_faulting():
+    w = REDUCED["tiny"]()
+    d = to_device(w)
+    dev = torch.device("cuda", 0)
+    s1 = torch.tensor([-1.0], dtype=torch.float32, device=dev)
+    s2 = torch.tensor([1.0], dtype=torch.float32, device=dev)
+    d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, lse=d.lse,
+               workspace=d.workspace, bmm1_scale=s1, bmm2_scale=s2)
+    assert device_status(d) & 64
+    out, _ = results(d)
+    assert np.isfinite(out).all()  # read as bmm1 = 0: the mean of the visible V rows
+
+
+@pytest.mark.parametrize("name", ["tiny", "mtp"])
+def test_zero_bmm1_gives_the_mean_of_the_visible_rows(name):
+    """bmm1 = 0 is within the contract: every visible score is 0, so each row
+    returns the mean of its visible V rows (also on masked tiles)."""
+    w = REDUCED[name]()
+    w.bmm1_scale = 0.0
+    full_parity(w)
