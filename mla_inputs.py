@@ -56,13 +56,16 @@ class Workload:
     seq_lens: np.ndarray               # [B] int32
     max_seq_len_q: int
     max_seq_len: int
-    query: np.ndarray                  # uint16 bf16 bits, [B,SQ,H,576] or [total_q,H,576]
+    query: np.ndarray                  # uint16 bf16 bits or uint8 e4m3 codes (q_dtype),
+                                       # [B,SQ,H,576] or [total_q,H,576]
     qo_indptr: Optional[np.ndarray]    # [B+1] int32 when packed
     kv_cache: np.ndarray               # uint16 (bf16) or uint8 (e4m3), [pages, ps, 576]
     block_tables: np.ndarray           # [B, max_pages_per_req] int32
     bmm1_scale: float                  # exactly representable in fp32
     bmm2_scale: float
     k_scale: Optional[float] = None
+    q_dtype: str = "bf16"              # "bf16" or "e4m3" (query quantised, q_scale in bmm1)
+    q_scale: Optional[float] = None
 
     @property
     def total_q(self) -> int:
@@ -116,7 +119,7 @@ def build(name: str, seed: int, *, num_heads: int, page_size: int,
           bmm2_scale: float = 1.0, num_pages: Optional[int] = None,
           block_tables: Optional[np.ndarray] = None, poison: bool = True,
           max_seq_len_q: Optional[int] = None, max_seq_len: Optional[int] = None,
-          rng: Optional[np.random.Generator] = None) -> Workload:
+          rng: Optional[np.random.Generator] = None, q_dtype: str = "bf16") -> Workload:
     """Draw one workload.  Draw order: pool permutation, query, KV values."""
     rng = rng if rng is not None else np.random.default_rng(seed)
     seq_lens = np.asarray(seq_lens, dtype=np.int32)
@@ -158,7 +161,18 @@ def build(name: str, seed: int, *, num_heads: int, page_size: int,
         qo_indptr = None
         sq = int(q_lens[0]) if B else int(max_seq_len_q or 1)
         qshape = (B, sq, H, HEAD_DIM_QK)
-    query = bf16_bits(_normal(rng, qshape))
+    q32 = _normal(rng, qshape)
+    q_scale = None
+    if q_dtype == "bf16":
+        query = bf16_bits(q32)
+    elif q_dtype == "e4m3":
+        # per-tensor q_scale = amax / 448, folded into bmm1 (as for k_scale)
+        q_scale = f32(float(np.abs(q32).max()) / E4M3_MAX) if q32.size else 1.0
+        query = e4m3_bits(q32 / np.float32(q_scale))
+        bmm1_scale = bmm1_scale * q_scale
+    else:
+        raise ValueError(q_dtype)
+    del q32
 
     kv32 = _normal(rng, (pool, ps, HEAD_DIM_QK))
     used = np.zeros((pool, ps), dtype=bool)
@@ -192,7 +206,8 @@ def build(name: str, seed: int, *, num_heads: int, page_size: int,
         max_seq_len_q=sq,
         max_seq_len=int(max_seq_len if max_seq_len is not None else (seq_lens.max() if B else 1)),
         query=query, qo_indptr=qo_indptr, kv_cache=kv, block_tables=block_tables,
-        bmm1_scale=f32(bmm1_scale), bmm2_scale=f32(bmm2_scale), k_scale=k_scale)
+        bmm1_scale=f32(bmm1_scale), bmm2_scale=f32(bmm2_scale), k_scale=k_scale,
+        q_dtype=q_dtype, q_scale=q_scale)
 
 
 # ---------------------------------------------------------------------------

@@ -63,6 +63,13 @@ def _load():
             ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
             ctypes.c_double, ctypes.c_double, ctypes.c_int64, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_mla_decode_q.restype = ctypes.c_int
+        lib.oracle_mla_decode_q.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+            ctypes.c_double, ctypes.c_double, ctypes.c_int64, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
@@ -89,10 +96,12 @@ def default_threads() -> int:
 def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
                block_tables: np.ndarray, seq_lens: np.ndarray, *, kv_dtype: str,
                causal: bool, bmm1_scale: float, bmm2_scale: float,
-               sel: Optional[np.ndarray] = None, n_threads: Optional[int] = None):
+               sel: Optional[np.ndarray] = None, n_threads: Optional[int] = None,
+               q_dtype: str = "bf16"):
     """fp64 O and LSE.
 
-    query:   uint16 bf16 bits viewed as [tokens, H, 576]
+    query:   uint16 bf16 bits (q_dtype "bf16") or uint8 e4m3 codes ("e4m3")
+             viewed as [tokens, H, 576]
     q_start: [B+1] token offset of each request (fixed launches: b * SQ)
     kv_cache: uint16 (bf16) or uint8 (e4m3) [pages, page_size, 576]
     sel:     optional [n, 2] (token, head) pairs; default every pair.
@@ -100,7 +109,15 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
     """
     lib = _load()
     H = int(query.shape[-2])
-    q = np.ascontiguousarray(query.reshape(-1, H, QK_DIM), dtype=np.uint16)
+    if q_dtype == "bf16":
+        assert query.dtype == np.uint16
+        qd = 0
+    elif q_dtype == "e4m3":
+        assert query.dtype == np.uint8
+        qd = 1
+    else:
+        raise ValueError(q_dtype)
+    q = np.ascontiguousarray(query.reshape(-1, H, QK_DIM))
     qs = np.ascontiguousarray(q_start, dtype=np.int64)
     kv = np.ascontiguousarray(kv_cache)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
@@ -127,8 +144,8 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
     lse = np.zeros(lse_shape, dtype=np.float64)
     if n == 0 or B == 0:
         return out, lse
-    rc = lib.oracle_mla_decode(
-        B, H, kd, q.ctypes.data, qs.ctypes.data, kv.ctypes.data, int(kv.shape[0]),
+    rc = lib.oracle_mla_decode_q(
+        B, H, kd, qd, q.ctypes.data, qs.ctypes.data, kv.ctypes.data, int(kv.shape[0]),
         int(kv.shape[1]), bt.ctypes.data, int(bt.shape[1]), sl.ctypes.data, int(bool(causal)),
         float(bmm1_scale), float(bmm2_scale), n,
         sel_arr.ctypes.data if sel_arr is not None else None,
@@ -144,4 +161,4 @@ def run(w, sel: Optional[np.ndarray] = None, n_threads: Optional[int] = None,
     return mla_decode(w.query_rows(), w.q_start(), w.kv_cache, w.block_tables, w.seq_lens,
                       kv_dtype=w.kv_dtype, causal=w.causal if causal is None else causal,
                       bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, sel=sel,
-                      n_threads=n_threads)
+                      n_threads=n_threads, q_dtype=getattr(w, "q_dtype", "bf16"))

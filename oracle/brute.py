@@ -33,9 +33,10 @@ def e4m3_value(bits: int) -> float:
 
 
 def mla_decode(query, q_start, kv_cache, block_tables, seq_lens, *, kv_dtype, causal,
-               bmm1_scale, bmm2_scale):
+               bmm1_scale, bmm2_scale, q_dtype="bf16"):
     """Return (out[tokens][H][512], lse[tokens][H]) as nested Python lists."""
     decode = bf16_value if kv_dtype == "bf16" else e4m3_value
+    q_decode = bf16_value if q_dtype == "bf16" else e4m3_value
     tokens, H, D = query.shape
     ps = kv_cache.shape[1]
     out = [[None] * H for _ in range(tokens)]
@@ -51,7 +52,7 @@ def mla_decode(query, q_start, kv_cache, block_tables, seq_lens, *, kv_dtype, ca
         for i in range(q):
             visible = [j for j in range(L) if (j - (L - q) <= i if causal else True)]
             for h in range(H):
-                qv = [bf16_value(x) for x in query[t0 + i][h]]
+                qv = [q_decode(x) for x in query[t0 + i][h]]
                 s = [bmm1_scale * math.fsum(qv[d] * rows[j][d] for d in range(D))
                      for j in visible]
                 mx = max(s)

@@ -17,7 +17,10 @@
  *             as the vLLM FlashInferMLAImpl page states for its LSE)
  *     O[:]  = bmm2_scale * sum_j exp(s_j - lse) * V_b[j][:]
  *
- * Everything is accumulated in double.  bf16 and e4m3 inputs are decoded
+ * Everything is accumulated in double.  bf16 and e4m3 inputs (the cache,
+ * and the query, which is e4m3 when the caller quantised it with a q_scale
+ * folded into bmm1, as the FlashInfer pull request "dynamic scale factor
+ * interface and one-copy kvcache on trtllm-gen mla" describes) are decoded
  * exactly from their bit patterns (both formats are subsets of double).
  * Work is split over (query token, head) pairs with POSIX threads; each pair
  * is computed independently, so the thread count never changes a result.
@@ -31,7 +34,7 @@
 #define QK_DIM 576
 #define V_DIM 512
 
-enum { ORACLE_KV_BF16 = 0, ORACLE_KV_E4M3 = 1 };
+enum { ORACLE_KV_BF16 = 0, ORACLE_KV_E4M3 = 1 };  /* also the query's element type */
 
 /* bf16 -> double: a bf16 is the upper half of an IEEE binary32. */
 static double bf16_to_double(uint16_t bits) {
@@ -60,8 +63,8 @@ double oracle_decode_bf16(uint16_t bits) { return bf16_to_double(bits); }
 double oracle_decode_e4m3(uint8_t bits) { return e4m3_to_double(bits); }
 
 typedef struct {
-  int batch, num_heads, kv_dtype, page_size, max_pages_per_req, causal;
-  const uint16_t *query;     /* [tokens, H, 576] bf16 bits */
+  int batch, num_heads, kv_dtype, q_dtype, page_size, max_pages_per_req, causal;
+  const void *query;         /* [tokens, H, 576] bf16 bits or e4m3 codes (q_dtype) */
   const int64_t *q_start;    /* [B + 1] token offsets */
   const void *kv_cache;      /* [num_pages, ps, 576] */
   int64_t num_pages;
@@ -105,8 +108,11 @@ static int one_unit(job_t *J, int64_t u, double *s, double *qv) {
   if (last > L - 1) last = L - 1;
   int64_t n = last + 1;
   double *o = J->out + u * V_DIM;
-  for (int d = 0; d < QK_DIM; ++d)
-    qv[d] = bf16_to_double(J->query[(t * J->num_heads + h) * QK_DIM + d]);
+  for (int d = 0; d < QK_DIM; ++d) {
+    const int64_t off = (t * J->num_heads + h) * QK_DIM + d;
+    qv[d] = J->q_dtype == ORACLE_KV_BF16 ? bf16_to_double(((const uint16_t *)J->query)[off])
+                                         : e4m3_to_double(((const uint8_t *)J->query)[off]);
+  }
 
   if (n <= 0) {  /* nothing visible: empty sum (a contract violation) */
     for (int d = 0; d < V_DIM; ++d) o[d] = 0.0;
@@ -172,17 +178,17 @@ static void *worker(void *arg) {
  * sel == NULL, in [token][head] order).  Returns 0 on success, 1 if a page
  * id read for a visible row was out of range, 2 on allocation failure.
  */
-int oracle_mla_decode(int batch, int num_heads, int kv_dtype,
-                      const uint16_t *query, const int64_t *q_start,
-                      const void *kv_cache, int64_t num_pages, int page_size,
-                      const int32_t *block_tables, int max_pages_per_req,
-                      const int32_t *seq_lens, int causal,
-                      double bmm1_scale, double bmm2_scale,
-                      int64_t n_sel, const int64_t *sel,
-                      double *out, double *lse, int n_threads) {
+int oracle_mla_decode_q(int batch, int num_heads, int kv_dtype, int q_dtype,
+                        const void *query, const int64_t *q_start,
+                        const void *kv_cache, int64_t num_pages, int page_size,
+                        const int32_t *block_tables, int max_pages_per_req,
+                        const int32_t *seq_lens, int causal,
+                        double bmm1_scale, double bmm2_scale,
+                        int64_t n_sel, const int64_t *sel,
+                        double *out, double *lse, int n_threads) {
   job_t J;
   memset(&J, 0, sizeof J);
-  J.batch = batch; J.num_heads = num_heads; J.kv_dtype = kv_dtype;
+  J.batch = batch; J.num_heads = num_heads; J.kv_dtype = kv_dtype; J.q_dtype = q_dtype;
   J.page_size = page_size; J.max_pages_per_req = max_pages_per_req; J.causal = causal;
   J.query = query; J.q_start = q_start; J.kv_cache = kv_cache; J.num_pages = num_pages;
   J.block_tables = block_tables; J.seq_lens = seq_lens;
@@ -201,4 +207,18 @@ int oracle_mla_decode(int batch, int num_heads, int kv_dtype,
   for (int k = 0; k < started; ++k) pthread_join(th[k], NULL);
   pthread_mutex_destroy(&J.lock);
   return J.status;
+}
+
+/* The same with a bf16 query. */
+int oracle_mla_decode(int batch, int num_heads, int kv_dtype,
+                      const uint16_t *query, const int64_t *q_start,
+                      const void *kv_cache, int64_t num_pages, int page_size,
+                      const int32_t *block_tables, int max_pages_per_req,
+                      const int32_t *seq_lens, int causal,
+                      double bmm1_scale, double bmm2_scale,
+                      int64_t n_sel, const int64_t *sel,
+                      double *out, double *lse, int n_threads) {
+  return oracle_mla_decode_q(batch, num_heads, kv_dtype, ORACLE_KV_BF16, query, q_start, kv_cache,
+                             num_pages, page_size, block_tables, max_pages_per_req, seq_lens,
+                             causal, bmm1_scale, bmm2_scale, n_sel, sel, out, lse, n_threads);
 }

@@ -18,10 +18,11 @@ from oracle import brute
 
 
 def small(seed, *, H=2, ps=4, seq_lens=(9, 5), q_lens=(1, 1), packed=False, causal=True,
-          kv_dtype="bf16", bmm1=0.125, bmm2=1.0, poison=True):
+          kv_dtype="bf16", bmm1=0.125, bmm2=1.0, poison=True, q_dtype="bf16"):
     return mi.build("pin", seed, num_heads=H, page_size=ps, seq_lens=list(seq_lens),
                     q_lens=list(q_lens), packed=packed, causal=causal, kv_dtype=kv_dtype,
-                    bmm1_scale=bmm1, bmm2_scale=bmm2, poison=poison, return_lse=True)
+                    bmm1_scale=bmm1, bmm2_scale=bmm2, poison=poison, return_lse=True,
+                    q_dtype=q_dtype)
 
 
 def as_f64(bits, kv_dtype="bf16"):
@@ -71,13 +72,16 @@ def test_e4m3_decoder_matches_torch_all_codes():
     dict(seq_lens=(6, 3, 11), q_lens=(2, 3, 1), packed=True),
     dict(seq_lens=(10, 4), q_lens=(2, 2), kv_dtype="e4m3", bmm1=0.5, bmm2=0.75),
     dict(seq_lens=(13,), q_lens=(4,), ps=8, bmm1=3.0),
+    dict(seq_lens=(8, 11), q_lens=(2, 2), q_dtype="e4m3", bmm1=0.5),
+    dict(seq_lens=(9, 6), q_lens=(1, 1), q_dtype="e4m3", kv_dtype="e4m3", bmm1=4.0),
 ])
 def test_c_oracle_matches_python_brute_force(case):
     w = small(7, **case)
     out, lse = oracle.run(w)
     bo, bl = brute.mla_decode(w.query_rows(), w.q_start(), w.kv_cache, w.block_tables,
                               w.seq_lens, kv_dtype=w.kv_dtype, causal=w.causal,
-                              bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale)
+                              bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
+                              q_dtype=w.q_dtype)
     np.testing.assert_allclose(out, np.array(bo), rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(lse, np.array(bl), rtol=1e-12, atol=1e-12)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
@@ -326,3 +330,29 @@ def test_tiny_workload_matches_recorded_oracle_output():
     out, lse = oracle.run(w)
     np.testing.assert_allclose(lse, np.array(doc["lse"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(out[..., doc["out_dims"]], np.array(doc["out"]), rtol=0, atol=1e-12)
+
+
+def test_e4m3_query_equals_the_same_values_as_bf16():
+    """Every e4m3 value is a bf16 value: an e4m3 query and the bf16 query
+    holding the decoded values give bitwise-equal oracle outputs, so the query
+    decoding is the only thing an e4m3 query changes."""
+    w = small(11, H=3, seq_lens=(9, 14), q_lens=(2, 2), q_dtype="e4m3", bmm1=0.7)
+    assert w.query.dtype == np.uint8 and w.q_scale is not None
+    out8, lse8 = oracle.run(w)
+    vals = as_f64(w.query, "e4m3")
+    wb = dataclasses.replace(w, query=mi.bf16_bits(vals.astype(np.float32)), q_dtype="bf16")
+    assert np.array_equal(as_f64(wb.query), vals)  # exact in bf16
+    out16, lse16 = oracle.run(wb)
+    assert np.array_equal(out8, out16) and np.array_equal(lse8, lse16)
+
+
+def test_e4m3_query_quantisation_folds_q_scale_into_bmm1():
+    """q_scale = amax / 448 maps the largest |q| to 448 and is folded into
+    bmm1, so scores use the dequantised query: q_scale * e4m3(q / q_scale)."""
+    wb = small(12, seq_lens=(7,), q_lens=(1,), bmm1=0.25)
+    w8 = small(12, seq_lens=(7,), q_lens=(1,), bmm1=0.25, q_dtype="e4m3")
+    q = as_f64(wb.query)
+    assert np.abs(as_f64(w8.query, "e4m3")).max() == 448.0
+    assert w8.bmm1_scale == np.float32(0.25 * w8.q_scale)
+    deq = as_f64(w8.query, "e4m3") * w8.q_scale
+    assert np.abs(deq - q).max() <= 2.0 ** -4 * np.abs(q).max()  # e4m3 keeps 3 mantissa bits
