@@ -55,6 +55,7 @@ typedef enum {
 
 typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 typedef enum { MLA_MASK_CAUSAL = 0, MLA_MASK_DENSE = 1 } mla_mask;
+typedef enum { MLA_Q_BF16 = 0, MLA_Q_FP8_E4M3 = 1 } mla_q_dtype;
 
 /*
  * Static parameters of a launch (the "semantic key" of the problem
@@ -77,6 +78,8 @@ typedef struct mla_decode_params {
   int32_t mask;              /* mla_mask */
   int32_t return_lse;        /* nonzero: mla_decode_run writes lse */
   int32_t device;            /* CUDA device ordinal the plan is for */
+  int32_t q_dtype;           /* mla_q_dtype: bf16, or e4m3 with the caller's q_scale
+                                folded into bmm1 (bmm1 = q_scale * k_scale * softmax scale) */
 } mla_decode_params;
 
 typedef struct mla_plan_s mla_plan_t; /* opaque; host memory only */
@@ -95,7 +98,8 @@ int mla_decode_plan(const mla_decode_params *params, mla_plan_t **plan,
 /*
  * Enqueue one decode on `stream` (a cudaStream_t; NULL = legacy default).
  *
- * query        bf16, fixed [B, SQ, H, 576] or packed [total_q, H, 576], contiguous.
+ * query        bf16 or fp8-e4m3 (per params.q_dtype), fixed [B, SQ, H, 576] or
+ *              packed [total_q, H, 576], contiguous.
  * kv_cache     bf16 or fp8-e4m3 (per params.kv_dtype), [num_pages, page_size, 576]
  *              (a rank-4 [num_pages, 1, page_size, 576] cache is the same memory).
  * block_tables int32 [B, max_pages_per_req]; entries at or past a request's

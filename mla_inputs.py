@@ -231,23 +231,24 @@ def _uniform_lens(rng, lo, hi, n):
 
 
 def deepseek_v3(seed: int = 1002, batch: int = 64, lo: int = 1024, hi: int = 8192,
-                return_lse: bool = False, poison: bool = True) -> Workload:
+                return_lse: bool = False, poison: bool = True, q_dtype: str = "bf16") -> Workload:
     """B=64, H=128, q_len=1, page_size 64, seq_lens ~ U[1024, 8192]."""
     rng = np.random.default_rng(seed)
     L = _uniform_lens(rng, lo, hi, batch)
     return build(f"deepseek_v3_b{batch}_h128_q1_ps64", seed, num_heads=128, page_size=64,
                  seq_lens=L, q_lens=np.ones(batch, np.int32), packed=False,
-                 return_lse=return_lse, poison=poison, rng=rng)
+                 return_lse=return_lse, poison=poison, rng=rng, q_dtype=q_dtype)
 
 
 def mtp(seed: int = 1003, batch: int = 32, lo: int = 2048, hi: int = 16384,
-        q_len: int = 4, return_lse: bool = False, poison: bool = True) -> Workload:
+        q_len: int = 4, return_lse: bool = False, poison: bool = True,
+        q_dtype: str = "bf16") -> Workload:
     """B=32, H=128, fixed q_len=4, bottom-right causal, seq_lens ~ U[2048, 16384]."""
     rng = np.random.default_rng(seed)
     L = _uniform_lens(rng, lo, hi, batch)
     return build(f"mtp_b{batch}_h128_q{q_len}_ps64", seed, num_heads=128, page_size=64,
                  seq_lens=L, q_lens=np.full(batch, q_len, np.int32), packed=False,
-                 return_lse=return_lse, poison=poison, rng=rng)
+                 return_lse=return_lse, poison=poison, rng=rng, q_dtype=q_dtype)
 
 
 def ragged(seed: int = 1004, batch: int = 128, median: float = 4096.0, sigma: float = 1.0,
@@ -265,14 +266,16 @@ def ragged(seed: int = 1004, batch: int = 128, median: float = 4096.0, sigma: fl
 
 
 def fp8_long(seed: int = 1005, batch: int = 8, lo: int = 65536, hi: int = 131072,
-             q_len: int = 2, return_lse: bool = False, poison: bool = True) -> Workload:
+             q_len: int = 2, return_lse: bool = False, poison: bool = True,
+             q_dtype: str = "bf16") -> Workload:
     """B=8, H=128, fixed q_len=2, page_size 64, seq_lens ~ U[65536, 131072],
     e4m3 KV with k_scale = amax/448 folded into bmm1 and bmm2."""
     rng = np.random.default_rng(seed)
     L = _uniform_lens(rng, lo, hi, batch)
     return build(f"fp8_long_b{batch}_h128_q{q_len}_ps64", seed, num_heads=128, page_size=64,
                  seq_lens=L, q_lens=np.full(batch, q_len, np.int32), packed=False,
-                 kv_dtype="e4m3", return_lse=return_lse, poison=poison, rng=rng)
+                 kv_dtype="e4m3", return_lse=return_lse, poison=poison, rng=rng,
+                 q_dtype=q_dtype)
 
 
 WORKLOADS = {

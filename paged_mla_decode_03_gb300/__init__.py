@@ -32,6 +32,7 @@ HEAD_DIM_V = 512
 MLA_OK = 0
 MLA_STATIC_WORKSPACE_BYTES = 48 * 1024 * 1024  # scratch of mla_decode_run_static_workspace
 KV_BF16, KV_FP8_E4M3 = 0, 1
+Q_BF16, Q_FP8_E4M3 = 0, 1
 MASK_CAUSAL, MASK_DENSE = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -61,6 +62,7 @@ class MlaDecodeParams(ctypes.Structure):
         ("mask", ctypes.c_int32),
         ("return_lse", ctypes.c_int32),
         ("device", ctypes.c_int32),
+        ("q_dtype", ctypes.c_int32),
     ]
 
 
@@ -221,14 +223,15 @@ class Plan:
     def __init__(self, *, batch: int, num_heads: int, max_seq_len_q: int, max_seq_len: int,
                  page_size: int, max_pages_per_req: int, num_pages: int, packed: bool,
                  max_total_q: int = 0, kv_dtype: str = "bf16", causal: bool = True,
-                 return_lse: bool = False, device: int = 0):
+                 return_lse: bool = False, device: int = 0, q_dtype: str = "bf16"):
         self.params = MlaDecodeParams(
             batch=batch, num_heads=num_heads, max_seq_len_q=max_seq_len_q,
             max_seq_len=max_seq_len, page_size=page_size, max_pages_per_req=max_pages_per_req,
             num_pages=num_pages, packed=int(bool(packed)), max_total_q=max_total_q,
             kv_dtype=KV_FP8_E4M3 if kv_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else KV_BF16,
             mask=MASK_CAUSAL if causal else MASK_DENSE, return_lse=int(bool(return_lse)),
-            device=device)
+            device=device,
+            q_dtype=Q_FP8_E4M3 if q_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else Q_BF16)
         self.handle, self.workspace_bytes = mla_decode_plan(self.params)
 
     def run(self, query, kv_cache, block_tables, seq_lens, out, *, qo_indptr=None, total_q=0,
@@ -266,15 +269,17 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
            return_lse: bool = False):
     """Paged MLA decode.  Returns ``out`` (and ``lse`` when ``return_lse``).
 
-    ``query``: bf16 ``[B, SQ, H, 576]`` (qo_indptr None) or ``[total_q, H, 576]``.
+    ``query``: bf16 or float8_e4m3fn (quantised with a q_scale the caller folds
+    into ``bmm1_scale``), ``[B, SQ, H, 576]`` (qo_indptr None) or ``[total_q, H, 576]``.
     ``kv_cache``: bf16 or float8_e4m3fn, ``[pages, page_size, 576]`` or
     ``[pages, 1, page_size, 576]``.  ``workspace_buffer`` must hold at least
     the plan's workspace bytes (see ``Plan``).  Plans are cached per static key.
     ``bmm1_scale`` / ``bmm2_scale``: floats, or one-element fp32 CUDA tensors the
     kernels read at run time (for scales that change between graph replays).
     """
-    if query.dtype != torch.bfloat16 or not query.is_cuda:
-        raise ValueError("query must be a bf16 CUDA tensor")
+    if query.dtype not in (torch.bfloat16, torch.float8_e4m3fn) or not query.is_cuda:
+        raise ValueError("query must be a bf16 or float8_e4m3fn CUDA tensor")
+    q_dtype = "bf16" if query.dtype == torch.bfloat16 else "e4m3"
     if kv_cache.dim() == 4:
         if kv_cache.shape[1] != 1:
             raise ValueError("rank-4 kv_cache must be [pages, 1, page_size, 576]")
@@ -307,14 +312,14 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
         raise ValueError(mask_type)
     key = (B, H, sq, int(max_seq_len), int(kv_cache.shape[1]), int(block_tables.shape[1]),
            int(kv_cache.shape[0]), packed, total_q if packed else 0, kv_dtype, causal,
-           bool(return_lse), query.device.index or 0)
+           bool(return_lse), query.device.index or 0, q_dtype)
     plan = _plans.get(key)
     if plan is None:
         plan = Plan(batch=B, num_heads=H, max_seq_len_q=sq, max_seq_len=int(max_seq_len),
                     page_size=int(kv_cache.shape[1]), max_pages_per_req=int(block_tables.shape[1]),
                     num_pages=int(kv_cache.shape[0]), packed=packed, max_total_q=total_q,
                     kv_dtype=kv_dtype, causal=causal, return_lse=return_lse,
-                    device=query.device.index or 0)
+                    device=query.device.index or 0, q_dtype=q_dtype)
         _plans[key] = plan
     if workspace_buffer.numel() * workspace_buffer.element_size() < plan.workspace_bytes:
         raise ValueError(f"workspace_buffer needs {plan.workspace_bytes} bytes")

@@ -100,6 +100,7 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (p.packed != 0 && p.packed != 1) return MLA_ERR_INVALID_ARG;
   if (p.packed && p.max_total_q < 0) return MLA_ERR_INVALID_ARG;
   if (p.kv_dtype != MLA_KV_BF16 && p.kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p.q_dtype != MLA_Q_BF16 && p.q_dtype != MLA_Q_FP8_E4M3) return MLA_ERR_INVALID_ARG;
   if (p.mask != MLA_MASK_CAUSAL && p.mask != MLA_MASK_DENSE) return MLA_ERR_INVALID_ARG;
   if (!supported_heads(p.num_heads)) return MLA_ERR_UNSUPPORTED;
   if (p.page_size != 32 && p.page_size != 64) return MLA_ERR_UNSUPPORTED;
@@ -177,6 +178,7 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
   p.max_pages = prm.max_pages_per_req;
   p.packed = prm.packed;
   p.kv_dtype = prm.kv_dtype;
+  p.q_fp8 = prm.q_dtype == MLA_Q_FP8_E4M3;
   p.causal = prm.mask == MLA_MASK_CAUSAL;
   p.return_lse = prm.return_lse != 0;
   p.num_pages = prm.num_pages;

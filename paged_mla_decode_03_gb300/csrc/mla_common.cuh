@@ -24,11 +24,12 @@ constexpr int kStatusSeqLen = 1, kStatusQLen = 2, kStatusCausal = 4, kStatusCapa
 struct Problem {
   int batch, num_heads, max_q, max_seq_len, page_size, max_pages;
   int packed, kv_dtype, causal, return_lse;
+  int q_fp8;                     // 1: query is e4m3 (widened to bf16 on load)
   long long num_pages, total_q;  // total_q: rows of the query tensor (tokens)
   float bmm1_scale, bmm2_scale;
   const float* bmm1_dev;         // non-null: read bmm1 from device memory at run time
   const float* bmm2_dev;         // non-null: read bmm2 from device memory at run time
-  const void* query;             // bf16 [tokens, H, 576]
+  const void* query;             // bf16 or e4m3 [tokens, H, 576]
   const void* kv_cache;          // bf16 or e4m3 [num_pages, page_size, 576]
   const int* block_tables;       // [B, max_pages]
   const int* seq_lens;           // [B]

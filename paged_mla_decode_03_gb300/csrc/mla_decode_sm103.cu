@@ -271,9 +271,13 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
         if (!wait_bar(c, Q_FREE, (n_item & 1) ^ 1)) goto done_producer;
         ++n_item;
-        mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
-        tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank, it.q_start * H + it.g * kRows,
-                    &c.bars[Q_FULL]);
+        if (p.q_fp8) {
+          mbar_arrive(&c.bars[Q_FULL]);  // the RoPE half is widened into smem with the latent part
+        } else {
+          mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
+          tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank,
+                      it.q_start * H + it.g * kRows, &c.bars[Q_FULL]);
+        }
         for (int t = 0; t < nt; ++t, ++g) {
           // bf16: load straight into the bf16 ring; e4m3: into the staging ring
           const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
@@ -707,24 +711,66 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     auto write_q = [&](const WorkItem& it) {
       const long long qrow = (long long)it.q_start * H + (long long)it.g * kRows + q;
       const bool in = qrow < q_rows;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim +
-          256 * (int)rank);
+      if (!p.q_fp8) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim +
+            256 * (int)rank);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w[64];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[64];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const uint4 x = in ? __ldg(src + 16 * half + u) : make_uint4(0, 0, 0, 0);
-          w[4 * u] = x.x;
-          w[4 * u + 1] = x.y;
-          w[4 * u + 2] = x.z;
-          w[4 * u + 3] = x.w;
+          for (int u = 0; u < 16; ++u) {
+            const uint4 x = in ? __ldg(src + 16 * half + u) : make_uint4(0, 0, 0, 0);
+            w[4 * u] = x.x;
+            w[4 * u + 1] = x.y;
+            w[4 * u + 2] = x.z;
+            w[4 * u + 3] = x.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tmem_st_32x32b_x16(tmem + lane_base + TM_Q + 64 * half + 16 * j,
+                               *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
         }
+      } else {
+        // e4m3 query: widen exactly to bf16, latent dims into TMEM, RoPE dims
+        // into the 64B-swizzled smem tile the RoPE MMAs read
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const unsigned char*>(p.query) + (in ? qrow : 0) * kQkDim);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tmem_st_32x32b_x16(tmem + lane_base + TM_Q + 64 * half + 16 * j,
-                             *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[64];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {  // 16 codes -> 8 bf16 pairs
+            const uint4 x = in ? __ldg(src + 16 * (int)rank + 8 * half + u) : make_uint4(0, 0, 0, 0);
+            const uint32_t c4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              w[8 * u + 2 * e] = e4m3x2_to_bf16x2(c4[e] & 0xFFFFu);
+              w[8 * u + 2 * e + 1] = e4m3x2_to_bf16x2(c4[e] >> 16);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tmem_st_32x32b_x16(tmem + lane_base + TM_Q + 64 * half + 16 * j,
+                               *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
+        }
+        const int sw = (q >> 1) & 3;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {  // RoPE dims 512 + 32 r + [16 k, 16 k + 16)
+          const uint4 x = in ? __ldg(src + 32 + 2 * (int)rank + k) : make_uint4(0, 0, 0, 0);
+          const uint32_t c4[4] = {x.x, x.y, x.z, x.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o[2 * e] = e4m3x2_to_bf16x2(c4[e] & 0xFFFFu);
+            o[2 * e + 1] = e4m3x2_to_bf16x2(c4[e] >> 16);
+          }
+          *reinterpret_cast<uint4*>(sm + OFF_QROPE + q * 64 + (((2 * k) ^ sw) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(sm + OFF_QROPE + q * 64 + (((2 * k + 1) ^ sw) << 4)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_smem();  // read by the RoPE MMAs
       }
       tmem_wait_st();
       tc_fence_before();
@@ -981,8 +1027,11 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
   CUtensorMap tm_q_rope, tm_kv, tm_kv_rope;
   const uint64_t q_rows = std::max<uint64_t>(1, (uint64_t)p.total_q * p.num_heads);
   const uint64_t kv_rows = (uint64_t)p.num_pages * p.page_size;
-  if (!encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 32, kRows,
-                 CU_TENSOR_MAP_SWIZZLE_64B))
+  // (an e4m3 query is read with plain loads; its map is encoded but unused)
+  if (!(p.q_fp8 ? encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_rows, 32,
+                            kRows, CU_TENSOR_MAP_SWIZZLE_NONE)
+                : encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 32,
+                            kRows, CU_TENSOR_MAP_SWIZZLE_64B)))
     return cudaErrorInvalidValue;
   const bool fp8 = p.kv_dtype == 1;
   if (fp8) {

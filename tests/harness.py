@@ -34,7 +34,10 @@ class DeviceCase:
 def to_device(w, *, return_lse=None, causal=None, workspace_fill=None, max_total_q=None,
               plan_batch=None):
     dev = torch.device("cuda", 0)
-    q = torch.from_numpy(w.query.view(np.int16)).to(dev).view(torch.bfloat16)
+    if getattr(w, "q_dtype", "bf16") == "e4m3":
+        q = torch.from_numpy(w.query).to(dev).view(torch.float8_e4m3fn)
+    else:
+        q = torch.from_numpy(w.query.view(np.int16)).to(dev).view(torch.bfloat16)
     if w.kv_dtype == "bf16":
         kv = torch.from_numpy(w.kv_cache.view(np.int16)).to(dev).view(torch.bfloat16)
     else:
@@ -49,7 +52,8 @@ def to_device(w, *, return_lse=None, causal=None, workspace_fill=None, max_total
                     max_seq_len=w.max_seq_len, page_size=w.page_size,
                     max_pages_per_req=w.block_tables.shape[1], num_pages=w.num_pages,
                     packed=w.packed, max_total_q=max_total_q if max_total_q else tokens,
-                    kv_dtype=w.kv_dtype, causal=cz, return_lse=ret)
+                    kv_dtype=w.kv_dtype, causal=cz, return_lse=ret,
+                    q_dtype=getattr(w, "q_dtype", "bf16"))
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     if workspace_fill is not None:
         ws.fill_(workspace_fill)

@@ -417,3 +417,30 @@ def test_zero_bmm1_gives_the_mean_of_the_visible_rows(name):
     w = REDUCED[name]()
     w.bmm1_scale = 0.0
     full_parity(w)
+
+
+@pytest.mark.parametrize("make", [
+    lambda: mi.deepseek_v3(batch=6, lo=100, hi=700, return_lse=True, q_dtype="e4m3"),
+    lambda: mi.mtp(batch=3, lo=64, hi=400, return_lse=True, q_dtype="e4m3"),
+    lambda: mi.fp8_long(batch=2, lo=300, hi=900, return_lse=True, q_dtype="e4m3"),
+])
+def test_e4m3_query_full_parity(make):
+    """e4m3 query (q_scale folded into bmm1), with bf16 and e4m3 caches: the
+    kernel widens Q exactly, so the cache's tolerance applies unchanged."""
+    w = make()
+    assert w.q_dtype == "e4m3"
+    full_parity(w)
+
+
+def test_e4m3_query_through_decode_api():
+    import paged_mla_decode_03_gb300 as mla
+    w = mi.deepseek_v3(batch=3, lo=64, hi=300, return_lse=True, q_dtype="e4m3")
+    d = to_device(w)
+    q4 = d.query.view(w.batch, 1, w.num_heads, 576)
+    out, lse = mla.decode(q4, d.kv_cache, d.workspace, d.block_tables, d.seq_lens,
+                          w.max_seq_len, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
+                          return_lse=True)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.run(w)
+    check(w.kv_dtype, out.float().cpu().numpy().reshape(-1, w.num_heads, 512), ref_o,
+          lse.cpu().numpy(), ref_l, what="decode api e4m3 q")
