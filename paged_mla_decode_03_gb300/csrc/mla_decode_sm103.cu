@@ -179,6 +179,55 @@ __device__ __forceinline__ bool rescale_requested(const unsigned char* sm, uint3
 
 }  // namespace
 
+// Row `q` of a work item's e4m3 query, for the CTA of cluster rank `rank`:
+// its latent dims [256 rank, 256 rank + 256) widened exactly to bf16 pairs
+// into the TMEM columns at `tmem_q` (lane already in the address), where they
+// are the A operand of the ts QK MMAs, and its RoPE dims [512 + 32 rank, +32)
+// widened into the 64B-swizzled smem tile at `q_rope` (a bf16 query's RoPE
+// half comes by TMA).  Rows past the query tensor are zero.  Called once per
+// item and kept out of line, away from the per-tile loop of the calling warps.
+__device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, bool in, int q,
+                                             uint32_t rank, uint32_t tmem_q,
+                                             unsigned char* q_rope) {
+  const uint4* src = reinterpret_cast<const uint4*>(
+      reinterpret_cast<const unsigned char*>(p.query) + (in ? qrow : 0) * kQkDim);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint32_t w[64];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {  // 16 codes -> 8 bf16 pairs
+      const uint4 x = in ? __ldg(src + 16 * (int)rank + 8 * half + u) : make_uint4(0, 0, 0, 0);
+      const uint32_t c4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        w[8 * u + 2 * e] = e4m3x2_to_bf16x2(c4[e] & 0xFFFFu);
+        w[8 * u + 2 * e + 1] = e4m3x2_to_bf16x2(c4[e] >> 16);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      tmem_st_32x32b_x16(tmem_q + 64 * half + 16 * j,
+                         *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
+  }
+  const int sw = (q >> 1) & 3;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {  // RoPE dims 512 + 32 r + [16 k, 16 k + 16)
+    const uint4 x = in ? __ldg(src + 32 + 2 * (int)rank + k) : make_uint4(0, 0, 0, 0);
+    const uint32_t c4[4] = {x.x, x.y, x.z, x.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      o[2 * e] = e4m3x2_to_bf16x2(c4[e] & 0xFFFFu);
+      o[2 * e + 1] = e4m3x2_to_bf16x2(c4[e] >> 16);
+    }
+    *reinterpret_cast<uint4*>(q_rope + q * 64 + (((2 * k) ^ sw) << 4)) =
+        make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(q_rope + q * 64 + (((2 * k + 1) ^ sw) << 4)) =
+        make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  fence_proxy_async_smem();  // read by the RoPE MMAs
+}
+
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
@@ -704,8 +753,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       return true;
     };
     // Row q of the item's Q latent dims of this CTA ([256 r, 256 r + 256)) into
-    // TMEM, where they are the A operand of the ts QK MMAs.  Called only when
-    // no QK of an earlier item is pending.
+    // TMEM, where they are the A operand of the ts QK MMAs (and, for an e4m3
+    // query, its RoPE dims into smem).  Called only when no QK of an earlier
+    // item is pending.
     const long long q_rows = p.total_q * H;
     const float bmm2 = run_bmm2(p);
     auto write_q = [&](const WorkItem& it) {
@@ -732,45 +782,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                                *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
         }
       } else {
-        // e4m3 query: widen exactly to bf16, latent dims into TMEM, RoPE dims
-        // into the 64B-swizzled smem tile the RoPE MMAs read
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const unsigned char*>(p.query) + (in ? qrow : 0) * kQkDim);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t w[64];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {  // 16 codes -> 8 bf16 pairs
-            const uint4 x = in ? __ldg(src + 16 * (int)rank + 8 * half + u) : make_uint4(0, 0, 0, 0);
-            const uint32_t c4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              w[8 * u + 2 * e] = e4m3x2_to_bf16x2(c4[e] & 0xFFFFu);
-              w[8 * u + 2 * e + 1] = e4m3x2_to_bf16x2(c4[e] >> 16);
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tmem_st_32x32b_x16(tmem + lane_base + TM_Q + 64 * half + 16 * j,
-                               *reinterpret_cast<const uint32_t(*)[16]>(w + 16 * j));
-        }
-        const int sw = (q >> 1) & 3;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {  // RoPE dims 512 + 32 r + [16 k, 16 k + 16)
-          const uint4 x = in ? __ldg(src + 32 + 2 * (int)rank + k) : make_uint4(0, 0, 0, 0);
-          const uint32_t c4[4] = {x.x, x.y, x.z, x.w};
-          uint32_t o[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            o[2 * e] = e4m3x2_to_bf16x2(c4[e] & 0xFFFFu);
-            o[2 * e + 1] = e4m3x2_to_bf16x2(c4[e] >> 16);
-          }
-          *reinterpret_cast<uint4*>(sm + OFF_QROPE + q * 64 + (((2 * k) ^ sw) << 4)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(sm + OFF_QROPE + q * 64 + (((2 * k + 1) ^ sw) << 4)) =
-              make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        fence_proxy_async_smem();  // read by the RoPE MMAs
+        load_q_row_e4m3(p, qrow, in, q, rank, tmem + lane_base + TM_Q, sm + OFF_QROPE);
       }
       tmem_wait_st();
       tc_fence_before();
