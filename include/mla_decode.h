@@ -204,6 +204,28 @@ int mla_decode_run_static_workspace(const mla_plan_t *plan, const void *query,
 /* Free a plan (NULL is allowed). */
 void mla_decode_destroy(mla_plan_t *plan);
 
+/*
+ * Merge n partial attention states of the same query rows into one: the
+ * exchange step of decode-context parallelism (DCP), where each rank runs
+ * mla_decode_run over its own shard of every request's KV rows with
+ * return_lse and the ranks all-gather (O, lse) (the vLLM "FlashInferMLAImpl"
+ * page merges DCP shards by this natural-log LSE).  For every row r:
+ *   lse[r] = ln sum_k exp(lse_k[r]),   out[r] = scale * sum_k exp(lse_k[r] - lse[r]) O_k[r]
+ * which equals a single pass over the union of the shards.  A shard with no
+ * visible row for r (lse_k = -inf) contributes nothing.
+ *
+ * o_parts    bf16 [n_parts, rows, 512], each shard's normalised output (run
+ *            the shards with bmm2_scale = 1 and pass bmm2 here as `scale`)
+ * lse_parts  fp32 [n_parts, rows] natural-log LSEs (mla_decode_run's lse)
+ * rows       tokens * H
+ * out        bf16 [rows, 512]; lse_out fp32 [rows] or NULL
+ * All device pointers; o_parts and out 16-byte aligned.  Enqueued on
+ * `stream`, capture-safe, allocates nothing.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_ALIGNMENT, MLA_ERR_CUDA.
+ */
+int mla_merge_states(const void *o_parts, const float *lse_parts, int32_t n_parts, int64_t rows,
+                     float scale, void *out, float *lse_out, void *stream);
+
 /* Workspace bytes of a plan (the value mla_decode_plan returned). */
 size_t mla_decode_workspace_size(const mla_plan_t *plan);
 

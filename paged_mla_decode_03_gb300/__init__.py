@@ -91,6 +91,8 @@ def load_library():
     lib.mla_decode_run_device_scales.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp,
                                                  sz, vp]
     lib.mla_decode_run_device_scales.restype = ctypes.c_int
+    lib.mla_merge_states.argtypes = [vp, vp, i32, i64, ctypes.c_float, vp, vp, vp]
+    lib.mla_merge_states.restype = ctypes.c_int
     lib.mla_decode_destroy.argtypes = [vp]
     lib.mla_decode_destroy.restype = None
     lib.mla_decode_workspace_size.argtypes = [vp]
@@ -331,3 +333,52 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
              lse=lse if return_lse else None, workspace=workspace_buffer,
              bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale)
     return (out, lse) if return_lse else out
+
+
+def merge_states(o_parts: torch.Tensor, lse_parts: torch.Tensor, *, scale: float = 1.0,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 stream=None):
+    """Merge partial attention states of the same rows by their natural-log
+    LSEs (``mla_merge_states``): ``o_parts`` bf16 ``[n, ..., 512]``,
+    ``lse_parts`` fp32 ``[n, ...]`` (the leading dims after ``n`` flattened to
+    rows).  Returns ``(out, lse)`` with the parts' row shape."""
+    if o_parts.dtype != torch.bfloat16 or lse_parts.dtype != torch.float32:
+        raise TypeError("o_parts must be bf16 and lse_parts fp32")
+    if not (o_parts.is_cuda and lse_parts.is_cuda):
+        raise ValueError("merge_states runs on the GPU")
+    n = int(o_parts.shape[0])
+    row_shape = tuple(o_parts.shape[1:-1])
+    if o_parts.shape[-1] != HEAD_DIM_V or tuple(lse_parts.shape) != (n,) + row_shape:
+        raise ValueError("o_parts [n, ..., 512] and lse_parts [n, ...] disagree")
+    o_parts = o_parts.contiguous()
+    lse_parts = lse_parts.contiguous()
+    rows = 1
+    for d in row_shape:
+        rows *= int(d)
+    if out is None:
+        out = torch.empty(row_shape + (HEAD_DIM_V,), dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(row_shape, dtype=torch.float32, device=o_parts.device)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    rc = load_library().mla_merge_states(_ptr(o_parts), _ptr(lse_parts), n, rows, float(scale),
+                                         _ptr(out), _ptr(lse), stream)
+    if rc != 0:
+        raise MlaDecodeError(rc, "mla_merge_states")
+    return out, lse
+
+
+def dcp_gather(out: torch.Tensor, lse: torch.Tensor, group=None):
+    """The exchange step of decode-context parallelism: all-gather this rank's
+    partial state (``out`` [..., 512], ``lse`` [...]) over ``group`` (a
+    torch.distributed process group; default the world) into stacked
+    ``[world, ...]`` tensors, to be merged with ``merge_states``."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    outs = [torch.empty_like(out) for _ in range(world)]
+    lses = [torch.empty_like(lse) for _ in range(world)]
+    dist.all_gather(outs, out.contiguous(), group=group)
+    dist.all_gather(lses, lse.contiguous(), group=group)
+    return torch.stack(outs), torch.stack(lses)

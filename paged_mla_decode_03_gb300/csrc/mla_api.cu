@@ -20,6 +20,8 @@ cudaError_t partition_setup();
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream);
 cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs);
+cudaError_t launch_merge_states(const void* o_parts, const float* lse_parts, int n, long long rows,
+                                float scale, void* out, float* lse_out, cudaStream_t stream);
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                                 cudaStream_t stream);
 }  // namespace mla
@@ -253,6 +255,20 @@ int mla_decode_run(const mla_plan_t* plan, const void* query, const void* kv_cac
   return mla_decode_run_profiled(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q,
                                  bmm1_scale, bmm2_scale, out, lse, workspace, workspace_bytes,
                                  stream, nullptr, nullptr);
+}
+
+int mla_merge_states(const void* o_parts, const float* lse_parts, int32_t n_parts, int64_t rows,
+                     float scale, void* out, float* lse_out, void* stream) {
+  if (n_parts < 1 || rows < 0 || rows > (1LL << 40)) return MLA_ERR_INVALID_ARG;
+  if (rows == 0) return MLA_OK;
+  if (!o_parts || !lse_parts || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(o_parts, 16) || !aligned(out, 16) || !aligned(lse_parts, 4) ||
+      (lse_out && !aligned(lse_out, 4)))
+    return MLA_ERR_ALIGNMENT;
+  return mla::launch_merge_states(o_parts, lse_parts, n_parts, rows, scale, out, lse_out,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 void mla_decode_destroy(mla_plan_t* plan) { delete plan; }

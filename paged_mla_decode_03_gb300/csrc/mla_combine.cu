@@ -116,3 +116,84 @@ cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int gr
 }
 
 }  // namespace mla
+
+namespace mla {
+
+// Merge of n partial attention states of the same rows (the exchange step of
+// decode-context parallelism, where each rank attends over its own KV shard;
+// the vLLM "FlashInferMLAImpl" page merges such shards by their natural-log
+// LSE).  For row r with shard outputs O_k (already normalised, bf16) and
+// lse_k:  lse = ln sum_k exp(lse_k),  out = scale * sum_k exp(lse_k - lse) O_k.
+// A shard with no visible key (lse = -inf) contributes nothing.  One warp
+// per row, 16 dims per lane, every shard's loads issued before any use
+// (batches of kBatch shards).
+__global__ void __launch_bounds__(256)
+merge_states_kernel(const __nv_bfloat16* __restrict__ o_parts, const float* __restrict__ lse_parts,
+                    int n, long long rows, float scale, __nv_bfloat16* __restrict__ out,
+                    float* __restrict__ lse_out) {
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int t = threadIdx.x & 31;  // dims [16 t, 16 t + 16)
+  if (r >= rows) return;
+  float m = -INFINITY, sum = 0.f;
+  float acc[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+  for (int k0 = 0; k0 < n; k0 += kBatch) {
+    uint4 x[kBatch][2];
+    float l[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      l[u] = -INFINITY;
+      x[u][0] = x[u][1] = make_uint4(0, 0, 0, 0);
+      if (k0 + u < n) {
+        const size_t base = ((size_t)(k0 + u) * rows + r) * kVDim + 16 * t;
+        const uint4* src = reinterpret_cast<const uint4*>(o_parts + base);
+        x[u][0] = src[0];
+        x[u][1] = src[1];
+        l[u] = lse_parts[(size_t)(k0 + u) * rows + r];
+      }
+    }
+    float m_new = m;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) m_new = fmaxf(m_new, l[u]);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    const float f = expf(m - m_use);
+    sum *= f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] *= f;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float w = expf(l[u] - m_use);
+      sum += w;
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(x[u]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 v = __bfloat1622float2(h[e]);
+        acc[2 * e] += w * v.x;
+        acc[2 * e + 1] += w * v.y;
+      }
+    }
+    m = m_new;
+  }
+  const float s2 = sum > 0.f ? scale / sum : 0.f;
+  __nv_bfloat162 o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
+  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * kVDim + 16 * t);
+  dst[0] = *reinterpret_cast<uint4*>(o);
+  dst[1] = *reinterpret_cast<uint4*>(o + 4);
+  const float m_use = (m == -INFINITY) ? 0.f : m;
+  if (lse_out && t == 0) lse_out[r] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
+}
+
+cudaError_t launch_merge_states(const void* o_parts, const float* lse_parts, int n, long long rows,
+                                float scale, void* out, float* lse_out, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;
+  merge_states_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o_parts), lse_parts, n, rows, scale,
+      static_cast<__nv_bfloat16*>(out), lse_out);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -63,3 +63,37 @@ def test_roofline_picks_the_binding_resource():
     wm = {"flops": 4e12, "bytes": 1e9}
     r = bench.roofline(w, wm, 8e-3, peaks)
     assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-12
+
+
+def _dcp_worker(rank, world, port, out):
+    """One DCP rank on CPU: its shard's partial state (from the oracle), the
+    library's all-gather step over gloo, then the reference LSE merge."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    import dcp_shards
+    import oracle
+    import paged_mla_decode_03_gb300 as mla
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    w = mi.build("dcp", 77, num_heads=2, page_size=4, seq_lens=[23, 17, 30], q_lens=[3, 3, 3],
+                 packed=False, causal=True, return_lse=True, bmm1_scale=0.3, bmm2_scale=1.5)
+    shard = dcp_shards.shards(w)[rank]
+    o, l = oracle.run(shard)
+    outs, lses = mla.dcp_gather(torch.from_numpy(o), torch.from_numpy(l))
+    merged, lse = dcp_shards.merge_reference(outs.numpy(), lses.numpy(), w.bmm2_scale)
+    ref_o, ref_l = oracle.run(w)
+    out[rank] = (float(np.abs(merged - ref_o).max()), float(np.abs(lse - ref_l).max()),
+                 tuple(outs.shape))
+    dist.destroy_process_group()
+
+
+def test_dcp_two_ranks_gather_and_merge_equal_single_pass_over_gloo():
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_dcp_worker, args=(2, _free_port(), out), nprocs=2, join=True,
+                       start_method="spawn")
+    for r in range(2):
+        d_o, d_l, shape = out[r]
+        assert shape == (2, 9, 2, 512)
+        assert d_o < 1e-12 and d_l < 1e-12

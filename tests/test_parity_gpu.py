@@ -444,3 +444,51 @@ def test_e4m3_query_through_decode_api():
     ref_o, ref_l = oracle.run(w)
     check(w.kv_dtype, out.float().cpu().numpy().reshape(-1, w.num_heads, 512), ref_o,
           lse.cpu().numpy(), ref_l, what="decode api e4m3 q")
+
+
+@pytest.mark.parametrize("n", [1, 3, 7])
+def test_merge_states_matches_the_float64_lse_merge(n):
+    import dcp_shards
+    import paged_mla_decode_03_gb300 as mla
+    dev = torch.device("cuda", 0)
+    rng = np.random.default_rng(n)
+    rows = (37, 5)
+    o = rng.standard_normal((n,) + rows + (512,)).astype(np.float32)
+    lse = (rng.standard_normal((n,) + rows) * 4).astype(np.float32)
+    if n > 1:
+        lse[0, 3, :] = -np.inf  # a shard that saw nothing for these rows
+    o_t = torch.from_numpy(o).to(dev).to(torch.bfloat16)
+    l_t = torch.from_numpy(lse).to(dev)
+    out, lse_out = mla.merge_states(o_t, l_t, scale=0.75)
+    torch.cuda.synchronize()
+    ref_o, ref_l = dcp_shards.merge_reference(o_t.float().cpu().numpy(), lse, 0.75)
+    got = out.float().cpu().numpy()
+    assert np.abs(got - ref_o).max() <= 1e-2 * np.abs(ref_o).max() + 1e-3
+    assert np.abs(lse_out.cpu().numpy() - ref_l).max() <= 1e-4
+
+
+@pytest.mark.parametrize("make", [
+    lambda: mi.mtp(batch=3, lo=300, hi=700, q_len=2, return_lse=True),
+    lambda: mi.fp8_long(batch=2, lo=400, hi=900, return_lse=True),
+])
+def test_dcp_two_shards_merged_equal_the_single_pass(make):
+    """Decode-context parallelism emulated on one GPU: each request's KV cut
+    into a prefix shard (dense) and a suffix shard (causal), each decoded
+    with its LSE, merged by mla_merge_states: equal to the single pass."""
+    import dcp_shards
+    import paged_mla_decode_03_gb300 as mla
+    w = make()
+    parts = []
+    for sh in dcp_shards.shards(w):
+        d = to_device(sh)
+        run(sh, d)
+        torch.cuda.synchronize()
+        assert device_status(d) == 0
+        parts.append((d.out, d.lse))
+    o_parts = torch.stack([p[0] for p in parts])
+    l_parts = torch.stack([p[1] for p in parts])
+    out, lse = mla.merge_states(o_parts, l_parts, scale=w.bmm2_scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.run(w)
+    check(w.kv_dtype, out.float().cpu().numpy(), ref_o, lse.cpu().numpy(), ref_l,
+          what="dcp two shards")
