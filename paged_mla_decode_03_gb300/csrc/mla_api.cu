@@ -19,7 +19,8 @@ cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cuda
 cudaError_t partition_setup();
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream);
-cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs);
+cudaError_t decode_sm103_setup(int kv_dtype, int num_heads, int max_q, int packed, int sm_count,
+                               int* n_pairs);
 cudaError_t launch_merge_states(const void* o_parts, const float* lse_parts, int n, long long rows,
                                 float scale, void* out, float* lse_out, cudaStream_t stream);
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
@@ -117,7 +118,9 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (cudaSetDevice(p.device) != cudaSuccess) return MLA_ERR_CUDA;
   int sms = 0, n_pairs = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
-  if (e == cudaSuccess) e = mla::decode_sm103_setup(p.kv_dtype, sms, &n_pairs);
+  if (e == cudaSuccess)
+    e = mla::decode_sm103_setup(p.kv_dtype, p.num_heads, p.max_seq_len_q, p.packed, sms,
+                                &n_pairs);
   if (e == cudaSuccess) e = mla::partition_setup();
   cudaSetDevice(prev);
   if (e != cudaSuccess || sms <= 0) return MLA_ERR_CUDA;

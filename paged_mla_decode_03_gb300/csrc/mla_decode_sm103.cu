@@ -28,8 +28,8 @@
 //  * O = P V with P from shared memory: M = 128 query rows, N = 256 (CTA r's
 //    V dims, read MN-major from its latent chunks), K = 64 KV rows, into a
 //    128 x 256 fp32 TMEM accumulator.  The PV commit is multicast to both CTAs,
-//    so a P buffer is reused only after both CTAs' PV read it.
-// Warp roles (448 threads, 704 with e4m3): warp 0 TMA producer (4-stage KV ring), warp 1
+//    so the (single) P tile is rewritten only after both CTAs' PV read it.
+// Warp roles (448 threads, 704 with e4m3): warp 0 TMA producer (5-stage KV ring), warp 1
 // MMA issuer and TMEM owner (QK runs up to two tiles ahead of PV), warps 2-9
 // softmax of the 64 owned rows (four threads per row, 16 KV columns each:
 // warp w covers the owned lanes 32 (w mod 4) + 16 r .. + 15, columns
@@ -38,7 +38,7 @@
 // epilogue and the Q latent load into TMEM (thread = query row = TMEM lane).
 // With an e4m3 cache eight more warps (14-21) widen each staged e4m3 tile to
 // bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and the
-// bf16 ring is 3 deep.
+// bf16 ring is 4 deep.
 // The running max is only raised, and O rescaled, when it grows by more than
 // 2^8.  Every wait is bounded; a timeout sets an error bit in the workspace
 // status word and the kernel unwinds.
@@ -62,20 +62,14 @@ constexpr int kTile = kKvTile;    // 64 KV rows per tile
 constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
 constexpr int kSoftmaxWarps = 8;
 constexpr int kCeWarps = 4;       // senders / correction / epilogue
-// bf16 KV: a 4-deep ring of bf16 tiles.  e4m3 KV: a 3-deep ring of bf16
-// tiles fed by a 2-deep ring of e4m3 staging tiles (converted in smem).
-constexpr int kMaxStages = 4;
-template <bool kFp8> struct Cfg {
-  static constexpr int kStages = kFp8 ? 3 : 4;
-  static constexpr int kThreads = kFp8 ? 704 : 448;  // + 8 converter warps
-};
 constexpr int kConvThreads = 256;  // four per KV row of a tile
 constexpr uint32_t kWaitLimit = 1u << 26;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// shared-memory layout (bytes from a 1024-aligned base)
+// shared-memory layout (bytes from a 1024-aligned base): fixed regions first,
+// then the KV ring, whose depth depends on the configuration (below)
 constexpr uint32_t kRopeQ = kRows * 64;     // 32-dim RoPE half of Q, 64B-swizzled rows
 constexpr uint32_t kChunkKV = kTile * 128;  // 64-dim chunk of a KV tile
 constexpr uint32_t kRopeKV = kTile * 64;    // 32-dim RoPE half of a KV tile
@@ -86,10 +80,8 @@ constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 ti
 constexpr uint32_t kXRowBytes = kTile * 2;
 constexpr uint32_t kXBytes = kOwnRows * kXRowBytes + kOwnRows * 4;
 constexpr uint32_t OFF_QROPE = 0;
-constexpr uint32_t OFF_KV = OFF_QROPE + kRopeQ;
-constexpr uint32_t OFF_STG = OFF_KV + 3 * kStageBytes;  // e4m3 staging (fp8 only)
-constexpr uint32_t OFF_P = OFF_KV + kMaxStages * kStageBytes;
-constexpr uint32_t OFF_X = OFF_P + 2 * kPBytes;
+constexpr uint32_t OFF_P = OFF_QROPE + kRopeQ;  // first (or only) P tile
+constexpr uint32_t OFF_X = OFF_P + kPBytes;
 constexpr uint32_t OFF_BARS = OFF_X + 2 * kXBytes;
 constexpr uint32_t OFF_FAC = OFF_BARS + 512;        // float fac[2][128]: rescale factor per row
 constexpr uint32_t OFF_LROW = OFF_FAC + 2 * kRows * 4;  // float l[128]: row sums, last tile
@@ -98,12 +90,27 @@ constexpr uint32_t OFF_MX = OFF_FLAG + 2 * 16 * 4;      // float [2][2][128]: ha
 constexpr uint32_t OFF_LX = OFF_MX + 2 * 2 * kRows * 4;  // float [2][128]: half-row sums
 constexpr uint32_t OFF_TMEM = OFF_LX + 2 * kRows * 4;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
-constexpr uint32_t kSmemUsed = OFF_ABORT + 16;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;     // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(OFF_STG + 2 * kStgBytes == OFF_P, "e4m3 staging fills the last bf16 stage");
-static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_STG % 1024 == 0 &&
-                  OFF_P % 1024 == 0 && OFF_X % 16 == 0,
+constexpr uint32_t OFF_KV = (OFF_ABORT + 16 + 1023) / 1024 * 1024;
+
+// Two configurations share the code.  Two P tiles (kDoubleP): the softmax
+// writes P(g) while PV(g - 1) may still read the other tile; the ring is 4
+// bf16 stages (e4m3 KV: 3 bf16 stages + a 2-deep e4m3 staging ring), and the
+// second P tile follows the ring.  One P tile: P(g) waits for both CTAs'
+// PV(g - 1), which frees the smem for a 5-stage ring; it pays off when the
+// softmax is the longer step (every item row valid: H q_len >= 128, packed:
+// H >= 128), and the e4m3 kernel always uses two P tiles.
+template <bool kFp8, bool kDoubleP> struct Cfg {
+  static constexpr int kStages = (kFp8 ? 3 : 4) + (kDoubleP ? 0 : 1);
+  static constexpr int kThreads = kFp8 ? 704 : 448;  // + 8 converter warps
+  static constexpr uint32_t OFF_STG = OFF_KV + kStages * kStageBytes;  // e4m3 staging
+  static constexpr uint32_t kRingEnd = OFF_STG + (kFp8 ? 2 * kStgBytes : 0);
+  static constexpr uint32_t OFF_P1 = kRingEnd;  // second P tile (kDoubleP only)
+  static constexpr uint32_t kSmemBytes = kRingEnd + (kDoubleP ? kPBytes : 0) + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(OFF_STG % 1024 == 0 && OFF_P1 % 1024 == 0, "alignment");
+};
+static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0 &&
+                  OFF_X % 16 == 0 && 2 * kStgBytes == kStageBytes,
               "alignment");
 // bytes the peer pushes into this CTA's P tile per KV tile (P rows, factors,
 // flags), plus the row sums on an item's last tile
@@ -118,10 +125,11 @@ constexpr uint32_t TM_Q = 384;  // Q latent: 128 rows x 256 dims (bf16 pairs)
 
 enum Bar {
   Q_FULL, Q_FREE, QT_FULL,
-  KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3, KV_EMPTY0, KV_EMPTY1, KV_EMPTY2, KV_EMPTY3,
+  KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3, KV_FULL4,
+  KV_EMPTY0, KV_EMPTY1, KV_EMPTY2, KV_EMPTY3, KV_EMPTY4,
   S_FULL0, S_FULL1, S_FREE0, S_FREE1,
   X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1,
-  P_FULL0, P_FULL1, P_FREE0, P_FREE1,
+  P_FULL0, P_FULL1, P_FREE0, P_FREE1,  // one P tile: only P_FREE0, one phase per tile
   MX_FULL0,                    // 8: [subpartition][tile parity]
   LX_FULL0 = MX_FULL0 + 8,     // 4: [subpartition]
   LROW_FREE = LX_FULL0 + 4,
@@ -228,13 +236,14 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
   fence_proxy_async_smem();  // read by the RoPE MMAs
 }
 
-template <bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
+template <bool kFp8, bool kDoubleP>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8, kDoubleP>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                     const __grid_constant__ CUtensorMap tm_q_rope,
                     const __grid_constant__ CUtensorMap tm_kv,
                     const __grid_constant__ CUtensorMap tm_kv_rope) {
-  constexpr int kStages = Cfg<kFp8>::kStages;
+  using C = Cfg<kFp8, kDoubleP>;
+  constexpr int kStages = C::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -359,7 +368,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
             if (pages[pg] < 0) continue;
             const int y = pages[pg] * ps;
             if (kFp8) {
-              unsigned char* stg = sm + OFF_STG + s * kStgBytes;
+              unsigned char* stg = sm + C::OFF_STG + s * kStgBytes;
               for (int lc = 0; lc < kLatChunks; ++lc)
                 tma_load_2d(stg + lc * kTile * 64 + pg * ps * 64, &tm_kv, 256 * (int)rank + 64 * lc,
                             y, full);
@@ -390,6 +399,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const uint32_t qr_base = smem_u32(sm + OFF_QROPE);
       const uint32_t kv_base = smem_u32(sm + OFF_KV);
       const uint32_t p_base = smem_u32(sm + OFF_P);
+      const uint32_t p1_base = smem_u32(sm + C::OFF_P1);
       uint32_t g0 = 0, n_rescale = 0;
       int n_item = 0;
       for (int idx = item_begin; idx < item_end; ++idx) {
@@ -432,12 +442,14 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               const int s = gp % kStages;
               const uint32_t stage = kv_base + s * kStageBytes;
               for (int ks = 0; ks < kTile / 16; ++ks) {
-                const uint64_t a = smem_desc(p_base + pb * kPBytes + ks * 32, 16, 1024, kSwizzle128B);
+                const uint64_t a = smem_desc(
+                    (kDoubleP && pb ? p1_base : p_base) + ks * 32, 16, 1024, kSwizzle128B);
                 const uint64_t b = smem_desc(stage + ks * 16 * 128, 8192, 1024, kSwizzle128B);
                 mma_bf16_ss(tmem + TM_O, a, b, idesc_pv, (pv == 0 && ks == 0) ? 0u : 1u);
               }
               mma_commit(&c.bars[KV_EMPTY0 + s]);
-              mma_commit_multicast(&c.bars[P_FREE0 + pb], 0x3);  // both CTAs' P buffer pb
+              // both CTAs' P tiles (of this parity) are free
+              mma_commit_multicast(&c.bars[kDoubleP ? P_FREE0 + pb : P_FREE0], 0x3);
               if (pv + 1 == nt) mma_commit(&c.bars[O_FINAL]);
               ++pv;
               pv_state = 0;
@@ -503,6 +515,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const uint32_t xfree_peer0 = map_to_rank(smem_u32(&c.bars[PEER_X_FREE0]), peer);
     const uint32_t pfull_peer0 = map_to_rank(smem_u32(&c.bars[P_FULL0]), peer);
     const uint32_t p_peer0 = map_to_rank(smem_u32(sm + OFF_P), peer);
+    const uint32_t p_peer1 = map_to_rank(smem_u32(sm + C::OFF_P1), peer);
     const uint32_t fac_peer0 = map_to_rank(smem_u32(sm + OFF_FAC), peer);
     const uint32_t flag_peer0 = map_to_rank(smem_u32(sm + OFF_FLAG), peer);
     const uint32_t lrow_peer = map_to_rank(smem_u32(sm + OFF_LROW), peer);
@@ -631,9 +644,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                 make_uint4(0, 0, 0, 0);
           }
         }
-        // P (bf16) of this row into both CTAs' P tiles once both PVs that last
-        // read them are done
-        if (!wait_bar(c, P_FREE0 + sb, ((g >> 1) & 1) ^ 1)) goto done_softmax;
+        // P (bf16) of this row into both CTAs' (single) P tiles once both
+        // CTAs' PV of the previous tile read them
+        if (kDoubleP ? !wait_bar(c, P_FREE0 + sb, ((g >> 1) & 1) ^ 1)
+                     : (g > 0 && !wait_bar(c, P_FREE0, (g - 1) & 1)))
+          goto done_softmax;
         {
           uint32_t w[8];
 #pragma unroll
@@ -641,10 +656,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           const uint32_t pbar = pfull_peer0 + 8u * sb;
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const uint32_t off = sb * kPBytes + q * 128 + (((2 * kq + u) ^ (q & 7)) << 4);
+            const uint32_t off = q * 128 + (((2 * kq + u) ^ (q & 7)) << 4);
+            const uint32_t tile = kDoubleP && sb ? C::OFF_P1 : OFF_P;
             const uint4 val = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            *reinterpret_cast<uint4*>(sm + OFF_P + off) = val;
-            st_async_v4_b32(p_peer0 + off, val, pbar);
+            *reinterpret_cast<uint4*>(sm + tile + off) = val;
+            st_async_v4_b32((kDoubleP && sb ? p_peer1 : p_peer0) + off, val, pbar);
           }
           if (kq == 0) {
             fac[sb * kRows + q] = f;
@@ -896,7 +912,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         const int s = g % kStages;   // bf16 slot
         if (!wait_bar(c, STG_FULL0 + ss, (g >> 1) & 1)) goto done_conv;
         if (!wait_bar(c, KV_EMPTY0 + s, ((g / kStages) & 1) ^ 1)) goto done_conv;
-        const unsigned char* src = sm + OFF_STG + ss * kStgBytes;
+        const unsigned char* src = sm + C::OFF_STG + ss * kStgBytes;
         unsigned char* dst = sm + OFF_KV + s * kStageBytes;
         {
           const int lc = part;
@@ -985,16 +1001,17 @@ bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int e
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kDoubleP>
 cudaError_t setup_one(int sm_count, int* n_pairs) {
-  auto kernel = decode_sm103_kernel<kFp8>;
+  using C = Cfg<kFp8, kDoubleP>;
+  auto kernel = decode_sm103_kernel<kFp8, kDoubleP>;
   cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sm_count / 2), 1, 1);
-  cfg.blockDim = dim3(Cfg<kFp8>::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = 2;
@@ -1011,27 +1028,38 @@ cudaError_t setup_one(int sm_count, int* n_pairs) {
 }
 
 // Launch as a programmatic dependent of the previous kernel in the stream.
-template <typename Kernel>
-cudaError_t launch_pdl(Kernel kernel, int grid, int threads, cudaStream_t stream, const Problem& p,
-                       const Layout& lay, char* ws, const CUtensorMap& a, const CUtensorMap& b,
-                       const CUtensorMap& c) {
+template <bool kFp8, bool kDoubleP>
+cudaError_t launch_pdl(int grid, cudaStream_t stream, const Problem& p, const Layout& lay, char* ws,
+                       const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c) {
+  using C = Cfg<kFp8, kDoubleP>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(threads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, p, lay, ws, a, b, c);
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kFp8, kDoubleP>, p, lay, ws, a, b, c);
 }
 
 }  // namespace
 
-cudaError_t decode_sm103_setup(int kv_dtype, int sm_count, int* n_pairs) {
-  return kv_dtype == 1 ? setup_one<true>(sm_count, n_pairs) : setup_one<false>(sm_count, n_pairs);
+// The configuration a problem runs with (see Cfg): one P tile and a deeper
+// ring when every row of a 128-row item is a real (token, head) row, i.e.
+// H q_len >= 128 (packed launches: H >= 128, their q_len varies).
+static bool single_p_tile(int kv_dtype, int num_heads, int max_q, int packed) {
+  return kv_dtype != 1 && (long long)num_heads * (packed ? 1 : max_q) >= kRows;
+}
+
+cudaError_t decode_sm103_setup(int kv_dtype, int num_heads, int max_q, int packed, int sm_count,
+                               int* n_pairs) {
+  if (kv_dtype == 1) return setup_one<true, true>(sm_count, n_pairs);
+  return single_p_tile(kv_dtype, num_heads, max_q, packed)
+             ? setup_one<false, false>(sm_count, n_pairs)
+             : setup_one<false, true>(sm_count, n_pairs);
 }
 
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
@@ -1053,16 +1081,19 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
         !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 32,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    return launch_pdl(decode_sm103_kernel<true>, lay.n_ctas, Cfg<true>::kThreads, stream, p, lay,
-                      static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
+    return launch_pdl<true, true>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope,
+                                  tm_kv, tm_kv_rope);
   } else {
     if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 32,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
-    return launch_pdl(decode_sm103_kernel<false>, lay.n_ctas, Cfg<false>::kThreads, stream, p, lay,
-                      static_cast<char*>(ws), tm_q_rope, tm_kv, tm_kv_rope);
+    if (single_p_tile(p.kv_dtype, p.num_heads, p.max_q, p.packed))
+      return launch_pdl<false, false>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws),
+                                      tm_q_rope, tm_kv, tm_kv_rope);
+    return launch_pdl<false, true>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope,
+                                   tm_kv, tm_kv_rope);
   }
 }
 
