@@ -15,7 +15,9 @@
 // corresponding tile and each piece becomes a separate item writing a
 // partial; every other group is one item writing the output directly.  So
 // workers are balanced to within one tile plus one overhead, and there are at
-// most n + #groups items and n - 1 cut points.  One CTA of 1024 threads.
+// most n + #groups items and n - 1 cut points.  One CTA of 128-1024 threads.
+#include <algorithm>
+
 #include "mla_common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -23,7 +25,9 @@ namespace mla {
 
 namespace {
 
-constexpr int kThreads = 1024;
+// One CTA of 128..1024 threads, sized by the launch from the plan's bounds
+// (fewer warps make the block-wide steps cheaper on small problems).
+constexpr int kMaxThreads = 1024;
 constexpr long long kOverheadTiles = 3;  // c0: query load + epilogue, in tile units (measured ~3.2)
 
 struct Shared {
@@ -40,7 +44,7 @@ __device__ int block_or(int v, Shared& sh) {
   if (lane == 0) sh.warp_i[warp] = v;
   __syncthreads();
   int t = 0;
-  for (int w = 0; w < kThreads / 32; ++w) t |= sh.warp_i[w];
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t |= sh.warp_i[w];
   __syncthreads();
   return t;
 }
@@ -52,7 +56,7 @@ __device__ int block_min(int v, Shared& sh) {
   if (lane == 0) sh.warp_i[warp] = v;
   __syncthreads();
   int t = sh.warp_i[0];
-  for (int w = 1; w < kThreads / 32; ++w) t = min(t, sh.warp_i[w]);
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) t = min(t, sh.warp_i[w]);
   __syncthreads();
   return t;
 }
@@ -65,9 +69,10 @@ __device__ int block_max(int v, Shared& sh) {
 template <typename T>
 __device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
   if (threadIdx.x == 0) sh.carry_ll = 0;
   __syncthreads();
-  for (int base = 0; base < n; base += kThreads) {
+  for (int base = 0; base < n; base += blockDim.x) {
     const int i = base + threadIdx.x;
     const T v = i < n ? data[i] : T(0);
     T x = v;
@@ -78,7 +83,7 @@ __device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
     if (lane == 31) sh.warp_ll[warp] = (long long)x;
     __syncthreads();
     if (warp == 0) {
-      long long w = sh.warp_ll[lane];
+      long long w = lane < nw ? sh.warp_ll[lane] : 0;
       for (int o = 1; o < 32; o <<= 1) {
         const long long y = __shfl_up_sync(0xffffffffu, w, o);
         if (lane >= o) w += y;
@@ -90,7 +95,7 @@ __device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
     const long long carry = sh.carry_ll;
     if (i < n) data[i] = (T)(carry + warp_excl + (long long)(x - v));
     __syncthreads();
-    if (threadIdx.x == 0) sh.carry_ll = carry + sh.warp_ll[31];
+    if (threadIdx.x == 0) sh.carry_ll = carry + sh.warp_ll[nw - 1];
     __syncthreads();
   }
   return (T)sh.carry_ll;
@@ -128,7 +133,7 @@ __device__ __forceinline__ int cut_tile(const Bounds& bd, long long p, long long
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMaxThreads, 1)
 partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   __shared__ Shared sh;
   // the decode kernel may set up its barriers and TMEM meanwhile; it reads
@@ -165,7 +170,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   // 1. Per-request lengths, clamped so that nothing downstream leaves the
   //    caller's buffers; contract violations are flagged in the status word.
   int status = 0;
-  for (int b = threadIdx.x; b < B; b += kThreads) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
     int q, qs;
     if (p.packed) {
       int lo = p.qo_indptr[b], hi = p.qo_indptr[b + 1];
@@ -191,7 +196,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   status = __syncthreads_or(status) ? block_or(status, sh) : 0;
   // do all requests that have row groups have the same number of them?
   int g_min = 1 << 30, g_max = 0;
-  for (int b = threadIdx.x; b < B; b += kThreads)
+  for (int b = threadIdx.x; b < B; b += blockDim.x)
     if (r_gbase[b] > 0) {
       g_min = min(g_min, r_gbase[b]);
       g_max = max(g_max, r_gbase[b]);
@@ -216,7 +221,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   const int G = g_max;
   const int lanes = (g_min == g_max && G >= 2 && n / G >= 2) ? G : 1;
   const int n_req_groups = lanes > 1 ? n_groups / G : 0;  // requests that have groups
-  for (int b = threadIdx.x; b < B; b += kThreads) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int gb = r_gbase[b];
     const int ge = (b + 1 < B) ? r_gbase[b + 1] : n_groups;
     const int T = (r_len[b] + kKvTile - 1) / kKvTile;
@@ -238,7 +243,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   bd.WL = W / lanes;  // every lane has the same cost
 
   // 3. Cut points inside each group -> chunk counts.
-  for (int g = threadIdx.x; g < n_groups; g += kThreads) {
+  for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
     const int b = g_req[g];
     const int T = (r_len[b] + kKvTile - 1) / kKvTile;
     const long long S = g_start[g], c = kOverheadTiles + T;
@@ -271,7 +276,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
 
   // 4. Items (group order, then chunk order) and combine entries.
   if (n_items > 0) {
-    for (int g = threadIdx.x; g < n_groups; g += kThreads) {
+    for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
       const int b = g_req[g];
       const int L = r_len[b];
       const int T = (L + kKvTile - 1) / kKvTile;
@@ -324,7 +329,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   }
   __syncthreads();
   // 5. Worker ranges: worker w owns items [begin[w], begin[w + 1]).
-  for (int w = threadIdx.x; w <= (int)n; w += kThreads) {
+  for (int w = threadIdx.x; w <= (int)n; w += blockDim.x) {
     int lo = 0, hi = n_items;  // first item with owner >= w
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -344,7 +349,11 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
 
 cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cudaStream_t stream) {
   const size_t smem = lay.scratch_in_smem ? lay.scratch_bytes : 0;
-  partition_kernel<<<1, kThreads, smem, stream>>>(p, lay, static_cast<char*>(ws));
+  long long need = std::max<long long>(std::max<long long>(p.batch, lay.max_groups),
+                                       (long long)lay.n_workers + 1);
+  const int threads = (int)std::min<long long>(kMaxThreads,
+                                                std::max<long long>(128, (need + 31) / 32 * 32));
+  partition_kernel<<<1, threads, smem, stream>>>(p, lay, static_cast<char*>(ws));
   return cudaGetLastError();
 }
 
