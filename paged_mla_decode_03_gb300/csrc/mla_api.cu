@@ -85,6 +85,8 @@ int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int row
   off = align_up(off + sizeof(float) * R * kVDim * (size_t)lay->max_partials, 256);
   lay->part_lse = off;
   off = align_up(off + sizeof(float) * R * (size_t)lay->max_partials, 256);
+  lay->comb_done = off;
+  off = align_up(off + sizeof(int) * (size_t)std::max(lay->max_combine, 1), 256);
   lay->total = off;
   return MLA_OK;
 }

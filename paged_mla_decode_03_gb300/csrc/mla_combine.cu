@@ -8,6 +8,10 @@
 // the vLLM "FlashInferMLAImpl" page uses to merge partial attention across
 // decode-context-parallel shards; here the shards are KV chunks of one GPU.
 //
+// An entry is merged once both CTAs of each of its chunks have counted their
+// partial (a bounded acquire spin by one thread of the block), so entries
+// whose chunks finished early are merged while the decode kernel still runs.
+//
 // Grid: (row blocks of 8 rows) x (combine entries), 256 threads; 32 threads
 // per row, 16 output dims per thread.  Every load of a thread (the LSEs and
 // the 16-dim slices of up to kBatch chunks) is issued before any is used, so
@@ -27,9 +31,28 @@ constexpr int kRowsPerBlock = 8;
 constexpr int kBatch = 4;  // chunks loaded per round trip
 }  // namespace
 
+// Waits (bounded) until the counter reaches `target`; acquire ordering makes
+// the counted partials visible.  Gives up at once if a wait already timed out.
+__device__ bool wait_count(const int* counter, int target, int* status) {
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) return true;
+    if ((i & 255) == 255 && (*reinterpret_cast<volatile int*>(status) & kStatusTimeout)) return false;
+    __nanosleep(128);
+  }
+  atomicOr(status, kStatusTimeout);
+  return false;
+}
+
+// No grid-dependency wait: launched as a programmatic dependent of the decode
+// kernel, whose CTAs release it right after their prologue, the combine's
+// CTAs run on SMs the decode kernel has finished with and merge a group as
+// soon as both CTAs of every chunk of it have counted their partial.
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
-  ptx::pdl_wait();  // the decode kernel's partials are complete and visible
+  int* status = reinterpret_cast<int*>(ws) + kHdrStatus;
+  const int* done = reinterpret_cast<const int*>(ws + lay.comb_done);
   const int* hdr = reinterpret_cast<const int*>(ws);
   const CombineItem* comb = reinterpret_cast<const CombineItem*>(ws + lay.combine);
   const float* part_o = reinterpret_cast<const float*>(ws + lay.part_o);
@@ -44,6 +67,9 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     const CombineItem c = comb[ci];
     const int rows = min(R, c.q_len * H - c.g * R);
     const int r = blockIdx.x * kRowsPerBlock + row_in_block;
+    if (blockIdx.x * kRowsPerBlock >= rows) continue;  // uniform over the block
+    if (!__syncthreads_and(threadIdx.x != 0 || wait_count(done + ci, 2 * c.n_chunks, status)))
+      return;
     if (r >= rows) continue;
     // running merge over batches of chunks: (m, sum, acc) rescaled per batch
     float m = -INFINITY, sum = 0.f;

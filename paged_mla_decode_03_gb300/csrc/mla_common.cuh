@@ -60,6 +60,7 @@ __device__ __forceinline__ float run_bmm2(const Problem& p) {
 struct WorkItem {
   int b, g, kv_begin, kv_end;
   int slot, q_len, seq_len, q_start;  // q_start: first token of request b
+  int comb;                           // combine entry of a split group, else -1
 };
 
 // One split (request, row group): partials live in slots first + k * stride.
@@ -90,6 +91,7 @@ struct Layout {
   int scratch_in_smem;   // 1: the partitioner keeps its scratch in shared memory
   size_t part_o;         // float[max_partials][rows_per_group][512]
   size_t part_lse;       // float[max_partials][rows_per_group]
+  size_t comb_done;      // int[max_combine]: CTAs that finished a chunk of each split group
   size_t total;
   int max_items, max_combine, max_partials, max_groups;
   int n_workers;       // persistent workers (CTAs, or CTA pairs)

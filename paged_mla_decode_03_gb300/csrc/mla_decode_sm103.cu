@@ -256,6 +256,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   const int* worker_begin = reinterpret_cast<const int*>(ws + lay.worker_ranges);
   float* part_o = reinterpret_cast<float*>(ws + lay.part_o);
   float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
+  int* comb_done = reinterpret_cast<int*>(ws + lay.comb_done);
 
   Ctx c;
   c.bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
@@ -299,7 +300,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote access
   // the work list comes from the partition kernel; the combine kernel may be
-  // scheduled as soon as SMs free up (it waits for this grid to complete)
+  // scheduled as soon as SMs free up (it waits on the per-entry counters that
+  // the epilogues bump, so every CTA here is resident before it can spin)
   pdl_wait();
   pdl_launch_dependents();
   const uint32_t tmem = *tmem_slot;
@@ -693,6 +695,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                 if (p.return_lse) p.lse[grow] = lse;
               } else {
                 part_lse[(size_t)it.slot * kRows + q] = lse;
+                __threadfence();  // visible GPU-wide before the epilogue counts the chunk
               }
             }
           }
@@ -890,8 +893,19 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
       }
       tc_fence_before();
+      if (it.slot >= 0) __threadfence();  // the partial is visible GPU-wide before it is counted
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.bars[EPI_DONE]);
+      if (it.comb >= 0 && warp == 2 + kSoftmaxWarps) {
+        // all four warps' partials (and the owners' LSEs) are written: count
+        // this CTA's chunk, so the combine can merge the group (it merges
+        // once both CTAs of every chunk have counted)
+        if (!wait_bar(c, EPI_DONE, n_item & 1)) goto done_epi;
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(comb_done + it.comb, 1);
+        }
+      }
       ++n_item;
     }
   done_epi:;

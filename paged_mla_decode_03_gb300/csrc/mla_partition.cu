@@ -293,6 +293,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
         it.kv_begin = t0 * kKvTile;
         it.kv_end = min(L, t1 * kKvTile);
         it.slot = nch > 1 ? g_slot[g] + k : -1;
+        it.comb = nch > 1 ? g_comb[g] : -1;
         it.q_len = r_qlen[b];
         it.seq_len = L;
         it.q_start = r_qstart[b];
@@ -327,6 +328,9 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
       }
     }
   }
+  // completion counters of the combine entries (bumped by the decode kernel)
+  int* comb_done = reinterpret_cast<int*>(ws + lay.comb_done);
+  for (int e = threadIdx.x; e < lay.max_combine; e += blockDim.x) comb_done[e] = 0;
   __syncthreads();
   // 5. Worker ranges: worker w owns items [begin[w], begin[w + 1]).
   for (int w = threadIdx.x; w <= (int)n; w += blockDim.x) {
