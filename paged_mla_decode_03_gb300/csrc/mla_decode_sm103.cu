@@ -310,27 +310,32 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Lane 0 waits for ring slots and issues the copies.  The whole warp
+    // fetches the item's page ids in batches of 32 (one per lane), one batch
+    // ahead, so no page-table read latency sits between two tiles' copies.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q_rope);
       tma_prefetch_desc(&tm_kv);
       tma_prefetch_desc(&tm_kv_rope);
-      uint32_t g = 0;
-      int n_item = 0;
-      const int ps = p.page_size;
-      const int npg = kTile / ps;
-      for (int idx = item_begin; idx < item_end; ++idx) {
-        const WorkItem it = items[idx];
-        const int nt = n_tiles_of(it);
-        if (nt <= 0) continue;
-        const int* bt = p.block_tables + (size_t)it.b * p.max_pages;
-        // page ids of the first tile (later tiles are read one tile ahead)
-        int pages[2] = {-1, -1};
-        for (int pg = 0; pg < npg; ++pg) {
-          const int jr = it.kv_begin + pg * ps;
-          if (jr < it.kv_end) pages[pg] = bt[jr / ps];
-        }
-        if (!wait_bar(c, Q_FREE, (n_item & 1) ^ 1)) goto done_producer;
-        ++n_item;
+    }
+    uint32_t g = 0;
+    int n_item = 0;
+    const int ps = p.page_size;
+    const int npg = kTile / ps;  // 1 or 2 pages per tile
+    for (int idx = item_begin; idx < item_end; ++idx) {
+      const WorkItem it = items[idx];
+      const int nt = n_tiles_of(it);
+      if (nt <= 0) continue;
+      // page slot i of the item = block-table entry first + i (tiles start on
+      // a page boundary); only the pages the item's rows touch are read
+      const int* bt = p.block_tables + (size_t)it.b * p.max_pages + it.kv_begin / ps;
+      const int n_pages = (it.kv_end - it.kv_begin + ps - 1) / ps;
+      int cur = lane < n_pages ? bt[lane] : -1;
+      int nxt = 32 + lane < n_pages ? bt[32 + lane] : -1;
+      const bool q_ok = lane == 0 ? wait_bar(c, Q_FREE, (n_item & 1) ^ 1) : false;
+      if (!__shfl_sync(0xffffffffu, q_ok, 0)) goto done_producer;
+      ++n_item;
+      if (lane == 0) {
         if (p.q_fp8) {
           mbar_arrive(&c.bars[Q_FULL]);  // the RoPE half is widened into smem with the latent part
         } else {
@@ -338,18 +343,24 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank,
                       it.q_start * H + it.g * kRows, &c.bars[Q_FULL]);
         }
-        for (int t = 0; t < nt; ++t, ++g) {
-          // bf16: load straight into the bf16 ring; e4m3: into the staging ring
-          const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
-          const uint32_t use = kFp8 ? (g >> 1) : g / kStages;
-          int next[2] = {-1, -1};
-          if (t + 1 < nt)
-            for (int pg = 0; pg < npg; ++pg) {
-              const int jr = it.kv_begin + (t + 1) * kTile + pg * ps;
-              if (jr < it.kv_end) next[pg] = bt[jr / ps];
-            }
-          if (!wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1))
-            goto done_producer;
+      }
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int slot0 = t * npg;  // never straddles a batch: npg divides 32
+        if (slot0 > 0 && (slot0 & 31) == 0) {
+          cur = nxt;
+          const int i = slot0 + 32 + lane;
+          nxt = i < n_pages ? bt[i] : -1;
+        }
+        int pages[2];
+        pages[0] = __shfl_sync(0xffffffffu, cur, slot0 & 31);
+        pages[1] = __shfl_sync(0xffffffffu, cur, (slot0 + 1) & 31);
+        // bf16: load straight into the bf16 ring; e4m3: into the staging ring
+        const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
+        const uint32_t use = kFp8 ? (g >> 1) : g / kStages;
+        const bool ok =
+            lane == 0 ? wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1) : false;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) goto done_producer;
+        if (lane == 0) {
           const int j0 = it.kv_begin + t * kTile;
           uint32_t bytes = 0;
           for (int pg = 0; pg < npg; ++pg) {
@@ -385,12 +396,10 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                           512 + 32 * (int)rank, y, full);
             }
           }
-          pages[0] = next[0];
-          pages[1] = next[1];
         }
       }
-    done_producer:;
     }
+  done_producer:;
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Within an item QK(g) is issued as soon as its KV tile and S buffer are
