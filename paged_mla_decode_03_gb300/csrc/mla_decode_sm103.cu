@@ -110,6 +110,7 @@ template <bool kFp8, bool kDoubleP> struct Cfg {
   static_assert(OFF_STG % 1024 == 0 && OFF_P1 % 1024 == 0, "alignment");
 };
 static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0 &&
+                  OFF_FLAG % 16 == 0 &&
                   OFF_X % 16 == 0 && 2 * kStgBytes == kStageBytes,
               "alignment");
 // bytes the peer pushes into this CTA's P tile per KV tile (P rows, factors,
@@ -178,10 +179,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // True if any softmax warp of either CTA asked for an O rescale at global tile g.
 __device__ __forceinline__ bool rescale_requested(const unsigned char* sm, uint32_t g) {
-  const volatile int* f = reinterpret_cast<const volatile int*>(sm + OFF_FLAG) + 16 * (g & 1);
+  const unsigned char* f = sm + OFF_FLAG + 64 * (g & 1);
   bool r = false;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) r |= f[k] == (int)g;
+  for (int k = 0; k < 4; ++k) {
+    const uint4 v = ld_volatile_shared_v4(f + 16 * k);
+    r |= (v.x == g) | (v.y == g) | (v.z == g) | (v.w == g);
+  }
   return r;
 }
 

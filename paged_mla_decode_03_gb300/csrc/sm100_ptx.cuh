@@ -279,6 +279,15 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar)
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                : "memory");
 }
+// 16 bytes of shared memory that other threads (or the peer CTA) may write
+__device__ __forceinline__ uint4 ld_volatile_shared_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
