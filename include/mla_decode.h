@@ -22,9 +22,11 @@
  * Calling sequence:  mla_decode_plan (host only; before any graph capture)
  * -> mla_decode_run (any number of times; capture-safe) -> mla_decode_destroy.
  *
- * Every tensor argument is a DEVICE pointer owned by the caller.  The library
- * allocates no device memory, performs no device-to-host copy and never
- * synchronises the stream: all per-launch metadata (seq_lens, qo_indptr,
+ * Every tensor argument is a DEVICE pointer owned by the caller (except in
+ * mla_decode_run_host, which copies a step's host-side inputs and results
+ * itself).  The library allocates no device memory, performs no
+ * device-to-host copy (outside mla_decode_run_host) and never synchronises
+ * the stream: all per-launch metadata (seq_lens, qo_indptr,
  * block_tables) is read on the device.  Status codes are returned only for
  * what the host can check; violations of the device-side contract below are
  * undefined behaviour, except that out-of-range lengths and offsets are
@@ -200,6 +202,50 @@ int mla_decode_run_static_workspace(const mla_plan_t *plan, const void *query,
                                     const int32_t *seq_lens, const int32_t *qo_indptr,
                                     int64_t total_q, float bmm1_scale, float bmm2_scale,
                                     void *out, float *lse, void *stream);
+
+/*
+ * Device bytes mla_decode_run_host needs for its staging buffer: the query,
+ * block_tables, seq_lens, qo_indptr (packed), out and lse (return_lse) of one
+ * step, each 256-byte aligned.  total_q as for mla_decode_run (packed: the
+ * step's query rows, 0 <= total_q <= max_total_q; fixed: ignored).  Returns 0
+ * for a NULL plan or an out-of-range packed total_q.
+ */
+size_t mla_decode_host_staging_bytes(const mla_plan_t *plan, int64_t total_q);
+
+/*
+ * One decode step whose per-step inputs and results live in HOST memory: the
+ * query and the metadata are copied host-to-device into `staging`, the decode
+ * runs as mla_decode_run, and out (and lse) are copied device-to-host, all
+ * enqueued on `stream` with one cudaMemcpyAsync per buffer.  The KV cache
+ * stays in device memory (the persistent state of a serving loop).
+ *
+ * This entry point is the exception to the device-pointers rule above: it
+ * exists for callers that hold the step's query and metadata on the host.
+ * The call returns once everything is enqueued; the host buffers must stay
+ * valid (and h_out / h_lse unread) until the stream has passed the copies.
+ * Page-locked host buffers keep the copies asynchronous; pageable ones work
+ * but make the CUDA runtime stage (and partly synchronise) the copies.
+ *
+ * h_query, h_block_tables, h_seq_lens, h_qo_indptr, h_out, h_lse
+ *              host pointers with the shapes and dtypes of mla_decode_run's
+ *              query, block_tables, seq_lens, qo_indptr (packed only; NULL
+ *              for a fixed launch), out and lse (return_lse only).
+ * kv_cache     device pointer, as for mla_decode_run.
+ * staging      caller-owned device buffer of >= mla_decode_host_staging_bytes
+ *              bytes, 256-byte aligned, exclusive to this step until the
+ *              stream has passed it.
+ * workspace    as for mla_decode_run.
+ * Errors (nothing enqueued unless stated): MLA_ERR_INVALID_ARG,
+ * MLA_ERR_WORKSPACE_TOO_SMALL (staging or workspace), MLA_ERR_ALIGNMENT;
+ * MLA_ERR_CUDA if a copy or launch fails (earlier copies may be enqueued).
+ * Not for stream capture with pageable host buffers.
+ */
+int mla_decode_run_host(const mla_plan_t *plan, const void *h_query, const void *kv_cache,
+                        const int32_t *h_block_tables, const int32_t *h_seq_lens,
+                        const int32_t *h_qo_indptr, int64_t total_q, float bmm1_scale,
+                        float bmm2_scale, void *h_out, float *h_lse, void *staging,
+                        size_t staging_bytes, void *workspace, size_t workspace_bytes,
+                        void *stream);
 
 /* Free a plan (NULL is allowed). */
 void mla_decode_destroy(mla_plan_t *plan);

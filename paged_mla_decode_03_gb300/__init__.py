@@ -91,6 +91,11 @@ def load_library():
     lib.mla_decode_run_device_scales.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp,
                                                  sz, vp]
     lib.mla_decode_run_device_scales.restype = ctypes.c_int
+    lib.mla_decode_host_staging_bytes.argtypes = [vp, i64]
+    lib.mla_decode_host_staging_bytes.restype = sz
+    lib.mla_decode_run_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, ctypes.c_float,
+                                        ctypes.c_float, vp, vp, vp, sz, vp, sz, vp]
+    lib.mla_decode_run_host.restype = ctypes.c_int
     lib.mla_merge_states.argtypes = [vp, vp, i32, i64, ctypes.c_float, vp, vp, vp]
     lib.mla_merge_states.restype = ctypes.c_int
     lib.mla_decode_destroy.argtypes = [vp]
@@ -164,6 +169,36 @@ def mla_decode_run(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr
                             int(workspace_bytes), stream)
     if rc != MLA_OK:
         raise MlaDecodeError(rc, "mla_decode_run")
+
+
+def mla_decode_host_staging_bytes(plan: int, total_q: int = 0) -> int:
+    """Device staging bytes of ``mla_decode_run_host`` for one step."""
+    return int(load_library().mla_decode_host_staging_bytes(ctypes.c_void_p(plan), int(total_q)))
+
+
+def mla_decode_run_host(plan: int, h_query, kv_cache, h_block_tables, h_seq_lens, h_qo_indptr,
+                        total_q: int, bmm1_scale: float, bmm2_scale: float, h_out, h_lse,
+                        staging, workspace, staging_bytes: Optional[int] = None,
+                        workspace_bytes: Optional[int] = None, stream=None) -> None:
+    """Enqueue one decode whose query, metadata and results are host buffers
+    (CPU tensors, ideally pinned); ``kv_cache``, ``staging`` and ``workspace``
+    are device buffers.  The copies are enqueued on ``stream`` with the decode."""
+    lib = load_library()
+    if staging_bytes is None:
+        staging_bytes = _nbytes(staging)
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    rc = lib.mla_decode_run_host(ctypes.c_void_p(plan), _ptr(h_query), _ptr(kv_cache),
+                                 _ptr(h_block_tables), _ptr(h_seq_lens), _ptr(h_qo_indptr),
+                                 int(total_q), float(bmm1_scale), float(bmm2_scale), _ptr(h_out),
+                                 _ptr(h_lse), _ptr(staging), int(staging_bytes), _ptr(workspace),
+                                 int(workspace_bytes), stream)
+    if rc != MLA_OK:
+        raise MlaDecodeError(rc, "mla_decode_run_host")
 
 
 def mla_decode_run_device_scales(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr,
@@ -247,6 +282,24 @@ class Plan:
             return
         mla_decode_run(self.handle, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q,
                        bmm1_scale, bmm2_scale, out, lse, workspace, None, stream)
+
+    def staging_bytes(self, total_q: int = 0) -> int:
+        """Device staging bytes ``run_host`` needs for a step of ``total_q`` rows."""
+        return mla_decode_host_staging_bytes(self.handle, total_q)
+
+    def run_host(self, h_query, kv_cache, h_block_tables, h_seq_lens, h_out, *, staging,
+                 workspace, h_qo_indptr=None, total_q=0, h_lse=None, bmm1_scale=1.0,
+                 bmm2_scale=1.0, stream=None):
+        """One step with host-side query, metadata and results (see
+        ``mla_decode_run_host``); returns once the copies and kernels are enqueued."""
+        for name, t in (("h_query", h_query), ("h_block_tables", h_block_tables),
+                        ("h_seq_lens", h_seq_lens), ("h_out", h_out), ("h_qo_indptr", h_qo_indptr),
+                        ("h_lse", h_lse)):
+            if isinstance(t, torch.Tensor) and (t.is_cuda or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous host tensor")
+        mla_decode_run_host(self.handle, h_query, kv_cache, h_block_tables, h_seq_lens,
+                            h_qo_indptr, total_q, bmm1_scale, bmm2_scale, h_out, h_lse, staging,
+                            workspace, None, None, stream)
 
     def close(self):
         if self.handle:

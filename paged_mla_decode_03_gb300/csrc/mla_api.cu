@@ -147,6 +147,41 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
 
 namespace {
 
+// Device staging of mla_decode_run_host: the per-step inputs and results,
+// each region 256-byte aligned.
+struct HostStaging {
+  size_t query, block_tables, seq_lens, qo_indptr, out, lse, total;
+  size_t query_bytes, block_tables_bytes, seq_lens_bytes, qo_indptr_bytes, out_bytes, lse_bytes;
+};
+
+HostStaging host_staging(const mla_decode_params& prm, int64_t total_q) {
+  const size_t B = (size_t)std::max(prm.batch, 0);
+  const size_t tokens = prm.packed ? (size_t)std::max<int64_t>(total_q, 0)
+                                   : B * (size_t)std::max(prm.max_seq_len_q, 0);
+  const size_t H = (size_t)prm.num_heads;
+  HostStaging st{};
+  st.query_bytes = tokens * H * MLA_HEAD_DIM_QK * (prm.q_dtype == MLA_Q_FP8_E4M3 ? 1 : 2);
+  st.block_tables_bytes = B * (size_t)std::max(prm.max_pages_per_req, 0) * sizeof(int32_t);
+  st.seq_lens_bytes = B * sizeof(int32_t);
+  st.qo_indptr_bytes = prm.packed ? (B + 1) * sizeof(int32_t) : 0;
+  st.out_bytes = tokens * H * MLA_HEAD_DIM_V * 2;
+  st.lse_bytes = prm.return_lse ? tokens * H * sizeof(float) : 0;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t at = off;
+    off = mla::align_up(off + n, 256);
+    return at;
+  };
+  st.query = take(st.query_bytes);
+  st.block_tables = take(st.block_tables_bytes);
+  st.seq_lens = take(st.seq_lens_bytes);
+  st.qo_indptr = take(st.qo_indptr_bytes);
+  st.out = take(st.out_bytes);
+  st.lse = take(st.lse_bytes);
+  st.total = std::max<size_t>(off, 256);
+  return st;
+}
+
 // Shared body of the run entry points.  Device scales (bmm1_dev / bmm2_dev
 // non-null) replace the host values and are read by the kernels.
 int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
@@ -274,6 +309,66 @@ int mla_merge_states(const void* o_parts, const float* lse_parts, int32_t n_part
                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
+}
+
+size_t mla_decode_host_staging_bytes(const mla_plan_t* plan, int64_t total_q) {
+  if (!plan) return 0;
+  const mla_decode_params& prm = plan->prm;
+  if (prm.packed && (total_q < 0 || total_q > prm.max_total_q)) return 0;
+  const HostStaging st = host_staging(prm, total_q);
+  return st.total;
+}
+
+int mla_decode_run_host(const mla_plan_t* plan, const void* h_query, const void* kv_cache,
+                        const int32_t* h_block_tables, const int32_t* h_seq_lens,
+                        const int32_t* h_qo_indptr, int64_t total_q, float bmm1_scale,
+                        float bmm2_scale, void* h_out, float* h_lse, void* staging,
+                        size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  const mla_decode_params& prm = plan->prm;
+  if (prm.batch == 0) return MLA_OK;
+  if (!h_query || !kv_cache || !h_block_tables || !h_seq_lens || !h_out || !staging ||
+      !workspace)
+    return MLA_ERR_INVALID_ARG;
+  if (prm.return_lse && !h_lse) return MLA_ERR_INVALID_ARG;
+  if (prm.packed) {
+    if (!h_qo_indptr || total_q < 0 || total_q > prm.max_total_q) return MLA_ERR_INVALID_ARG;
+  } else if (h_qo_indptr) {
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!(bmm1_scale >= 0.f) || bmm1_scale > 3.0e38f) return MLA_ERR_INVALID_ARG;
+  const HostStaging st = host_staging(prm, total_q);
+  if (staging_bytes < st.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < plan->lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(staging, 256)) return MLA_ERR_ALIGNMENT;
+  char* base = static_cast<char*>(staging);
+  void* d_query = base + st.query;
+  int32_t* d_bt = reinterpret_cast<int32_t*>(base + st.block_tables);
+  int32_t* d_sl = reinterpret_cast<int32_t*>(base + st.seq_lens);
+  int32_t* d_qo = prm.packed ? reinterpret_cast<int32_t*>(base + st.qo_indptr) : nullptr;
+  void* d_out = base + st.out;
+  float* d_lse = prm.return_lse ? reinterpret_cast<float*>(base + st.lse) : nullptr;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // one copy per buffer, in stream order with the decode
+  auto h2d = [&](void* dst, const void* src, size_t n) {
+    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  };
+  if (!h2d(d_query, h_query, st.query_bytes) || !h2d(d_bt, h_block_tables, st.block_tables_bytes) ||
+      !h2d(d_sl, h_seq_lens, st.seq_lens_bytes) ||
+      (d_qo && !h2d(d_qo, h_qo_indptr, st.qo_indptr_bytes)))
+    return MLA_ERR_CUDA;
+  const int rc = run_impl(plan, d_query, kv_cache, d_bt, d_sl, d_qo, total_q, bmm1_scale,
+                          bmm2_scale, nullptr, nullptr, d_out, d_lse, workspace, workspace_bytes,
+                          stream, nullptr, nullptr);
+  if (rc != MLA_OK) return rc;
+  if (st.out_bytes &&
+      cudaMemcpyAsync(h_out, d_out, st.out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (d_lse && st.lse_bytes &&
+      cudaMemcpyAsync(h_lse, d_lse, st.lse_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 void mla_decode_destroy(mla_plan_t* plan) { delete plan; }

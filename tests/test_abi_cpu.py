@@ -92,6 +92,9 @@ def test_null_arguments_are_rejected(lib):
                               0, None) == -1
     assert lib.mla_decode_run_device_scales(None, None, None, None, None, None, 0, None, None,
                                             None, None, None, 0, None) == -1
+    assert lib.mla_decode_run_host(None, None, None, None, None, None, 0, 1.0, 1.0, None, None,
+                                   None, 0, None, 0, None) == -1
+    assert lib.mla_decode_host_staging_bytes(None, 0) == 0
     lib.mla_decode_destroy(None)
     assert lib.mla_decode_workspace_size(None) == 0
 

@@ -354,6 +354,45 @@ def test_ragged_request_equals_its_own_single_request_launch():
         assert np.abs(l1 - lb).max() <= 1e-3, b
 
 
+@pytest.mark.parametrize("name", ["deepseek_v3", "ragged"])
+def test_host_buffer_entry_equals_device_entry(name):
+    """mla_decode_run_host (host query, metadata and results, staged by the
+    library) gives bitwise the device entry's results: same kernels, same
+    inputs, fixed and packed launches."""
+    import paged_mla_decode_03_gb300 as mla
+
+    w = REDUCED[name]()
+    d = to_device(w, return_lse=True)
+    run(w, d)
+    torch.cuda.synchronize()
+    total_q = w.total_q if w.packed else 0
+    tokens = d.out.shape[0]
+    need = d.plan.staging_bytes(total_q)
+    assert need > 0
+    staging = torch.empty(need, dtype=torch.uint8, device=d.workspace.device)
+    h_q = d.query.cpu().pin_memory()
+    h_bt = d.block_tables.cpu().pin_memory()
+    h_sl = d.seq_lens.cpu().pin_memory()
+    h_qo = d.qo_indptr.cpu().pin_memory() if w.packed else None
+    h_out = torch.full((tokens, w.num_heads, 512), float("nan"), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.full((tokens, w.num_heads), float("nan"), dtype=torch.float32).pin_memory()
+    # a staging buffer one byte short is refused before anything is enqueued
+    with pytest.raises(mla.MlaDecodeError):
+        mla.mla_decode_run_host(d.plan.handle, h_q, d.kv_cache, h_bt, h_sl, h_qo, total_q,
+                                w.bmm1_scale, w.bmm2_scale, h_out, h_lse, staging, d.workspace,
+                                staging_bytes=need - 1)
+    stream = torch.cuda.Stream()
+    d.plan.run_host(h_q, d.kv_cache, h_bt, h_sl, h_out, staging=staging, workspace=d.workspace,
+                    h_qo_indptr=h_qo, total_q=total_q, h_lse=h_lse, bmm1_scale=w.bmm1_scale,
+                    bmm2_scale=w.bmm2_scale, stream=stream)
+    stream.synchronize()
+    assert device_status(d) == 0
+    got = h_out.view(torch.int16).numpy()
+    want = d.out.cpu().view(torch.int16).numpy()
+    assert np.array_equal(got.reshape(want.shape), want)
+    assert np.array_equal(h_lse.numpy(), d.lse.cpu().numpy())
+
+
 def test_device_scales_equal_host_scales_and_follow_graph_replays():
     """mla_decode_run_device_scales reads bmm1/bmm2 from device memory when the
     kernels run: with the same values it is bitwise equal to the by-value
