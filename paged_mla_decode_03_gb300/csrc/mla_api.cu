@@ -341,7 +341,9 @@ int mla_decode_run_host(const mla_plan_t* plan, const void* h_query, const void*
   const HostStaging st = host_staging(prm, total_q);
   if (staging_bytes < st.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
   if (workspace_bytes < plan->lay.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  if (!aligned(staging, 256)) return MLA_ERR_ALIGNMENT;
+  // everything the decode itself would refuse is refused before a copy is enqueued
+  if (!aligned(staging, 256) || !aligned(kv_cache, 16) || !aligned(workspace, 256))
+    return MLA_ERR_ALIGNMENT;
   char* base = static_cast<char*>(staging);
   void* d_query = base + st.query;
   int32_t* d_bt = reinterpret_cast<int32_t*>(base + st.block_tables);
