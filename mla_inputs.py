@@ -66,6 +66,11 @@ class Workload:
     k_scale: Optional[float] = None
     q_dtype: str = "bf16"              # "bf16" or "e4m3" (query quantised, q_scale in bmm1)
     q_scale: Optional[float] = None
+    # decode-context parallelism: this workload is rank cp_rank's share of a
+    # sequence sharded over cp_world ranks (seq_lens local, seq_lens_global global)
+    cp_world: int = 1
+    cp_rank: int = 0
+    seq_lens_global: Optional[np.ndarray] = None
 
     @property
     def total_q(self) -> int:
@@ -285,6 +290,51 @@ WORKLOADS = {
     "ragged": ragged,
     "fp8_long": fp8_long,
 }
+
+
+def dcp_shard(w: Workload, world: int, rank: int, seed: int = 0) -> Workload:
+    """Rank ``rank``'s share of workload ``w`` under decode-context
+    parallelism over ``world`` ranks.
+
+    The KV rows of each request are dealt round robin: global row g lives on
+    rank g mod world as its local row g div world (the pages do not state the
+    layout; this is the plainest reading, with an interleave of one row).  The
+    rank's rows are copied, unchanged, into a fresh paged pool of the same
+    page size (1.25x the pages needed, shuffled, unused rows NaN-poisoned, as
+    ``build`` does); ``seq_lens`` become the local counts, which may be 0, and
+    ``seq_lens_global`` keeps the global lengths.  Query, scales and flags are
+    w's.  Pure data movement: no attention arithmetic.
+    """
+    assert w.cp_world == 1 and 0 <= rank < world
+    rng = np.random.default_rng(seed + 7919 * rank)
+    ps = w.page_size
+    B = w.batch
+    local = [np.arange(rank, int(L), world, dtype=np.int64) for L in w.seq_lens]
+    n_loc = np.array([len(g) for g in local], dtype=np.int32)
+    n_pages = (n_loc.astype(np.int64) + ps - 1) // ps
+    needed = int(n_pages.sum())
+    pool = max(1, math.ceil(1.25 * needed))
+    perm = rng.permutation(pool).astype(np.int32)
+    max_pages = max(1, int(n_pages.max()) if B else 1)
+    bt = np.empty((B, max_pages), dtype=np.int32)
+    nan = BF16_NAN if w.kv_dtype == "bf16" else E4M3_NAN
+    kv = np.full((pool, ps, HEAD_DIM_QK), nan, dtype=w.kv_cache.dtype)
+    pos = 0
+    for b in range(B):
+        k = int(n_pages[b])
+        bt[b, :k] = perm[pos:pos + k]
+        pos += k
+        tail = bt[b, k:]
+        tail[0::2] = -1
+        tail[1::2] = pool + 7
+        g = local[b]
+        src = w.kv_cache[w.block_tables[b, g // ps], g % ps]      # [n_loc, 576]
+        j = np.arange(len(g))
+        kv[bt[b, j // ps], j % ps] = src
+    return dataclasses.replace(
+        w, name=f"{w.name}_dcp{rank}of{world}", seq_lens=n_loc, kv_cache=kv, block_tables=bt,
+        max_seq_len=max(1, int(n_loc.max()) if B else 1), cp_world=world, cp_rank=rank,
+        seq_lens_global=w.seq_lens.copy())
 
 
 def permute_pages(w: Workload, seed: int) -> Workload:

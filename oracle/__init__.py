@@ -20,7 +20,11 @@ and causal rule from the FlashInfer page
     O   = bmm2_scale * sum_j exp(s_j - lse) * K_b[j,:512]
 
 with K_b gathered through ``block_tables`` and row i of a request of q_len q
-seeing rows 0 .. seq_len - q + i (causal) or 0 .. seq_len - 1 (dense).
+seeing rows 0 .. seq_len - q + i (causal) or 0 .. seq_len - 1 (dense).  Under
+decode-context parallelism (``cp_world`` > 1; the vLLM ``FlashInferMLAImpl``
+page passes cp_world, cp_rank and the global KV lengths to the kernel) a
+rank's local row j is global row j * cp_world + cp_rank and the causal bound
+is taken on that global position against the global length.
 
 Parity status of each function is pinned by ``tests/test_oracle_pins.py``.
 """
@@ -70,6 +74,9 @@ def _load():
             ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
             ctypes.c_double, ctypes.c_double, ctypes.c_int64, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_mla_decode_dcp.restype = ctypes.c_int
+        lib.oracle_mla_decode_dcp.argtypes = lib.oracle_mla_decode_q.argtypes + [
+            ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
@@ -97,7 +104,8 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
                block_tables: np.ndarray, seq_lens: np.ndarray, *, kv_dtype: str,
                causal: bool, bmm1_scale: float, bmm2_scale: float,
                sel: Optional[np.ndarray] = None, n_threads: Optional[int] = None,
-               q_dtype: str = "bf16"):
+               q_dtype: str = "bf16", cp_world: int = 1, cp_rank: int = 0,
+               seq_lens_global: Optional[np.ndarray] = None):
     """fp64 O and LSE.
 
     query:   uint16 bf16 bits (q_dtype "bf16") or uint8 e4m3 codes ("e4m3")
@@ -105,7 +113,12 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
     q_start: [B+1] token offset of each request (fixed launches: b * SQ)
     kv_cache: uint16 (bf16) or uint8 (e4m3) [pages, page_size, 576]
     sel:     optional [n, 2] (token, head) pairs; default every pair.
+    cp_world, cp_rank, seq_lens_global: decode-context parallelism -- this
+             rank holds the global rows g with g mod cp_world == cp_rank as
+             its local rows g div cp_world; the causal bound applies to the
+             global positions, with global lengths seq_lens_global [B].
     Returns (out, lse): [tokens, H, 512] and [tokens, H], or [n, 512] and [n].
+    Rows that see no key get O = 0 and lse = -inf (the empty sum).
     """
     lib = _load()
     H = int(query.shape[-2])
@@ -144,12 +157,17 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
     lse = np.zeros(lse_shape, dtype=np.float64)
     if n == 0 or B == 0:
         return out, lse
-    rc = lib.oracle_mla_decode_q(
+    slg = None
+    if cp_world > 1 and seq_lens_global is not None:
+        slg = np.ascontiguousarray(seq_lens_global, dtype=np.int32)
+        assert slg.shape == sl.shape
+    rc = lib.oracle_mla_decode_dcp(
         B, H, kd, qd, q.ctypes.data, qs.ctypes.data, kv.ctypes.data, int(kv.shape[0]),
         int(kv.shape[1]), bt.ctypes.data, int(bt.shape[1]), sl.ctypes.data, int(bool(causal)),
         float(bmm1_scale), float(bmm2_scale), n,
         sel_arr.ctypes.data if sel_arr is not None else None,
-        out.ctypes.data, lse.ctypes.data, int(n_threads or default_threads()))
+        out.ctypes.data, lse.ctypes.data, int(n_threads or default_threads()),
+        int(cp_world), int(cp_rank), slg.ctypes.data if slg is not None else None)
     if rc != 0:
         raise RuntimeError(f"oracle_mla_decode failed with status {rc}")
     return out, lse
@@ -161,4 +179,6 @@ def run(w, sel: Optional[np.ndarray] = None, n_threads: Optional[int] = None,
     return mla_decode(w.query_rows(), w.q_start(), w.kv_cache, w.block_tables, w.seq_lens,
                       kv_dtype=w.kv_dtype, causal=w.causal if causal is None else causal,
                       bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, sel=sel,
-                      n_threads=n_threads, q_dtype=getattr(w, "q_dtype", "bf16"))
+                      n_threads=n_threads, q_dtype=getattr(w, "q_dtype", "bf16"),
+                      cp_world=getattr(w, "cp_world", 1), cp_rank=getattr(w, "cp_rank", 0),
+                      seq_lens_global=getattr(w, "seq_lens_global", None))

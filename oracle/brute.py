@@ -8,7 +8,11 @@ rounded), so on tiny inputs the two implementations must agree to ~1e-12.
 The mask follows the FlashInfer page "prims_ts_batch_decode_with_kv_cache_mla":
 query row i of a request with q rows and L cached rows attends through KV row
 L - q + i; written here as the predicate ``j - (L - q) <= i`` (causal) or
-``j < L`` (dense).
+``j < L`` (dense).  Under decode-context parallelism (the vLLM
+``FlashInferMLAImpl`` page passes cp_world, cp_rank and the global KV lengths
+to the kernel) local row j of rank r holds global row j * W + r, and the
+causal predicate is applied to that global position against the global
+length: ``(j * W + r) - (Lg - q) <= i``.
 """
 from __future__ import annotations
 
@@ -33,8 +37,10 @@ def e4m3_value(bits: int) -> float:
 
 
 def mla_decode(query, q_start, kv_cache, block_tables, seq_lens, *, kv_dtype, causal,
-               bmm1_scale, bmm2_scale, q_dtype="bf16"):
-    """Return (out[tokens][H][512], lse[tokens][H]) as nested Python lists."""
+               bmm1_scale, bmm2_scale, q_dtype="bf16", cp_world=1, cp_rank=0,
+               seq_lens_global=None):
+    """Return (out[tokens][H][512], lse[tokens][H]) as nested Python lists.
+    A row with no visible key gets zeros and -inf."""
     decode = bf16_value if kv_dtype == "bf16" else e4m3_value
     q_decode = bf16_value if q_dtype == "bf16" else e4m3_value
     tokens, H, D = query.shape
@@ -49,8 +55,21 @@ def mla_decode(query, q_start, kv_cache, block_tables, seq_lens, *, kv_dtype, ca
         for j in range(L):
             page = int(block_tables[b][j // ps])
             rows.append([decode(x) for x in kv_cache[page][j % ps]])
+        if cp_world > 1:
+            Lg = int(seq_lens_global[b])
+
+            def seen(j, i):
+                return (j * cp_world + cp_rank) - (Lg - q) <= i
+        else:
+            def seen(j, i):
+                return j - (L - q) <= i
         for i in range(q):
-            visible = [j for j in range(L) if (j - (L - q) <= i if causal else True)]
+            visible = [j for j in range(L) if (seen(j, i) if causal else True)]
+            if not visible:
+                for h in range(H):
+                    lse[t0 + i][h] = float("-inf")
+                    out[t0 + i][h] = [0.0] * 512
+                continue
             for h in range(H):
                 qv = [q_decode(x) for x in query[t0 + i][h]]
                 s = [bmm1_scale * math.fsum(qv[d] * rows[j][d] for d in range(D))

@@ -12,6 +12,12 @@
  *   for query row i in [0, q) and head h:
  *     visible j: 0 <= j <= L - q + i        (bottom-right causal)
  *                0 <= j <  L                (dense)
+ *     under decode-context parallelism (the vLLM FlashInferMLAImpl page,
+ *     forward_mqa, passes cp_world, cp_rank and causal_seqlens_kv_global to
+ *     the kernel): this rank r of W holds the rows g of the global sequence
+ *     (length Lg) with g mod W == r as its local rows j = g div W, and the
+ *     causal bound applies to global positions: local row j is visible
+ *     iff j * W + r <= Lg - q + i
  *     s_j   = bmm1_scale * sum_{d < 576} Q[b,i,h,d] * K_b[j][d]
  *     lse   = m + ln(sum_j exp(s_j - m)),  m = max_j s_j      (natural log,
  *             as the vLLM FlashInferMLAImpl page states for its LSE)
@@ -64,6 +70,8 @@ double oracle_decode_e4m3(uint8_t bits) { return e4m3_to_double(bits); }
 
 typedef struct {
   int batch, num_heads, kv_dtype, q_dtype, page_size, max_pages_per_req, causal;
+  int cp_world, cp_rank;               /* decode-context parallelism (cp_world 1: off) */
+  const int32_t *seq_lens_global;      /* [B] global KV lengths when cp_world > 1 */
   const void *query;         /* [tokens, H, 576] bf16 bits or e4m3 codes (q_dtype) */
   const int64_t *q_start;    /* [B + 1] token offsets */
   const void *kv_cache;      /* [num_pages, ps, 576] */
@@ -104,7 +112,19 @@ static int one_unit(job_t *J, int64_t u, double *s, double *qv) {
   int64_t i = t - J->q_start[b];
   int64_t q = J->q_start[b + 1] - J->q_start[b];
   int64_t L = J->seq_lens[b];
-  int64_t last = J->causal ? (L - q + i) : (L - 1);   /* inclusive */
+  int64_t last;   /* inclusive */
+  if (!J->causal) {
+    last = L - 1;
+  } else if (J->cp_world > 1) {
+    /* local row j holds global row j * W + r; the visible ones are those
+       whose global position is at most Lg - q + i (a prefix of the rows) */
+    const int64_t W = J->cp_world, r = J->cp_rank, Lg = J->seq_lens_global[b];
+    int64_t n_vis = 0;
+    while (n_vis < L && n_vis * W + r <= Lg - q + i) ++n_vis;
+    last = n_vis - 1;
+  } else {
+    last = L - q + i;
+  }
   if (last > L - 1) last = L - 1;
   int64_t n = last + 1;
   double *o = J->out + u * V_DIM;
@@ -175,21 +195,29 @@ static void *worker(void *arg) {
 
 /*
  * Compute O and LSE for the selected (token, head) pairs (all pairs when
- * sel == NULL, in [token][head] order).  Returns 0 on success, 1 if a page
- * id read for a visible row was out of range, 2 on allocation failure.
+ * sel == NULL, in [token][head] order) on rank cp_rank of cp_world
+ * decode-context-parallel ranks (cp_world 1: the whole sequence is local and
+ * seq_lens_global is not read).  Returns 0 on success, 1 if a page id read
+ * for a visible row was out of range, 2 on allocation failure, 3 on a bad
+ * rank description.
  */
-int oracle_mla_decode_q(int batch, int num_heads, int kv_dtype, int q_dtype,
-                        const void *query, const int64_t *q_start,
-                        const void *kv_cache, int64_t num_pages, int page_size,
-                        const int32_t *block_tables, int max_pages_per_req,
-                        const int32_t *seq_lens, int causal,
-                        double bmm1_scale, double bmm2_scale,
-                        int64_t n_sel, const int64_t *sel,
-                        double *out, double *lse, int n_threads) {
+int oracle_mla_decode_dcp(int batch, int num_heads, int kv_dtype, int q_dtype,
+                          const void *query, const int64_t *q_start,
+                          const void *kv_cache, int64_t num_pages, int page_size,
+                          const int32_t *block_tables, int max_pages_per_req,
+                          const int32_t *seq_lens, int causal,
+                          double bmm1_scale, double bmm2_scale,
+                          int64_t n_sel, const int64_t *sel,
+                          double *out, double *lse, int n_threads,
+                          int cp_world, int cp_rank, const int32_t *seq_lens_global) {
   job_t J;
+  if (cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world ||
+      (cp_world > 1 && causal && !seq_lens_global))
+    return 3;
   memset(&J, 0, sizeof J);
   J.batch = batch; J.num_heads = num_heads; J.kv_dtype = kv_dtype; J.q_dtype = q_dtype;
   J.page_size = page_size; J.max_pages_per_req = max_pages_per_req; J.causal = causal;
+  J.cp_world = cp_world; J.cp_rank = cp_rank; J.seq_lens_global = seq_lens_global;
   J.query = query; J.q_start = q_start; J.kv_cache = kv_cache; J.num_pages = num_pages;
   J.block_tables = block_tables; J.seq_lens = seq_lens;
   J.bmm1_scale = bmm1_scale; J.bmm2_scale = bmm2_scale;
@@ -207,6 +235,21 @@ int oracle_mla_decode_q(int batch, int num_heads, int kv_dtype, int q_dtype,
   for (int k = 0; k < started; ++k) pthread_join(th[k], NULL);
   pthread_mutex_destroy(&J.lock);
   return J.status;
+}
+
+/* The whole sequence on one rank. */
+int oracle_mla_decode_q(int batch, int num_heads, int kv_dtype, int q_dtype,
+                        const void *query, const int64_t *q_start,
+                        const void *kv_cache, int64_t num_pages, int page_size,
+                        const int32_t *block_tables, int max_pages_per_req,
+                        const int32_t *seq_lens, int causal,
+                        double bmm1_scale, double bmm2_scale,
+                        int64_t n_sel, const int64_t *sel,
+                        double *out, double *lse, int n_threads) {
+  return oracle_mla_decode_dcp(batch, num_heads, kv_dtype, q_dtype, query, q_start, kv_cache,
+                               num_pages, page_size, block_tables, max_pages_per_req, seq_lens,
+                               causal, bmm1_scale, bmm2_scale, n_sel, sel, out, lse, n_threads,
+                               1, 0, NULL);
 }
 
 /* The same with a bf16 query. */

@@ -1,9 +1,11 @@
 """CPU tests of bench.py's host logic: the algorithmic work model and the
 multi-rank reductions (world_size 2 over gloo on 127.0.0.1)."""
+import dataclasses
 import os
 import socket
 
 import numpy as np
+import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -65,9 +67,12 @@ def test_roofline_picks_the_binding_resource():
     assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-12
 
 
-def _dcp_worker(rank, world, port, out):
+def _dcp_worker(rank, world, port, out, layout):
     """One DCP rank on CPU: its shard's partial state (from the oracle), the
-    library's all-gather step over gloo, then the reference LSE merge."""
+    library's all-gather step over gloo, then the reference LSE merge.
+    layout "round_robin": global KV row g on rank g mod world, causal bound on
+    global positions (the per-rank decode the vLLM FlashInferMLAImpl page asks
+    of the kernel); "prefix_suffix": a dense prefix and a causal suffix."""
     import sys
     sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
     import dcp_shards
@@ -78,7 +83,10 @@ def _dcp_worker(rank, world, port, out):
     dist.init_process_group("gloo", rank=rank, world_size=world)
     w = mi.build("dcp", 77, num_heads=2, page_size=4, seq_lens=[23, 17, 30], q_lens=[3, 3, 3],
                  packed=False, causal=True, return_lse=True, bmm1_scale=0.3, bmm2_scale=1.5)
-    shard = dcp_shards.shards(w)[rank]
+    if layout == "round_robin":  # shards run with bmm2 = 1; the merge applies w's
+        shard = dataclasses.replace(mi.dcp_shard(w, world, rank), bmm2_scale=1.0)
+    else:
+        shard = dcp_shards.shards(w)[rank]
     o, l = oracle.run(shard)
     outs, lses = mla.dcp_gather(torch.from_numpy(o), torch.from_numpy(l))
     merged, lse = dcp_shards.merge_reference(outs.numpy(), lses.numpy(), w.bmm2_scale)
@@ -88,10 +96,11 @@ def _dcp_worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
-def test_dcp_two_ranks_gather_and_merge_equal_single_pass_over_gloo():
+@pytest.mark.parametrize("layout", ["round_robin", "prefix_suffix"])
+def test_dcp_two_ranks_gather_and_merge_equal_single_pass_over_gloo(layout):
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
-    mp.start_processes(_dcp_worker, args=(2, _free_port(), out), nprocs=2, join=True,
+    mp.start_processes(_dcp_worker, args=(2, _free_port(), out, layout), nprocs=2, join=True,
                        start_method="spawn")
     for r in range(2):
         d_o, d_l, shape = out[r]

@@ -356,3 +356,64 @@ def test_e4m3_query_quantisation_folds_q_scale_into_bmm1():
     assert w8.bmm1_scale == np.float32(0.25 * w8.q_scale)
     deq = as_f64(w8.query, "e4m3") * w8.q_scale
     assert np.abs(deq - q).max() <= 2.0 ** -4 * np.abs(q).max()  # e4m3 keeps 3 mantissa bits
+
+
+# ---------------------------------------------------------------- decode-context parallelism
+
+@pytest.mark.parametrize("world,case", [
+    (2, dict(seq_lens=(9, 14, 3), q_lens=(3, 3, 3), causal=True)),
+    (3, dict(seq_lens=(9, 14, 4), q_lens=(2, 2, 2), causal=True)),
+    (4, dict(seq_lens=(2, 11, 7), q_lens=(2, 2, 2), causal=True)),   # ranks with no rows
+    (4, dict(seq_lens=(6, 3, 11), q_lens=(2, 3, 1), packed=True)),
+    (3, dict(seq_lens=(7, 12), q_lens=(3, 3), causal=False)),
+])
+def test_dcp_rank_states_merge_to_the_single_pass(world, case):
+    """Each rank's oracle state over its round-robin share of the rows, with the
+    causal bound taken on global positions, merged across ranks by natural-log
+    LSE (the vLLM FlashInferMLAImpl page's DCP merge) equals the one-pass
+    oracle on the whole sequence.  A wrong global/local index map or a causal
+    bound on local positions double-counts or drops rows and fails this."""
+    w = small(61, H=2, **case)
+    full_o, full_l = oracle.run(w)
+    parts = [oracle.run(mi.dcp_shard(w, world, r)) for r in range(world)]
+    lses = np.stack([p[1] for p in parts])
+    lse = np.logaddexp.reduce(lses, axis=0)
+    o = sum(np.exp(p[1] - lse)[..., None] * p[0] for p in parts)
+    np.testing.assert_allclose(lse, full_l, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(o, full_o, rtol=1e-11, atol=1e-14)
+
+
+def test_dcp_with_one_rank_is_the_plain_oracle():
+    w = small(62, H=2, seq_lens=(9, 5), q_lens=(2, 2))
+    o1, l1 = oracle.run(w)
+    o2, l2 = oracle.run(mi.dcp_shard(w, 1, 0))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_dcp_rows_without_keys_are_empty_sums():
+    """Global length 2, q = 2, four ranks: rank 1 sees its one row only from
+    query row 1 on, ranks 2 and 3 hold nothing, so those rows are the empty
+    sum (O = 0, lse = -inf), which the LSE merge ignores."""
+    w = small(63, H=2, seq_lens=(2,), q_lens=(2,))
+    o1, l1 = oracle.run(mi.dcp_shard(w, 4, 1))
+    assert np.all(np.isneginf(l1[0])) and np.all(o1[0] == 0) and np.all(np.isfinite(l1[1]))
+    for r in (2, 3):
+        o, l = oracle.run(mi.dcp_shard(w, 4, r))
+        assert np.all(np.isneginf(l)) and np.all(o == 0)
+
+
+@pytest.mark.parametrize("world,rank,causal", [(2, 1, True), (3, 0, True), (3, 2, True),
+                                               (4, 3, False)])
+def test_dcp_c_oracle_matches_python_brute_force(world, rank, causal):
+    w = small(64, H=2, seq_lens=(9, 14, 5), q_lens=(3, 3, 3), causal=causal, bmm1=0.5)
+    sh = mi.dcp_shard(w, world, rank)
+    out, lse = oracle.run(sh)
+    bo, bl = brute.mla_decode(sh.query_rows(), sh.q_start(), sh.kv_cache, sh.block_tables,
+                              sh.seq_lens, kv_dtype=sh.kv_dtype, causal=sh.causal,
+                              bmm1_scale=sh.bmm1_scale, bmm2_scale=sh.bmm2_scale,
+                              cp_world=world, cp_rank=rank, seq_lens_global=sh.seq_lens_global)
+    bl = np.array(bl)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(bl))
+    fin = np.isfinite(bl)
+    np.testing.assert_allclose(out, np.array(bo), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse[fin], bl[fin], rtol=1e-12, atol=1e-12)
