@@ -82,6 +82,9 @@ typedef struct mla_decode_params {
   int32_t device;            /* CUDA device ordinal the plan is for */
   int32_t q_dtype;           /* mla_q_dtype: bf16, or e4m3 with the caller's q_scale
                                 folded into bmm1 (bmm1 = q_scale * k_scale * softmax scale) */
+  int32_t cp_world;          /* decode-context parallelism: ranks the KV sequence is
+                                sharded over (0 or 1: off; > 1: run with mla_decode_run_dcp) */
+  int32_t cp_rank;           /* this rank, 0 <= cp_rank < cp_world (0 when off) */
 } mla_decode_params;
 
 typedef struct mla_plan_s mla_plan_t; /* opaque; host memory only */
@@ -123,8 +126,13 @@ int mla_decode_plan(const mla_decode_params *params, mla_plan_t **plan,
  *              graph) and not overlapping any other argument.  Needs no
  *              zeroing: every launch re-initialises what it uses.
  *
- * Errors (synchronous, nothing enqueued): MLA_ERR_INVALID_ARG,
- * MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_ALIGNMENT; MLA_ERR_CUDA if a launch fails.
+ * Call with params.device current (the kernels launch on the current
+ * device; the plan's launch shapes belong to params.device).
+ *
+ * Errors (synchronous, nothing enqueued): MLA_ERR_INVALID_ARG (also: another
+ * device current, or a causal decode-context-parallel plan, which needs
+ * mla_decode_run_dcp), MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_ALIGNMENT;
+ * MLA_ERR_CUDA if a launch fails.
  */
 int mla_decode_run(const mla_plan_t *plan, const void *query, const void *kv_cache,
                    const int32_t *block_tables, const int32_t *seq_lens,
@@ -190,12 +198,17 @@ int mla_decode_run_device_scales(const mla_plan_t *plan, const void *query, cons
  *
  * Same arguments and errors as mla_decode_run, minus the workspace.  Returns
  * MLA_ERR_WORKSPACE_TOO_SMALL if the plan needs more scratch than
- * MLA_STATIC_WORKSPACE_BYTES.  The first call on each device resolves the
- * array's device address (cudaGetSymbolAddress, with that device current);
- * make that first call before any stream capture that includes this entry
- * point.  All calls on a device share the one array: calls that may overlap
- * on the GPU race, so the caller must order them (one stream, or events).
- * Nothing needs clearing between calls; each run re-initialises what it uses.
+ * MLA_STATIC_WORKSPACE_BYTES.  The array used is the current device's, so
+ * call with the plan's device current (else MLA_ERR_INVALID_ARG).  Every call
+ * made outside stream capture resolves the array's device address
+ * (cudaGetSymbolAddress, with that device current); a call made while its
+ * stream is being captured uses the address the last uncaptured call on the
+ * device resolved, so make one uncaptured call on each device before any
+ * stream capture that includes this entry point (MLA_ERR_CUDA otherwise),
+ * and again after a device reset.  All calls on a device share the one
+ * array: calls that may overlap on the GPU race, so the caller must order
+ * them (one stream, or events).  Nothing needs clearing between calls; each
+ * run re-initialises what it uses.
  */
 int mla_decode_run_static_workspace(const mla_plan_t *plan, const void *query,
                                     const void *kv_cache, const int32_t *block_tables,
@@ -251,6 +264,40 @@ int mla_decode_run_host(const mla_plan_t *plan, const void *h_query, const void 
 void mla_decode_destroy(mla_plan_t *plan);
 
 /*
+ * One rank's share of a decode under decode-context parallelism (DCP): the
+ * vLLM "FlashInferMLAImpl" page (forward_mqa, its dcp_world_size > 1 branch)
+ * hands the kernel enable_dcp, cp_world, cp_rank and causal_seqlens_kv_global.
+ * The pages do not spell out the shard layout; this library reads it as a
+ * round robin of single rows: global KV row g of a request lives on rank
+ * g mod cp_world, as that rank's local row g div cp_world.  So, for request b
+ * of global length Lg = causal_seqlens_kv_global[b]:
+ *   seq_lens[b]      the rank's local row count, the number of g < Lg with
+ *                    g mod cp_world == cp_rank (0 is allowed);
+ *   block_tables     page the local rows as usual;
+ *   causal masking   query row i sees the local rows j whose global position
+ *                    j * cp_world + cp_rank is <= Lg - q_len + i;
+ *   dense masking    sees every local row (causal_seqlens_kv_global may be NULL).
+ * A query row that sees no local row gets out = 0 and lse = -inf, the empty
+ * sum, which mla_merge_states ignores.  Merging every rank's (out, lse) with
+ * mla_merge_states (bmm2_scale = 1 here, bmm2 there) gives the single pass
+ * over the whole sequence.
+ *
+ * plan         made with params.cp_world > 1 and params.cp_rank.
+ * causal_seqlens_kv_global
+ *              device int32 [B], 1 <= Lg, q_len(b) <= Lg (causal); required
+ *              for causal plans, NULL for dense ones.
+ * All other arguments, errors and capture rules as mla_decode_run
+ * (return_lse is what makes the result mergeable).  mla_decode_run and the
+ * other run entry points refuse a causal DCP plan (MLA_ERR_INVALID_ARG).
+ */
+int mla_decode_run_dcp(const mla_plan_t *plan, const void *query, const void *kv_cache,
+                       const int32_t *block_tables, const int32_t *seq_lens,
+                       const int32_t *qo_indptr, int64_t total_q,
+                       const int32_t *causal_seqlens_kv_global, float bmm1_scale,
+                       float bmm2_scale, void *out, float *lse, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
  * Merge n partial attention states of the same query rows into one: the
  * exchange step of decode-context parallelism (DCP), where each rank runs
  * mla_decode_run over its own shard of every request's KV rows with
@@ -267,7 +314,8 @@ void mla_decode_destroy(mla_plan_t *plan);
  * out        bf16 [rows, 512]; lse_out fp32 [rows] or NULL
  * All device pointers; o_parts and out 16-byte aligned.  Enqueued on
  * `stream`, capture-safe, allocates nothing.
- * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_ALIGNMENT, MLA_ERR_CUDA.
+ * Errors: MLA_ERR_INVALID_ARG (n_parts < 1, rows < 0 or > 2^40, n_parts * rows
+ * > 9e15), MLA_ERR_ALIGNMENT, MLA_ERR_CUDA.
  */
 int mla_merge_states(const void *o_parts, const float *lse_parts, int32_t n_parts, int64_t rows,
                      float scale, void *out, float *lse_out, void *stream);

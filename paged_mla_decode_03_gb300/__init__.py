@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "MLA_OK", "MlaDecodeError", "MlaDecodeParams", "load_library", "library_path",
-    "mla_decode_plan", "mla_decode_run", "mla_decode_run_profiled", "mla_decode_destroy", "mla_decode_workspace_size",
+    "mla_decode_plan", "mla_decode_run", "mla_decode_run_profiled", "mla_decode_run_dcp", "mla_decode_destroy", "mla_decode_workspace_size",
     "mla_decode_status_offset", "mla_decode_status_string", "Plan", "decode",
     "HEAD_DIM_QK", "HEAD_DIM_V",
 ]
@@ -63,6 +63,8 @@ class MlaDecodeParams(ctypes.Structure):
         ("return_lse", ctypes.c_int32),
         ("device", ctypes.c_int32),
         ("q_dtype", ctypes.c_int32),
+        ("cp_world", ctypes.c_int32),
+        ("cp_rank", ctypes.c_int32),
     ]
 
 
@@ -96,6 +98,9 @@ def load_library():
     lib.mla_decode_run_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, ctypes.c_float,
                                         ctypes.c_float, vp, vp, vp, sz, vp, sz, vp]
     lib.mla_decode_run_host.restype = ctypes.c_int
+    lib.mla_decode_run_dcp.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, ctypes.c_float,
+                                       ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.mla_decode_run_dcp.restype = ctypes.c_int
     lib.mla_merge_states.argtypes = [vp, vp, i32, i64, ctypes.c_float, vp, vp, vp]
     lib.mla_merge_states.restype = ctypes.c_int
     lib.mla_decode_destroy.argtypes = [vp]
@@ -169,6 +174,29 @@ def mla_decode_run(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr
                             int(workspace_bytes), stream)
     if rc != MLA_OK:
         raise MlaDecodeError(rc, "mla_decode_run")
+
+
+def mla_decode_run_dcp(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr,
+                       total_q: int, seq_lens_global, bmm1_scale: float, bmm2_scale: float,
+                       out, lse, workspace, workspace_bytes: Optional[int] = None,
+                       stream=None) -> None:
+    """One decode-context-parallel rank's decode (``mla_decode_run_dcp``):
+    ``seq_lens`` are the rank's local row counts, ``seq_lens_global`` the
+    global KV lengths the causal bound is taken against (None for dense)."""
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    rc = lib.mla_decode_run_dcp(ctypes.c_void_p(plan), _ptr(query), _ptr(kv_cache),
+                                _ptr(block_tables), _ptr(seq_lens), _ptr(qo_indptr), int(total_q),
+                                _ptr(seq_lens_global), float(bmm1_scale), float(bmm2_scale),
+                                _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                stream)
+    if rc != MLA_OK:
+        raise MlaDecodeError(rc, "mla_decode_run_dcp")
 
 
 def mla_decode_host_staging_bytes(plan: int, total_q: int = 0) -> int:
@@ -260,7 +288,8 @@ class Plan:
     def __init__(self, *, batch: int, num_heads: int, max_seq_len_q: int, max_seq_len: int,
                  page_size: int, max_pages_per_req: int, num_pages: int, packed: bool,
                  max_total_q: int = 0, kv_dtype: str = "bf16", causal: bool = True,
-                 return_lse: bool = False, device: int = 0, q_dtype: str = "bf16"):
+                 return_lse: bool = False, device: int = 0, q_dtype: str = "bf16",
+                 cp_world: int = 1, cp_rank: int = 0):
         self.params = MlaDecodeParams(
             batch=batch, num_heads=num_heads, max_seq_len_q=max_seq_len_q,
             max_seq_len=max_seq_len, page_size=page_size, max_pages_per_req=max_pages_per_req,
@@ -268,13 +297,23 @@ class Plan:
             kv_dtype=KV_FP8_E4M3 if kv_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else KV_BF16,
             mask=MASK_CAUSAL if causal else MASK_DENSE, return_lse=int(bool(return_lse)),
             device=device,
-            q_dtype=Q_FP8_E4M3 if q_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else Q_BF16)
+            q_dtype=Q_FP8_E4M3 if q_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else Q_BF16,
+            cp_world=cp_world, cp_rank=cp_rank)
+        self.cp_world = cp_world
         self.handle, self.workspace_bytes = mla_decode_plan(self.params)
 
     def run(self, query, kv_cache, block_tables, seq_lens, out, *, qo_indptr=None, total_q=0,
-            lse=None, workspace=None, bmm1_scale=1.0, bmm2_scale=1.0, stream=None):
+            lse=None, workspace=None, bmm1_scale=1.0, bmm2_scale=1.0, stream=None,
+            seq_lens_global=None):
         """Scales are Python floats, or one-element fp32 CUDA tensors (then both
-        must be, and the kernels read them when they run)."""
+        must be, and the kernels read them when they run).  A plan with
+        ``cp_world`` > 1 runs one DCP rank's decode (``seq_lens_global``: the
+        global KV lengths, required under causal masking)."""
+        if self.cp_world > 1:
+            mla_decode_run_dcp(self.handle, query, kv_cache, block_tables, seq_lens, qo_indptr,
+                               total_q, seq_lens_global, bmm1_scale, bmm2_scale, out, lse,
+                               workspace, None, stream)
+            return
         if isinstance(bmm1_scale, torch.Tensor) or isinstance(bmm2_scale, torch.Tensor):
             mla_decode_run_device_scales(self.handle, query, kv_cache, block_tables, seq_lens,
                                          qo_indptr, total_q, bmm1_scale, bmm2_scale, out, lse,
@@ -321,7 +360,8 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
            qo_indptr: Optional[torch.Tensor] = None, max_seq_len_q: Optional[int] = None,
            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
            bmm1_scale=1.0, bmm2_scale=1.0, mask_type: str = "causal",
-           return_lse: bool = False):
+           return_lse: bool = False, cp_world: int = 1, cp_rank: int = 0,
+           causal_seqlens_kv_global: Optional[torch.Tensor] = None):
     """Paged MLA decode.  Returns ``out`` (and ``lse`` when ``return_lse``).
 
     ``query``: bf16 or float8_e4m3fn (quantised with a q_scale the caller folds
@@ -331,6 +371,9 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
     the plan's workspace bytes (see ``Plan``).  Plans are cached per static key.
     ``bmm1_scale`` / ``bmm2_scale``: floats, or one-element fp32 CUDA tensors the
     kernels read at run time (for scales that change between graph replays).
+    ``cp_world`` / ``cp_rank`` / ``causal_seqlens_kv_global``: one rank of a
+    decode-context-parallel decode (the vLLM FlashInferMLAImpl page's DCP
+    keyword arguments); ``seq_lens`` are then the rank's local row counts.
     """
     if query.dtype not in (torch.bfloat16, torch.float8_e4m3fn) or not query.is_cuda:
         raise ValueError("query must be a bf16 or float8_e4m3fn CUDA tensor")
@@ -367,14 +410,15 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
         raise ValueError(mask_type)
     key = (B, H, sq, int(max_seq_len), int(kv_cache.shape[1]), int(block_tables.shape[1]),
            int(kv_cache.shape[0]), packed, total_q if packed else 0, kv_dtype, causal,
-           bool(return_lse), query.device.index or 0, q_dtype)
+           bool(return_lse), query.device.index or 0, q_dtype, int(cp_world), int(cp_rank))
     plan = _plans.get(key)
     if plan is None:
         plan = Plan(batch=B, num_heads=H, max_seq_len_q=sq, max_seq_len=int(max_seq_len),
                     page_size=int(kv_cache.shape[1]), max_pages_per_req=int(block_tables.shape[1]),
                     num_pages=int(kv_cache.shape[0]), packed=packed, max_total_q=total_q,
                     kv_dtype=kv_dtype, causal=causal, return_lse=return_lse,
-                    device=query.device.index or 0, q_dtype=q_dtype)
+                    device=query.device.index or 0, q_dtype=q_dtype, cp_world=int(cp_world),
+                    cp_rank=int(cp_rank))
         _plans[key] = plan
     if workspace_buffer.numel() * workspace_buffer.element_size() < plan.workspace_bytes:
         raise ValueError(f"workspace_buffer needs {plan.workspace_bytes} bytes")
@@ -384,7 +428,8 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
         lse = torch.empty(lse_shape, dtype=torch.float32, device=query.device)
     plan.run(query, kv_cache, block_tables, seq_lens, out, qo_indptr=qo_indptr, total_q=total_q,
              lse=lse if return_lse else None, workspace=workspace_buffer,
-             bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale)
+             bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale,
+             seq_lens_global=causal_seqlens_kv_global if causal else None)
     return (out, lse) if return_lse else out
 
 

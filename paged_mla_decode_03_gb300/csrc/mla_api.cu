@@ -61,7 +61,11 @@ int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int row
   lay->n_ctas = n_ctas;
   lay->max_groups = (int)groups;
   lay->max_items = (int)max_items;
-  lay->max_combine = (int)std::min(groups, (long long)n_workers);
+  // split groups (at most one per worker boundary), plus, under decode-context
+  // parallelism, one empty entry per row group of a request the rank holds no
+  // row of: never more than one entry per group
+  lay->max_combine =
+      (int)(prm.cp_world > 1 ? groups : std::min(groups, (long long)n_workers));
   lay->max_partials = (int)std::min(max_items, 2LL * n_workers);
   size_t off = kHeaderBytes;
   lay->items = off;
@@ -71,7 +75,7 @@ int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int row
   lay->worker_ranges = off;
   off = align_up(off + sizeof(int) * (n_workers + 1), 256);
   lay->req_scratch = off;
-  const size_t req_bytes = align_up(sizeof(int) * 4 * std::max(B, 1LL), 256);
+  const size_t req_bytes = align_up(sizeof(int) * 6 * std::max(B, 1LL), 256);
   off += req_bytes;
   lay->group_scratch = off;
   const size_t grp_bytes = align_up(sizeof(long long) * lay->max_groups +
@@ -107,6 +111,9 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (p.kv_dtype != MLA_KV_BF16 && p.kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
   if (p.q_dtype != MLA_Q_BF16 && p.q_dtype != MLA_Q_FP8_E4M3) return MLA_ERR_INVALID_ARG;
   if (p.mask != MLA_MASK_CAUSAL && p.mask != MLA_MASK_DENSE) return MLA_ERR_INVALID_ARG;
+  if (p.cp_world < 0 || (p.cp_world <= 1 && p.cp_rank != 0) ||
+      (p.cp_world > 1 && (p.cp_rank < 0 || p.cp_rank >= p.cp_world)))
+    return MLA_ERR_INVALID_ARG;
   if (!supported_heads(p.num_heads)) return MLA_ERR_UNSUPPORTED;
   if (p.page_size != 32 && p.page_size != 64) return MLA_ERR_UNSUPPORTED;
   if ((long long)p.max_pages_per_req * p.page_size < p.max_seq_len) return MLA_ERR_INVALID_ARG;
@@ -189,10 +196,21 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
              int64_t total_q, float bmm1_scale, float bmm2_scale, const float* bmm1_dev,
              const float* bmm2_dev, void* out, float* lse, void* workspace,
              size_t workspace_bytes, void* stream, void* event_before_decode,
-             void* event_after_decode) {
+             void* event_after_decode, const int32_t* seq_lens_global = nullptr) {
   if (!plan) return MLA_ERR_INVALID_ARG;
   const mla_decode_params& prm = plan->prm;
   if (prm.batch == 0) return MLA_OK;
+  // a causal decode-context-parallel plan needs the global lengths; no other
+  // plan takes them
+  const bool dcp = prm.cp_world > 1;
+  if (dcp && prm.mask == MLA_MASK_CAUSAL ? !seq_lens_global : seq_lens_global != nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (seq_lens_global && !aligned(seq_lens_global, 4)) return MLA_ERR_ALIGNMENT;
+  // the plan's SM count, cluster occupancy and kernel attributes belong to
+  // params.device, and the kernels launch on the current device
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cur != prm.device) return MLA_ERR_INVALID_ARG;
   if (!query || !kv_cache || !block_tables || !seq_lens || !out || !workspace)
     return MLA_ERR_INVALID_ARG;
   if (prm.return_lse && !lse) return MLA_ERR_INVALID_ARG;
@@ -221,6 +239,9 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
   p.packed = prm.packed;
   p.kv_dtype = prm.kv_dtype;
   p.q_fp8 = prm.q_dtype == MLA_Q_FP8_E4M3;
+  p.cp_world = dcp ? prm.cp_world : 1;
+  p.cp_rank = dcp ? prm.cp_rank : 0;
+  p.seq_lens_global = seq_lens_global;
   p.causal = prm.mask == MLA_MASK_CAUSAL;
   p.return_lse = prm.return_lse != 0;
   p.num_pages = prm.num_pages;
@@ -297,9 +318,22 @@ int mla_decode_run(const mla_plan_t* plan, const void* query, const void* kv_cac
                                  stream, nullptr, nullptr);
 }
 
+int mla_decode_run_dcp(const mla_plan_t* plan, const void* query, const void* kv_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens,
+                       const int32_t* qo_indptr, int64_t total_q,
+                       const int32_t* causal_seqlens_kv_global, float bmm1_scale,
+                       float bmm2_scale, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (!plan || plan->prm.cp_world <= 1) return MLA_ERR_INVALID_ARG;
+  return run_impl(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q, bmm1_scale,
+                  bmm2_scale, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream,
+                  nullptr, nullptr, causal_seqlens_kv_global);
+}
+
 int mla_merge_states(const void* o_parts, const float* lse_parts, int32_t n_parts, int64_t rows,
                      float scale, void* out, float* lse_out, void* stream) {
-  if (n_parts < 1 || rows < 0 || rows > (1LL << 40)) return MLA_ERR_INVALID_ARG;
+  if (n_parts < 1 || rows < 0 || rows > (1LL << 40) || (double)n_parts * (double)rows > 9.0e15)
+    return MLA_ERR_INVALID_ARG;
   if (rows == 0) return MLA_OK;
   if (!o_parts || !lse_parts || !out) return MLA_ERR_INVALID_ARG;
   if (!aligned(o_parts, 16) || !aligned(out, 16) || !aligned(lse_parts, 4) ||
@@ -330,6 +364,10 @@ int mla_decode_run_host(const mla_plan_t* plan, const void* h_query, const void*
   if (prm.batch == 0) return MLA_OK;
   if (!h_query || !kv_cache || !h_block_tables || !h_seq_lens || !h_out || !staging ||
       !workspace)
+    return MLA_ERR_INVALID_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cur != prm.device || (prm.cp_world > 1 && prm.mask == MLA_MASK_CAUSAL))
     return MLA_ERR_INVALID_ARG;
   if (prm.return_lse && !h_lse) return MLA_ERR_INVALID_ARG;
   if (prm.packed) {

@@ -11,6 +11,8 @@
 // An entry is merged once both CTAs of each of its chunks have counted their
 // partial (a bounded acquire spin by one thread of the block), so entries
 // whose chunks finished early are merged while the decode kernel still runs.
+// An entry with no chunk (a decode-context-parallel rank that holds no row of
+// the request) writes the empty sum: O = 0 and lse = -inf.
 //
 // Grid: (row blocks of 8 rows) x (combine entries), 256 threads; 32 threads
 // per row, 16 output dims per thread.  Every load of a thread (the LSEs and
@@ -19,6 +21,8 @@
 // wave.  Blocks past the live number of entries exit at once, so the grid
 // depends only on plan-time bounds.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "mla_common.cuh"
 #include "sm100_ptx.cuh"
@@ -68,61 +72,65 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     const int rows = min(R, c.q_len * H - c.g * R);
     const int r = blockIdx.x * kRowsPerBlock + row_in_block;
     if (blockIdx.x * kRowsPerBlock >= rows) continue;  // uniform over the block
+    // every thread of the block reaches this barrier on every entry it visits
+    // (the loop bounds and the test above are uniform); rows past the group's
+    // end skip only the merge below
     if (!__syncthreads_and(threadIdx.x != 0 || wait_count(done + ci, 2 * c.n_chunks, status)))
       return;
-    if (r >= rows) continue;
-    // running merge over batches of chunks: (m, sum, acc) rescaled per batch
-    float m = -INFINITY, sum = 0.f;
-    float acc[16];
+    if (r < rows) {
+      // running merge over batches of chunks: (m, sum, acc) rescaled per batch
+      float m = -INFINITY, sum = 0.f;
+      float acc[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-    for (int k0 = 0; k0 < c.n_chunks; k0 += kBatch) {
-      float4 x[kBatch][4];
-      float l[kBatch];
+      for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+      for (int k0 = 0; k0 < c.n_chunks; k0 += kBatch) {
+        float4 x[kBatch][4];
+        float l[kBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        l[u] = -INFINITY;
-        if (k0 + u < c.n_chunks) {
-          const size_t slot = (size_t)(c.first_slot + (k0 + u) * c.stride);
-          const float4* src =
-              reinterpret_cast<const float4*>(part_o + (slot * R + r) * kVDim) + 4 * t;
+        for (int u = 0; u < kBatch; ++u) {
+          l[u] = -INFINITY;
+          if (k0 + u < c.n_chunks) {
+            const size_t slot = (size_t)(c.first_slot + (k0 + u) * c.stride);
+            const float4* src =
+                reinterpret_cast<const float4*>(part_o + (slot * R + r) * kVDim) + 4 * t;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) x[u][v] = src[v];
-          l[u] = part_lse[slot * R + r];
-        } else {
+            for (int v = 0; v < 4; ++v) x[u][v] = src[v];
+            l[u] = part_lse[slot * R + r];
+          } else {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
+        float m_new = m;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) m_new = fmaxf(m_new, l[u]);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float f = expf(m - m_use);  // m = -inf: 0
+        sum *= f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] *= f;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const float w = expf(l[u] - m_use);  // absent chunks: l = -inf, w = 0
+          sum += w;
+          const float* xv = reinterpret_cast<const float*>(x[u]);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] += w * xv[e];
+        }
+        m = m_new;
       }
-      float m_new = m;
+      const float s2 = sum > 0.f ? run_bmm2(p) / sum : 0.f;
+      const size_t grow = (size_t)c.q_start * H + (size_t)c.g * R + r;
+      __nv_bfloat162 o[8];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) m_new = fmaxf(m_new, l[u]);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float f = expf(m - m_use);  // m = -inf: 0
-      sum *= f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) acc[e] *= f;
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const float w = expf(l[u] - m_use);  // absent chunks: l = -inf, w = 0
-        sum += w;
-        const float* xv = reinterpret_cast<const float*>(x[u]);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] += w * xv[e];
-      }
-      m = m_new;
+      for (int e = 0; e < 8; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kVDim +
+                                            16 * t);
+      dst[0] = *reinterpret_cast<uint4*>(o);
+      dst[1] = *reinterpret_cast<uint4*>(o + 4);
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+      if (p.return_lse && t == 0) p.lse[grow] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
     }
-    const float s2 = sum > 0.f ? run_bmm2(p) / sum : 0.f;
-    const size_t grow = (size_t)c.q_start * H + (size_t)c.g * R + r;
-    __nv_bfloat162 o[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kVDim +
-                                          16 * t);
-    dst[0] = *reinterpret_cast<uint4*>(o);
-    dst[1] = *reinterpret_cast<uint4*>(o + 4);
-    const float m_use = (m == -INFINITY) ? 0.f : m;
-    if (p.return_lse && t == 0) p.lse[grow] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
   }
 }
 
@@ -157,65 +165,67 @@ __global__ void __launch_bounds__(256)
 merge_states_kernel(const __nv_bfloat16* __restrict__ o_parts, const float* __restrict__ lse_parts,
                     int n, long long rows, float scale, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse_out) {
-  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int t = threadIdx.x & 31;  // dims [16 t, 16 t + 16)
-  if (r >= rows) return;
-  float m = -INFINITY, sum = 0.f;
-  float acc[16];
+  // grid-stride over blocks of 8 rows (rows may exceed what one grid covers)
+  for (long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows;
+       r += (long long)gridDim.x * 8) {
+    float m = -INFINITY, sum = 0.f;
+    float acc[16];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-  for (int k0 = 0; k0 < n; k0 += kBatch) {
-    uint4 x[kBatch][2];
-    float l[kBatch];
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    for (int k0 = 0; k0 < n; k0 += kBatch) {
+      uint4 x[kBatch][2];
+      float l[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      l[u] = -INFINITY;
-      x[u][0] = x[u][1] = make_uint4(0, 0, 0, 0);
-      if (k0 + u < n) {
-        const size_t base = ((size_t)(k0 + u) * rows + r) * kVDim + 16 * t;
-        const uint4* src = reinterpret_cast<const uint4*>(o_parts + base);
-        x[u][0] = src[0];
-        x[u][1] = src[1];
-        l[u] = lse_parts[(size_t)(k0 + u) * rows + r];
+      for (int u = 0; u < kBatch; ++u) {
+        l[u] = -INFINITY;
+        x[u][0] = x[u][1] = make_uint4(0, 0, 0, 0);
+        if (k0 + u < n) {
+          const size_t base = ((size_t)(k0 + u) * rows + r) * kVDim + 16 * t;
+          const uint4* src = reinterpret_cast<const uint4*>(o_parts + base);
+          x[u][0] = src[0];
+          x[u][1] = src[1];
+          l[u] = lse_parts[(size_t)(k0 + u) * rows + r];
+        }
       }
-    }
-    float m_new = m;
+      float m_new = m;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) m_new = fmaxf(m_new, l[u]);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float f = expf(m - m_use);
-    sum *= f;
+      for (int u = 0; u < kBatch; ++u) m_new = fmaxf(m_new, l[u]);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float f = expf(m - m_use);
+      sum *= f;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] *= f;
+      for (int e = 0; e < 16; ++e) acc[e] *= f;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const float w = expf(l[u] - m_use);
-      sum += w;
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(x[u]);
+      for (int u = 0; u < kBatch; ++u) {
+        const float w = expf(l[u] - m_use);
+        sum += w;
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(x[u]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 v = __bfloat1622float2(h[e]);
-        acc[2 * e] += w * v.x;
-        acc[2 * e + 1] += w * v.y;
+        for (int e = 0; e < 8; ++e) {
+          const float2 v = __bfloat1622float2(h[e]);
+          acc[2 * e] += w * v.x;
+          acc[2 * e + 1] += w * v.y;
+        }
       }
+      m = m_new;
     }
-    m = m_new;
+    const float s2 = sum > 0.f ? scale / sum : 0.f;
+    __nv_bfloat162 o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
+    uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * kVDim + 16 * t);
+    dst[0] = *reinterpret_cast<uint4*>(o);
+    dst[1] = *reinterpret_cast<uint4*>(o + 4);
+    const float m_use = (m == -INFINITY) ? 0.f : m;
+    if (lse_out && t == 0) lse_out[r] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
   }
-  const float s2 = sum > 0.f ? scale / sum : 0.f;
-  __nv_bfloat162 o[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] = __floats2bfloat162_rn(acc[2 * e] * s2, acc[2 * e + 1] * s2);
-  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)r * kVDim + 16 * t);
-  dst[0] = *reinterpret_cast<uint4*>(o);
-  dst[1] = *reinterpret_cast<uint4*>(o + 4);
-  const float m_use = (m == -INFINITY) ? 0.f : m;
-  if (lse_out && t == 0) lse_out[r] = (sum > 0.f) ? m_use + logf(sum) : -INFINITY;
 }
 
 cudaError_t launch_merge_states(const void* o_parts, const float* lse_parts, int n, long long rows,
                                 float scale, void* out, float* lse_out, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  const long long blocks = (rows + 7) / 8;
+  const long long blocks = std::min<long long>((rows + 7) / 8, 1LL << 20);
   merge_states_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o_parts), lse_parts, n, rows, scale,
       static_cast<__nv_bfloat16*>(out), lse_out);

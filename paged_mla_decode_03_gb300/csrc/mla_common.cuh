@@ -25,6 +25,7 @@ struct Problem {
   int batch, num_heads, max_q, max_seq_len, page_size, max_pages;
   int packed, kv_dtype, causal, return_lse;
   int q_fp8;                     // 1: query is e4m3 (widened to bf16 on load)
+  int cp_world, cp_rank;         // decode-context parallelism (cp_world 1: off)
   long long num_pages, total_q;  // total_q: rows of the query tensor (tokens)
   float bmm1_scale, bmm2_scale;
   const float* bmm1_dev;         // non-null: read bmm1 from device memory at run time
@@ -34,6 +35,7 @@ struct Problem {
   const int* block_tables;       // [B, max_pages]
   const int* seq_lens;           // [B]
   const int* qo_indptr;          // [B + 1] or nullptr
+  const int* seq_lens_global;    // [B] global KV lengths (causal, cp_world > 1) or nullptr
   void* out;                     // bf16 [tokens, H, 512]
   float* lse;                    // fp32 [tokens, H] or nullptr
 };
@@ -61,7 +63,21 @@ struct WorkItem {
   int b, g, kv_begin, kv_end;
   int slot, q_len, seq_len, q_start;  // q_start: first token of request b
   int comb;                           // combine entry of a split group, else -1
+  int mask_base;                      // causal bound of query row i: causal_last(mask_base, i, W)
 };
+
+// Last local KV row (inclusive) that query row qi of a request may see under
+// causal masking, from the request's mask_base.  On one rank (W = 1)
+// mask_base = L - q and the bound is L - q + qi (the bottom-right rule of the
+// FlashInfer page "prims_ts_batch_decode_with_kv_cache_mla").  Under
+// decode-context parallelism rank r of W holds global row g (g mod W == r)
+// as local row g div W, and row qi sees the global rows g <= Lg - q + qi, so
+// with mask_base = Lg - q - r the bound is floor((mask_base + qi) / W).
+// A negative result means the row sees no local row.
+__host__ __device__ inline int causal_last(int mask_base, int qi, int W) {
+  const int x = mask_base + qi;
+  return x >= 0 ? x / W : -((W - 1 - x) / W);
+}
 
 // One split (request, row group): partials live in slots first + k * stride.
 struct CombineItem {

@@ -20,10 +20,9 @@
 //    N = 64 KV rows, fp32 in TMEM);
 //  * each query row (TMEM lane l) has an owner CTA, (l / 16) mod 2.  The
 //    owner runs that row's softmax: the other CTA pushes its partial scores of
-//    the row into the owner's shared memory with st.async (16-bit fixed point
-//    with a per-row power-of-two scale: error <= 2^-14 of the row's largest
-//    partial score), the owner adds them to its own and forms P (bf16), which
-//    it writes into the P tile of both CTAs (its own with st.shared, the
+//    the row (fp32, exactly as the MMA produced them) into the owner's shared
+//    memory with st.async, the owner adds them to its own and forms P (bf16),
+//    which it writes into the P tile of both CTAs (its own with st.shared, the
 //    peer's with st.async), together with the row's rescale factor;
 //  * O = P V with P from shared memory: M = 128 query rows, N = 256 (CTA r's
 //    V dims, read MN-major from its latent chunks), K = 64 KV rows, into a
@@ -76,13 +75,14 @@ constexpr uint32_t kRopeKV = kTile * 64;    // 32-dim RoPE half of a KV tile
 constexpr uint32_t kStageBytes = kLatChunks * kChunkKV + kRopeKV;  // 36 KB
 constexpr uint32_t kPBytes = kRows * 128;   // P: 128 rows x 64 KV rows bf16, 128B-swizzled
 constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 tile, 18 KB
-// peer's partial scores of the owned rows: [64 rows][64] int16 + [64] fp32 scales
-constexpr uint32_t kXRowBytes = kTile * 2;
-constexpr uint32_t kXBytes = kOwnRows * kXRowBytes + kOwnRows * 4;
+// peer's partial scores of the owned rows: [64 rows][64] fp32, one buffer
+// (16-byte units of a row XOR-swizzled by the row index)
+constexpr uint32_t kXRowBytes = kTile * 4;
+constexpr uint32_t kXBytes = kOwnRows * kXRowBytes;
 constexpr uint32_t OFF_QROPE = 0;
 constexpr uint32_t OFF_P = OFF_QROPE + kRopeQ;  // first (or only) P tile
 constexpr uint32_t OFF_X = OFF_P + kPBytes;
-constexpr uint32_t OFF_BARS = OFF_X + 2 * kXBytes;
+constexpr uint32_t OFF_BARS = OFF_X + kXBytes;
 constexpr uint32_t OFF_FAC = OFF_BARS + 512;        // float fac[2][128]: rescale factor per row
 constexpr uint32_t OFF_LROW = OFF_FAC + 2 * kRows * 4;  // float l[128]: row sums, last tile
 constexpr uint32_t OFF_FLAG = OFF_LROW + kRows * 4;     // int flag[2][16]: 8 own + 8 peer warps
@@ -129,7 +129,7 @@ enum Bar {
   KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3, KV_FULL4,
   KV_EMPTY0, KV_EMPTY1, KV_EMPTY2, KV_EMPTY3, KV_EMPTY4,
   S_FULL0, S_FULL1, S_FREE0, S_FREE1,
-  X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1,
+  X_FULL, PEER_X_FREE,
   P_FULL0, P_FULL1, P_FREE0, P_FREE1,  // one P tile: only P_FREE0, one phase per tile
   MX_FULL0,                    // 8: [subpartition][tile parity]
   LX_FULL0 = MX_FULL0 + 8,     // 4: [subpartition]
@@ -276,7 +276,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
     // thread groups arrive once per warp (lane 0, after __syncwarp)
     counts[S_FREE0] = counts[S_FREE1] = kSoftmaxWarps + kCeWarps;
-    counts[PEER_X_FREE0] = counts[PEER_X_FREE1] = kSoftmaxWarps;  // the peer's softmax warps
+    counts[PEER_X_FREE] = kSoftmaxWarps;                          // the peer's softmax warps
     counts[P_FULL0] = counts[P_FULL1] = kSoftmaxWarps;            // + the peer's bytes
     counts[P_FREE0] = counts[P_FREE1] = 2;                        // both CTAs' PV
     for (int i = 0; i < 8; ++i) counts[MX_FULL0 + i] = 2;
@@ -291,9 +291,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     *c.abort = 0;
     for (int k = 0; k < 32; ++k) flags[k] = -1;
     fence_mbar_init();
-    // the first two tiles' peer scores may arrive as soon as the cluster is up
-    mbar_arrive_expect_tx(&c.bars[X_FULL0], kXBytes);
-    mbar_arrive_expect_tx(&c.bars[X_FULL1], kXBytes);
+    // the first tile's peer scores may arrive as soon as the cluster is up
+    mbar_arrive_expect_tx(&c.bars[X_FULL], kXBytes);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -527,7 +526,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const float scale = run_bmm1(p, c.status) * kLog2e;
     float* mx = reinterpret_cast<float*>(sm + OFF_MX);  // [parity][hw][lane]
     float* lx = reinterpret_cast<float*>(sm + OFF_LX);  // [hw][lane]
-    const uint32_t xfree_peer0 = map_to_rank(smem_u32(&c.bars[PEER_X_FREE0]), peer);
+    const uint32_t xfree_peer = map_to_rank(smem_u32(&c.bars[PEER_X_FREE]), peer);
     const uint32_t pfull_peer0 = map_to_rank(smem_u32(&c.bars[P_FULL0]), peer);
     const uint32_t p_peer0 = map_to_rank(smem_u32(sm + OFF_P), peer);
     const uint32_t p_peer1 = map_to_rank(smem_u32(sm + C::OFF_P1), peer);
@@ -544,11 +543,12 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const int row0 = it.g * kRows;
       const bool row_ok = q < rows_total - row0;
       const int qi = (row0 + q) / H;
-      const int last = p.causal ? it.seq_len - it.q_len + qi : it.seq_len - 1;
+      const int W = max(p.cp_world, 1);
+      const int last = p.causal ? causal_last(it.mask_base, qi, W) : it.seq_len - 1;
       // tiles ending at or before `clean_end` need no mask for any valid row
       const int first_qi = row0 / H;
       const int clean_end =
-          min(it.kv_end, p.causal ? it.seq_len - it.q_len + first_qi + 1 : it.seq_len);
+          min(it.kv_end, p.causal ? causal_last(it.mask_base, first_qi, W) + 1 : it.seq_len);
       float m_ref = -INFINITY, l_part = 0.f;  // l_part: this thread's 16 columns only
       for (int t = 0; t < nt; ++t, ++g) {
         const int sb = g & 1;
@@ -566,30 +566,28 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.bars[S_FREE0 + sb]);
-        // add the peer's partial scores of this row (16-bit fixed point with a
-        // per-row power-of-two scale)
-        if (!wait_bar(c, X_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
+        // add the peer's partial scores of this row (fp32, columns
+        // [16 kq, 16 kq + 16) = 16-byte units 4 kq .. 4 kq + 3 of the row)
+        if (!wait_bar(c, X_FULL, g & 1)) goto done_softmax;
         {
-          const unsigned char* xb = sm + OFF_X + sb * kXBytes;
-          const float inv = 1.f / reinterpret_cast<const float*>(xb + kOwnRows * kXRowBytes)[k];
+          const unsigned char* xb = sm + OFF_X + k * kXRowBytes;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint4 x =
-                *reinterpret_cast<const uint4*>(xb + k * kXRowBytes + (((2 * kq + u) ^ (k & 7)) << 4));
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f2 = unpack_fix16x2(w[e]);
-              sv[8 * u + 2 * e] += f2.x * inv;
-              sv[8 * u + 2 * e + 1] += f2.y * inv;
-            }
+          for (int u = 0; u < 4; ++u) {
+            const float4 x = *reinterpret_cast<const float4*>(xb + (((4 * kq + u) ^ (k & 7)) << 4));
+            sv[4 * u] += x.x;
+            sv[4 * u + 1] += x.y;
+            sv[4 * u + 2] += x.z;
+            sv[4 * u + 3] += x.w;
           }
         }
-        if (designated) mbar_arrive_expect_tx(&c.bars[X_FULL0 + sb], kXBytes);  // tile g + 2
+        // the buffer's next phase (tile g + 1) completes once the peer's bytes
+        // for it land, which the peer sends only after every softmax warp here
+        // released this tile's scores (PEER_X_FREE)
+        if (designated) mbar_arrive_expect_tx(&c.bars[X_FULL], kXBytes);
         // relaxed: the warp's reads of the buffer have returned their values
         // (release at cluster scope would cost a cluster-wide fence per tile)
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer0 + 8u * sb);
+        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer);
         // mask, online softmax (scale folded into the exponent)
         const int j0 = it.kv_begin + t * kTile;
         const int c0 = j0 + 16 * kq;  // KV index of sv[0]
@@ -737,8 +735,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
     const uint32_t peer_lanes = (uint32_t)(32 * sp + 16 * (int)peer) << 16;
     const int kp = 16 * sp + (lane & 15);  // the peer's owned-row index of my send row
-    const uint32_t x_peer0 = map_to_rank(smem_u32(sm + OFF_X), peer);
-    const uint32_t xfull_peer0 = map_to_rank(smem_u32(&c.bars[X_FULL0]), peer);
+    const uint32_t x_peer = map_to_rank(smem_u32(sm + OFF_X), peer);
+    const uint32_t xfull_peer = map_to_rank(smem_u32(&c.bars[X_FULL]), peer);
     const uint32_t lfree_peer = map_to_rank(smem_u32(&c.bars[LROW_FREE]), peer);
     uint32_t g = 0, n_rescale = 0;
     int n_item = 0;
@@ -754,34 +752,18 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.bars[S_FREE0 + sb]);
-      // 16-bit fixed point with a power-of-two scale that puts the row's largest
-      // magnitude in [2^13, 2^14): absolute error <= 2^-14 of that magnitude,
-      // i.e. the softmax's dominant scores keep ~14 bits (finer than the bf16
-      // rounding of P)
-      float am[4] = {0.f, 0.f, 0.f, 0.f};
+      // the scores go over unrounded (fp32): the logits' error stays that of
+      // the MMA's fp32 accumulation whatever the size of bmm1 * |S|
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 32; ++j)
         if (32 * hh + j >= valid) v[j] = 0u;
-        am[j & 3] = fmaxf(am[j & 3], fabsf(__uint_as_float(v[j])));
-      }
-      float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-      const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-      const int k2 = (e == 0) ? 0 : min(max(140 - e, -126), 127);
-      const float fscale = __uint_as_float((uint32_t)(k2 + 127) << 23);
-      uint32_t h[16];
+      // the peer's softmax released the previous tile's scores
+      if (!wait_bar_cluster(c, PEER_X_FREE, (gs & 1) ^ 1)) return false;
+      const uint32_t xb = x_peer + (uint32_t)(kp * kXRowBytes);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        h[j] = pack_fix16x2(__uint_as_float(v[2 * j]) * fscale,
-                            __uint_as_float(v[2 * j + 1]) * fscale);
-      if (!wait_bar_cluster(c, PEER_X_FREE0 + sb, ((gs >> 1) & 1) ^ 1)) return false;
-      const uint32_t xb = x_peer0 + (uint32_t)sb * kXBytes;
-      const uint32_t bar = xfull_peer0 + 8u * sb;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        st_async_v4_b32(xb + kp * kXRowBytes + (uint32_t)(((4 * hh + u) ^ (kp & 7)) << 4),
-                        make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]), bar);
-      if (hh == 0) st_async_b32(xb + kOwnRows * kXRowBytes + 4 * kp, __float_as_uint(fscale), bar);
+      for (int u = 0; u < 8; ++u)
+        st_async_v4_b32(xb + (uint32_t)(((8 * hh + u) ^ (kp & 7)) << 4),
+                        make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]), xfull_peer);
       return true;
     };
     // Row q of the item's Q latent dims of this CTA ([256 r, 256 r + 256)) into

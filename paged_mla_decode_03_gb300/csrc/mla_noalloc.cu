@@ -27,17 +27,25 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_address[kMaxDevices] = {};
 
-// Device address of the static workspace on the current device, resolved
-// once per device (cudaGetSymbolAddress must run with that device current).
-int static_workspace_address(void** out) {
+// Device address of the static workspace on the current device (the host
+// symbol is only a stand-in; cudaGetSymbolAddress must run with the device
+// current).  Outside stream capture it is resolved on every call, so a
+// device reset, which reloads the module and may move the array, is picked
+// up; during capture the address cached by the last call outside capture is
+// used, which is why the first call on a device must precede any capture.
+int static_workspace_address(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MLA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_address[dev]) {
+  if (cs == cudaStreamCaptureStatusNone) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr)
       return MLA_ERR_CUDA;
     g_address[dev] = ptr;
+  } else if (!g_address[dev]) {
+    return MLA_ERR_CUDA;  // never called outside capture on this device
   }
   *out = g_address[dev];
   return MLA_OK;
@@ -55,7 +63,7 @@ extern "C" int mla_decode_run_static_workspace(const mla_plan_t* plan, const voi
   if (mla_decode_workspace_size(plan) > (size_t)MLA_STATIC_WORKSPACE_BYTES)
     return MLA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
-  const int rc = static_workspace_address(&ws);
+  const int rc = static_workspace_address(static_cast<cudaStream_t>(stream), &ws);
   if (rc != MLA_OK) return rc;
   return mla_decode_run(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q,
                         bmm1_scale, bmm2_scale, out, lse, ws, (size_t)MLA_STATIC_WORKSPACE_BYTES,

@@ -157,6 +157,8 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   int* r_qstart = r_qlen + B;
   int* r_len = r_qstart + B;
   int* r_gbase = r_len + B;  // first group index of the request
+  int* r_mbase = r_gbase + B;  // causal mask base of the request (see causal_last)
+  int* r_empty = r_mbase + B;  // empty combine entries of the request (DCP, no local rows)
   // per-group scratch
   long long* g_start = reinterpret_cast<long long*>(grp_base);  // unit offset
   int* g_items = reinterpret_cast<int*>(g_start + lay.max_groups);              // -> item base
@@ -185,13 +187,32 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
       qs = b * p.max_q;
     }
     int L = p.seq_lens[b];
-    if (L < 1 || L > p.max_seq_len) status |= kStatusSeqLen;
-    L = min(max(L, 0), p.max_seq_len);
-    if (p.causal && q > L) status |= kStatusCausal;
+    int mbase;
+    if (p.cp_world > 1) {
+      // decode-context parallelism: a rank may hold no row of a request
+      if (L < 0 || L > p.max_seq_len) status |= kStatusSeqLen;
+      L = min(max(L, 0), p.max_seq_len);
+      mbase = 0;
+      if (p.causal) {
+        const int Lg = p.seq_lens_global[b];
+        if (Lg < 1) status |= kStatusSeqLen;
+        if (q > Lg) status |= kStatusCausal;
+        mbase = Lg - q - p.cp_rank;
+      }
+    } else {
+      if (L < 1 || L > p.max_seq_len) status |= kStatusSeqLen;
+      L = min(max(L, 0), p.max_seq_len);
+      if (p.causal && q > L) status |= kStatusCausal;
+      mbase = L - q;
+    }
     r_qlen[b] = q;
     r_qstart[b] = qs;
     r_len[b] = L;
+    r_mbase[b] = mbase;
     r_gbase[b] = (L > 0) ? (q * H + R - 1) / R : 0;
+    // a DCP rank with no row of the request still owes its rows O = 0 and
+    // lse = -inf (the empty sum); the combine kernel writes them
+    r_empty[b] = (p.cp_world > 1 && L == 0) ? (q * H + R - 1) / R : 0;
   }
   status = __syncthreads_or(status) ? block_or(status, sh) : 0;
   // do all requests that have row groups have the same number of them?
@@ -297,6 +318,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
         it.q_len = r_qlen[b];
         it.seq_len = L;
         it.q_start = r_qstart[b];
+        it.mask_base = r_mbase[b];
         items[g_items[g] + k] = it;
         it_owner[g_items[g] + k] = (int)bd.owner_of(unit);
         ++k;
@@ -328,6 +350,34 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
       }
     }
   }
+  // Empty entries after the split ones: every row group of a request this
+  // DCP rank holds no row of (no chunk: the combine writes zeros and -inf).
+  const int comb_base = n_items > 0 ? n_combine : 0;
+  int n_empty = 0;
+  if (p.cp_world > 1) {
+    n_empty = block_exclusive_scan(r_empty, B, sh);
+    if (comb_base + n_empty > lay.max_combine) {  // unreachable within the contract
+      status |= kStatusCapacity;
+      n_empty = 0;
+    } else {
+      for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        if (r_len[b] > 0) continue;
+        const int cnt = (r_qlen[b] * H + R - 1) / R;
+        for (int k = 0; k < cnt; ++k) {
+          CombineItem ci;
+          ci.b = b;
+          ci.g = k;
+          ci.first_slot = 0;
+          ci.stride = 1;
+          ci.n_chunks = 0;
+          ci.q_len = r_qlen[b];
+          ci.q_start = r_qstart[b];
+          ci.pad = 0;
+          comb[comb_base + r_empty[b] + k] = ci;
+        }
+      }
+    }
+  }
   // completion counters of the combine entries (bumped by the decode kernel)
   int* comb_done = reinterpret_cast<int*>(ws + lay.comb_done);
   for (int e = threadIdx.x; e < lay.max_combine; e += blockDim.x) comb_done[e] = 0;
@@ -345,7 +395,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     hdr[kHdrStatus] = status;
     hdr[kHdrNumItems] = n_items;
     hdr[kHdrWorkCounter] = 0;
-    hdr[kHdrNumCombine] = n_items > 0 ? n_combine : 0;
+    hdr[kHdrNumCombine] = comb_base + n_empty;
     hdr[kHdrChunkTiles] = (int)min(W, (long long)1 << 30);
     hdr[kHdrCombineCounter] = 0;
   }

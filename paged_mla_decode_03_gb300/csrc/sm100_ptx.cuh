@@ -415,29 +415,6 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
 namespace mla {
 namespace ptx {
 
-// 16-bit fixed point through the float pipe.  For |x| < 2^15, adding
-// 1.5 * 2^23 + 2^15 rounds x to the nearest integer (ties to even) and leaves
-// x + 2^15 in the low 16 mantissa bits; OR-ing 16 such bits back under the
-// exponent of 1.5 * 2^23 and subtracting the same constant recovers x.
-constexpr float kFixBias = 12615680.0f;  // 1.5 * 2^23 + 2^15
-__device__ __forceinline__ uint32_t pack_fix16x2(float lo, float hi) {
-  const uint32_t a = __float_as_uint(lo + kFixBias), b = __float_as_uint(hi + kFixBias);
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ float2 unpack_fix16x2(uint32_t v) {
-  const float lo = __uint_as_float((v & 0xFFFFu) | 0x4B400000u) - kFixBias;
-  const float hi = __uint_as_float((v >> 16) | 0x4B400000u) - kFixBias;
-  return make_float2(lo, hi);
-}
-
-}  // namespace ptx
-}  // namespace mla
-
-namespace mla {
-namespace ptx {
-
 // Arrive on the mbarrier at the same shared-memory offset in every CTA of
 // `cta_mask` once every MMA previously issued by this thread completes.
 __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {

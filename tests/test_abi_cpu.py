@@ -77,6 +77,10 @@ def _params(**kw):
     (dict(mask=3), -1),
     (dict(max_pages_per_req=1), -1),   # 1 page of 32 rows < max_seq_len 64
     (dict(packed=1, max_total_q=-5), -1),
+    (dict(cp_world=-1), -1),
+    (dict(cp_world=4, cp_rank=4), -1),
+    (dict(cp_world=4, cp_rank=-1), -1),
+    (dict(cp_world=1, cp_rank=1), -1),
 ])
 def test_plan_rejects_bad_static_parameters_on_host(lib, kw, status):
     handle = ctypes.c_void_p()
@@ -95,6 +99,8 @@ def test_null_arguments_are_rejected(lib):
     assert lib.mla_decode_run_host(None, None, None, None, None, None, 0, 1.0, 1.0, None, None,
                                    None, 0, None, 0, None) == -1
     assert lib.mla_decode_host_staging_bytes(None, 0) == 0
+    assert lib.mla_decode_run_dcp(None, None, None, None, None, None, 0, None, 1.0, 1.0, None,
+                                  None, None, 0, None) == -1
     lib.mla_decode_destroy(None)
     assert lib.mla_decode_workspace_size(None) == 0
 

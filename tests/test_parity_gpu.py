@@ -46,8 +46,12 @@ def test_reduced_workload_full_parity(name):
 
 @pytest.mark.parametrize("name", ["deepseek_v3", "mtp", "ragged", "fp8_long"])
 def test_full_size_workload_sampled_parity(name):
+    """The full-size workloads in the launch shapes the bench times (many-way
+    lanes, long split items, every worker busy), checked on sampled pairs
+    with their LSE (at long lengths |O| is small, so the LSE and the
+    relative-L2 gate carry most of the check)."""
     w = mi.WORKLOADS[name]()
-    d = to_device(w)
+    d = to_device(w, return_lse=True)
     run(w, d)
     out, lse = results(d)
     sel = sample_pairs(w, 48, seed=1)
@@ -531,3 +535,125 @@ def test_dcp_two_shards_merged_equal_the_single_pass(make):
     ref_o, ref_l = oracle.run(w)
     check(w.kv_dtype, out.float().cpu().numpy(), ref_o, lse.cpu().numpy(), ref_l,
           what="dcp two shards")
+
+
+@pytest.mark.parametrize("bmm1", [0.5, 1.0, 2.0])
+@pytest.mark.parametrize("name", ["deepseek_v3", "mtp"])
+def test_wide_logits_full_parity(name, bmm1):
+    """bmm1 * |s| up to ~150 (N(0,1) data, 576-dim dot products): the scores'
+    precision, not the softmax's range, decides the LSE error here, so this
+    bounds every rounding between the MMA and the softmax (the partial-score
+    exchange between the two CTAs of a pair included)."""
+    w = REDUCED[name]()
+    w.bmm1_scale = mi.f32(bmm1)
+    w.return_lse = True
+    full_parity(w)
+
+
+@pytest.mark.parametrize("case", [
+    dict(name="e4m3_ps32_h128_q2", num_heads=128, page_size=32, seq_lens=[40, 300, 129, 777],
+         q_lens=[2] * 4, packed=False),
+    dict(name="e4m3_ragged_h16_ps32", num_heads=16, page_size=32,
+         seq_lens=[8, 40, 100, 63, 64, 65, 300, 900], q_lens=[1, 2, 3, 4, 5, 6, 7, 8], packed=True,
+         max_seq_len_q=8),
+    dict(name="e4m3_ragged_h128_ps64", num_heads=128, page_size=64, seq_lens=[70, 3, 500, 129],
+         q_lens=[1, 3, 2, 2], packed=True, max_seq_len_q=3),
+    dict(name="e4m3_dense_h32_q3", num_heads=32, page_size=64, seq_lens=[70, 300, 129],
+         q_lens=[3, 3, 3], packed=False, causal=False),
+    dict(name="e4m3_dense_ragged_h64_ps32", num_heads=64, page_size=32, seq_lens=[33, 250, 5],
+         q_lens=[2, 1, 4], packed=True, causal=False, max_seq_len_q=4),
+])
+def test_e4m3_cache_page_sizes_packed_and_dense(case):
+    """The e4m3 cache's own staging path at page size 32, with packed ragged
+    queries and with the dense mask."""
+    case = dict(case)
+    name = case.pop("name")
+    w = mi.build(name, 95, kv_dtype="e4m3", return_lse=True, **case)
+    full_parity(w)
+
+
+def _dcp_case(world, make):
+    """The workload and its ranks' shares.  The shares keep the workload's
+    bmm2 (each rank's output is then on the scale the tolerances are stated
+    for) and the merge uses scale 1, which is the same by linearity."""
+    w = make()
+    w.return_lse = True
+    return w, [mi.dcp_shard(w, world, r) for r in range(world)]
+
+
+DCP_CASES = {
+    "mtp_q4_w2": (2, lambda: mi.mtp(batch=3, lo=64, hi=400, return_lse=True)),
+    "deepseek_q1_w3": (3, lambda: mi.deepseek_v3(batch=4, lo=100, hi=700, return_lse=True)),
+    "ragged_short_w4": (4, lambda: mi.build(
+        "dcp_ragged", 96, num_heads=16, page_size=32, seq_lens=[1, 2, 3, 9, 200, 77, 4, 600],
+        q_lens=[1, 2, 3, 4, 8, 2, 1, 5], packed=True, return_lse=True, max_seq_len_q=8)),
+    "fp8_q2_w4": (4, lambda: mi.fp8_long(batch=2, lo=300, hi=900, return_lse=True)),
+    "dense_q3_w2": (2, lambda: mi.build("dcp_dense", 97, num_heads=32, page_size=64,
+                                        seq_lens=[70, 300, 5], q_lens=[3, 3, 3], packed=False,
+                                        causal=False, return_lse=True)),
+}
+
+
+@pytest.mark.parametrize("case", list(DCP_CASES))
+def test_dcp_rank_decode_matches_oracle_and_merges_to_single_pass(case):
+    """Decode-context parallelism, every rank emulated on this GPU in turn:
+    each rank decodes its round-robin share of the rows through
+    mla_decode_run_dcp (causal bound on global positions; ranks that hold no
+    row of a request return O = 0, lse = -inf) and is compared element by
+    element with the oracle's state for that rank; mla_merge_states then
+    merges the ranks, which must equal the single pass over the whole
+    sequence."""
+    import paged_mla_decode_03_gb300 as mla
+    world, make = DCP_CASES[case]
+    w, shards = _dcp_case(world, make)
+    outs, lses = [], []
+    for sh in shards:
+        d = to_device(sh)
+        run(sh, d)
+        out, lse = results(d)
+        assert device_status(d) == 0
+        ref_o, ref_l = oracle.run(sh)
+        check(sh.kv_dtype, out.reshape(-1, sh.num_heads, 512), ref_o, lse, ref_l,
+              what=f"{case} rank {sh.cp_rank}")
+        outs.append(d.out)
+        lses.append(d.lse)
+    merged, mlse = mla.merge_states(torch.stack(outs), torch.stack(lses), scale=1.0)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.run(w)
+    check(w.kv_dtype, merged.float().cpu().numpy().reshape(-1, w.num_heads, 512), ref_o,
+          mlse.cpu().numpy(), ref_l, what=f"{case} merged")
+
+
+def test_dcp_causal_plan_refuses_the_plain_entry_point():
+    import paged_mla_decode_03_gb300 as mla
+    w, shards = _dcp_case(2, lambda: mi.mtp(batch=2, lo=64, hi=200, return_lse=True))
+    sh = shards[1]
+    d = to_device(sh)
+    with pytest.raises(mla.MlaDecodeError) as e:
+        mla.mla_decode_run(d.plan.handle, d.query, d.kv_cache, d.block_tables, d.seq_lens, None,
+                           0, sh.bmm1_scale, sh.bmm2_scale, d.out, d.lse, d.workspace)
+    assert e.value.status == -1
+
+
+@pytest.mark.parametrize("H,B,qlo,qhi,lhi", [(128, 512, 24, 48, 2048), (16, 4096, 1, 8, 300)])
+def test_prefill_scale_packed_launch(H, B, qlo, qhi, lhi):
+    """Prefill through the decode path (the FlashInfer issue "Support
+    cum_seq_lens_q in trtllm_batch_decode_with_kv_cache_mla", point 1): more
+    than 16k packed query tokens.  At this size the partitioner's per-group
+    scratch no longer fits its shared memory and lives in the workspace."""
+    rng = np.random.default_rng(86 + H)
+    q = rng.integers(qlo, qhi, size=B, endpoint=True).astype(np.int32)
+    L = rng.integers(q + 1, lhi, endpoint=True).astype(np.int32)
+    w = mi.build(f"prefill_h{H}", 86 + H, num_heads=H, page_size=64 if H == 128 else 32,
+                 seq_lens=L, q_lens=q, packed=True, return_lse=True, max_seq_len_q=int(qhi))
+    assert w.total_q >= 16384
+    d = to_device(w)
+    assert d.plan.workspace_bytes > 0
+    run(w, d)
+    out, lse = results(d)
+    assert device_status(d) == 0
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    sel = sample_pairs(w, 96, seed=3)
+    ref_o, ref_l = oracle.run(w, sel=sel)
+    check("bf16", out[sel[:, 0], sel[:, 1]], ref_o, lse[sel[:, 0], sel[:, 1]], ref_l,
+          what=f"prefill H={H}")

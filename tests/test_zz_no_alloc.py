@@ -71,3 +71,46 @@ def test_static_workspace_rejects_plans_that_do_not_fit():
     rc = _entry()(plan.handle, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 16, 1.0, 1.0, 1 << 20,
                   None, torch.cuda.current_stream().cuda_stream)
     assert rc == -3  # MLA_ERR_WORKSPACE_TOO_SMALL, nothing enqueued
+
+
+def test_static_workspace_captured_in_a_graph_follows_new_lengths():
+    """The documented sequence for capture: one call outside capture (it
+    resolves the array's device address), then a captured call, replayed with
+    new seq_lens written in place between replays.  Each replay must equal
+    the caller-workspace path on the same lengths."""
+    w = mi.build("graph_static", 98, num_heads=16, page_size=32, seq_lens=[300, 120, 77],
+                 q_lens=[2, 3, 1], packed=True, return_lse=True, max_seq_len_q=4)
+    d = to_device(w)
+    fn = _entry()
+    s = torch.cuda.Stream()
+
+    def call(out, lse):
+        return fn(d.plan.handle, d.query.data_ptr(), d.kv_cache.data_ptr(),
+                  d.block_tables.data_ptr(), d.seq_lens.data_ptr(), d.qo_indptr.data_ptr(),
+                  w.total_q, w.bmm1_scale, w.bmm2_scale, out.data_ptr(), lse.data_ptr(),
+                  s.cuda_stream)
+
+    out_g = torch.full_like(d.out, float("nan"))
+    lse_g = torch.full_like(d.lse, float("nan"))
+    with torch.cuda.stream(s):
+        assert call(out_g, lse_g) == 0  # outside capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rc = call(out_g, lse_g)
+    assert rc == 0
+    atol, rtol = TOL["bf16"]
+    for lens in ([250, 64, 77], [300, 3, 40]):
+        d.seq_lens.copy_(torch.tensor(lens, dtype=torch.int32))
+        out_g.fill_(float("nan"))
+        lse_g.fill_(float("nan"))
+        with torch.cuda.stream(s):
+            g.replay()
+        s.synchronize()
+        run(w, d)  # caller workspace, same lengths, into d.out / d.lse
+        torch.cuda.synchronize()
+        o = out_g.float().cpu().numpy()
+        ref_o = d.out.float().cpu().numpy()
+        assert np.isfinite(o).all()
+        assert np.all(np.abs(o - ref_o) <= atol + rtol * np.abs(ref_o)), lens
+        assert np.abs(lse_g.cpu().numpy() - d.lse.cpu().numpy()).max() <= LSE_TOL, lens
