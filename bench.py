@@ -96,6 +96,10 @@ def make_workload(name):
     return mi.WORKLOADS[name]()
 
 
+def wmx_flops(w) -> int:
+    return work_model(w)["flops"]
+
+
 # ----------------------------------------------------------------- distributed
 
 def dist_env():
@@ -282,15 +286,21 @@ def gpu_case(w, dev, steps, warmup, with_e2e):
     # gives the kernel's duration for the roofline; event-record nodes between
     # the kernels cost ~10 us of their own, so they stay out of the per-call
     # figure).  Each graph is replayed once untimed, then once timed.
+    # The profiled graph holds at least 200 calls (its untimed replay is the
+    # warm-up), so the kernel figure is a median over >= 200 calls whatever
+    # `steps` is.
+    n_prof = max(steps, 200)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
-    g_plain, g_prof = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+          for _ in range(n_prof)]
+    g_plain, g_prof, g_one = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_plain, stream=stream):
         for k in range(steps):
             step()
     with torch.cuda.graph(g_prof, stream=stream):
-        for k in range(steps):
+        for k in range(n_prof):
             step(ev[k])
+    with torch.cuda.graph(g_one, stream=stream):
+        step()
 
     def timed(graph):
         with torch.cuda.stream(stream):
@@ -310,8 +320,22 @@ def gpu_case(w, dev, steps, warmup, with_e2e):
     total_ms = timed(g_plain)
     prof_total_ms = timed(g_prof)
     kernel_ms = [a.elapsed_time(b) for a, b in ev]
-    del g_plain, g_prof
+    # Per-call median: a one-call graph replayed 20 times untimed, then
+    # n_prof times back to back with an event between consecutive replays.
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_prof + 1)]
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            g_one.replay()
+        for k in range(n_prof):
+            marks[k].record(stream)
+            g_one.replay()
+        marks[n_prof].record(stream)
+    stream.synchronize()
+    call_ms = [marks[k].elapsed_time(marks[k + 1]) for k in range(n_prof)]
+    del g_plain, g_prof, g_one
     res = {"ms_per_step": total_ms / steps, "kernel_ms": statistics.mean(kernel_ms),
+           "kernel_ms_median": statistics.median(kernel_ms),
+           "call_ms_median": statistics.median(call_ms), "n_median": n_prof,
            "ms_per_step_with_events": prof_total_ms / steps, "launches_per_step": 3}
 
     if with_e2e:
@@ -389,7 +413,9 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         r = gpu_case(w, dev, args.steps, args.warmup, with_e2e=True)
     step_s = reduce_max(r["ms_per_step"] / 1e3, dev)
-    kern_s = reduce_max(r["kernel_ms"] / 1e3, dev)
+    kern_s = reduce_max(r["kernel_ms_median"] / 1e3, dev)
+    kern_mean_s = reduce_max(r["kernel_ms"] / 1e3, dev)
+    call_med_s = reduce_max(r["call_ms_median"] / 1e3, dev)
     e2e_s = reduce_max(r["e2e_ms"] / 1e3, dev)
     ev_s = reduce_max(r["ms_per_step_with_events"] / 1e3, dev)
     n = ws_
@@ -400,28 +426,38 @@ def run_gpu(args):
     rf["peak_source"] = peaks["source"]
     step_rf = roofline(w, wm, step_s, peaks)
 
+    def oracle_line(wx, seconds):
+        tf, dt, pairs, cores, fl = time_oracle(wx, target_s=seconds)
+        return {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                "us_per_call": wmx_flops(wx) / (tf * 1e12) * 1e6 if tf > 0 else None,
+                "sample": f"{pairs} (token, head) pairs of {wx.name} drawn with seed 0, "
+                          f"{fl / 1e9:.2f} GFLOP in {dt:.1f} s (fp64 C oracle, all pairs' "
+                          f"visible KV rows)"}
+
     per_config = []
     if not args.no_extra:
         for name in [n for n in mi.WORKLOADS if n != args.workload]:
             wx = make_workload(name)
             wmx = work_model(wx)
             rx = gpu_case(wx, dev, max(5, args.steps // 4), max(3, args.warmup), with_e2e=False)
-            tx = reduce_max(rx["ms_per_step"] / 1e3, dev)
-            kx = reduce_max(rx["kernel_ms"] / 1e3, dev)
+            tx = reduce_max(rx["call_ms_median"] / 1e3, dev)
+            kx = reduce_max(rx["kernel_ms_median"] / 1e3, dev)
             rfx = roofline(wx, wmx, tx, peaks)
-            per_config.append({
+            rkx = roofline(wx, wmx, kx, peaks)
+            entry = {
                 "workload": wx.name, "us_per_call": tx * 1e6, "decode_kernel_us": kx * 1e6,
+                "median_of_calls": rx["n_median"],
                 "tflops": wmx["flops"] / tx / 1e12, "kv_gbs": wmx["kv_bytes"] / tx / 1e9,
-                "bound": rfx["bound"], "roofline_frac": rfx["frac"], "dtype": wx.kv_dtype})
+                "bound": rfx["bound"], "roofline_frac": rfx["frac"],
+                "kernel_roofline_frac": rkx["frac"], "dtype": wx.kv_dtype}
+            if rank == 0 and not args.no_cpu_baseline:
+                entry["cpu_baseline"] = oracle_line(wx, args.cpu_seconds_extra)
+            per_config.append(entry)
             del wx
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        tf, dt, pairs, cores, fl = time_oracle(w, target_s=args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"{pairs} (token, head) pairs of {w.name} drawn with seed 0, "
-                         f"{fl / 1e9:.2f} GFLOP in {dt:.1f} s (fp64 C oracle, all pairs' "
-                         f"visible KV rows)"}
+        cpu = oracle_line(w, args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -434,10 +470,16 @@ def run_gpu(args):
                        "parallelism": f"replicas x{n}",
                        "l2": "inputs larger than L2 (KV pool > 129 MB), no flush",
                        "timing": "CUDA graph of `steps` plain calls, replayed warm then timed "
-                                 "(per call); a second graph with an event pair around each "
-                                 "decode kernel, replayed likewise (roofline kernel time)"},
+                                 "(value, ms_per_step); a graph of max(steps, 200) calls with an "
+                                 "event pair around each decode kernel, replayed warm then timed "
+                                 "(roofline: median kernel time); a one-call graph replayed 20 "
+                                 "times untimed then max(steps, 200) times with an event between "
+                                 "calls (us_per_call_median)"},
             "us_per_call": step_s * 1e6,
+            "us_per_call_median": call_med_s * 1e6,
             "decode_kernel_us": kern_s * 1e6,
+            "decode_kernel_us_mean": kern_mean_s * 1e6,
+            "median_of_calls": r["n_median"],
             "us_per_call_with_kernel_events": ev_s * 1e6,
             "kv_gbs": wm["kv_bytes"] / step_s / 1e9,
             "roofline_frac_per_call": step_rf["frac"],
@@ -452,6 +494,36 @@ def run_gpu(args):
             "work": {"flops": wm["flops"], "bytes": wm["bytes"], "kv_bytes": wm["kv_bytes"]},
         }
         print(json.dumps(line), flush=True)
+
+
+def run_profile_target(args):
+    """Plain eager calls of one workload and nothing else: the command the
+    ncu captures under profiles/ run (no graphs, no timing, no oracle)."""
+    import torch
+    import paged_mla_decode_03_gb300 as mla
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    mla.load_library()
+    w = make_workload(args.workload)
+    q, kv, bt, sl, qo = to_device(w, dev)
+    tokens = w.total_q
+    plan = mla.Plan(batch=w.batch, num_heads=w.num_heads, max_seq_len_q=w.max_seq_len_q,
+                    max_seq_len=w.max_seq_len, page_size=w.page_size,
+                    max_pages_per_req=w.block_tables.shape[1], num_pages=w.num_pages,
+                    packed=w.packed, max_total_q=tokens, kv_dtype=w.kv_dtype, causal=w.causal,
+                    return_lse=w.return_lse, device=0)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((tokens, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((tokens, w.num_heads), dtype=torch.float32, device=dev) if w.return_lse else None
+    for _ in range(args.warmup + args.steps):
+        plan.run(q, kv, bt, sl, out, qo_indptr=qo, total_q=tokens if w.packed else 0, lse=lse,
+                 workspace=ws, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale)
+    torch.cuda.synchronize()
+    status = int(ws[:4].view(torch.int32).item())
+    print(json.dumps({"profile_target": w.name, "calls": args.warmup + args.steps,
+                      "launches_per_call": 3, "status_word": status}), flush=True)
+    if status != 0:
+        raise SystemExit(f"device status word {status}")
 
 
 def run_reference(args):
@@ -491,15 +563,21 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--profile-target", action="store_true",
+                    help="only run warmup + steps eager calls of --workload (for ncu)")
     ap.add_argument("--workload", default=HEADLINE, choices=list(mi.WORKLOADS),
                     help="workload timed for the JSON line (default: the B=64, H=128 decode)")
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds-extra", type=float, default=3.0,
+                    help="oracle seconds per extra workload in per_config")
     ap.add_argument("--ref-step-seconds", type=float, default=5.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile_target:
+        run_profile_target(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

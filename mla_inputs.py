@@ -283,12 +283,28 @@ def fp8_long(seed: int = 1005, batch: int = 8, lo: int = 65536, hi: int = 131072
                  q_dtype=q_dtype)
 
 
+def prefill(seed: int = 1006, batch: int = 512, q_lo: int = 24, q_hi: int = 48,
+            max_len: int = 2048, poison: bool = True) -> Workload:
+    """Prefill through the decode path (the FlashInfer issue "Support
+    cum_seq_lens_q in trtllm_batch_decode_with_kv_cache_mla", point 1):
+    B=512, H=128, packed q_len ~ U{24..48} (about 18k query tokens),
+    page_size 64, seq_lens ~ U[q_len + 1, 2048], bottom-right causal, out + LSE.
+    Not one of the five decode workloads: a size check of the packed path."""
+    rng = np.random.default_rng(seed)
+    q = rng.integers(q_lo, q_hi, size=batch, endpoint=True).astype(np.int32)
+    L = rng.integers(q + 1, max_len, endpoint=True).astype(np.int32)
+    return build(f"prefill_b{batch}_h128_packed_ps64", seed, num_heads=128, page_size=64,
+                 seq_lens=L, q_lens=q, packed=True, return_lse=True, max_seq_len_q=q_hi,
+                 poison=poison, rng=rng)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "deepseek_v3": deepseek_v3,
     "mtp": mtp,
     "ragged": ragged,
     "fp8_long": fp8_long,
+    "prefill": prefill,
 }
 
 
