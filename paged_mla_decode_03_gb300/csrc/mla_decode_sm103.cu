@@ -28,16 +28,21 @@
 //    V dims, read MN-major from its latent chunks), K = 64 KV rows, into a
 //    128 x 256 fp32 TMEM accumulator.  The PV commit is multicast to both CTAs,
 //    so the (single) P tile is rewritten only after both CTAs' PV read it.
-// Warp roles (448 threads, 704 with e4m3): warp 0 TMA producer (5-stage KV ring), warp 1
-// MMA issuer and TMEM owner (QK runs up to two tiles ahead of PV), warps 2-9
-// softmax of the 64 owned rows (four threads per row, 16 KV columns each:
-// warp w covers the owned lanes 32 (w mod 4) + 16 r .. + 15, columns
-// [32 h, 32 h + 32), h = (w - 2) / 4, with the 16x32bx2 access shape),
-// warps 10-13 partial-score senders (the peer-owned lanes), O correction,
-// epilogue and the Q latent load into TMEM (thread = query row = TMEM lane).
+// Warp roles (448 threads, 704 with e4m3): warp 0 TMA producer (4-stage KV
+// ring), warp 1 MMA issuer and TMEM owner (QK runs up to two tiles ahead of
+// PV), warps 2-9 softmax of the 64 owned rows in two groups of four that take
+// alternate KV tiles (group G the tiles of global parity G), so that two
+// tiles' softmax latencies overlap; in a group, warp w covers the 16 owned
+// lanes 32 (w mod 4) + 16 r .. + 15 of its TMEM subpartition, two threads per
+// row (32 KV columns each, the 16x32bx2 access shape), so a row's maximum
+// needs one shuffle.  Only the running-max reference passes from tile to
+// tile between the groups; each group keeps its own row-sum partial, and the
+// group of an item's last tile merges the two.  Warps 10-13 are the
+// partial-score senders (the peer-owned lanes), O correction, epilogue and
+// the Q latent load into TMEM (thread = query row = TMEM lane).
 // With an e4m3 cache eight more warps (14-21) widen each staged e4m3 tile to
 // bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and the
-// bf16 ring is 4 deep.
+// bf16 ring is 3 deep beside a 2-deep e4m3 staging ring.
 // The running max is only raised, and O rescaled, when it grows by more than
 // 2^8.  Every wait is bounded; a timeout sets an error bit in the workspace
 // status word and the kernel unwinds.
@@ -59,7 +64,8 @@ constexpr int kRows = 128;        // query rows per work item
 constexpr int kOwnRows = 64;      // rows whose softmax this CTA runs
 constexpr int kTile = kKvTile;    // 64 KV rows per tile
 constexpr int kLatChunks = 4;     // 64-dim latent chunks per CTA (= its V dims)
-constexpr int kSoftmaxWarps = 8;
+constexpr int kSoftmaxWarps = 8;  // two groups of four
+constexpr int kGroupWarps = 4;
 constexpr int kCeWarps = 4;       // senders / correction / epilogue
 constexpr int kConvThreads = 256;  // four per KV row of a tile
 constexpr uint32_t kWaitLimit = 1u << 26;
@@ -68,54 +74,48 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // shared-memory layout (bytes from a 1024-aligned base): fixed regions first,
-// then the KV ring, whose depth depends on the configuration (below)
+// then the KV ring
 constexpr uint32_t kRopeQ = kRows * 64;     // 32-dim RoPE half of Q, 64B-swizzled rows
 constexpr uint32_t kChunkKV = kTile * 128;  // 64-dim chunk of a KV tile
 constexpr uint32_t kRopeKV = kTile * 64;    // 32-dim RoPE half of a KV tile
 constexpr uint32_t kStageBytes = kLatChunks * kChunkKV + kRopeKV;  // 36 KB
 constexpr uint32_t kPBytes = kRows * 128;   // P: 128 rows x 64 KV rows bf16, 128B-swizzled
 constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 tile, 18 KB
-// peer's partial scores of the owned rows: [64 rows][64] fp32, one buffer
+// peer's partial scores of the owned rows: [64 rows][64] fp32 per tile parity
 // (16-byte units of a row XOR-swizzled by the row index)
 constexpr uint32_t kXRowBytes = kTile * 4;
 constexpr uint32_t kXBytes = kOwnRows * kXRowBytes;
 constexpr uint32_t OFF_QROPE = 0;
-constexpr uint32_t OFF_P = OFF_QROPE + kRopeQ;  // first (or only) P tile
-constexpr uint32_t OFF_X = OFF_P + kPBytes;
-constexpr uint32_t OFF_BARS = OFF_X + kXBytes;
+constexpr uint32_t OFF_P = OFF_QROPE + kRopeQ;   // P tiles of tile parity 0 and 1
+constexpr uint32_t OFF_X = OFF_P + 2 * kPBytes;  // peer scores of tile parity 0 and 1
+constexpr uint32_t OFF_BARS = OFF_X + 2 * kXBytes;
 constexpr uint32_t OFF_FAC = OFF_BARS + 512;        // float fac[2][128]: rescale factor per row
 constexpr uint32_t OFF_LROW = OFF_FAC + 2 * kRows * 4;  // float l[128]: row sums, last tile
-constexpr uint32_t OFF_FLAG = OFF_LROW + kRows * 4;     // int flag[2][16]: 8 own + 8 peer warps
-constexpr uint32_t OFF_MX = OFF_FLAG + 2 * 16 * 4;      // float [2][2][128]: half-row maxima
-constexpr uint32_t OFF_LX = OFF_MX + 2 * 2 * kRows * 4;  // float [2][128]: half-row sums
-constexpr uint32_t OFF_TMEM = OFF_LX + 2 * kRows * 4;
+constexpr uint32_t OFF_FLAG = OFF_LROW + kRows * 4;     // int flag[2][16]: own + peer warps
+constexpr uint32_t OFF_MREF = OFF_FLAG + 2 * 16 * 4;    // float [2][128]: running max by tile parity
+constexpr uint32_t OFF_LX = OFF_MREF + 2 * kRows * 4;   // float [2][2][128]: group (l, m) per slot
+constexpr uint32_t OFF_TMEM = OFF_LX + 4 * kRows * 4;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
 constexpr uint32_t OFF_KV = (OFF_ABORT + 16 + 1023) / 1024 * 1024;
 
-// Two configurations share the code.  Two P tiles (kDoubleP): the softmax
-// writes P(g) while PV(g - 1) may still read the other tile; the ring is 4
-// bf16 stages (e4m3 KV: 3 bf16 stages + a 2-deep e4m3 staging ring), and the
-// second P tile follows the ring.  One P tile: P(g) waits for both CTAs'
-// PV(g - 1), which frees the smem for a 5-stage ring; it pays off when the
-// softmax is the longer step (every item row valid: H q_len >= 128, packed:
-// H >= 128), and the e4m3 kernel always uses two P tiles.
-template <bool kFp8, bool kDoubleP> struct Cfg {
-  static constexpr int kStages = (kFp8 ? 3 : 4) + (kDoubleP ? 0 : 1);
+// bf16 cache: a 4-stage ring.  e4m3 cache: 3 bf16 stages and a 2-deep e4m3
+// staging ring in the fourth stage's space.
+template <bool kFp8> struct Cfg {
+  static constexpr int kStages = kFp8 ? 3 : 4;
   static constexpr int kThreads = kFp8 ? 704 : 448;  // + 8 converter warps
   static constexpr uint32_t OFF_STG = OFF_KV + kStages * kStageBytes;  // e4m3 staging
   static constexpr uint32_t kRingEnd = OFF_STG + (kFp8 ? 2 * kStgBytes : 0);
-  static constexpr uint32_t OFF_P1 = kRingEnd;  // second P tile (kDoubleP only)
-  static constexpr uint32_t kSmemBytes = kRingEnd + (kDoubleP ? kPBytes : 0) + 1024;
+  static constexpr uint32_t kSmemBytes = kRingEnd + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(OFF_STG % 1024 == 0 && OFF_P1 % 1024 == 0, "alignment");
+  static_assert(OFF_STG % 1024 == 0, "alignment");
 };
 static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0 &&
-                  OFF_FLAG % 16 == 0 &&
-                  OFF_X % 16 == 0 && 2 * kStgBytes == kStageBytes,
+                  kPBytes % 1024 == 0 && OFF_FLAG % 16 == 0 && OFF_X % 16 == 0 &&
+                  2 * kStgBytes == kStageBytes,
               "alignment");
 // bytes the peer pushes into this CTA's P tile per KV tile (P rows, factors,
-// flags), plus the row sums on an item's last tile
-constexpr uint32_t kPeerPBytes = kOwnRows * 128 + kOwnRows * 4 + kSoftmaxWarps * 4;
+// the group's four flags), plus the row sums on an item's last tile
+constexpr uint32_t kPeerPBytes = kOwnRows * 128 + kOwnRows * 4 + kGroupWarps * 4;
 constexpr uint32_t kPeerLBytes = kOwnRows * 4;
 
 // TMEM columns
@@ -126,16 +126,17 @@ constexpr uint32_t TM_Q = 384;  // Q latent: 128 rows x 256 dims (bf16 pairs)
 
 enum Bar {
   Q_FULL, Q_FREE, QT_FULL,
-  KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3, KV_FULL4,
-  KV_EMPTY0, KV_EMPTY1, KV_EMPTY2, KV_EMPTY3, KV_EMPTY4,
+  KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3,
+  KV_EMPTY0, KV_EMPTY1, KV_EMPTY2, KV_EMPTY3,
   S_FULL0, S_FULL1, S_FREE0, S_FREE1,
-  X_FULL, PEER_X_FREE,
-  P_FULL0, P_FULL1, P_FREE0, P_FREE1,  // one P tile: only P_FREE0, one phase per tile
-  MX_FULL0,                    // 8: [subpartition][tile parity]
-  LX_FULL0 = MX_FULL0 + 8,     // 4: [subpartition]
-  LROW_FREE = LX_FULL0 + 4,
+  X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1,
+  P_FULL0, P_FULL1, P_FREE0, P_FREE1,
+  MREF0,                       // 8: [tile parity][subpartition], running max published
+  LX0 = MREF0 + 8,             // 8: [slot][subpartition], a group's (l, m) published
+  LROW_FREE = LX0 + 8,
   O_STABLE, CORR_DONE, O_FINAL, EPI_DONE,
   STG_FULL0, STG_FULL1, STG_EMPTY0, STG_EMPTY1,
+  MMA_DRAIN,                   // the issuer's last commit: every MMA it issued has completed
   NUM_BARS
 };
 static_assert(NUM_BARS * 8 <= 512, "barrier area");
@@ -143,8 +144,17 @@ static_assert(NUM_BARS * 8 <= 512, "barrier area");
 struct Ctx {
   uint64_t* bars;
   volatile int* abort;
+  uint32_t peer_abort;  // the peer CTA's abort word (shared::cluster address)
   int* status;
 };
+
+// A wait that ran out: flag the status word and make both CTAs of the pair
+// unwind (each waits for its own copies and MMAs in flight before leaving).
+__device__ __forceinline__ void give_up(const Ctx& c) {
+  *c.abort = 1;
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(c.peer_abort), "r"(1) : "memory");
+  atomicOr(c.status, kStatusTimeout);
+}
 
 __device__ __forceinline__ bool wait_bar(const Ctx& c, int bar, uint32_t parity) {
   uint64_t* b = &c.bars[bar];
@@ -152,8 +162,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, int bar, uint32_t parity)
     if (mbar_try_wait(b, parity)) return true;
     if ((i & 1023) == 1023 && *c.abort) return false;
   }
-  *c.abort = 1;
-  atomicOr(c.status, kStatusTimeout);
+  give_up(c);
   return false;
 }
 
@@ -163,9 +172,15 @@ __device__ __forceinline__ bool wait_bar_cluster(const Ctx& c, int bar, uint32_t
     if (mbar_try_wait_acq_cluster(b, parity)) return true;
     if ((i & 1023) == 1023 && *c.abort) return false;
   }
-  *c.abort = 1;
-  atomicOr(c.status, kStatusTimeout);
+  give_up(c);
   return false;
+}
+
+// Bounded wait that ignores the abort word: used on the way out, for the
+// completion of this CTA's own asynchronous copies and MMAs.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return;
 }
 
 __device__ __forceinline__ int n_tiles_of(const WorkItem& it) {
@@ -240,13 +255,13 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
   fence_proxy_async_smem();  // read by the RoPE MMAs
 }
 
-template <bool kFp8, bool kDoubleP>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8, kDoubleP>::kThreads, 1)
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                     const __grid_constant__ CUtensorMap tm_q_rope,
                     const __grid_constant__ CUtensorMap tm_kv,
                     const __grid_constant__ CUtensorMap tm_kv_rope) {
-  using C = Cfg<kFp8, kDoubleP>;
+  using C = Cfg<kFp8>;
   constexpr int kStages = C::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -265,6 +280,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   Ctx c;
   c.bars = reinterpret_cast<uint64_t*>(sm + OFF_BARS);
   c.abort = reinterpret_cast<volatile int*>(sm + OFF_ABORT);
+  c.peer_abort = map_to_rank(smem_u32(sm + OFF_ABORT), peer);
   c.status = &hdr[kHdrStatus];
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
   float* fac = reinterpret_cast<float*>(sm + OFF_FAC);
@@ -274,13 +290,12 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   if (tid == 0) {
     uint32_t counts[NUM_BARS];
     for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
-    // thread groups arrive once per warp (lane 0, after __syncwarp)
-    counts[S_FREE0] = counts[S_FREE1] = kSoftmaxWarps + kCeWarps;
-    counts[PEER_X_FREE] = kSoftmaxWarps;                          // the peer's softmax warps
-    counts[P_FULL0] = counts[P_FULL1] = kSoftmaxWarps;            // + the peer's bytes
+    // thread groups arrive once per warp (lane 0, after __syncwarp); a tile
+    // of parity G is handled by softmax group G (four warps)
+    counts[S_FREE0] = counts[S_FREE1] = kGroupWarps + kCeWarps;
+    counts[PEER_X_FREE0] = counts[PEER_X_FREE1] = kGroupWarps;    // the peer's group
+    counts[P_FULL0] = counts[P_FULL1] = kGroupWarps;              // + the peer's bytes
     counts[P_FREE0] = counts[P_FREE1] = 2;                        // both CTAs' PV
-    for (int i = 0; i < 8; ++i) counts[MX_FULL0 + i] = 2;
-    for (int i = 0; i < 4; ++i) counts[LX_FULL0 + i] = 2;
     counts[LROW_FREE] = 2 * kCeWarps;                             // both CTAs' epilogues
     counts[CORR_DONE] = counts[EPI_DONE] = counts[QT_FULL] = kCeWarps;
     if (kFp8) {
@@ -291,8 +306,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     *c.abort = 0;
     for (int k = 0; k < 32; ++k) flags[k] = -1;
     fence_mbar_init();
-    // the first tile's peer scores may arrive as soon as the cluster is up
-    mbar_arrive_expect_tx(&c.bars[X_FULL], kXBytes);
+    // the first two tiles' peer scores may arrive as soon as the cluster is up
+    mbar_arrive_expect_tx(&c.bars[X_FULL0], kXBytes);
+    mbar_arrive_expect_tx(&c.bars[X_FULL1], kXBytes);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -402,7 +418,20 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         }
       }
     }
-  done_producer:;
+  done_producer:
+    // however the loop ended, no copy issued here may still be landing in
+    // shared memory when the CTA leaves: wait for the last ones (the tiles of
+    // the ring and the last query load; phases already complete pass at once)
+    if (lane == 0) {
+      const uint32_t depth = kFp8 ? 2u : (uint32_t)kStages;
+      for (uint32_t k = 0; k < depth && k < g; ++k) {
+        const uint32_t gi = g - 1 - k;
+        const int s = kFp8 ? (int)(gi & 1) : (int)(gi % kStages);
+        const uint32_t use = kFp8 ? (gi >> 1) : gi / kStages;
+        drain_wait(&c.bars[kFp8 ? STG_FULL0 + s : KV_FULL0 + s], use & 1);
+      }
+      if (n_item > 0) drain_wait(&c.bars[Q_FULL], (uint32_t)(n_item - 1) & 1);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // Within an item QK(g) is issued as soon as its KV tile and S buffer are
@@ -413,7 +442,6 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const uint32_t qr_base = smem_u32(sm + OFF_QROPE);
       const uint32_t kv_base = smem_u32(sm + OFF_KV);
       const uint32_t p_base = smem_u32(sm + OFF_P);
-      const uint32_t p1_base = smem_u32(sm + C::OFF_P1);
       uint32_t g0 = 0, n_rescale = 0;
       int n_item = 0;
       for (int idx = item_begin; idx < item_end; ++idx) {
@@ -456,14 +484,14 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               const int s = gp % kStages;
               const uint32_t stage = kv_base + s * kStageBytes;
               for (int ks = 0; ks < kTile / 16; ++ks) {
-                const uint64_t a = smem_desc(
-                    (kDoubleP && pb ? p1_base : p_base) + ks * 32, 16, 1024, kSwizzle128B);
+                const uint64_t a =
+                    smem_desc(p_base + pb * kPBytes + ks * 32, 16, 1024, kSwizzle128B);
                 const uint64_t b = smem_desc(stage + ks * 16 * 128, 8192, 1024, kSwizzle128B);
                 mma_bf16_ss(tmem + TM_O, a, b, idesc_pv, (pv == 0 && ks == 0) ? 0u : 1u);
               }
               mma_commit(&c.bars[KV_EMPTY0 + s]);
               // both CTAs' P tiles (of this parity) are free
-              mma_commit_multicast(&c.bars[kDoubleP ? P_FREE0 + pb : P_FREE0], 0x3);
+              mma_commit_multicast(&c.bars[P_FREE0 + pb], 0x3);
               if (pv + 1 == nt) mma_commit(&c.bars[O_FINAL]);
               ++pv;
               pv_state = 0;
@@ -499,42 +527,45 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
             idle = 0;
           } else if (++idle > kWaitLimit || ((idle & 1023) == 0 && *c.abort)) {
             if (idle > kWaitLimit) {
-              *c.abort = 1;
-              atomicOr(c.status, kStatusTimeout);
+              give_up(c);
             }
             goto done_mma;
           }
         }
         g0 += nt;
       }
-    done_mma:;
+    done_mma:
+      mma_commit(&c.bars[MMA_DRAIN]);
+      drain_wait(&c.bars[MMA_DRAIN], 0);
     }
   } else if (warp >= 2 && warp < 2 + kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax (owned rows)
-    // Warp w covers the 16 owned lanes of subpartition sp = w mod 4 and KV
-    // columns [32 hw, 32 hw + 32), hw = (w - 2) / 4; its thread t takes lane
-    // 32 sp + 16 r + (t mod 16), columns 32 hw + 16 (t / 16) + [0, 16).  The
-    // two warps of a subpartition combine their row maxima (and, on an item's
-    // last tile, row sums) through shared memory.
-    const int sp = warp & 3, hw = (warp - 2) >> 2, hh = lane >> 4;
-    const int kq = 2 * hw + hh;                           // column quarter
-    const int k = 16 * sp + (lane & 15);                  // owned-row index
+    // Group grp = (w - 2) / 4 takes the KV tiles of global parity grp.  Its
+    // warp w covers the 16 owned lanes of subpartition sp = w mod 4: thread t
+    // takes lane 32 sp + 16 r + (t mod 16) and KV columns [32 hh, 32 hh + 32),
+    // hh = t / 16, so a row's two threads meet in one shuffle.  Tile g's
+    // running-max reference comes from the other group (tile g - 1) through
+    // shared memory; each group keeps its own share of the row sum.
+    const int sp = warp & 3, grp = (warp - 2) >> 2, hh = lane >> 4;
+    const int fw = (warp - 2) & 3;                         // warp within the group
+    const int k = 16 * sp + (lane & 15);                   // owned-row index
     const int q = 32 * sp + 16 * (int)rank + (lane & 15);  // query row == TMEM lane
     const uint32_t lane_addr = (uint32_t)(32 * sp + 16 * (int)rank) << 16;
-    const bool designated = warp == 2 && lane == 0;
-    const int sm_tid = (warp - 2) * 32 + lane;
+    const bool designated = fw == 0 && lane == 0;
+    const int g_tid = fw * 32 + lane;  // thread within the group
     const float scale = run_bmm1(p, c.status) * kLog2e;
-    float* mx = reinterpret_cast<float*>(sm + OFF_MX);  // [parity][hw][lane]
-    float* lx = reinterpret_cast<float*>(sm + OFF_LX);  // [hw][lane]
-    const uint32_t xfree_peer = map_to_rank(smem_u32(&c.bars[PEER_X_FREE]), peer);
+    float* mref = reinterpret_cast<float*>(sm + OFF_MREF);  // [tile parity][row]
+    float* lx = reinterpret_cast<float*>(sm + OFF_LX);      // [item parity][l, m][row]
+    const uint32_t xfree_peer0 = map_to_rank(smem_u32(&c.bars[PEER_X_FREE0]), peer);
     const uint32_t pfull_peer0 = map_to_rank(smem_u32(&c.bars[P_FULL0]), peer);
     const uint32_t p_peer0 = map_to_rank(smem_u32(sm + OFF_P), peer);
-    const uint32_t p_peer1 = map_to_rank(smem_u32(sm + C::OFF_P1), peer);
     const uint32_t fac_peer0 = map_to_rank(smem_u32(sm + OFF_FAC), peer);
     const uint32_t flag_peer0 = map_to_rank(smem_u32(sm + OFF_FLAG), peer);
     const uint32_t lrow_peer = map_to_rank(smem_u32(sm + OFF_LROW), peer);
+    const int W = max(p.cp_world, 1);
     uint32_t g = 0;
     int n_item = 0;
+    int n_multi = 0;  // items of two or more tiles so far: they alone use the (l, m) hand-off
     for (int idx = item_begin; idx < item_end; ++idx) {
       const WorkItem it = items[idx];
       const int nt = n_tiles_of(it);
@@ -543,164 +574,173 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const int row0 = it.g * kRows;
       const bool row_ok = q < rows_total - row0;
       const int qi = (row0 + q) / H;
-      const int W = max(p.cp_world, 1);
       const int last = p.causal ? causal_last(it.mask_base, qi, W) : it.seq_len - 1;
       // tiles ending at or before `clean_end` need no mask for any valid row
       const int first_qi = row0 / H;
-      const int clean_end =
-          min(it.kv_end, p.causal ? causal_last(it.mask_base, first_qi, W) + 1 : it.seq_len);
-      float m_ref = -INFINITY, l_part = 0.f;  // l_part: this thread's 16 columns only
+      const int clean_end = min(
+          it.kv_end, p.causal ? causal_last(it.mask_base, first_qi, W) + 1 : it.seq_len);
+      const uint32_t g_last = g + (uint32_t)nt - 1;
+      // (l, m) hand-off slot of this item and the phase of its barrier: only
+      // items of two or more tiles (both groups take part) count
+      const int ip = n_multi & 1;
+      const uint32_t lx_phase = (uint32_t)(n_multi >> 1) & 1;
+      // this group's share of the row sum (this thread's 32 columns), relative
+      // to the reference m_grp of the group's latest tile of the item
+      float l_part = 0.f, m_grp = -INFINITY;
       for (int t = 0; t < nt; ++t, ++g) {
-        const int sb = g & 1;
-        const bool last_tile = t + 1 == nt;
-        float sv[16];
+        if ((int)(g & 1) != grp) continue;
+        const int sb = grp;
+        float sv[32];
         if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
         tc_fence_after();
         {
-          uint32_t v[16];
-          tmem_ld_16x32bx2_x16_s16(tmem + lane_addr + TM_S + 64 * sb + 32 * hw, v);
+          uint32_t v[32];
+          tmem_ld_16x32bx2_x32(tmem + lane_addr + TM_S + 64 * sb, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.bars[S_FREE0 + sb]);
         // add the peer's partial scores of this row (fp32, columns
-        // [16 kq, 16 kq + 16) = 16-byte units 4 kq .. 4 kq + 3 of the row)
-        if (!wait_bar(c, X_FULL, g & 1)) goto done_softmax;
+        // [32 hh, 32 hh + 32) = 16-byte units 8 hh .. 8 hh + 7 of the row)
+        if (!wait_bar(c, X_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
         {
-          const unsigned char* xb = sm + OFF_X + k * kXRowBytes;
+          const unsigned char* xb = sm + OFF_X + sb * kXBytes + k * kXRowBytes;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float4 x = *reinterpret_cast<const float4*>(xb + (((4 * kq + u) ^ (k & 7)) << 4));
+          for (int u = 0; u < 8; ++u) {
+            const float4 x = *reinterpret_cast<const float4*>(xb + (((8 * hh + u) ^ (k & 7)) << 4));
             sv[4 * u] += x.x;
             sv[4 * u + 1] += x.y;
             sv[4 * u + 2] += x.z;
             sv[4 * u + 3] += x.w;
           }
         }
-        // the buffer's next phase (tile g + 1) completes once the peer's bytes
-        // for it land, which the peer sends only after every softmax warp here
-        // released this tile's scores (PEER_X_FREE)
-        if (designated) mbar_arrive_expect_tx(&c.bars[X_FULL], kXBytes);
+        // the buffer's next phase (tile g + 2) completes once the peer's bytes
+        // for it land, which the peer sends only after this group released
+        // this tile's scores (PEER_X_FREE)
+        if (designated) mbar_arrive_expect_tx(&c.bars[X_FULL0 + sb], kXBytes);
         // relaxed: the warp's reads of the buffer have returned their values
         // (release at cluster scope would cost a cluster-wide fence per tile)
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer);
-        // mask, online softmax (scale folded into the exponent)
+        if (lane == 0) mbar_arrive_cluster_relaxed(xfree_peer0 + 8u * sb);
+        // mask, then the row maximum of the tile (log2 units)
         const int j0 = it.kv_begin + t * kTile;
-        const int c0 = j0 + 16 * kq;  // KV index of sv[0]
-        float f = 1.f;
-        bool need = false;
-        float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 chains for ILP
+        const int c0 = j0 + 32 * hh;  // KV index of sv[0]
         // tiles with masked columns are scaled before the -inf mask goes in,
         // so that bmm1 = 0 never multiplies -inf (the same for the whole tile)
         const bool pre_scaled = j0 + kTile > clean_end;
+        const float sc = pre_scaled ? 1.f : scale;  // what the scores still need
+        float m_tile = -INFINITY;
         if (row_ok) {
+          float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 chains for ILP
           if (!pre_scaled) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
+            for (int j = 0; j < 32; ++j) tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 32; ++j) {
               const int col = c0 + j;
               sv[j] = (col <= last && col < it.kv_end) ? sv[j] * scale : -INFINITY;
               tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
             }
           }
+          m_tile = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
         }
-        float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
-        // the row's four threads: lanes t and t + 16 of this warp and of the
-        // partner warp (same subpartition, other column half)
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-        {
-          float* slot = mx + sb * 2 * kRows;
-          if (hh == 0) slot[hw * kRows + q] = tmax;
-          __syncwarp();
-          const int bar = MX_FULL0 + 2 * sp + sb;
-          if (lane == 0) mbar_arrive(&c.bars[bar]);
-          if (!wait_bar(c, bar, (g >> 1) & 1)) goto done_softmax;
-          tmax = fmaxf(tmax, slot[(hw ^ 1) * kRows + q]);
+        m_tile = fmaxf(m_tile, __shfl_xor_sync(0xffffffffu, m_tile, 16)) * sc;
+        // The item's running reference after tile g - 1 (the other group's
+        // tile); every tile but the very first waits for it, even where it
+        // starts an item and ignores the value, so that the barrier phases of
+        // the two groups stay in step.
+        float m_prev = -INFINITY;
+        if (g > 0) {
+          const uint32_t gp = g - 1;
+          if (!wait_bar(c, MREF0 + 4 * (gp & 1) + sp, (gp >> 1) & 1)) goto done_softmax;
+          if (t > 0) m_prev = mref[(gp & 1) * kRows + q];
+        }
+        // raised (and O rescaled) only when the tile's maximum passes it by
+        // more than the threshold; the first tile of an item sets it
+        const float m_new =
+            (t == 0 || m_tile > m_prev + kRescaleThreshold) ? (row_ok ? m_tile : m_prev) : m_prev;
+        if (hh == 0) mref[sb * kRows + q] = m_new;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.bars[MREF0 + 4 * sb + sp]);
+        const bool need = t > 0 && m_new != m_prev;
+        const float f = need ? ex2(m_prev - m_new) : 1.f;  // m_prev = -inf gives 0
+        if (m_new > m_grp) {  // rebase this group's share (0 while m_grp = -inf)
+          l_part *= ex2(m_grp - m_new);
+          m_grp = m_new;
         }
         if (row_ok) {
-          const float sc = pre_scaled ? 1.f : scale;  // what the scores still need
-          const float m_new = fmaxf(m_ref, tmax * sc);
-          if (t == 0) {
-            m_ref = m_new;
-          } else if (m_new > m_ref + kRescaleThreshold) {
-            f = ex2(m_ref - m_new);  // m_ref = -inf gives 0
-            need = true;
-            l_part *= f;
-            m_ref = m_new;
-          }
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
           float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 32; ++j) {
             sv[j] = ex2(fmaf(sv[j], sc, -m_use));
             rs[j & 3] += sv[j];
           }
           l_part += (rs[0] + rs[1]) + (rs[2] + rs[3]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[j] = 0.f;
+          for (int j = 0; j < 32; ++j) sv[j] = 0.f;
         }
         // zero V rows past the end of the KV range (last tile of the item)
         const int valid = it.kv_end - j0;
         if (valid < kTile) {
           unsigned char* stage = sm + OFF_KV + (g % kStages) * kStageBytes;
           const int nz = (kTile - valid) * kLatChunks * 8;  // 16-byte units
-          for (int e = sm_tid; e < nz; e += kSoftmaxWarps * 32) {
+          for (int e = g_tid; e < nz; e += kGroupWarps * 32) {
             const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
             *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
                 make_uint4(0, 0, 0, 0);
           }
         }
-        // P (bf16) of this row into both CTAs' (single) P tiles once both
-        // CTAs' PV of the previous tile read them
-        if (kDoubleP ? !wait_bar(c, P_FREE0 + sb, ((g >> 1) & 1) ^ 1)
-                     : (g > 0 && !wait_bar(c, P_FREE0, (g - 1) & 1)))
-          goto done_softmax;
+        // P (bf16) of this row into both CTAs' P tiles of this parity once both
+        // CTAs' PV of tile g - 2 read them
+        if (!wait_bar(c, P_FREE0 + sb, ((g >> 1) & 1) ^ 1)) goto done_softmax;
         {
-          uint32_t w[8];
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) w[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
+          for (int e = 0; e < 16; ++e) w[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
           const uint32_t pbar = pfull_peer0 + 8u * sb;
+          unsigned char* ptile = sm + OFF_P + sb * kPBytes;
+          const uint32_t ppeer = p_peer0 + sb * kPBytes;
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint32_t off = q * 128 + (((2 * kq + u) ^ (q & 7)) << 4);
-            const uint32_t tile = kDoubleP && sb ? C::OFF_P1 : OFF_P;
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t off = q * 128 + (((4 * hh + u) ^ (q & 7)) << 4);
             const uint4 val = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            *reinterpret_cast<uint4*>(sm + tile + off) = val;
-            st_async_v4_b32((kDoubleP && sb ? p_peer1 : p_peer0) + off, val, pbar);
+            *reinterpret_cast<uint4*>(ptile + off) = val;
+            st_async_v4_b32(ppeer + off, val, pbar);
           }
-          if (kq == 0) {
+          if (hh == 0) {
             fac[sb * kRows + q] = f;
             st_async_b32(fac_peer0 + 4u * (sb * kRows + q), __float_as_uint(f), pbar);
           }
           const bool any = __any_sync(0xffffffffu, need);
           if (lane == 0) {
             const int fv = any ? (int)g : -1;
-            flags[16 * sb + (warp - 2)] = fv;
-            st_async_b32(flag_peer0 + 4u * (16 * sb + 8 + (warp - 2)), (uint32_t)fv, pbar);
+            flags[16 * sb + fw] = fv;
+            st_async_b32(flag_peer0 + 4u * (16 * sb + 8 + fw), (uint32_t)fv, pbar);
           }
         }
-        if (last_tile) {
-          // row sum over the row's four threads -> both CTAs' l (epilogue) and the LSE
-          float l_pair = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
-          if (hh == 0) lx[hw * kRows + q] = l_pair;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&c.bars[LX_FULL0 + sp]);
-          if (!wait_bar(c, LX_FULL0 + sp, n_item & 1)) goto done_softmax;
-          const float l_row = l_pair + lx[(hw ^ 1) * kRows + q];
-          if (kq == 0) {
-            // the previous item's epilogues (both CTAs) have read l
-            if (n_item > 0 && !wait_bar_cluster(c, LROW_FREE, (n_item - 1) & 1)) goto done_softmax;
+        if (g == g_last) {
+          // the row sum of the item: this group's share plus the other
+          // group's, published when it finished its tiles of the item
+          float l_row = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+          if (nt > 1) {
+            if (!wait_bar(c, LX0 + 4 * ip + sp, lx_phase)) goto done_softmax;
+            const float l_o = lx[(2 * ip) * kRows + q];
+            const float m_o = lx[(2 * ip + 1) * kRows + q];
+            if (l_o > 0.f) l_row += l_o * ex2(m_o - m_new);
+          }
+          // the previous item's epilogues (both CTAs) have read l
+          if (n_item > 0 && !wait_bar_cluster(c, LROW_FREE, (n_item - 1) & 1)) goto done_softmax;
+          if (hh == 0) {
             lrow[q] = l_row;
             st_async_b32(lrow_peer + 4u * q, __float_as_uint(l_row), pfull_peer0 + 8u * sb);
             if (row_ok) {
-              const float lse = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -INFINITY;
+              const float lse = l_row > 0.f ? (m_new + log2f(l_row)) * kLn2 : -INFINITY;
               const size_t grow = (size_t)it.q_start * H + row0 + q;
               if (it.slot < 0) {
                 if (p.return_lse) p.lse[grow] = lse;
@@ -714,13 +754,24 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         fence_proxy_async_smem();  // P and zeroed V rows are read by the MMA
         __syncwarp();
         if (lane == 0) {
-          if (warp == 2)
+          if (fw == 0)
             mbar_arrive_expect_tx(&c.bars[P_FULL0 + sb],
-                                  kPeerPBytes + (last_tile ? kPeerLBytes : 0u));
+                                  kPeerPBytes + (g == g_last ? kPeerLBytes : 0u));
           else
             mbar_arrive(&c.bars[P_FULL0 + sb]);
         }
       }
+      if (nt > 1 && grp != (int)(g_last & 1)) {
+        // hand this group's share of the row sum to the group of the last tile
+        const float l_row = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+        if (hh == 0) {
+          lx[(2 * ip) * kRows + q] = l_row;
+          lx[(2 * ip + 1) * kRows + q] = m_grp;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.bars[LX0 + 4 * ip + sp]);
+      }
+      if (nt > 1) ++n_multi;
       ++n_item;
     }
   done_softmax:;
@@ -735,8 +786,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
     const uint32_t peer_lanes = (uint32_t)(32 * sp + 16 * (int)peer) << 16;
     const int kp = 16 * sp + (lane & 15);  // the peer's owned-row index of my send row
-    const uint32_t x_peer = map_to_rank(smem_u32(sm + OFF_X), peer);
-    const uint32_t xfull_peer = map_to_rank(smem_u32(&c.bars[X_FULL]), peer);
+    const uint32_t x_peer0 = map_to_rank(smem_u32(sm + OFF_X), peer);
+    const uint32_t xfull_peer0 = map_to_rank(smem_u32(&c.bars[X_FULL0]), peer);
     const uint32_t lfree_peer = map_to_rank(smem_u32(&c.bars[LROW_FREE]), peer);
     uint32_t g = 0, n_rescale = 0;
     int n_item = 0;
@@ -757,13 +808,14 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (32 * hh + j >= valid) v[j] = 0u;
-      // the peer's softmax released the previous tile's scores
-      if (!wait_bar_cluster(c, PEER_X_FREE, (gs & 1) ^ 1)) return false;
-      const uint32_t xb = x_peer + (uint32_t)(kp * kXRowBytes);
+      // the peer's softmax released the buffer (tile gs - 2's scores)
+      if (!wait_bar_cluster(c, PEER_X_FREE0 + sb, ((gs >> 1) & 1) ^ 1)) return false;
+      const uint32_t xb = x_peer0 + (uint32_t)(sb * kXBytes + kp * kXRowBytes);
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         st_async_v4_b32(xb + (uint32_t)(((8 * hh + u) ^ (kp & 7)) << 4),
-                        make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]), xfull_peer);
+                        make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]),
+                        xfull_peer0 + 8u * sb);
       return true;
     };
     // Row q of the item's Q latent dims of this CTA ([256 r, 256 r + 256)) into
@@ -1010,10 +1062,10 @@ bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int e
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kFp8, bool kDoubleP>
+template <bool kFp8>
 cudaError_t setup_one(int sm_count, int* n_pairs) {
-  using C = Cfg<kFp8, kDoubleP>;
-  auto kernel = decode_sm103_kernel<kFp8, kDoubleP>;
+  using C = Cfg<kFp8>;
+  auto kernel = decode_sm103_kernel<kFp8>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1037,10 +1089,10 @@ cudaError_t setup_one(int sm_count, int* n_pairs) {
 }
 
 // Launch as a programmatic dependent of the previous kernel in the stream.
-template <bool kFp8, bool kDoubleP>
+template <bool kFp8>
 cudaError_t launch_pdl(int grid, cudaStream_t stream, const Problem& p, const Layout& lay, char* ws,
                        const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c) {
-  using C = Cfg<kFp8, kDoubleP>;
+  using C = Cfg<kFp8>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -1051,24 +1103,18 @@ cudaError_t launch_pdl(int grid, cudaStream_t stream, const Problem& p, const La
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kFp8, kDoubleP>, p, lay, ws, a, b, c);
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kFp8>, p, lay, ws, a, b, c);
 }
 
 }  // namespace
 
-// The configuration a problem runs with (see Cfg): one P tile and a deeper
-// ring when every row of a 128-row item is a real (token, head) row, i.e.
-// H q_len >= 128 (packed launches: H >= 128, their q_len varies).
-static bool single_p_tile(int kv_dtype, int num_heads, int max_q, int packed) {
-  return kv_dtype != 1 && (long long)num_heads * (packed ? 1 : max_q) >= kRows;
-}
-
 cudaError_t decode_sm103_setup(int kv_dtype, int num_heads, int max_q, int packed, int sm_count,
                                int* n_pairs) {
-  if (kv_dtype == 1) return setup_one<true, true>(sm_count, n_pairs);
-  return single_p_tile(kv_dtype, num_heads, max_q, packed)
-             ? setup_one<false, false>(sm_count, n_pairs)
-             : setup_one<false, true>(sm_count, n_pairs);
+  (void)num_heads;
+  (void)max_q;
+  (void)packed;
+  if (kv_dtype == 1) return setup_one<true>(sm_count, n_pairs);
+  return setup_one<false>(sm_count, n_pairs);
 }
 
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
@@ -1082,28 +1128,23 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                 : encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 32,
                             kRows, CU_TENSOR_MAP_SWIZZLE_64B)))
     return cudaErrorInvalidValue;
-  const bool fp8 = p.kv_dtype == 1;
-  if (fp8) {
+  if (p.kv_dtype == 1) {
     // e4m3 bytes land row-major in the staging ring; the converter swizzles
     if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 64,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 32,
                    p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    return launch_pdl<true, true>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope,
-                                  tm_kv, tm_kv_rope);
-  } else {
-    if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64,
-                   p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 32,
-                   p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
-      return cudaErrorInvalidValue;
-    if (single_p_tile(p.kv_dtype, p.num_heads, p.max_q, p.packed))
-      return launch_pdl<false, false>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws),
-                                      tm_q_rope, tm_kv, tm_kv_rope);
-    return launch_pdl<false, true>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope,
-                                   tm_kv, tm_kv_rope);
+    return launch_pdl<true>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv,
+                            tm_kv_rope);
   }
+  if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64,
+                 p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 32,
+                 p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  return launch_pdl<false>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv,
+                           tm_kv_rope);
 }
 
 }  // namespace mla

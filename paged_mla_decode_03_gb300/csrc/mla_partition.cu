@@ -70,6 +70,9 @@ template <typename T>
 __device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
+  // every thread has read the previous scan's total (returned from carry_ll)
+  // before it is reset
+  __syncthreads();
   if (threadIdx.x == 0) sh.carry_ll = 0;
   __syncthreads();
   for (int base = 0; base < n; base += blockDim.x) {

@@ -657,3 +657,33 @@ def test_prefill_scale_packed_launch(H, B, qlo, qhi, lhi):
     ref_o, ref_l = oracle.run(w, sel=sel)
     check("bf16", out[sel[:, 0], sel[:, 1]], ref_o, lse[sel[:, 0], sel[:, 1]], ref_l,
           what=f"prefill H={H}")
+
+
+def test_prefill_scale_repeats_are_finite_and_bitwise_equal():
+    """Ten back-to-back launches of the >16k-token packed case on one
+    workspace, refilled with 0x00 / 0xFF between them: every launch must
+    finish clean and give the same bits.  (The partitioner once read a
+    block scan's total after the next scan had reset it, so on a large work
+    list some threads saw no items: unwritten rows or stalled workers, on
+    roughly one launch in five.)"""
+    rng = np.random.default_rng(86 + 128)
+    q = rng.integers(24, 48, size=512, endpoint=True).astype(np.int32)
+    L = rng.integers(q + 1, 2048, endpoint=True).astype(np.int32)
+    w = mi.build("prefill_h128", 86 + 128, num_heads=128, page_size=64, seq_lens=L, q_lens=q,
+                 packed=True, return_lse=True, max_seq_len_q=48)
+    d = to_device(w)
+    first = None
+    for rep in range(10):
+        d.out.fill_(float("nan"))
+        d.lse.fill_(float("nan"))
+        d.workspace.fill_(0xFF if rep % 2 else 0x00)
+        run(w, d)
+        torch.cuda.synchronize()
+        assert device_status(d) == 0, rep
+        o = d.out.view(torch.int16).clone()
+        l = d.lse.clone()
+        assert torch.isfinite(d.out.float()).all() and torch.isfinite(l).all(), rep
+        if first is None:
+            first = (o, l)
+        else:
+            assert torch.equal(first[0], o) and torch.equal(first[1], l), rep
