@@ -324,6 +324,24 @@ int mla_merge_states(const void *o_parts, const float *lse_parts, int32_t n_part
 size_t mla_decode_workspace_size(const mla_plan_t *plan);
 
 /*
+ * Where a run leaves its split-KV work list in the workspace, for tests and
+ * tools that check the on-device partition (decoding never needs it).  After
+ * a run has completed:
+ *   int32 at byte 4             number of work items
+ *   items_offset                the items, 10 int32 each: request b, row group
+ *                               g (rows [128 g, 128 g + 128) of the request's
+ *                               q_len * H rows), KV rows [kv_begin, kv_end),
+ *                               partial slot (-1: writes out directly), q_len,
+ *                               seq_len, first token, combine entry (-1: none),
+ *                               causal mask base
+ *   worker_ranges_offset        int32[n_workers + 1]: persistent worker w (a CTA
+ *                               pair) runs items [r[w], r[w + 1])
+ * Errors: MLA_ERR_INVALID_ARG on a NULL argument.
+ */
+int mla_decode_work_list_layout(const mla_plan_t *plan, size_t *items_offset,
+                                size_t *worker_ranges_offset, int32_t *n_workers);
+
+/*
  * Byte offset, inside the workspace, of the int32 device status word the last
  * run left behind.  0: every device-side value was within the contract.
  * Bits (values are clamped and never read out of bounds):

@@ -107,6 +107,9 @@ def load_library():
     lib.mla_decode_destroy.restype = None
     lib.mla_decode_workspace_size.argtypes = [vp]
     lib.mla_decode_workspace_size.restype = sz
+    lib.mla_decode_work_list_layout.argtypes = [vp, ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                                ctypes.POINTER(i32)]
+    lib.mla_decode_work_list_layout.restype = ctypes.c_int
     lib.mla_decode_status_offset.argtypes = []
     lib.mla_decode_status_offset.restype = sz
     lib.mla_decode_status_string.argtypes = [ctypes.c_int]
@@ -141,6 +144,17 @@ def mla_decode_destroy(plan: Optional[int]) -> None:
 
 def mla_decode_workspace_size(plan: int) -> int:
     return int(load_library().mla_decode_workspace_size(ctypes.c_void_p(plan)))
+
+
+def mla_decode_work_list_layout(plan: int) -> Tuple[int, int, int]:
+    """(items offset, worker-ranges offset, workers) of a plan's work list in
+    the workspace (see include/mla_decode.h); for tests and tools."""
+    a, b, n = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int32()
+    rc = load_library().mla_decode_work_list_layout(ctypes.c_void_p(plan), ctypes.byref(a),
+                                                    ctypes.byref(b), ctypes.byref(n))
+    if rc != MLA_OK:
+        raise MlaDecodeError(rc, "mla_decode_work_list_layout")
+    return a.value, b.value, n.value
 
 
 def _nbytes(x) -> int:

@@ -415,6 +415,16 @@ void mla_decode_destroy(mla_plan_t* plan) { delete plan; }
 
 size_t mla_decode_workspace_size(const mla_plan_t* plan) { return plan ? plan->lay.total : 0; }
 
+int mla_decode_work_list_layout(const mla_plan_t* plan, size_t* items_offset,
+                                size_t* worker_ranges_offset, int32_t* n_workers) {
+  if (!plan || !items_offset || !worker_ranges_offset || !n_workers) return MLA_ERR_INVALID_ARG;
+  static_assert(sizeof(mla::WorkItem) == 10 * sizeof(int32_t), "work item record");
+  *items_offset = plan->lay.items;
+  *worker_ranges_offset = plan->lay.worker_ranges;
+  *n_workers = plan->lay.n_workers;
+  return MLA_OK;
+}
+
 size_t mla_decode_status_offset(void) { return sizeof(int) * mla::kHdrStatus; }
 
 const char* mla_decode_status_string(int status) {

@@ -10,12 +10,15 @@
 // Cost model: a request with q query rows and H heads has G = ceil(q H / R)
 // row groups of R rows; each group costs c0 + T units, T = ceil(L / 64) KV
 // tiles plus a fixed overhead c0 (query load, epilogue).  Laying all groups
-// end to end gives W units; worker p owns units [floor(p W / n),
-// floor((p+1) W / n)).  A group that straddles a range boundary is cut at the
-// corresponding tile and each piece becomes a separate item writing a
-// partial; every other group is one item writing the output directly.  So
-// workers are balanced to within one tile plus one overhead, and there are at
-// most n + #groups items and n - 1 cut points.  One CTA of 128-1024 threads.
+// end to end gives W units; with n' = min(n, W / kMinUnits) workers (a
+// worker gets at least about one item's worth; the others stay idle), worker
+// p owns units [floor(p W / n'), floor((p+1) W / n')).  A group that
+// straddles a range boundary is cut at the corresponding tile and each piece
+// becomes a separate item writing a partial; every other group is one item
+// writing the output directly.  So workers are balanced to within one tile
+// plus one overhead, and there are at most n + #groups items and n - 1 cut
+// points.  One CTA of 128-1024 threads; the range boundaries are tabulated in
+// shared memory once, so cut points and owners are table lookups.
 #include <algorithm>
 
 #include "mla_common.cuh"
@@ -29,12 +32,15 @@ namespace {
 // (fewer warps make the block-wide steps cheaper on small problems).
 constexpr int kMaxThreads = 1024;
 constexpr long long kOverheadTiles = 3;  // c0: query load + epilogue, in tile units (measured ~3.2)
+constexpr long long kMinUnits = 4;       // least work per busy worker: one item of one tile
+constexpr int kBoundTable = 512;         // workers whose range boundaries are tabulated
 
 struct Shared {
   long long warp_ll[32];
   int warp_i[32];
   int carry;
   long long carry_ll;
+  long long bound[kBoundTable + 1];  // start unit of every worker's range (and W)
 };
 
 __device__ int block_or(int v, Shared& sh) {
@@ -110,14 +116,25 @@ __device__ T block_exclusive_scan(T* data, int n, Shared& sh) {
 // With one lane this is the plain split of [0, W) into n near-equal ranges.
 struct Bounds {
   long long W, n, lanes, nl, WL;
-  // start unit of worker p's range
-  __device__ long long boundary(long long p) const {
+  const long long* table;  // boundary(p) for p in [0, n], or nullptr
+  // start unit of worker p's range (the arithmetic behind the table)
+  __device__ long long boundary_of(long long p) const {
     if (p >= lanes * nl) return W;
     const long long k = p / nl, i = p - k * nl;
     return k * WL + (i * WL) / nl;
   }
-  // first worker p whose range starts after unit x (0 <= x < W)
+  __device__ long long boundary(long long p) const { return table ? table[p] : boundary_of(p); }
+  // first worker p whose range starts after unit x (0 <= x < W); boundaries
+  // are nondecreasing in p and boundary(n) = W > x
   __device__ long long first_above(long long x) const {
+    if (table) {
+      long long lo = 0, hi = n;
+      while (lo < hi) {
+        const long long mid = (lo + hi) >> 1;
+        if (table[mid] > x) hi = mid; else lo = mid + 1;
+      }
+      return lo;
+    }
     const long long k = x / WL, r = x - k * WL;
     const long long i = ((r + 1) * nl + WL - 1) / WL;
     return i >= nl ? (k + 1) * nl : k * nl + i;
@@ -243,7 +260,22 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   //    groups are laid out in request order on one lane.
   const long long n = lay.n_workers;
   const int G = g_max;
-  const int lanes = (g_min == g_max && G >= 2 && n / G >= 2) ? G : 1;
+  // groups' total cost first (lane order does not change it), then the
+  // number of busy workers and the lanes
+  long long W_total = 0;
+  for (int b = threadIdx.x; b < B && n_groups > 0; b += blockDim.x) {
+    const int gb = r_gbase[b];  // scanned: first group of request b
+    const int ge = (b + 1 < B) ? r_gbase[b + 1] : n_groups;
+    W_total += (long long)(ge - gb) * (kOverheadTiles + (r_len[b] + kKvTile - 1) / kKvTile);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sh.carry_ll = 0;
+  __syncthreads();
+  atomicAdd(reinterpret_cast<unsigned long long*>(&sh.carry_ll), (unsigned long long)W_total);
+  __syncthreads();
+  W_total = sh.carry_ll;
+  const long long n_eff = max(1LL, min(n, W_total / kMinUnits));
+  const int lanes = (g_min == g_max && G >= 2 && n_eff / G >= 2) ? G : 1;
   const int n_req_groups = lanes > 1 ? n_groups / G : 0;  // requests that have groups
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int gb = r_gbase[b];
@@ -263,8 +295,14 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   bd.W = W;
   bd.n = n;
   bd.lanes = lanes;
-  bd.nl = n / lanes;
-  bd.WL = W / lanes;  // every lane has the same cost
+  bd.nl = n_eff / lanes;  // busy workers per lane; the rest get empty ranges
+  bd.WL = W / lanes;      // every lane has the same cost
+  bd.table = nullptr;
+  if (n <= kBoundTable) {
+    for (long long q = threadIdx.x; q <= n; q += blockDim.x) sh.bound[q] = bd.boundary_of(q);
+    __syncthreads();
+    bd.table = sh.bound;
+  }
 
   // 3. Cut points inside each group -> chunk counts.
   for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {

@@ -64,9 +64,9 @@ def test_full_size_workload_sampled_parity(name):
 
 
 def test_many_way_split_and_long_combine():
-    """One long request on a 16-head group: the partitioner cuts it into far
-    more than 32 chunks, exercising the multi-pass LSE merge."""
-    w = mi.build("split", 77, num_heads=16, page_size=64, seq_lens=[9000], q_lens=[1],
+    """One long request on a 16-head group: the partitioner cuts it into more
+    than 32 chunks (one per busy worker), exercising the multi-pass LSE merge."""
+    w = mi.build("split", 77, num_heads=16, page_size=64, seq_lens=[20000], q_lens=[1],
                  packed=False, return_lse=True)
     full_parity(w)
 
@@ -687,3 +687,27 @@ def test_prefill_scale_repeats_are_finite_and_bitwise_equal():
             first = (o, l)
         else:
             assert torch.equal(first[0], o) and torch.equal(first[1], l), rep
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek_v3", "mtp", "ragged", "fp8_long", "prefill"])
+def test_partition_work_list_matches_host_model(name):
+    """The work list the on-device partitioner leaves in the workspace equals
+    the host model of the same arithmetic (tests/partition_model.py), item by
+    item and worker range by worker range, on every bench workload."""
+    import paged_mla_decode_03_gb300 as mla
+    from partition_model import partition
+    w = mi.WORKLOADS[name]()
+    d = to_device(w)
+    run(w, d)
+    torch.cuda.synchronize()
+    assert device_status(d) == 0
+    items_off, wr_off, n_workers = mla.mla_decode_work_list_layout(d.plan.handle)
+    n_items = int(d.workspace[4:8].view(torch.int32).item())
+    got = d.workspace[items_off:items_off + 40 * n_items].view(torch.int32).cpu().numpy()
+    got = got.reshape(-1, 10).tolist()
+    got_wb = d.workspace[wr_off:wr_off + 4 * (n_workers + 1)].view(torch.int32).cpu().tolist()
+    qs = w.q_start()[:-1]
+    items, wb, _ = partition(w.seq_lens, w.q_lens, qs, w.num_heads, n_workers,
+                             w.seq_lens.astype(np.int64) - w.q_lens)
+    assert got == [list(t) for t in items]
+    assert got_wb == wb
