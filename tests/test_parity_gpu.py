@@ -711,3 +711,46 @@ def test_partition_work_list_matches_host_model(name):
                              w.seq_lens.astype(np.int64) - w.q_lens)
     assert got == [list(t) for t in items]
     assert got_wb == wb
+
+
+@pytest.mark.parametrize("name", ["tiny", "uniform76", "deepseek_v3"])
+def test_back_to_back_calls_do_not_disturb_each_other(name):
+    """Sixteen calls on one stream and one workspace with no synchronisation
+    between them, alternating two sets of lengths, each into its own output
+    buffer: every output equals its set's synchronised result bit for bit.
+    With nothing split ("tiny", and "uniform76": one 128-row group per
+    worker) the combine kernel of a call has no work, so this checks that the
+    next call's partitioner never rewrites the work list under a decode grid
+    that is still running."""
+    if name == "tiny":
+        w = mi.tiny()
+        lens_b = np.array([64, 20], np.int32)
+    elif name == "uniform76":
+        w = mi.build("uniform76", 99, num_heads=128, page_size=64, seq_lens=[3000] * 76,
+                     q_lens=[1] * 76, packed=False, return_lse=True)
+        lens_b = np.array([2000 + 13 * i for i in range(76)], np.int32)
+    else:
+        w = mi.deepseek_v3(batch=64, return_lse=True)
+        lens_b = np.minimum(w.seq_lens[::-1].copy(), w.seq_lens)
+    d = to_device(w)
+    sl_a = d.seq_lens.clone()
+    sl_b = torch.from_numpy(np.minimum(lens_b, w.seq_lens)).to(sl_a.device)
+    refs = []
+    for sl in (sl_a, sl_b):
+        d.plan.run(d.query, d.kv_cache, d.block_tables, sl, d.out, lse=d.lse,
+                   workspace=d.workspace, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale)
+        torch.cuda.synchronize()
+        refs.append((d.out.clone(), d.lse.clone()))
+    outs = [torch.full_like(d.out, float("nan")) for _ in range(16)]
+    lses = [torch.full_like(d.lse, float("nan")) for _ in range(16)]
+    torch.cuda.synchronize()
+    for k in range(16):
+        d.plan.run(d.query, d.kv_cache, d.block_tables, sl_a if k % 2 == 0 else sl_b, outs[k],
+                   lse=lses[k], workspace=d.workspace, bmm1_scale=w.bmm1_scale,
+                   bmm2_scale=w.bmm2_scale)
+    torch.cuda.synchronize()
+    assert device_status(d) == 0
+    for k in range(16):
+        ro, rl = refs[k % 2]
+        assert torch.equal(outs[k].view(torch.int16), ro.view(torch.int16)), k
+        assert torch.equal(lses[k], rl), k
