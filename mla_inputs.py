@@ -71,6 +71,13 @@ class Workload:
     cp_world: int = 1
     cp_rank: int = 0
     seq_lens_global: Optional[np.ndarray] = None
+    # sparse top-k selection: int32 [tokens, k] logical KV positions per query
+    # token (-1: unused entry), or None for the causal / dense mask
+    sparse_idx: Optional[np.ndarray] = None
+
+    @property
+    def sparse_k(self) -> int:
+        return 0 if self.sparse_idx is None else int(self.sparse_idx.shape[1])
 
     @property
     def total_q(self) -> int:
@@ -298,6 +305,50 @@ def prefill(seed: int = 1006, batch: int = 512, q_lo: int = 24, q_hi: int = 48,
                  poison=poison, rng=rng)
 
 
+def with_topk(w: Workload, k: int, seed: int = 0) -> Workload:
+    """``w`` with a sparse top-k list per query token.
+
+    The pages name the launcher argument ``sparse_mla_top_k`` and nothing
+    more, so the lists are drawn to look like an indexer's output: token i
+    of a request with q tokens and L cached rows picks min(k, L - q + i + 1)
+    distinct positions of its causal prefix [0, L - q + i], uniformly at
+    random and in random order, and pads the rest of its k entries with -1.
+    Sampling only: no attention arithmetic.
+    """
+    rng = np.random.default_rng(seed)
+    qs = w.q_start()
+    idx = np.full((int(qs[-1]), int(k)), -1, dtype=np.int32)
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        q = int(qs[b + 1] - qs[b])
+        for i in range(q):
+            n = max(0, L - q + i + 1)
+            m = min(int(k), n)
+            if m == 0:
+                continue
+            if n <= 4 * m:
+                pick = rng.permutation(n)[:m]
+            else:  # sparse pick from a long prefix without an O(n) permutation
+                pick = rng.choice(n, size=m, replace=False)
+            idx[int(qs[b]) + i, :m] = pick.astype(np.int32)
+    return dataclasses.replace(w, name=f"{w.name}_top{k}", sparse_idx=idx)
+
+
+def sparse_topk(seed: int = 1007, batch: int = 64, k: int = 2048, lo: int = 3072,
+                hi: int = 12288, q_len: int = 1, return_lse: bool = False,
+                poison: bool = True, kv_dtype: str = "bf16") -> Workload:
+    """Sparse top-k decode: B=64, H=128, q_len=1, page_size 64,
+    seq_lens ~ U[3072, 12288], k = 2048 listed positions per token drawn by
+    ``with_topk`` (every list full: L > k).  The pages fix no sparse workload;
+    the shape is the headline decode shape with the selection on top."""
+    rng = np.random.default_rng(seed)
+    L = _uniform_lens(rng, lo, hi, batch)
+    w = build(f"sparse_b{batch}_h128_q{q_len}_ps64", seed, num_heads=128, page_size=64,
+              seq_lens=L, q_lens=[q_len] * batch, packed=False, causal=True,
+              return_lse=return_lse, poison=poison, kv_dtype=kv_dtype, rng=rng)
+    return with_topk(w, k, seed + 1)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "deepseek_v3": deepseek_v3,
@@ -305,6 +356,7 @@ WORKLOADS = {
     "ragged": ragged,
     "fp8_long": fp8_long,
     "prefill": prefill,
+    "sparse_topk": sparse_topk,
 }
 
 

@@ -24,7 +24,12 @@ seeing rows 0 .. seq_len - q + i (causal) or 0 .. seq_len - 1 (dense).  Under
 decode-context parallelism (``cp_world`` > 1; the vLLM ``FlashInferMLAImpl``
 page passes cp_world, cp_rank and the global KV lengths to the kernel) a
 rank's local row j is global row j * cp_world + cp_rank and the causal bound
-is taken on that global position against the global length.
+is taken on that global position against the global length.  Under sparse
+top-k selection (``sparse_idx``; the trtllm-gen MLA launcher in the FlashInfer
+issue "Support cum_seq_lens_q in trtllm_batch_decode_with_kv_cache_mla" takes a
+``sparse_mla_top_k`` argument and the pages say no more) query token t
+attends exactly the logical KV positions listed in row t of ``sparse_idx``
+that fall in [0, seq_len), once per listing; the list replaces the mask.
 
 Parity status of each function is pinned by ``tests/test_oracle_pins.py``.
 """
@@ -77,6 +82,9 @@ def _load():
         lib.oracle_mla_decode_dcp.restype = ctypes.c_int
         lib.oracle_mla_decode_dcp.argtypes = lib.oracle_mla_decode_q.argtypes + [
             ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        lib.oracle_mla_decode_full.restype = ctypes.c_int
+        lib.oracle_mla_decode_full.argtypes = lib.oracle_mla_decode_dcp.argtypes + [
+            ctypes.c_int, ctypes.c_void_p]
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
@@ -105,7 +113,8 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
                causal: bool, bmm1_scale: float, bmm2_scale: float,
                sel: Optional[np.ndarray] = None, n_threads: Optional[int] = None,
                q_dtype: str = "bf16", cp_world: int = 1, cp_rank: int = 0,
-               seq_lens_global: Optional[np.ndarray] = None):
+               seq_lens_global: Optional[np.ndarray] = None,
+               sparse_idx: Optional[np.ndarray] = None):
     """fp64 O and LSE.
 
     query:   uint16 bf16 bits (q_dtype "bf16") or uint8 e4m3 codes ("e4m3")
@@ -117,6 +126,10 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
              rank holds the global rows g with g mod cp_world == cp_rank as
              its local rows g div cp_world; the causal bound applies to the
              global positions, with global lengths seq_lens_global [B].
+    sparse_idx: optional int32 [tokens, k] logical KV positions per query
+             token (sparse top-k): the token attends the listed positions in
+             [0, seq_len) (an entry outside, e.g. -1, is unused; a repeated
+             one counts each time); ``causal`` is then not consulted.
     Returns (out, lse): [tokens, H, 512] and [tokens, H], or [n, 512] and [n].
     Rows that see no key get O = 0 and lse = -inf (the empty sum).
     """
@@ -161,13 +174,19 @@ def mla_decode(query: np.ndarray, q_start: np.ndarray, kv_cache: np.ndarray,
     if cp_world > 1 and seq_lens_global is not None:
         slg = np.ascontiguousarray(seq_lens_global, dtype=np.int32)
         assert slg.shape == sl.shape
-    rc = lib.oracle_mla_decode_dcp(
+    sk, sp = 0, None
+    if sparse_idx is not None:
+        sp = np.ascontiguousarray(sparse_idx, dtype=np.int32)
+        assert sp.ndim == 2 and sp.shape[0] == tokens and sp.shape[1] >= 1
+        sk = int(sp.shape[1])
+    rc = lib.oracle_mla_decode_full(
         B, H, kd, qd, q.ctypes.data, qs.ctypes.data, kv.ctypes.data, int(kv.shape[0]),
         int(kv.shape[1]), bt.ctypes.data, int(bt.shape[1]), sl.ctypes.data, int(bool(causal)),
         float(bmm1_scale), float(bmm2_scale), n,
         sel_arr.ctypes.data if sel_arr is not None else None,
         out.ctypes.data, lse.ctypes.data, int(n_threads or default_threads()),
-        int(cp_world), int(cp_rank), slg.ctypes.data if slg is not None else None)
+        int(cp_world), int(cp_rank), slg.ctypes.data if slg is not None else None,
+        sk, sp.ctypes.data if sp is not None else None)
     if rc != 0:
         raise RuntimeError(f"oracle_mla_decode failed with status {rc}")
     return out, lse
@@ -181,4 +200,5 @@ def run(w, sel: Optional[np.ndarray] = None, n_threads: Optional[int] = None,
                       bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, sel=sel,
                       n_threads=n_threads, q_dtype=getattr(w, "q_dtype", "bf16"),
                       cp_world=getattr(w, "cp_world", 1), cp_rank=getattr(w, "cp_rank", 0),
-                      seq_lens_global=getattr(w, "seq_lens_global", None))
+                      seq_lens_global=getattr(w, "seq_lens_global", None),
+                      sparse_idx=getattr(w, "sparse_idx", None))

@@ -12,7 +12,10 @@ L - q + i; written here as the predicate ``j - (L - q) <= i`` (causal) or
 ``FlashInferMLAImpl`` page passes cp_world, cp_rank and the global KV lengths
 to the kernel) local row j of rank r holds global row j * W + r, and the
 causal predicate is applied to that global position against the global
-length: ``(j * W + r) - (Lg - q) <= i``.
+length: ``(j * W + r) - (Lg - q) <= i``.  Under sparse top-k selection the
+token's list of logical positions is walked as given: an entry e is used iff
+``0 <= e < L``, and each use contributes one term (a repeated entry counts
+once per listing).
 """
 from __future__ import annotations
 
@@ -38,7 +41,7 @@ def e4m3_value(bits: int) -> float:
 
 def mla_decode(query, q_start, kv_cache, block_tables, seq_lens, *, kv_dtype, causal,
                bmm1_scale, bmm2_scale, q_dtype="bf16", cp_world=1, cp_rank=0,
-               seq_lens_global=None):
+               seq_lens_global=None, sparse_idx=None):
     """Return (out[tokens][H][512], lse[tokens][H]) as nested Python lists.
     A row with no visible key gets zeros and -inf."""
     decode = bf16_value if kv_dtype == "bf16" else e4m3_value
@@ -64,7 +67,10 @@ def mla_decode(query, q_start, kv_cache, block_tables, seq_lens, *, kv_dtype, ca
             def seen(j, i):
                 return j - (L - q) <= i
         for i in range(q):
-            visible = [j for j in range(L) if (seen(j, i) if causal else True)]
+            if sparse_idx is not None:
+                visible = [int(e) for e in sparse_idx[t0 + i] if 0 <= int(e) < L]
+            else:
+                visible = [j for j in range(L) if (seen(j, i) if causal else True)]
             if not visible:
                 for h in range(H):
                     lse[t0 + i][h] = float("-inf")

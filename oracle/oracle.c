@@ -18,6 +18,12 @@
  *     (length Lg) with g mod W == r as its local rows j = g div W, and the
  *     causal bound applies to global positions: local row j is visible
  *     iff j * W + r <= Lg - q + i
+ *     sparse top-k (the sparse_mla_top_k argument of the trtllm-gen MLA
+ *     launcher in the FlashInfer issue "Support cum_seq_lens_q in
+ *     trtllm_batch_decode_with_kv_cache_mla"; the pages name the argument
+ *     only): query token t carries k logical KV positions of its request;
+ *     the visible rows are exactly the listed ones that fall in [0, L), as
+ *     listed (a repeated position counts each time it is listed)
  *     s_j   = bmm1_scale * sum_{d < 576} Q[b,i,h,d] * K_b[j][d]
  *     lse   = m + ln(sum_j exp(s_j - m)),  m = max_j s_j      (natural log,
  *             as the vLLM FlashInferMLAImpl page states for its LSE)
@@ -72,6 +78,8 @@ typedef struct {
   int batch, num_heads, kv_dtype, q_dtype, page_size, max_pages_per_req, causal;
   int cp_world, cp_rank;               /* decode-context parallelism (cp_world 1: off) */
   const int32_t *seq_lens_global;      /* [B] global KV lengths when cp_world > 1 */
+  int sparse_k;                        /* > 0: sparse top-k positions per token */
+  const int32_t *sparse_idx;           /* [tokens, sparse_k] logical KV positions */
   const void *query;         /* [tokens, H, 576] bf16 bits or e4m3 codes (q_dtype) */
   const int64_t *q_start;    /* [B + 1] token offsets */
   const void *kv_cache;      /* [num_pages, ps, 576] */
@@ -105,6 +113,49 @@ static int owner(const job_t *J, int64_t t) {
   return lo;
 }
 
+/* One (token, head) pair under sparse top-k: the listed positions of token t
+ * that fall in [0, L), in list order; qv holds the decoded query row. */
+static int sparse_unit(job_t *J, int64_t u, int64_t t, int b, int64_t L, double *s,
+                       const double *qv) {
+  const int32_t *list = J->sparse_idx + t * (int64_t)J->sparse_k;
+  double *o = J->out + u * V_DIM;
+  double m = -INFINITY;
+  int64_t n = 0;
+  for (int e = 0; e < J->sparse_k; ++e) {
+    const int64_t j = list[e];
+    if (j < 0 || j >= L) continue;
+    int64_t page = J->block_tables[(int64_t)b * J->max_pages_per_req + j / J->page_size];
+    if (page < 0 || page >= J->num_pages) return 1;
+    int row = (int)(j % J->page_size);
+    double acc = 0.0;
+    for (int d = 0; d < QK_DIM; ++d) acc += qv[d] * kv_elem(J, page, row, d);
+    s[n] = J->bmm1_scale * acc;
+    if (s[n] > m) m = s[n];
+    ++n;
+  }
+  for (int d = 0; d < V_DIM; ++d) o[d] = 0.0;
+  if (n == 0) {
+    J->lse[u] = -INFINITY;
+    return 0;
+  }
+  double sum = 0.0;
+  for (int64_t e = 0; e < n; ++e) sum += exp(s[e] - m);
+  const double lse = m + log(sum);
+  J->lse[u] = lse;
+  n = 0;
+  for (int e = 0; e < J->sparse_k; ++e) {
+    const int64_t j = list[e];
+    if (j < 0 || j >= L) continue;
+    int64_t page = J->block_tables[(int64_t)b * J->max_pages_per_req + j / J->page_size];
+    int row = (int)(j % J->page_size);
+    const double pj = exp(s[n] - lse);
+    for (int d = 0; d < V_DIM; ++d) o[d] += pj * kv_elem(J, page, row, d);
+    ++n;
+  }
+  for (int d = 0; d < V_DIM; ++d) o[d] *= J->bmm2_scale;
+  return 0;
+}
+
 static int one_unit(job_t *J, int64_t u, double *s, double *qv) {
   int64_t t = J->sel ? J->sel[2 * u] : u / J->num_heads;
   int h = J->sel ? (int)J->sel[2 * u + 1] : (int)(u % J->num_heads);
@@ -134,6 +185,7 @@ static int one_unit(job_t *J, int64_t u, double *s, double *qv) {
                                          : e4m3_to_double(((const uint8_t *)J->query)[off]);
   }
 
+  if (J->sparse_k > 0) return sparse_unit(J, u, t, b, L, s, qv);
   if (n <= 0) {  /* nothing visible: empty sum (a contract violation) */
     for (int d = 0; d < V_DIM; ++d) o[d] = 0.0;
     J->lse[u] = -INFINITY;
@@ -167,7 +219,7 @@ static int one_unit(job_t *J, int64_t u, double *s, double *qv) {
 
 static void *worker(void *arg) {
   job_t *J = (job_t *)arg;
-  int64_t max_L = 1;
+  int64_t max_L = J->sparse_k > 1 ? J->sparse_k : 1;
   for (int b = 0; b < J->batch; ++b)
     if (J->seq_lens[b] > max_L) max_L = J->seq_lens[b];
   double *s = (double *)malloc(sizeof(double) * (size_t)max_L);
@@ -201,23 +253,26 @@ static void *worker(void *arg) {
  * for a visible row was out of range, 2 on allocation failure, 3 on a bad
  * rank description.
  */
-int oracle_mla_decode_dcp(int batch, int num_heads, int kv_dtype, int q_dtype,
-                          const void *query, const int64_t *q_start,
-                          const void *kv_cache, int64_t num_pages, int page_size,
-                          const int32_t *block_tables, int max_pages_per_req,
-                          const int32_t *seq_lens, int causal,
-                          double bmm1_scale, double bmm2_scale,
-                          int64_t n_sel, const int64_t *sel,
-                          double *out, double *lse, int n_threads,
-                          int cp_world, int cp_rank, const int32_t *seq_lens_global) {
+int oracle_mla_decode_full(int batch, int num_heads, int kv_dtype, int q_dtype,
+                           const void *query, const int64_t *q_start,
+                           const void *kv_cache, int64_t num_pages, int page_size,
+                           const int32_t *block_tables, int max_pages_per_req,
+                           const int32_t *seq_lens, int causal,
+                           double bmm1_scale, double bmm2_scale,
+                           int64_t n_sel, const int64_t *sel,
+                           double *out, double *lse, int n_threads,
+                           int cp_world, int cp_rank, const int32_t *seq_lens_global,
+                           int sparse_k, const int32_t *sparse_idx) {
   job_t J;
   if (cp_world < 1 || cp_rank < 0 || cp_rank >= cp_world ||
-      (cp_world > 1 && causal && !seq_lens_global))
+      (cp_world > 1 && causal && !seq_lens_global) || sparse_k < 0 ||
+      (sparse_k > 0 && (!sparse_idx || cp_world > 1)))
     return 3;
   memset(&J, 0, sizeof J);
   J.batch = batch; J.num_heads = num_heads; J.kv_dtype = kv_dtype; J.q_dtype = q_dtype;
   J.page_size = page_size; J.max_pages_per_req = max_pages_per_req; J.causal = causal;
   J.cp_world = cp_world; J.cp_rank = cp_rank; J.seq_lens_global = seq_lens_global;
+  J.sparse_k = sparse_k; J.sparse_idx = sparse_idx;
   J.query = query; J.q_start = q_start; J.kv_cache = kv_cache; J.num_pages = num_pages;
   J.block_tables = block_tables; J.seq_lens = seq_lens;
   J.bmm1_scale = bmm1_scale; J.bmm2_scale = bmm2_scale;
@@ -235,6 +290,22 @@ int oracle_mla_decode_dcp(int batch, int num_heads, int kv_dtype, int q_dtype,
   for (int k = 0; k < started; ++k) pthread_join(th[k], NULL);
   pthread_mutex_destroy(&J.lock);
   return J.status;
+}
+
+/* Decode-context parallelism, no sparse selection. */
+int oracle_mla_decode_dcp(int batch, int num_heads, int kv_dtype, int q_dtype,
+                          const void *query, const int64_t *q_start,
+                          const void *kv_cache, int64_t num_pages, int page_size,
+                          const int32_t *block_tables, int max_pages_per_req,
+                          const int32_t *seq_lens, int causal,
+                          double bmm1_scale, double bmm2_scale,
+                          int64_t n_sel, const int64_t *sel,
+                          double *out, double *lse, int n_threads,
+                          int cp_world, int cp_rank, const int32_t *seq_lens_global) {
+  return oracle_mla_decode_full(batch, num_heads, kv_dtype, q_dtype, query, q_start, kv_cache,
+                                num_pages, page_size, block_tables, max_pages_per_req, seq_lens,
+                                causal, bmm1_scale, bmm2_scale, n_sel, sel, out, lse, n_threads,
+                                cp_world, cp_rank, seq_lens_global, 0, NULL);
 }
 
 /* The whole sequence on one rank. */

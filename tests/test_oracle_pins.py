@@ -417,3 +417,135 @@ def test_dcp_c_oracle_matches_python_brute_force(world, rank, causal):
     fin = np.isfinite(bl)
     np.testing.assert_allclose(out, np.array(bo), rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(lse[fin], bl[fin], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- sparse top-k selection
+
+def _with_lists(w, lists):
+    """w with the given per-token position lists, -1 padded to a common k."""
+    k = max(len(x) for x in lists)
+    idx = np.full((len(lists), k), -1, dtype=np.int32)
+    for t, x in enumerate(lists):
+        idx[t, :len(x)] = x
+    return dataclasses.replace(w, sparse_idx=idx)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_sparse_list_of_every_position_is_the_dense_pass(causal):
+    """A token whose list holds every row 0 .. L-1 once, in any order, sees
+    exactly the dense set; the plan's causal flag is not consulted."""
+    w = small(81, H=2, seq_lens=(9, 14, 5), q_lens=(2, 2, 2), causal=causal)
+    rng = np.random.default_rng(3)
+    qs = w.q_start()
+    lists = [list(rng.permutation(int(w.seq_lens[b])))
+             for b in range(w.batch) for _ in range(int(qs[b + 1] - qs[b]))]
+    o_s, l_s = oracle.run(_with_lists(w, lists))
+    o_d, l_d = oracle.run(w, causal=False)
+    np.testing.assert_allclose(o_s, o_d, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l_s, l_d, rtol=1e-13, atol=1e-13)
+
+
+def test_sparse_list_of_the_causal_prefix_is_the_causal_pass():
+    """Token i's list = its causal prefix 0 .. L-q+i (padded with -1 and with
+    positions at or past L, which are unused) gives the causal result."""
+    w = small(82, H=3, seq_lens=(9, 14, 6), q_lens=(3, 1, 2), packed=True)
+    qs = w.q_start()
+    lists = []
+    for b in range(w.batch):
+        L, q = int(w.seq_lens[b]), int(qs[b + 1] - qs[b])
+        for i in range(q):
+            lists.append(list(range(L - q + i, -1, -1)) + [L, -1, L + 100, -7])
+    o_s, l_s = oracle.run(_with_lists(w, lists))
+    o_c, l_c = oracle.run(w, causal=True)
+    np.testing.assert_allclose(o_s, o_c, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l_s, l_c, rtol=1e-13, atol=1e-13)
+
+
+def test_sparse_single_position_returns_that_row():
+    """One listed row j: O = bmm2 * V_j and lse = bmm1 * q.k_j (softmax of one)."""
+    w = small(83, H=2, seq_lens=(9, 14), q_lens=(1, 1), bmm1=0.3, bmm2=1.5)
+    picks = [6, 11]
+    out, lse = oracle.run(_with_lists(w, [[-1, picks[0], 9], [picks[1], -1, 14]]))
+    Q = as_f64(w.query_rows())
+    for b, j in enumerate(picks):
+        kj = gather(w, b)[j]
+        for h in range(w.num_heads):
+            assert lse[b, h] == pytest.approx(w.bmm1_scale * np.dot(Q[b, h], kj), rel=1e-13,
+                                              abs=1e-13)
+            np.testing.assert_allclose(out[b, h], w.bmm2_scale * kj[:512], rtol=1e-14, atol=0)
+
+
+def test_sparse_repeated_position_counts_each_listing():
+    """[j, j] weighs row j twice: O is unchanged and lse grows by exactly ln 2;
+    with Q = 0, [a, a, b] gives O = (2 V_a + V_b) / 3 and lse = ln 3."""
+    w = small(84, H=2, seq_lens=(12,), q_lens=(1,), bmm2=1.0)
+    o1, l1 = oracle.run(_with_lists(w, [[5]]))
+    o2, l2 = oracle.run(_with_lists(w, [[5, 5]]))
+    np.testing.assert_allclose(o2, o1, rtol=1e-14, atol=0)
+    np.testing.assert_allclose(l2, l1 + math.log(2.0), rtol=0, atol=1e-13)
+    wz = dataclasses.replace(w, query=np.zeros_like(w.query))
+    o3, l3 = oracle.run(_with_lists(wz, [[3, 3, 8]]))
+    rows = gather(w, 0)
+    np.testing.assert_allclose(l3, math.log(3.0), atol=1e-14)
+    np.testing.assert_allclose(o3[0, 0], (2 * rows[3, :512] + rows[8, :512]) / 3, rtol=1e-13,
+                               atol=1e-16)
+
+
+def test_sparse_list_with_no_usable_entry_is_the_empty_sum():
+    w = small(85, H=2, seq_lens=(4, 9), q_lens=(1, 1))
+    out, lse = oracle.run(_with_lists(w, [[-1, 4, 100], [3, -1, -1]]))
+    assert np.all(np.isneginf(lse[0])) and np.all(out[0] == 0)
+    assert np.all(np.isfinite(lse[1]))
+
+
+def test_sparse_order_of_the_list_does_not_matter():
+    w = mi.with_topk(small(86, H=2, seq_lens=(40, 23), q_lens=(2, 2)), 16, seed=5)
+    rng = np.random.default_rng(8)
+    shuffled = np.stack([rng.permutation(r) for r in w.sparse_idx])
+    o1, l1 = oracle.run(w)
+    o2, l2 = oracle.run(dataclasses.replace(w, sparse_idx=shuffled))
+    np.testing.assert_allclose(o2, o1, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(l2, l1, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("case", [
+    dict(seq_lens=(40, 23), q_lens=(2, 2), k=16),
+    dict(seq_lens=(9, 30, 5), q_lens=(3, 1, 2), packed=True, k=8, kv_dtype="e4m3", bmm1=0.5),
+    dict(seq_lens=(70,), q_lens=(1,), k=32, q_dtype="e4m3", bmm1=2.0),
+])
+def test_sparse_c_oracle_matches_python_brute_force(case):
+    k = case.pop("k")
+    w = mi.with_topk(small(87, H=2, **case), k, seed=9)
+    # add a repeated entry, an out-of-range one and a -1 to every full list
+    idx = w.sparse_idx.copy()
+    idx[:, -3] = idx[:, 0]
+    idx[:, -2] = 10 ** 6
+    idx[:, -1] = -1
+    w = dataclasses.replace(w, sparse_idx=idx)
+    out, lse = oracle.run(w)
+    bo, bl = brute.mla_decode(w.query_rows(), w.q_start(), w.kv_cache, w.block_tables,
+                              w.seq_lens, kv_dtype=w.kv_dtype, causal=w.causal,
+                              bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
+                              q_dtype=w.q_dtype, sparse_idx=w.sparse_idx)
+    np.testing.assert_allclose(out, np.array(bo), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, np.array(bl), rtol=1e-12, atol=1e-12)
+
+
+def test_sparse_lists_stay_inside_each_tokens_causal_prefix():
+    """The input generator's lists: distinct, inside [0, L - q + i], -1 padded."""
+    w = mi.with_topk(small(88, H=2, seq_lens=(40, 7, 100), q_lens=(3, 3, 3)), 24, seed=2)
+    qs = w.q_start()
+    for b in range(w.batch):
+        L, q = int(w.seq_lens[b]), int(qs[b + 1] - qs[b])
+        for i in range(q):
+            row = w.sparse_idx[int(qs[b]) + i]
+            used = row[row >= 0]
+            assert len(used) == min(24, L - q + i + 1) and np.all(row[len(used):] == -1)
+            assert len(set(used.tolist())) == len(used) and used.max() <= L - q + i
+
+
+def test_sparse_selection_is_refused_with_decode_context_parallelism():
+    w = mi.with_topk(small(89, H=2, seq_lens=(9, 5), q_lens=(1, 1)), 4)
+    with pytest.raises(RuntimeError):
+        oracle.run(dataclasses.replace(w, cp_world=2, cp_rank=0,
+                                       seq_lens_global=w.seq_lens.copy()))
