@@ -45,23 +45,39 @@ def work_model(w) -> dict:
     """Algorithmic FLOPs and bytes of one decode call on workload ``w``.
 
     FLOPs: 2 * H * (576 + 512) per visible (query row, KV row) pair; visible
-    pairs n_vis = sum_b sum_{i<q} (L - q + i + 1) (causal) or q * L (dense).
-    Bytes: KV rows read once + Q + O (+ LSE) + page-table/length metadata.
+    pairs n_vis = sum_b sum_{i<q} (L - q + i + 1) (causal) or q * L (dense),
+    or, under sparse top-k, the usable list entries of every token.
+    Bytes: KV rows read once + Q + O (+ LSE) + page-table/length metadata;
+    under sparse top-k the distinct listed rows of each request, the lists
+    and the page-table entries of the pages they touch.
     """
     q = w.q_lens.astype(np.int64)
     L = w.seq_lens.astype(np.int64)
-    if w.causal:
-        n_vis = int(np.sum(q * (L - q) + q * (q + 1) // 2))
-    else:
-        n_vis = int(np.sum(q * L))
     H = w.num_heads
     tokens = int(q.sum())
     e = 1 if w.kv_dtype == "e4m3" else 2
-    kv_bytes = int(L.sum()) * 576 * e
-    n_pages = (L + w.page_size - 1) // w.page_size
+    if w.sparse_idx is not None:
+        qs = w.q_start()
+        n_vis = rows = pages = 0
+        for b in range(w.batch):
+            lists = w.sparse_idx[int(qs[b]):int(qs[b + 1])]
+            usable = lists[(lists >= 0) & (lists < L[b])]
+            n_vis += int(usable.size)
+            uniq = np.unique(usable)
+            rows += int(uniq.size)
+            pages += int(np.unique(uniq // w.page_size).size)
+        kv_bytes = rows * 576 * e
+        meta = pages * 4 + int(w.sparse_idx.size) * 4
+    else:
+        if w.causal:
+            n_vis = int(np.sum(q * (L - q) + q * (q + 1) // 2))
+        else:
+            n_vis = int(np.sum(q * L))
+        kv_bytes = int(L.sum()) * 576 * e
+        meta = int(((L + w.page_size - 1) // w.page_size).sum()) * 4
     total = (kv_bytes + tokens * H * 576 * 2 + tokens * H * 512 * 2
              + (tokens * H * 4 if w.return_lse else 0)
-             + int(n_pages.sum()) * 4 + 4 * w.batch + (4 * (w.batch + 1) if w.packed else 0))
+             + meta + 4 * w.batch + (4 * (w.batch + 1) if w.packed else 0))
     return {"flops": 2 * H * (576 + 512) * n_vis, "bytes": total, "kv_bytes": kv_bytes,
             "n_vis": n_vis, "tokens": tokens}
 
@@ -221,7 +237,11 @@ def time_oracle(w, target_s: float, seed: int = 0, max_pairs: int = 1 << 20):
         i = t - qs[b]
         L = w.seq_lens[b].astype(np.int64)
         q = w.q_lens[b].astype(np.int64)
-        n = (L - q + i + 1) if w.causal else L
+        if w.sparse_idx is not None:
+            lists = w.sparse_idx[t]
+            n = np.sum((lists >= 0) & (lists < L[:, None]), axis=1)
+        else:
+            n = (L - q + i + 1) if w.causal else L
         return int(np.sum(2 * (576 + 512) * n))
 
     cores = oracle.default_threads()
@@ -254,6 +274,11 @@ def to_device(w, dev):
     return q, kv, bt, sl, qo
 
 
+def sparse_lists(w, dev):
+    import torch
+    return torch.from_numpy(w.sparse_idx).to(dev) if w.sparse_idx is not None else None
+
+
 def gpu_case(w, dev, steps, warmup, with_e2e):
     """Time ``steps`` decode calls; returns a dict of measurements."""
     import torch
@@ -265,7 +290,8 @@ def gpu_case(w, dev, steps, warmup, with_e2e):
                     max_seq_len=w.max_seq_len, page_size=w.page_size,
                     max_pages_per_req=w.block_tables.shape[1], num_pages=w.num_pages,
                     packed=w.packed, max_total_q=tokens, kv_dtype=w.kv_dtype, causal=w.causal,
-                    return_lse=w.return_lse, device=dev.index or 0)
+                    return_lse=w.return_lse, device=dev.index or 0, sparse_top_k=w.sparse_k)
+    sp = sparse_lists(w, dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((tokens, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((tokens, w.num_heads), dtype=torch.float32, device=dev) if w.return_lse else None
@@ -274,7 +300,8 @@ def gpu_case(w, dev, steps, warmup, with_e2e):
 
     def step(prof=None):
         mla.mla_decode_run_profiled(plan.handle, q, kv, bt, sl, qo, total_q, w.bmm1_scale,
-                                    w.bmm2_scale, out, lse, ws, None, stream, prof)
+                                    w.bmm2_scale, out, lse, ws, None, stream, prof,
+                                    sparse_indices=sp)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -377,7 +404,7 @@ def gpu_case(w, dev, steps, warmup, with_e2e):
         res["h2d_bytes"] = h2d
         res["d2h_bytes"] = d2h
     plan.close()
-    del q, kv, bt, sl, qo, ws, out, lse
+    del q, kv, bt, sl, qo, ws, out, lse, sp
     torch.cuda.empty_cache()
     return res
 
@@ -410,13 +437,15 @@ def run_gpu(args):
 
     w = make_workload(args.workload)
     wm = work_model(w)
+    # the host-buffer entry point has no sparse top-k form
+    with_e2e = w.sparse_idx is None
     with ClockSampler(local) as clk:
-        r = gpu_case(w, dev, args.steps, args.warmup, with_e2e=True)
+        r = gpu_case(w, dev, args.steps, args.warmup, with_e2e=with_e2e)
     step_s = reduce_max(r["ms_per_step"] / 1e3, dev)
     kern_s = reduce_max(r["kernel_ms_median"] / 1e3, dev)
     kern_mean_s = reduce_max(r["kernel_ms"] / 1e3, dev)
     call_med_s = reduce_max(r["call_ms_median"] / 1e3, dev)
-    e2e_s = reduce_max(r["e2e_ms"] / 1e3, dev)
+    e2e_s = reduce_max(r["e2e_ms"] / 1e3, dev) if with_e2e else None
     ev_s = reduce_max(r["ms_per_step_with_events"] / 1e3, dev)
     n = ws_
     value = n * wm["flops"] / step_s / 1e12
@@ -486,7 +515,7 @@ def run_gpu(args):
             "roofline": rf,
             "e2e": {"value": n * wm["flops"] / e2e_s / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d_bytes"], "d2h_bytes_per_step": r["d2h_bytes"],
-                    "us_per_call": e2e_s * 1e6},
+                    "us_per_call": e2e_s * 1e6} if with_e2e else None,
             "gpu_launches": r["launches_per_step"] * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
@@ -511,13 +540,15 @@ def run_profile_target(args):
                     max_seq_len=w.max_seq_len, page_size=w.page_size,
                     max_pages_per_req=w.block_tables.shape[1], num_pages=w.num_pages,
                     packed=w.packed, max_total_q=tokens, kv_dtype=w.kv_dtype, causal=w.causal,
-                    return_lse=w.return_lse, device=0)
+                    return_lse=w.return_lse, device=0, sparse_top_k=w.sparse_k)
+    sp = sparse_lists(w, dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((tokens, w.num_heads, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((tokens, w.num_heads), dtype=torch.float32, device=dev) if w.return_lse else None
     for _ in range(args.warmup + args.steps):
         plan.run(q, kv, bt, sl, out, qo_indptr=qo, total_q=tokens if w.packed else 0, lse=lse,
-                 workspace=ws, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale)
+                 workspace=ws, bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale,
+                 sparse_indices=sp)
     torch.cuda.synchronize()
     status = int(ws[:4].view(torch.int32).item())
     print(json.dumps({"profile_target": w.name, "calls": args.warmup + args.steps,

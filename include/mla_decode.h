@@ -85,6 +85,9 @@ typedef struct mla_decode_params {
   int32_t cp_world;          /* decode-context parallelism: ranks the KV sequence is
                                 sharded over (0 or 1: off; > 1: run with mla_decode_run_dcp) */
   int32_t cp_rank;           /* this rank, 0 <= cp_rank < cp_world (0 when off) */
+  int32_t sparse_top_k;      /* sparse top-k selection: entries k per query token of the
+                                position list (0: off; > 0: run with mla_decode_run_sparse;
+                                not with cp_world > 1) */
 } mla_decode_params;
 
 typedef struct mla_plan_s mla_plan_t; /* opaque; host memory only */
@@ -130,8 +133,9 @@ int mla_decode_plan(const mla_decode_params *params, mla_plan_t **plan,
  * device; the plan's launch shapes belong to params.device).
  *
  * Errors (synchronous, nothing enqueued): MLA_ERR_INVALID_ARG (also: another
- * device current, or a causal decode-context-parallel plan, which needs
- * mla_decode_run_dcp), MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_ALIGNMENT;
+ * device current, a causal decode-context-parallel plan, which needs
+ * mla_decode_run_dcp, or a sparse top-k plan, which needs
+ * mla_decode_run_sparse), MLA_ERR_WORKSPACE_TOO_SMALL, MLA_ERR_ALIGNMENT;
  * MLA_ERR_CUDA if a launch fails.
  */
 int mla_decode_run(const mla_plan_t *plan, const void *query, const void *kv_cache,
@@ -141,19 +145,20 @@ int mla_decode_run(const mla_plan_t *plan, const void *query, const void *kv_cac
                    size_t workspace_bytes, void *stream);
 
 /*
- * mla_decode_run, plus two CUDA events (cudaEvent_t, may be NULL) recorded on
- * `stream` immediately before and after the decode kernel, so that a caller
- * can time that kernel alone with cudaEventElapsedTime.  Same arguments,
- * errors and capture rules as mla_decode_run; while the stream is being
- * captured into a CUDA graph the two records become event-record nodes
- * (cudaEventRecordExternal), so every replay re-times the kernel.
+ * mla_decode_run (or, with sparse_indices non-NULL on a sparse top-k plan,
+ * mla_decode_run_sparse), plus two CUDA events (cudaEvent_t, may be NULL)
+ * recorded on `stream` immediately before and after the decode kernel, so
+ * that a caller can time that kernel alone with cudaEventElapsedTime.  Same
+ * arguments, errors and capture rules as those entry points; while the stream
+ * is being captured into a CUDA graph the two records become event-record
+ * nodes (cudaEventRecordExternal), so every replay re-times the kernel.
  */
 int mla_decode_run_profiled(const mla_plan_t *plan, const void *query, const void *kv_cache,
                             const int32_t *block_tables, const int32_t *seq_lens,
-                            const int32_t *qo_indptr, int64_t total_q, float bmm1_scale,
-                            float bmm2_scale, void *out, float *lse, void *workspace,
-                            size_t workspace_bytes, void *stream, void *event_before_decode,
-                            void *event_after_decode);
+                            const int32_t *qo_indptr, int64_t total_q,
+                            const int32_t *sparse_indices, float bmm1_scale, float bmm2_scale,
+                            void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream, void *event_before_decode, void *event_after_decode);
 
 /*
  * mla_decode_run with bmm1_scale and bmm2_scale read from device memory by
@@ -296,6 +301,36 @@ int mla_decode_run_dcp(const mla_plan_t *plan, const void *query, const void *kv
                        const int32_t *causal_seqlens_kv_global, float bmm1_scale,
                        float bmm2_scale, void *out, float *lse, void *workspace,
                        size_t workspace_bytes, void *stream);
+
+/*
+ * Sparse top-k decode.  The trtllm-gen MLA launcher in the FlashInfer issue
+ * "Support cum_seq_lens_q in trtllm_batch_decode_with_kv_cache_mla" takes a
+ * sparse_mla_top_k argument; the pages say no more, and this library reads it
+ * as a per-token list of KV positions that replaces the mask:
+ *
+ * sparse_indices  device int32 [tokens, k], k = params.sparse_top_k, row t for
+ *                 query token t in the query's row order (fixed: b * SQ + i;
+ *                 packed: qo_indptr[b] + i).  Entries are LOGICAL positions of
+ *                 the token's own request, resolved through block_tables like
+ *                 any other row.  The token attends exactly the listed
+ *                 positions j with 0 <= j < seq_lens[b]; any other entry
+ *                 (-1 padding, a position past the request's length) is unused
+ *                 and never dereferenced; a position listed twice counts twice.
+ *                 The plan's mask is not consulted.  A token with no usable
+ *                 entry gets out = 0 and lse = -inf.  4-byte aligned.
+ *
+ * Work items are one token each (its H query rows), so a token's KV tiles are
+ * gathered row by row from the list.  plan: made with params.sparse_top_k > 0
+ * (and cp_world <= 1).  All other arguments, errors and capture rules as
+ * mla_decode_run; the other run entry points refuse a sparse plan and this
+ * one refuses any other (MLA_ERR_INVALID_ARG).
+ */
+int mla_decode_run_sparse(const mla_plan_t *plan, const void *query, const void *kv_cache,
+                          const int32_t *block_tables, const int32_t *seq_lens,
+                          const int32_t *qo_indptr, int64_t total_q,
+                          const int32_t *sparse_indices, float bmm1_scale, float bmm2_scale,
+                          void *out, float *lse, void *workspace, size_t workspace_bytes,
+                          void *stream);
 
 /*
  * Merge n partial attention states of the same query rows into one: the

@@ -22,7 +22,8 @@ import torch
 
 __all__ = [
     "MLA_OK", "MlaDecodeError", "MlaDecodeParams", "load_library", "library_path",
-    "mla_decode_plan", "mla_decode_run", "mla_decode_run_profiled", "mla_decode_run_dcp", "mla_decode_destroy", "mla_decode_workspace_size",
+    "mla_decode_plan", "mla_decode_run", "mla_decode_run_profiled", "mla_decode_run_dcp",
+    "mla_decode_run_sparse", "mla_decode_destroy", "mla_decode_workspace_size",
     "mla_decode_status_offset", "mla_decode_status_string", "Plan", "decode",
     "HEAD_DIM_QK", "HEAD_DIM_V",
 ]
@@ -65,6 +66,7 @@ class MlaDecodeParams(ctypes.Structure):
         ("q_dtype", ctypes.c_int32),
         ("cp_world", ctypes.c_int32),
         ("cp_rank", ctypes.c_int32),
+        ("sparse_top_k", ctypes.c_int32),
     ]
 
 
@@ -88,7 +90,8 @@ def load_library():
     lib.mla_decode_run.argtypes = [vp, vp, vp, vp, vp, vp, i64, ctypes.c_float, ctypes.c_float,
                                    vp, vp, vp, sz, vp]
     lib.mla_decode_run.restype = ctypes.c_int
-    lib.mla_decode_run_profiled.argtypes = lib.mla_decode_run.argtypes + [vp, vp]
+    lib.mla_decode_run_profiled.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, ctypes.c_float,
+                                            ctypes.c_float, vp, vp, vp, sz, vp, vp, vp]
     lib.mla_decode_run_profiled.restype = ctypes.c_int
     lib.mla_decode_run_device_scales.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp,
                                                  sz, vp]
@@ -101,6 +104,9 @@ def load_library():
     lib.mla_decode_run_dcp.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, ctypes.c_float,
                                        ctypes.c_float, vp, vp, vp, sz, vp]
     lib.mla_decode_run_dcp.restype = ctypes.c_int
+    lib.mla_decode_run_sparse.argtypes = [vp, vp, vp, vp, vp, vp, i64, vp, ctypes.c_float,
+                                          ctypes.c_float, vp, vp, vp, sz, vp]
+    lib.mla_decode_run_sparse.restype = ctypes.c_int
     lib.mla_merge_states.argtypes = [vp, vp, i32, i64, ctypes.c_float, vp, vp, vp]
     lib.mla_merge_states.restype = ctypes.c_int
     lib.mla_decode_destroy.argtypes = [vp]
@@ -213,6 +219,33 @@ def mla_decode_run_dcp(plan: int, query, kv_cache, block_tables, seq_lens, qo_in
         raise MlaDecodeError(rc, "mla_decode_run_dcp")
 
 
+def mla_decode_run_sparse(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr,
+                          total_q: int, sparse_indices, bmm1_scale: float, bmm2_scale: float,
+                          out, lse, workspace, workspace_bytes: Optional[int] = None,
+                          stream=None) -> None:
+    """Sparse top-k decode (``mla_decode_run_sparse``): ``sparse_indices`` is
+    an int32 CUDA tensor ``[tokens, k]`` of logical KV positions per query
+    token; entries outside ``[0, seq_lens[b])`` are unused."""
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    if isinstance(sparse_indices, torch.Tensor) and (
+            sparse_indices.dtype != torch.int32 or not sparse_indices.is_cuda
+            or not sparse_indices.is_contiguous()):
+        raise TypeError("sparse_indices must be a contiguous int32 CUDA tensor")
+    rc = lib.mla_decode_run_sparse(ctypes.c_void_p(plan), _ptr(query), _ptr(kv_cache),
+                                   _ptr(block_tables), _ptr(seq_lens), _ptr(qo_indptr),
+                                   int(total_q), _ptr(sparse_indices), float(bmm1_scale),
+                                   float(bmm2_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                   int(workspace_bytes), stream)
+    if rc != MLA_OK:
+        raise MlaDecodeError(rc, "mla_decode_run_sparse")
+
+
 def mla_decode_host_staging_bytes(plan: int, total_q: int = 0) -> int:
     """Device staging bytes of ``mla_decode_run_host`` for one step."""
     return int(load_library().mla_decode_host_staging_bytes(ctypes.c_void_p(plan), int(total_q)))
@@ -271,9 +304,10 @@ def mla_decode_run_device_scales(plan: int, query, kv_cache, block_tables, seq_l
 def mla_decode_run_profiled(plan: int, query, kv_cache, block_tables, seq_lens, qo_indptr,
                             total_q: int, bmm1_scale: float, bmm2_scale: float, out, lse,
                             workspace, workspace_bytes: Optional[int] = None, stream=None,
-                            events=None) -> None:
-    """``mla_decode_run`` that also records ``events = (before, after)``
-    (torch.cuda.Event) around the decode kernel on the same stream."""
+                            events=None, sparse_indices=None) -> None:
+    """``mla_decode_run`` (``mla_decode_run_sparse`` with ``sparse_indices``)
+    that also records ``events = (before, after)`` (torch.cuda.Event) around
+    the decode kernel on the same stream."""
     lib = load_library()
     if workspace_bytes is None:
         workspace_bytes = _nbytes(workspace)
@@ -289,9 +323,9 @@ def mla_decode_run_profiled(plan: int, query, kv_cache, block_tables, seq_lens, 
         ev0, ev1 = events[0].cuda_event, events[1].cuda_event
     rc = lib.mla_decode_run_profiled(ctypes.c_void_p(plan), _ptr(query), _ptr(kv_cache),
                                      _ptr(block_tables), _ptr(seq_lens), _ptr(qo_indptr),
-                                     int(total_q), float(bmm1_scale), float(bmm2_scale),
-                                     _ptr(out), _ptr(lse), _ptr(workspace), int(workspace_bytes),
-                                     stream.cuda_stream, ev0, ev1)
+                                     int(total_q), _ptr(sparse_indices), float(bmm1_scale),
+                                     float(bmm2_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                     int(workspace_bytes), stream.cuda_stream, ev0, ev1)
     if rc != MLA_OK:
         raise MlaDecodeError(rc, "mla_decode_run_profiled")
 
@@ -303,7 +337,7 @@ class Plan:
                  page_size: int, max_pages_per_req: int, num_pages: int, packed: bool,
                  max_total_q: int = 0, kv_dtype: str = "bf16", causal: bool = True,
                  return_lse: bool = False, device: int = 0, q_dtype: str = "bf16",
-                 cp_world: int = 1, cp_rank: int = 0):
+                 cp_world: int = 1, cp_rank: int = 0, sparse_top_k: int = 0):
         self.params = MlaDecodeParams(
             batch=batch, num_heads=num_heads, max_seq_len_q=max_seq_len_q,
             max_seq_len=max_seq_len, page_size=page_size, max_pages_per_req=max_pages_per_req,
@@ -312,17 +346,24 @@ class Plan:
             mask=MASK_CAUSAL if causal else MASK_DENSE, return_lse=int(bool(return_lse)),
             device=device,
             q_dtype=Q_FP8_E4M3 if q_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else Q_BF16,
-            cp_world=cp_world, cp_rank=cp_rank)
+            cp_world=cp_world, cp_rank=cp_rank, sparse_top_k=sparse_top_k)
         self.cp_world = cp_world
+        self.sparse_top_k = sparse_top_k
         self.handle, self.workspace_bytes = mla_decode_plan(self.params)
 
     def run(self, query, kv_cache, block_tables, seq_lens, out, *, qo_indptr=None, total_q=0,
             lse=None, workspace=None, bmm1_scale=1.0, bmm2_scale=1.0, stream=None,
-            seq_lens_global=None):
+            seq_lens_global=None, sparse_indices=None):
         """Scales are Python floats, or one-element fp32 CUDA tensors (then both
         must be, and the kernels read them when they run).  A plan with
         ``cp_world`` > 1 runs one DCP rank's decode (``seq_lens_global``: the
-        global KV lengths, required under causal masking)."""
+        global KV lengths, required under causal masking); a plan with
+        ``sparse_top_k`` > 0 a sparse top-k decode over ``sparse_indices``."""
+        if self.sparse_top_k > 0:
+            mla_decode_run_sparse(self.handle, query, kv_cache, block_tables, seq_lens,
+                                  qo_indptr, total_q, sparse_indices, bmm1_scale, bmm2_scale,
+                                  out, lse, workspace, None, stream)
+            return
         if self.cp_world > 1:
             mla_decode_run_dcp(self.handle, query, kv_cache, block_tables, seq_lens, qo_indptr,
                                total_q, seq_lens_global, bmm1_scale, bmm2_scale, out, lse,
@@ -375,7 +416,8 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
            bmm1_scale=1.0, bmm2_scale=1.0, mask_type: str = "causal",
            return_lse: bool = False, cp_world: int = 1, cp_rank: int = 0,
-           causal_seqlens_kv_global: Optional[torch.Tensor] = None):
+           causal_seqlens_kv_global: Optional[torch.Tensor] = None,
+           sparse_indices: Optional[torch.Tensor] = None):
     """Paged MLA decode.  Returns ``out`` (and ``lse`` when ``return_lse``).
 
     ``query``: bf16 or float8_e4m3fn (quantised with a q_scale the caller folds
@@ -388,6 +430,9 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
     ``cp_world`` / ``cp_rank`` / ``causal_seqlens_kv_global``: one rank of a
     decode-context-parallel decode (the vLLM FlashInferMLAImpl page's DCP
     keyword arguments); ``seq_lens`` are then the rank's local row counts.
+    ``sparse_indices``: int32 ``[tokens, k]`` logical KV positions per query
+    token (sparse top-k, ``sparse_mla_top_k`` = k); the listed positions in
+    ``[0, seq_lens[b])`` replace the mask.
     """
     if query.dtype not in (torch.bfloat16, torch.float8_e4m3fn) or not query.is_cuda:
         raise ValueError("query must be a bf16 or float8_e4m3fn CUDA tensor")
@@ -422,9 +467,11 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
     causal = mask_type == "causal"
     if mask_type not in ("causal", "dense"):
         raise ValueError(mask_type)
+    top_k = int(sparse_indices.shape[-1]) if sparse_indices is not None else 0
     key = (B, H, sq, int(max_seq_len), int(kv_cache.shape[1]), int(block_tables.shape[1]),
            int(kv_cache.shape[0]), packed, total_q if packed else 0, kv_dtype, causal,
-           bool(return_lse), query.device.index or 0, q_dtype, int(cp_world), int(cp_rank))
+           bool(return_lse), query.device.index or 0, q_dtype, int(cp_world), int(cp_rank),
+           top_k)
     plan = _plans.get(key)
     if plan is None:
         plan = Plan(batch=B, num_heads=H, max_seq_len_q=sq, max_seq_len=int(max_seq_len),
@@ -432,7 +479,7 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
                     num_pages=int(kv_cache.shape[0]), packed=packed, max_total_q=total_q,
                     kv_dtype=kv_dtype, causal=causal, return_lse=return_lse,
                     device=query.device.index or 0, q_dtype=q_dtype, cp_world=int(cp_world),
-                    cp_rank=int(cp_rank))
+                    cp_rank=int(cp_rank), sparse_top_k=top_k)
         _plans[key] = plan
     if workspace_buffer.numel() * workspace_buffer.element_size() < plan.workspace_bytes:
         raise ValueError(f"workspace_buffer needs {plan.workspace_bytes} bytes")
@@ -443,7 +490,8 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
     plan.run(query, kv_cache, block_tables, seq_lens, out, qo_indptr=qo_indptr, total_q=total_q,
              lse=lse if return_lse else None, workspace=workspace_buffer,
              bmm1_scale=bmm1_scale, bmm2_scale=bmm2_scale,
-             seq_lens_global=causal_seqlens_kv_global if causal else None)
+             seq_lens_global=causal_seqlens_kv_global if causal else None,
+             sparse_indices=sparse_indices)
     return (out, lse) if return_lse else out
 
 

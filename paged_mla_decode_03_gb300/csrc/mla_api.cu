@@ -114,6 +114,8 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (p.cp_world < 0 || (p.cp_world <= 1 && p.cp_rank != 0) ||
       (p.cp_world > 1 && (p.cp_rank < 0 || p.cp_rank >= p.cp_world)))
     return MLA_ERR_INVALID_ARG;
+  if (p.sparse_top_k < 0 || p.sparse_top_k > (1 << 24) || (p.sparse_top_k > 0 && p.cp_world > 1))
+    return MLA_ERR_INVALID_ARG;
   if (!supported_heads(p.num_heads)) return MLA_ERR_UNSUPPORTED;
   if (p.page_size != 32 && p.page_size != 64) return MLA_ERR_UNSUPPORTED;
   if ((long long)p.max_pages_per_req * p.page_size < p.max_seq_len) return MLA_ERR_INVALID_ARG;
@@ -138,8 +140,10 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (!pl) return MLA_ERR_INVALID_ARG;
   pl->prm = p;
   pl->sm_count = sms;
-  // one work item = 128 query rows on one CTA pair
-  const int rc = make_layout(p, n_pairs, 2 * n_pairs, 128, &pl->lay);
+  // one work item = 128 query rows on one CTA pair; under sparse top-k one
+  // token's H rows (its own position list)
+  const int rc =
+      make_layout(p, n_pairs, 2 * n_pairs, p.sparse_top_k > 0 ? p.num_heads : 128, &pl->lay);
   if (rc != MLA_OK) {
     delete pl;
     return rc;
@@ -196,10 +200,14 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
              int64_t total_q, float bmm1_scale, float bmm2_scale, const float* bmm1_dev,
              const float* bmm2_dev, void* out, float* lse, void* workspace,
              size_t workspace_bytes, void* stream, void* event_before_decode,
-             void* event_after_decode, const int32_t* seq_lens_global = nullptr) {
+             void* event_after_decode, const int32_t* seq_lens_global = nullptr,
+             const int32_t* sparse_idx = nullptr) {
   if (!plan) return MLA_ERR_INVALID_ARG;
   const mla_decode_params& prm = plan->prm;
+  // a sparse plan needs its position lists; no other plan takes them
+  if ((prm.sparse_top_k > 0) != (sparse_idx != nullptr)) return MLA_ERR_INVALID_ARG;
   if (prm.batch == 0) return MLA_OK;
+  if (sparse_idx && !aligned(sparse_idx, 4)) return MLA_ERR_ALIGNMENT;
   // a causal decode-context-parallel plan needs the global lengths; no other
   // plan takes them
   const bool dcp = prm.cp_world > 1;
@@ -242,6 +250,8 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
   p.cp_world = dcp ? prm.cp_world : 1;
   p.cp_rank = dcp ? prm.cp_rank : 0;
   p.seq_lens_global = seq_lens_global;
+  p.sparse_k = prm.sparse_top_k > 0 ? prm.sparse_top_k : 0;
+  p.sparse_idx = sparse_idx;
   p.causal = prm.mask == MLA_MASK_CAUSAL;
   p.return_lse = prm.return_lse != 0;
   p.num_pages = prm.num_pages;
@@ -288,13 +298,13 @@ extern "C" {
 
 int mla_decode_run_profiled(const mla_plan_t* plan, const void* query, const void* kv_cache,
                             const int32_t* block_tables, const int32_t* seq_lens,
-                            const int32_t* qo_indptr, int64_t total_q, float bmm1_scale,
-                            float bmm2_scale, void* out, float* lse, void* workspace,
-                            size_t workspace_bytes, void* stream, void* event_before_decode,
-                            void* event_after_decode) {
+                            const int32_t* qo_indptr, int64_t total_q,
+                            const int32_t* sparse_indices, float bmm1_scale, float bmm2_scale,
+                            void* out, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream, void* event_before_decode, void* event_after_decode) {
   return run_impl(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q, bmm1_scale,
                   bmm2_scale, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream,
-                  event_before_decode, event_after_decode);
+                  event_before_decode, event_after_decode, nullptr, sparse_indices);
 }
 
 int mla_decode_run_device_scales(const mla_plan_t* plan, const void* query, const void* kv_cache,
@@ -313,9 +323,9 @@ int mla_decode_run(const mla_plan_t* plan, const void* query, const void* kv_cac
                    const int32_t* block_tables, const int32_t* seq_lens, const int32_t* qo_indptr,
                    int64_t total_q, float bmm1_scale, float bmm2_scale, void* out, float* lse,
                    void* workspace, size_t workspace_bytes, void* stream) {
-  return mla_decode_run_profiled(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q,
-                                 bmm1_scale, bmm2_scale, out, lse, workspace, workspace_bytes,
-                                 stream, nullptr, nullptr);
+  return run_impl(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q, bmm1_scale,
+                  bmm2_scale, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream,
+                  nullptr, nullptr);
 }
 
 int mla_decode_run_dcp(const mla_plan_t* plan, const void* query, const void* kv_cache,
@@ -328,6 +338,18 @@ int mla_decode_run_dcp(const mla_plan_t* plan, const void* query, const void* kv
   return run_impl(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q, bmm1_scale,
                   bmm2_scale, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream,
                   nullptr, nullptr, causal_seqlens_kv_global);
+}
+
+int mla_decode_run_sparse(const mla_plan_t* plan, const void* query, const void* kv_cache,
+                          const int32_t* block_tables, const int32_t* seq_lens,
+                          const int32_t* qo_indptr, int64_t total_q,
+                          const int32_t* sparse_indices, float bmm1_scale, float bmm2_scale,
+                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (!plan || plan->prm.sparse_top_k <= 0 || !sparse_indices) return MLA_ERR_INVALID_ARG;
+  return run_impl(plan, query, kv_cache, block_tables, seq_lens, qo_indptr, total_q, bmm1_scale,
+                  bmm2_scale, nullptr, nullptr, out, lse, workspace, workspace_bytes, stream,
+                  nullptr, nullptr, nullptr, sparse_indices);
 }
 
 int mla_merge_states(const void* o_parts, const float* lse_parts, int32_t n_parts, int64_t rows,
@@ -367,7 +389,8 @@ int mla_decode_run_host(const mla_plan_t* plan, const void* h_query, const void*
     return MLA_ERR_INVALID_ARG;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return MLA_ERR_CUDA;
-  if (cur != prm.device || (prm.cp_world > 1 && prm.mask == MLA_MASK_CAUSAL))
+  if (cur != prm.device || (prm.cp_world > 1 && prm.mask == MLA_MASK_CAUSAL) ||
+      prm.sparse_top_k > 0)
     return MLA_ERR_INVALID_ARG;
   if (prm.return_lse && !h_lse) return MLA_ERR_INVALID_ARG;
   if (prm.packed) {

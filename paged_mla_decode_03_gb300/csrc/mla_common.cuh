@@ -26,6 +26,7 @@ struct Problem {
   int packed, kv_dtype, causal, return_lse;
   int q_fp8;                     // 1: query is e4m3 (widened to bf16 on load)
   int cp_world, cp_rank;         // decode-context parallelism (cp_world 1: off)
+  int sparse_k;                  // > 0: sparse top-k, k listed KV positions per token
   long long num_pages, total_q;  // total_q: rows of the query tensor (tokens)
   float bmm1_scale, bmm2_scale;
   const float* bmm1_dev;         // non-null: read bmm1 from device memory at run time
@@ -36,6 +37,7 @@ struct Problem {
   const int* seq_lens;           // [B]
   const int* qo_indptr;          // [B + 1] or nullptr
   const int* seq_lens_global;    // [B] global KV lengths (causal, cp_world > 1) or nullptr
+  const int* sparse_idx;         // [tokens, sparse_k] logical KV positions, or nullptr
   void* out;                     // bf16 [tokens, H, 512]
   float* lse;                    // fp32 [tokens, H] or nullptr
 };
@@ -55,13 +57,14 @@ __device__ __forceinline__ float run_bmm2(const Problem& p) {
 
 // One unit of work of the decode kernel: query rows [R g, R g + R) of request
 // b (R = Layout::rows_per_group, clipped to its q_len * H rows) against KV rows
-// [kv_begin, kv_end).
+// [kv_begin, kv_end).  Under sparse top-k selection R = H (one token, q_start
+// + g) and [kv_begin, kv_end) indexes the token's position list.
 // slot < 0: the item covers the whole KV range and writes `out` directly;
 // otherwise it writes a normalised fp32 partial (O and natural-log LSE) into
 // partial slot `slot` for the combine kernel.
 struct WorkItem {
   int b, g, kv_begin, kv_end;
-  int slot, q_len, seq_len, q_start;  // q_start: first token of request b
+  int slot, q_len, seq_len, q_start;  // q_start: first token of request b; seq_len: its L
   int comb;                           // combine entry of a split group, else -1
   int mask_base;                      // causal bound of query row i: causal_last(mask_base, i, W)
 };

@@ -43,6 +43,9 @@
 // With an e4m3 cache eight more warps (14-21) widen each staged e4m3 tile to
 // bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and the
 // bf16 ring is 3 deep beside a 2-deep e4m3 staging ring.
+// Under sparse top-k selection a work item is one token's H query rows and
+// its KV tiles are 64 entries of the token's position list: warp 0 gathers
+// the listed rows itself (gather_producer) instead of issuing page copies.
 // The running max is only raised, and O rescaled, when it grows by more than
 // 2^8.  Every wait is bounded; a timeout sets an error bit in the workspace
 // status word and the kernel unwinds.
@@ -50,6 +53,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "mla_common.cuh"
 #include "sm100_ptx.cuh"
@@ -96,7 +100,8 @@ constexpr uint32_t OFF_MREF = OFF_FLAG + 2 * 16 * 4;    // float [2][128]: runni
 constexpr uint32_t OFF_LX = OFF_MREF + 2 * kRows * 4;   // float [2][2][128]: group (l, m) per slot
 constexpr uint32_t OFF_TMEM = OFF_LX + 4 * kRows * 4;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
-constexpr uint32_t OFF_KV = (OFF_ABORT + 16 + 1023) / 1024 * 1024;
+constexpr uint32_t OFF_VMASK = OFF_ABORT + 16;  // uint64 [8]: usable rows of a sparse tile, by g mod 8
+constexpr uint32_t OFF_KV = (OFF_VMASK + 64 + 1023) / 1024 * 1024;
 
 // bf16 cache: a 4-stage ring.  e4m3 cache: 3 bf16 stages and a 2-deep e4m3
 // staging ring in the fourth stage's space.
@@ -111,7 +116,7 @@ template <bool kFp8> struct Cfg {
 };
 static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0 &&
                   kPBytes % 1024 == 0 && OFF_FLAG % 16 == 0 && OFF_X % 16 == 0 &&
-                  2 * kStgBytes == kStageBytes,
+                  2 * kStgBytes == kStageBytes && OFF_VMASK % 8 == 0,
               "alignment");
 // bytes the peer pushes into this CTA's P tile per KV tile (P rows, factors,
 // the group's four flags), plus the row sums on an item's last tile
@@ -255,6 +260,169 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
   fence_proxy_async_smem();  // read by the RoPE MMAs
 }
 
+// Producer of a sparse top-k decode (warp 0 when p.sparse_k > 0).  A tile is
+// 64 entries of the item's token list; each entry is resolved through
+// block_tables and its row copied into the ring with 16-byte cp.async (L2
+// only) in the layout the tensor-map copies would leave: bf16 rows straight
+// into the 128B-swizzled latent chunks and the 64B-swizzled RoPE rows of the
+// stage, e4m3 rows into the plain staging rows the converter warps widen.
+// Lane i resolves entries i and 32 + i; an entry outside [0, L) (-1 padding,
+// a position past the request) or with a page id out of range (which also
+// sets kStatusPage) reads nothing and lands as zeros, and its bit in the
+// tile's usable-row mask (shared memory, slot g mod 8) is clear, so the
+// softmax masks its score.  cp.async completes per thread: a tile is signalled
+// full only after every lane has waited for its copies of it and fenced them
+// for the tensor cores, kLag tiles behind the newest one issued.  Every tile
+// still pending is signalled before the wait for the query buffer of the next
+// item: that wait needs the previous item's last QK, and so its last tiles
+// (the wait implies they have landed, so this costs no overlap).
+template <bool kFp8>
+__device__ __noinline__ void gather_producer(const Ctx& c, const Problem& p,
+                                             const WorkItem* items, int item_begin,
+                                             int item_end, unsigned char* sm, uint32_t rank,
+                                             int R, const CUtensorMap* tm_q_rope) {
+  using C = Cfg<kFp8>;
+  constexpr int kStages = C::kStages;
+  // the e4m3 staging ring is two deep: its tiles are signalled one behind
+  constexpr uint32_t kLag = kFp8 ? 1 : 2;
+  constexpr long long kRowBytes = kQkDim * (kFp8 ? 1 : 2);
+  const int lane = threadIdx.x & 31;
+  const int H = p.num_heads, ps = p.page_size;
+  const unsigned long long kv = reinterpret_cast<unsigned long long>(p.kv_cache);
+  unsigned long long* vmask = reinterpret_cast<unsigned long long*>(sm + OFF_VMASK);
+  uint32_t g = 0, g_sig = 0;  // tiles issued / tiles signalled full
+  int n_item = 0;
+  auto signal = [&](uint32_t gi) {
+    const int s = kFp8 ? (int)(gi & 1) : (int)(gi % kStages);
+    if (lane == 0) mbar_arrive(&c.bars[kFp8 ? STG_FULL0 + s : KV_FULL0 + s]);
+  };
+  auto flush = [&]() {  // signal every tile issued so far
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    __syncwarp();
+    while (g_sig < g) signal(g_sig++);
+  };
+  for (int idx = item_begin; idx < item_end; ++idx) {
+    const WorkItem it = items[idx];
+    const int nt = n_tiles_of(it);
+    if (nt <= 0) continue;
+    flush();
+    const bool q_ok = lane == 0 ? wait_bar(c, Q_FREE, (n_item & 1) ^ 1) : false;
+    if (!__shfl_sync(0xffffffffu, q_ok, 0)) goto out;
+    ++n_item;
+    if (lane == 0) {
+      if (p.q_fp8) {
+        mbar_arrive(&c.bars[Q_FULL]);  // the RoPE half is widened into smem with the latent part
+      } else {
+        mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
+        tma_load_2d(sm + OFF_QROPE, tm_q_rope, 512 + 32 * (int)rank, it.q_start * H + it.g * R,
+                    &c.bars[Q_FULL]);
+      }
+    }
+    {
+      const int* list = p.sparse_idx + (size_t)(it.q_start + it.g) * (size_t)p.sparse_k;
+      const int* bt = p.block_tables + (size_t)it.b * p.max_pages;
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
+        const uint32_t use = kFp8 ? (g >> 1) : g / kStages;
+        const bool ok =
+            lane == 0 ? wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1) : false;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) goto out;
+        const int n0 = it.kv_begin + t * kTile;
+        unsigned long long src[2];  // cache row address of entries n0 + lane, n0 + 32 + lane
+        uint32_t m[2];              // usable entries of the two halves of the tile
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = n0 + 32 * h + lane;
+          const int j = n < it.kv_end ? __ldg(list + n) : -1;
+          bool on = j >= 0 && j < it.seq_len;
+          long long row = 0;
+          if (on) {
+            const int pg = __ldg(bt + j / ps);
+            if (pg < 0 || (long long)pg >= p.num_pages) {
+              atomicOr(c.status, kStatusPage);
+              on = false;
+            } else {
+              row = (long long)pg * ps + j % ps;
+            }
+          }
+          src[h] = kv + (unsigned long long)(row * kRowBytes);
+          m[h] = __ballot_sync(0xffffffffu, on);
+        }
+        if (lane == 0) vmask[g & 7] = ((unsigned long long)m[1] << 32) | m[0];
+        if (!kFp8) {
+          const uint32_t st = smem_u32(sm + OFF_KV + s * kStageBytes);
+          // latent dims [256 r, +256): one row per instruction, lane = 16-byte
+          // unit (chunk lane / 8, unit lane mod 8 of its 128-byte row)
+          const uint32_t u = lane & 7, lc = lane >> 3;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll 8
+            for (int i = 0; i < 32; ++i) {
+              const int r = 32 * h + i;
+              const unsigned long long a = __shfl_sync(0xffffffffu, src[h], i);
+              cp_async_16(st + lc * kChunkKV + r * 128 + ((u ^ (r & 7)) << 4),
+                          reinterpret_cast<const void*>(a + 512 * rank + 16 * lane),
+                          (m[h] >> i) & 1 ? 16u : 0u);
+            }
+          }
+          // RoPE dims [512 + 32 r, +32): 64 bytes a row, eight rows per instruction
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int r = 8 * k + (lane >> 2);
+            const uint32_t u4 = lane & 3;
+            const unsigned long long a = __shfl_sync(0xffffffffu, src[k >> 2], r & 31);
+            cp_async_16(st + kLatChunks * kChunkKV + r * 64 + ((u4 ^ ((r >> 1) & 3)) << 4),
+                        reinterpret_cast<const void*>(a + 1024 + 64 * rank + 16 * u4),
+                        (m[k >> 2] >> (r & 31)) & 1 ? 16u : 0u);
+          }
+        } else {
+          const uint32_t st = smem_u32(sm + C::OFF_STG + s * kStgBytes);
+          // latent: 256 bytes a row, two rows per instruction (unit u = lane
+          // mod 16: chunk u / 4, 16-byte column u mod 4 of its 64-byte row)
+          const uint32_t u = lane & 15;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll 8
+            for (int i = 0; i < 16; ++i) {
+              const int ri = 2 * i + (lane >> 4), r = 32 * h + ri;
+              const unsigned long long a = __shfl_sync(0xffffffffu, src[h], ri);
+              cp_async_16(st + (u >> 2) * (kTile * 64) + r * 64 + (u & 3) * 16,
+                          reinterpret_cast<const void*>(a + 256 * rank + 16 * u),
+                          (m[h] >> ri) & 1 ? 16u : 0u);
+            }
+          }
+          // RoPE: 32 bytes a row, sixteen rows per instruction
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = 16 * k + (lane >> 1);
+            const uint32_t u2 = lane & 1;
+            const unsigned long long a = __shfl_sync(0xffffffffu, src[k >> 1], r & 31);
+            cp_async_16(st + kLatChunks * kTile * 64 + r * 32 + u2 * 16,
+                        reinterpret_cast<const void*>(a + 512 + 32 * rank + 16 * u2),
+                        (m[k >> 1] >> (r & 31)) & 1 ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        if (g + 1 - g_sig > kLag) {  // tile g_sig's copies are now the oldest in flight
+          cp_async_wait_group<kLag>();
+          fence_proxy_async_smem();
+          __syncwarp();
+          signal(g_sig++);
+        }
+      }
+    }
+  }
+  flush();
+  if (lane == 0 && n_item > 0) drain_wait(&c.bars[Q_FULL], (uint32_t)(n_item - 1) & 1);
+  return;
+out:
+  // a wait gave up: none of this warp's copies may still be landing in shared
+  // memory when the CTA leaves
+  cp_async_wait_all();
+  if (lane == 0 && n_item > 0) drain_wait(&c.bars[Q_FULL], (uint32_t)(n_item - 1) & 1);
+}
+
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
@@ -326,8 +494,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   const uint32_t tmem = *tmem_slot;
   const int item_begin = worker_begin[worker], item_end = worker_begin[worker + 1];
   const int H = p.num_heads;
+  const int R = lay.rows_per_group;  // query rows of a work item: 128, or H (sparse top-k)
 
-  if (warp == 0) {
+  if (warp == 0 && p.sparse_k > 0) {
+    gather_producer<kFp8>(c, p, items, item_begin, item_end, sm, rank, R, &tm_q_rope);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // Lane 0 waits for ring slots and issues the copies.  The whole warp
     // fetches the item's page ids in batches of 32 (one per lane), one batch
@@ -360,7 +531,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         } else {
           mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
           tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank,
-                      it.q_start * H + it.g * kRows, &c.bars[Q_FULL]);
+                      it.q_start * H + it.g * R, &c.bars[Q_FULL]);
         }
       }
       for (int t = 0; t < nt; ++t, ++g) {
@@ -563,6 +734,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const uint32_t flag_peer0 = map_to_rank(smem_u32(sm + OFF_FLAG), peer);
     const uint32_t lrow_peer = map_to_rank(smem_u32(sm + OFF_LROW), peer);
     const int W = max(p.cp_world, 1);
+    const bool sparse = p.sparse_k > 0;
+    const unsigned long long* vmask = reinterpret_cast<const unsigned long long*>(sm + OFF_VMASK);
     uint32_t g = 0;
     int n_item = 0;
     int n_multi = 0;  // items of two or more tiles so far: they alone use the (l, m) hand-off
@@ -571,14 +744,18 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const int nt = n_tiles_of(it);
       if (nt <= 0) continue;
       const int rows_total = it.q_len * H;
-      const int row0 = it.g * kRows;
-      const bool row_ok = q < rows_total - row0;
+      const int row0 = it.g * R;
+      const bool row_ok = q < min(R, rows_total - row0);
       const int qi = (row0 + q) / H;
-      const int last = p.causal ? causal_last(it.mask_base, qi, W) : it.seq_len - 1;
+      // sparse top-k: the producer's usable-row mask of each tile is the mask
+      const int last = sparse ? INT_MAX
+                              : (p.causal ? causal_last(it.mask_base, qi, W) : it.seq_len - 1);
       // tiles ending at or before `clean_end` need no mask for any valid row
       const int first_qi = row0 / H;
-      const int clean_end = min(
-          it.kv_end, p.causal ? causal_last(it.mask_base, first_qi, W) + 1 : it.seq_len);
+      const int clean_end =
+          sparse ? it.kv_begin
+                 : min(it.kv_end,
+                       p.causal ? causal_last(it.mask_base, first_qi, W) + 1 : it.seq_len);
       const uint32_t g_last = g + (uint32_t)nt - 1;
       // (l, m) hand-off slot of this item and the phase of its barrier: only
       // items of two or more tiles (both groups take part) count
@@ -632,6 +809,12 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         // so that bmm1 = 0 never multiplies -inf (the same for the whole tile)
         const bool pre_scaled = j0 + kTile > clean_end;
         const float sc = pre_scaled ? 1.f : scale;  // what the scores still need
+        uint32_t usable = 0xffffffffu;              // of this thread's 32 columns
+        if (sparse) {
+          // the mask was written before the tile's full barrier completed
+          if (!wait_bar(c, KV_FULL0 + (int)(g % kStages), (g / kStages) & 1)) goto done_softmax;
+          usable = (uint32_t)(vmask[g & 7] >> (32 * hh));
+        }
         float m_tile = -INFINITY;
         if (row_ok) {
           float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // 4 chains for ILP
@@ -642,7 +825,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int col = c0 + j;
-              sv[j] = (col <= last && col < it.kv_end) ? sv[j] * scale : -INFINITY;
+              sv[j] = (col <= last && col < it.kv_end && ((usable >> j) & 1u)) ? sv[j] * scale
+                                                                                : -INFINITY;
               tm[j & 3] = fmaxf(tm[j & 3], sv[j]);
             }
           }
@@ -745,7 +929,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               if (it.slot < 0) {
                 if (p.return_lse) p.lse[grow] = lse;
               } else {
-                part_lse[(size_t)it.slot * kRows + q] = lse;
+                part_lse[(size_t)it.slot * R + q] = lse;
                 __threadfence();  // visible GPU-wide before the epilogue counts the chunk
               }
             }
@@ -825,7 +1009,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const long long q_rows = p.total_q * H;
     const float bmm2 = run_bmm2(p);
     auto write_q = [&](const WorkItem& it) {
-      const long long qrow = (long long)it.q_start * H + (long long)it.g * kRows + q;
+      const long long qrow = (long long)it.q_start * H + (long long)it.g * R + q;
       const bool in = qrow < q_rows;
       if (!p.q_fp8) {
         const uint4* src = reinterpret_cast<const uint4*>(
@@ -903,8 +1087,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       tc_fence_after();
       {
         const int rows_total = it.q_len * H;
-        const int row0 = it.g * kRows;
-        const bool row_ok = q < min(kRows, rows_total - row0);
+        const int row0 = it.g * R;
+        const bool row_ok = q < min(R, rows_total - row0);
         const float l = lrow[q];
         __syncwarp();
         if (lane == 0) {  // both CTAs' softmax may overwrite l for the next item
@@ -931,7 +1115,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           } else {
-            float4* dst = reinterpret_cast<float4*>(part_o + ((size_t)it.slot * kRows + q) * kVDim + vd);
+            float4* dst = reinterpret_cast<float4*>(part_o + ((size_t)it.slot * R + q) * kVDim + vd);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               dst[k] = make_float4(__uint_as_float(x[4 * k]) * inv, __uint_as_float(x[4 * k + 1]) * inv,

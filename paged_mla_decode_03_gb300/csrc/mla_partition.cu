@@ -17,7 +17,8 @@
 // becomes a separate item writing a partial; every other group is one item
 // writing the output directly.  So workers are balanced to within one tile
 // plus one overhead, and there are at most n + #groups items and n - 1 cut
-// points.  One CTA of 128-1024 threads; the range boundaries are tabulated in
+// points.  Under sparse top-k selection a group is one token's H rows and its
+// KV range is the token's list of k positions (T = ceil(k / 64)).  One CTA of 128-1024 threads; the range boundaries are tabulated in
 // shared memory once, so cut points and owners are table lookups.
 #include <algorithm>
 
@@ -166,6 +167,9 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   const int B = p.batch;
   const int R = lay.rows_per_group;
   const int H = p.num_heads;
+  const bool sparse = p.sparse_k > 0;
+  // KV rows a group of request b walks: its cache rows, or the token's list
+  auto kv_rows = [&](int L) { return sparse ? p.sparse_k : L; };
   // per-request and per-group scratch: in shared memory when it fits (no
   // memory round trip between the phases below), else in the workspace
   extern __shared__ __align__(16) unsigned char scratch_smem[];
@@ -222,7 +226,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     } else {
       if (L < 1 || L > p.max_seq_len) status |= kStatusSeqLen;
       L = min(max(L, 0), p.max_seq_len);
-      if (p.causal && q > L) status |= kStatusCausal;
+      if (p.causal && !sparse && q > L) status |= kStatusCausal;
       mbase = L - q;
     }
     r_qlen[b] = q;
@@ -266,7 +270,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   for (int b = threadIdx.x; b < B && n_groups > 0; b += blockDim.x) {
     const int gb = r_gbase[b];  // scanned: first group of request b
     const int ge = (b + 1 < B) ? r_gbase[b + 1] : n_groups;
-    W_total += (long long)(ge - gb) * (kOverheadTiles + (r_len[b] + kKvTile - 1) / kKvTile);
+    W_total += (long long)(ge - gb) * (kOverheadTiles + (kv_rows(r_len[b]) + kKvTile - 1) / kKvTile);
   }
   __syncthreads();
   if (threadIdx.x == 0) sh.carry_ll = 0;
@@ -280,7 +284,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     const int gb = r_gbase[b];
     const int ge = (b + 1 < B) ? r_gbase[b + 1] : n_groups;
-    const int T = (r_len[b] + kKvTile - 1) / kKvTile;
+    const int T = (kv_rows(r_len[b]) + kKvTile - 1) / kKvTile;
     for (int g = gb; g < ge && g < n_groups; ++g) {
       const int k = g - gb;
       const int slot = lanes > 1 ? k * n_req_groups + gb / G : g;
@@ -307,7 +311,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   // 3. Cut points inside each group -> chunk counts.
   for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
     const int b = g_req[g];
-    const int T = (r_len[b] + kKvTile - 1) / kKvTile;
+    const int T = (kv_rows(r_len[b]) + kKvTile - 1) / kKvTile;
     const long long S = g_start[g], c = kOverheadTiles + T;
     int nch = 1;
     if (W > 0) {
@@ -341,7 +345,8 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
     for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
       const int b = g_req[g];
       const int L = r_len[b];
-      const int T = (L + kKvTile - 1) / kKvTile;
+      const int KV = kv_rows(L);
+      const int T = (KV + kKvTile - 1) / kKvTile;
       const long long S = g_start[g], c = kOverheadTiles + T;
       const int nch = g_nch[g];
       const int g_local = g_k[g];
@@ -353,7 +358,7 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
         it.b = b;
         it.g = g_local;
         it.kv_begin = t0 * kKvTile;
-        it.kv_end = min(L, t1 * kKvTile);
+        it.kv_end = min(KV, t1 * kKvTile);
         it.slot = nch > 1 ? g_slot[g] + k : -1;
         it.comb = nch > 1 ? g_comb[g] : -1;
         it.q_len = r_qlen[b];

@@ -452,5 +452,27 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// 16-byte global -> shared copy cached in L2 only (cp.async.cg); with
+// src_bytes = 0 nothing is read and the 16 destination bytes are zeroed.
+// Both addresses 16-byte aligned.  Completion is per thread: commit_group
+// closes the thread's current group, wait_group<N> waits until at most its N
+// newest groups are still in flight (their writes are then visible to the
+// thread; a fence.proxy.async orders them before tensor-core reads).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 }  // namespace ptx
 }  // namespace mla

@@ -39,6 +39,7 @@ class DeviceCase:
     workspace: torch.Tensor
     plan: mla.Plan
     seq_lens_global: object = None
+    sparse_idx: object = None
 
 
 def to_device(w, *, return_lse=None, causal=None, workspace_fill=None, max_total_q=None,
@@ -64,7 +65,8 @@ def to_device(w, *, return_lse=None, causal=None, workspace_fill=None, max_total
                     packed=w.packed, max_total_q=max_total_q if max_total_q else tokens,
                     kv_dtype=w.kv_dtype, causal=cz, return_lse=ret,
                     q_dtype=getattr(w, "q_dtype", "bf16"), cp_world=w.cp_world,
-                    cp_rank=w.cp_rank)
+                    cp_rank=w.cp_rank, sparse_top_k=w.sparse_k)
+    sp = torch.from_numpy(w.sparse_idx).to(dev) if w.sparse_idx is not None else None
     slg = None
     if w.cp_world > 1 and cz:
         slg = torch.from_numpy(w.seq_lens_global.astype(np.int32)).to(dev)
@@ -73,14 +75,14 @@ def to_device(w, *, return_lse=None, causal=None, workspace_fill=None, max_total
         ws.fill_(workspace_fill)
     out = torch.full((tokens, w.num_heads, 512), float("nan"), dtype=torch.bfloat16, device=dev)
     lse = torch.full((tokens, w.num_heads), float("nan"), dtype=torch.float32, device=dev) if ret else None
-    return DeviceCase(q, kv, bt, sl, qo, out, lse, ws, plan, slg)
+    return DeviceCase(q, kv, bt, sl, qo, out, lse, ws, plan, slg, sp)
 
 
 def run(w, d: DeviceCase, stream=None):
     d.plan.run(d.query, d.kv_cache, d.block_tables, d.seq_lens, d.out, qo_indptr=d.qo_indptr,
                total_q=w.total_q if w.packed else 0, lse=d.lse, workspace=d.workspace,
                bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, stream=stream,
-               seq_lens_global=d.seq_lens_global)
+               seq_lens_global=d.seq_lens_global, sparse_indices=d.sparse_idx)
 
 
 def results(d: DeviceCase):

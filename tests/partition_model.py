@@ -8,7 +8,9 @@ at least two); busy workers n' = min(n, W // 4); worker p's range of units
 starts at boundary(p); a group that straddles a boundary is cut at the
 corresponding tile; an item belongs to the worker whose range holds its
 first tile.  The CPU tests check its invariants, and a GPU test compares the
-kernel's work list with it field by field.
+kernel's work list with it field by field.  Under sparse top-k selection
+(``sparse_k`` > 0) a group is one token's H rows and walks the token's list
+of ``sparse_k`` entries instead of the request's cache rows.
 """
 from __future__ import annotations
 
@@ -22,11 +24,13 @@ def ceil_div(a, b):
     return -(-a // b)
 
 
-def partition(seq_lens, q_lens, q_starts, num_heads, n_workers, mask_bases):
+def partition(seq_lens, q_lens, q_starts, num_heads, n_workers, mask_bases, sparse_k=0):
     """Return (items, worker_begin).  items: tuples (b, g, kv_begin, kv_end,
     slot, q_len, seq_len, q_start, comb, mask_base) in the kernel's order."""
     B = len(seq_lens)
-    gcount = [ceil_div(int(q) * num_heads, ROWS) if int(L) > 0 else 0
+    rows = num_heads if sparse_k > 0 else ROWS
+    kv_rows = [sparse_k if sparse_k > 0 else int(L) for L in seq_lens]
+    gcount = [ceil_div(int(q) * num_heads, rows) if int(L) > 0 else 0
               for L, q in zip(seq_lens, q_lens)]
     n_groups = sum(gcount)
     gbase, acc = [], 0
@@ -35,7 +39,7 @@ def partition(seq_lens, q_lens, q_starts, num_heads, n_workers, mask_bases):
         acc += c
     nz = [c for c in gcount if c > 0]
     g_min, g_max = (min(nz), max(nz)) if nz else (1 << 30, 0)
-    tiles = [ceil_div(int(L), TILE) for L in seq_lens]
+    tiles = [ceil_div(n_kv, TILE) for n_kv in kv_rows]
     W_total = sum(gcount[b] * (OVERHEAD + tiles[b]) for b in range(B))
     n = n_workers
     n_eff = max(1, min(n, W_total // MIN_UNITS))
@@ -102,7 +106,7 @@ def partition(seq_lens, q_lens, q_starts, num_heads, n_workers, mask_bases):
         L = int(seq_lens[b])
         nch = len(chunks[g])
         for k, (t0, t1, o) in enumerate(chunks[g]):
-            items.append((b, slot_k[g], t0 * TILE, min(L, t1 * TILE),
+            items.append((b, slot_k[g], t0 * TILE, min(kv_rows[b], t1 * TILE),
                           n_slot + k if nch > 1 else -1, int(q_lens[b]), L, int(q_starts[b]),
                           n_comb if nch > 1 else -1, int(mask_bases[b])))
             owners.append(o)

@@ -81,6 +81,9 @@ def _params(**kw):
     (dict(cp_world=4, cp_rank=4), -1),
     (dict(cp_world=4, cp_rank=-1), -1),
     (dict(cp_world=1, cp_rank=1), -1),
+    (dict(sparse_top_k=-1), -1),
+    (dict(sparse_top_k=(1 << 24) + 1), -1),
+    (dict(sparse_top_k=64, cp_world=2, cp_rank=0), -1),  # sparse selection without DCP only
 ])
 def test_plan_rejects_bad_static_parameters_on_host(lib, kw, status):
     handle = ctypes.c_void_p()
@@ -101,6 +104,8 @@ def test_null_arguments_are_rejected(lib):
     assert lib.mla_decode_host_staging_bytes(None, 0) == 0
     assert lib.mla_decode_run_dcp(None, None, None, None, None, None, 0, None, 1.0, 1.0, None,
                                   None, None, 0, None) == -1
+    assert lib.mla_decode_run_sparse(None, None, None, None, None, None, 0, None, 1.0, 1.0, None,
+                                     None, None, 0, None) == -1
     lib.mla_decode_destroy(None)
     assert lib.mla_decode_workspace_size(None) == 0
 

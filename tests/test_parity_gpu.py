@@ -44,7 +44,7 @@ def test_reduced_workload_full_parity(name):
     full_parity(REDUCED[name]())
 
 
-@pytest.mark.parametrize("name", ["deepseek_v3", "mtp", "ragged", "fp8_long"])
+@pytest.mark.parametrize("name", ["deepseek_v3", "mtp", "ragged", "fp8_long", "sparse_topk"])
 def test_full_size_workload_sampled_parity(name):
     """The full-size workloads in the launch shapes the bench times (many-way
     lanes, long split items, every worker busy), checked on sampled pairs
@@ -689,7 +689,8 @@ def test_prefill_scale_repeats_are_finite_and_bitwise_equal():
             assert torch.equal(first[0], o) and torch.equal(first[1], l), rep
 
 
-@pytest.mark.parametrize("name", ["tiny", "deepseek_v3", "mtp", "ragged", "fp8_long", "prefill"])
+@pytest.mark.parametrize("name", ["tiny", "deepseek_v3", "mtp", "ragged", "fp8_long", "prefill",
+                                  "sparse_topk"])
 def test_partition_work_list_matches_host_model(name):
     """The work list the on-device partitioner leaves in the workspace equals
     the host model of the same arithmetic (tests/partition_model.py), item by
@@ -708,7 +709,7 @@ def test_partition_work_list_matches_host_model(name):
     got_wb = d.workspace[wr_off:wr_off + 4 * (n_workers + 1)].view(torch.int32).cpu().tolist()
     qs = w.q_start()[:-1]
     items, wb, _ = partition(w.seq_lens, w.q_lens, qs, w.num_heads, n_workers,
-                             w.seq_lens.astype(np.int64) - w.q_lens)
+                             w.seq_lens.astype(np.int64) - w.q_lens, sparse_k=w.sparse_k)
     assert got == [list(t) for t in items]
     assert got_wb == wb
 
