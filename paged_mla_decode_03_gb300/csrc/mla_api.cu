@@ -19,8 +19,7 @@ cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cuda
 cudaError_t partition_setup();
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream);
-cudaError_t decode_sm103_setup(int kv_dtype, int num_heads, int max_q, int packed, int sm_count,
-                               int* n_pairs);
+cudaError_t decode_sm103_setup(int kv_dtype, int sparse, int sm_count, int* n_pairs);
 cudaError_t launch_merge_states(const void* o_parts, const float* lse_parts, int n, long long rows,
                                 float scale, void* out, float* lse_out, cudaStream_t stream);
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
@@ -118,6 +117,8 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
     return MLA_ERR_INVALID_ARG;
   if (!supported_heads(p.num_heads)) return MLA_ERR_UNSUPPORTED;
   if (p.page_size != 32 && p.page_size != 64) return MLA_ERR_UNSUPPORTED;
+  // cache rows are addressed with 32-bit row coordinates
+  if (p.num_pages > (1LL << 31) / p.page_size) return MLA_ERR_UNSUPPORTED;
   if ((long long)p.max_pages_per_req * p.page_size < p.max_seq_len) return MLA_ERR_INVALID_ARG;
   if (!p.packed && (long long)p.batch * p.max_seq_len_q > (1LL << 31) / 128)
     return MLA_ERR_UNSUPPORTED;
@@ -130,8 +131,7 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   int sms = 0, n_pairs = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
   if (e == cudaSuccess)
-    e = mla::decode_sm103_setup(p.kv_dtype, p.num_heads, p.max_seq_len_q, p.packed, sms,
-                                &n_pairs);
+    e = mla::decode_sm103_setup(p.kv_dtype, p.sparse_top_k > 0, sms, &n_pairs);
   if (e == cudaSuccess) e = mla::partition_setup();
   cudaSetDevice(prev);
   if (e != cudaSuccess || sms <= 0) return MLA_ERR_CUDA;

@@ -43,9 +43,10 @@
 // With an e4m3 cache eight more warps (14-21) widen each staged e4m3 tile to
 // bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and the
 // bf16 ring is 3 deep beside a 2-deep e4m3 staging ring.
-// Under sparse top-k selection a work item is one token's H query rows and
-// its KV tiles are 64 entries of the token's position list: warp 0 gathers
-// the listed rows itself (gather_producer) instead of issuing page copies.
+// Under sparse top-k selection (a separate instantiation, two warps more) a
+// work item is one token's H query rows and its KV tiles are 64 entries of
+// the token's position list: warp 0 and the two extra warps gather the listed
+// rows (gather_producer) instead of warp 0 issuing page copies.
 // The running max is only raised, and O rescaled, when it grows by more than
 // 2^8.  Every wait is bounded; a timeout sets an error bit in the workspace
 // status word and the kernel unwinds.
@@ -100,14 +101,19 @@ constexpr uint32_t OFF_MREF = OFF_FLAG + 2 * 16 * 4;    // float [2][128]: runni
 constexpr uint32_t OFF_LX = OFF_MREF + 2 * kRows * 4;   // float [2][2][128]: group (l, m) per slot
 constexpr uint32_t OFF_TMEM = OFF_LX + 4 * kRows * 4;
 constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
-constexpr uint32_t OFF_VMASK = OFF_ABORT + 16;  // uint64 [8]: usable rows of a sparse tile, by g mod 8
-constexpr uint32_t OFF_KV = (OFF_VMASK + 64 + 1023) / 1024 * 1024;
+// uint64 [8][3]: usable rows of a sparse tile, by g mod 8 and gather warp
+constexpr uint32_t OFF_VMASK = OFF_ABORT + 16;
+constexpr int kGatherWarps = 3;  // sparse top-k: warps that gather KV rows
+constexpr uint32_t OFF_KV = (OFF_VMASK + 8 * kGatherWarps * 8 + 1023) / 1024 * 1024;
 
 // bf16 cache: a 4-stage ring.  e4m3 cache: 3 bf16 stages and a 2-deep e4m3
-// staging ring in the fourth stage's space.
-template <bool kFp8> struct Cfg {
+// staging ring in the fourth stage's space.  Sparse top-k: two more warps
+// (the last two) gather rows beside warp 0.
+template <bool kFp8, bool kSparse = false> struct Cfg {
   static constexpr int kStages = kFp8 ? 3 : 4;
-  static constexpr int kThreads = kFp8 ? 704 : 448;  // + 8 converter warps
+  static constexpr int kThreads =
+      (kFp8 ? 704 : 448) + (kSparse ? 32 * (kGatherWarps - 1) : 0);  // + 8 converter warps
+  static constexpr int kFirstExtraGatherWarp = kThreads / 32 - (kGatherWarps - 1);
   static constexpr uint32_t OFF_STG = OFF_KV + kStages * kStageBytes;  // e4m3 staging
   static constexpr uint32_t kRingEnd = OFF_STG + (kFp8 ? 2 * kStgBytes : 0);
   static constexpr uint32_t kSmemBytes = kRingEnd + 1024;
@@ -260,176 +266,172 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
   fence_proxy_async_smem();  // read by the RoPE MMAs
 }
 
-// Producer of a sparse top-k decode (warp 0 when p.sparse_k > 0).  A tile is
-// 64 entries of the item's token list; each entry is resolved through
-// block_tables and its row copied into the ring with 16-byte cp.async (L2
-// only) in the layout the tensor-map copies would leave: bf16 rows straight
-// into the 128B-swizzled latent chunks and the 64B-swizzled RoPE rows of the
-// stage, e4m3 rows into the plain staging rows the converter warps widen.
-// Lane i resolves entries i and 32 + i; an entry outside [0, L) (-1 padding,
-// a position past the request) or with a page id out of range (which also
-// sets kStatusPage) reads nothing and lands as zeros, and its bit in the
-// tile's usable-row mask (shared memory, slot g mod 8) is clear, so the
-// softmax masks its score.  cp.async completes per thread: a tile is signalled
-// full only after every lane has waited for its copies of it and fenced them
-// for the tensor cores, kLag tiles behind the newest one issued.  Every tile
-// still pending is signalled before the wait for the query buffer of the next
-// item: that wait needs the previous item's last QK, and so its last tiles
-// (the wait implies they have landed, so this costs no overlap).
+// Producer of a sparse top-k decode: kGatherWarps warps (role 0 = warp 0,
+// which also loads each item's query RoPE tile, and the last warps of the
+// block) fill the ring together.  A tile is 64 entries of the item's token
+// list, in 16 groups of four; role r takes the groups q = r, r + 3, ...  Its
+// lane e resolves the e-th entry of those groups (the list entry, then its
+// block-table page) into a cache row; an entry outside [0, L) (-1 padding, a
+// position past the request) or with a page id out of range (which also sets
+// kStatusPage) becomes the first row past the cache, which the copy fills
+// with zeros, and its bit in the role's word of the tile's usable-row mask
+// (shared memory, slot g mod 8) is clear, so the softmax masks its score.
+// The rows come by TMA four-row gathers from maps with one-row boxes, so each
+// row lands where, and swizzled as, a page copy would put it: per row group
+// one gather per 64-dim latent chunk and one for the RoPE dims, into the bf16
+// ring (e4m3: into the staging ring the converter warps widen).  A tile's full
+// barrier waits for one arrival per role (role 0's also expects the tile's
+// bytes), so it completes once every row has landed.  Issue from one warp
+// is the limit (about 3 us a tile), hence several warps.  The index loads run
+// ahead so that their latency stays off the tile period: during tile t the
+// list entries of tile t + 3 and the page-table entries of tile t + 2 are
+// loaded, and tile t + 1's rows are formed from loads issued a tile earlier.
 template <bool kFp8>
-__device__ __noinline__ void gather_producer(const Ctx& c, const Problem& p,
+__device__ __noinline__ void gather_producer(int role, const Ctx& c, const Problem& p,
                                              const WorkItem* items, int item_begin,
                                              int item_end, unsigned char* sm, uint32_t rank,
-                                             int R, const CUtensorMap* tm_q_rope) {
-  using C = Cfg<kFp8>;
+                                             int R, const CUtensorMap* tm_q_rope,
+                                             const CUtensorMap* tm_kv,
+                                             const CUtensorMap* tm_kv_rope) {
+  using C = Cfg<kFp8, true>;
   constexpr int kStages = C::kStages;
-  // the e4m3 staging ring is two deep: its tiles are signalled one behind
-  constexpr uint32_t kLag = kFp8 ? 1 : 2;
-  constexpr long long kRowBytes = kQkDim * (kFp8 ? 1 : 2);
+  constexpr int kGroups = kTile / 4;
   const int lane = threadIdx.x & 31;
   const int H = p.num_heads, ps = p.page_size;
-  const unsigned long long kv = reinterpret_cast<unsigned long long>(p.kv_cache);
+  const int past_end = (int)(p.num_pages * ps);  // first row past the cache: zero-filled
+  const int n_groups = (kGroups - role + kGatherWarps - 1) / kGatherWarps;
+  // the tile row this lane resolves (-1: none)
+  const int my_row = lane < 4 * n_groups ? 4 * (role + kGatherWarps * (lane >> 2)) + (lane & 3) : -1;
   unsigned long long* vmask = reinterpret_cast<unsigned long long*>(sm + OFF_VMASK);
-  uint32_t g = 0, g_sig = 0;  // tiles issued / tiles signalled full
+  if (lane == 0) {
+    if (role == 0) tma_prefetch_desc(tm_q_rope);
+    tma_prefetch_desc(tm_kv);
+    tma_prefetch_desc(tm_kv_rope);
+  }
+  uint32_t g = 0;
   int n_item = 0;
-  auto signal = [&](uint32_t gi) {
-    const int s = kFp8 ? (int)(gi & 1) : (int)(gi % kStages);
-    if (lane == 0) mbar_arrive(&c.bars[kFp8 ? STG_FULL0 + s : KV_FULL0 + s]);
-  };
-  auto flush = [&]() {  // signal every tile issued so far
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    __syncwarp();
-    while (g_sig < g) signal(g_sig++);
-  };
   for (int idx = item_begin; idx < item_end; ++idx) {
     const WorkItem it = items[idx];
     const int nt = n_tiles_of(it);
     if (nt <= 0) continue;
-    flush();
-    const bool q_ok = lane == 0 ? wait_bar(c, Q_FREE, (n_item & 1) ^ 1) : false;
-    if (!__shfl_sync(0xffffffffu, q_ok, 0)) goto out;
-    ++n_item;
-    if (lane == 0) {
-      if (p.q_fp8) {
-        mbar_arrive(&c.bars[Q_FULL]);  // the RoPE half is widened into smem with the latent part
-      } else {
-        mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
-        tma_load_2d(sm + OFF_QROPE, tm_q_rope, 512 + 32 * (int)rank, it.q_start * H + it.g * R,
-                    &c.bars[Q_FULL]);
+    const int* list = p.sparse_idx + (size_t)(it.q_start + it.g) * (size_t)p.sparse_k;
+    const int* bt = p.block_tables + (size_t)it.b * p.max_pages;
+    // list entry of this lane's row of tile t (-1 past the item's range)
+    auto load_list = [&](int t) -> int {
+      const int n = it.kv_begin + t * kTile + my_row;
+      return (my_row >= 0 && t < nt && n < it.kv_end) ? __ldg(list + n) : -1;
+    };
+    // its page-table entry (-1 for an unused entry)
+    auto load_page = [&](int j) -> int {
+      return (j >= 0 && j < it.seq_len) ? __ldg(bt + j / ps) : -1;
+    };
+    // its cache row, and this role's word of the usable-row mask
+    auto finish = [&](int j, int pg, int& row, unsigned long long& word) {
+      bool on = j >= 0 && j < it.seq_len;
+      if (on && (pg < 0 || (long long)pg >= p.num_pages)) {
+        atomicOr(c.status, kStatusPage);
+        on = false;
+      }
+      row = on ? pg * ps + j % ps : past_end;
+      const uint32_t lo = __reduce_or_sync(0xffffffffu, on && my_row < 32 ? 1u << my_row : 0u);
+      const uint32_t hi =
+          __reduce_or_sync(0xffffffffu, on && my_row >= 32 ? 1u << (my_row - 32) : 0u);
+      word = ((unsigned long long)hi << 32) | lo;
+    };
+    // j1, j2: list entries of tiles t + 1, t + 2; pg1: page entry of tile t + 1
+    const int j0 = load_list(0);
+    int j1 = load_list(1), j2 = load_list(2);
+    int pg1 = load_page(j1);
+    int row;
+    unsigned long long word;
+    finish(j0, load_page(j0), row, word);
+    if (role == 0) {
+      const bool q_ok = lane == 0 ? wait_bar(c, Q_FREE, (n_item & 1) ^ 1) : false;
+      if (!__shfl_sync(0xffffffffu, q_ok, 0)) goto out;
+      if (lane == 0) {
+        if (p.q_fp8) {
+          mbar_arrive(&c.bars[Q_FULL]);  // the RoPE half is widened into smem with the latent part
+        } else {
+          mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
+          tma_load_2d(sm + OFF_QROPE, tm_q_rope, 512 + 32 * (int)rank, it.q_start * H + it.g * R,
+                      &c.bars[Q_FULL]);
+        }
       }
     }
-    {
-      const int* list = p.sparse_idx + (size_t)(it.q_start + it.g) * (size_t)p.sparse_k;
-      const int* bt = p.block_tables + (size_t)it.b * p.max_pages;
-      for (int t = 0; t < nt; ++t, ++g) {
-        const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
-        const uint32_t use = kFp8 ? (g >> 1) : g / kStages;
-        const bool ok =
-            lane == 0 ? wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1) : false;
-        if (!__shfl_sync(0xffffffffu, ok, 0)) goto out;
-        const int n0 = it.kv_begin + t * kTile;
-        unsigned long long src[2];  // cache row address of entries n0 + lane, n0 + 32 + lane
-        uint32_t m[2];              // usable entries of the two halves of the tile
+    ++n_item;
+    for (int t = 0; t < nt; ++t, ++g) {
+      const int s = kFp8 ? (int)(g & 1) : (int)(g % kStages);
+      const uint32_t use = kFp8 ? (g >> 1) : g / kStages;
+      const bool ok =
+          lane == 0 ? wait_bar(c, kFp8 ? STG_EMPTY0 + s : KV_EMPTY0 + s, (use & 1) ^ 1) : false;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) goto out;
+      // index loads of later tiles, in flight during this tile's gathers
+      const int j3 = load_list(t + 3);
+      const int pg2 = load_page(j2);
+      uint64_t* full = &c.bars[kFp8 ? STG_FULL0 + s : KV_FULL0 + s];
+      if (lane == 0) {
+        vmask[kGatherWarps * (g & 7) + role] = word;
+        if (role == 0)
+          mbar_arrive_expect_tx(full, kFp8 ? kStgBytes : kStageBytes);
+        else
+          mbar_arrive(full);
+      }
+      // lane l < n_groups: row group q = role + 3 l, rows 4q .. 4q + 3
+      int y[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = n0 + 32 * h + lane;
-          const int j = n < it.kv_end ? __ldg(list + n) : -1;
-          bool on = j >= 0 && j < it.seq_len;
-          long long row = 0;
-          if (on) {
-            const int pg = __ldg(bt + j / ps);
-            if (pg < 0 || (long long)pg >= p.num_pages) {
-              atomicOr(c.status, kStatusPage);
-              on = false;
-            } else {
-              row = (long long)pg * ps + j % ps;
-            }
-          }
-          src[h] = kv + (unsigned long long)(row * kRowBytes);
-          m[h] = __ballot_sync(0xffffffffu, on);
-        }
-        if (lane == 0) vmask[g & 7] = ((unsigned long long)m[1] << 32) | m[0];
-        if (!kFp8) {
-          const uint32_t st = smem_u32(sm + OFF_KV + s * kStageBytes);
-          // latent dims [256 r, +256): one row per instruction, lane = 16-byte
-          // unit (chunk lane / 8, unit lane mod 8 of its 128-byte row)
-          const uint32_t u = lane & 7, lc = lane >> 3;
+      for (int i = 0; i < 4; ++i) y[i] = __shfl_sync(0xffffffffu, row, (4 * lane + i) & 31);
+      if (lane < n_groups) {
+        const int q = role + kGatherWarps * lane;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll 8
-            for (int i = 0; i < 32; ++i) {
-              const int r = 32 * h + i;
-              const unsigned long long a = __shfl_sync(0xffffffffu, src[h], i);
-              cp_async_16(st + lc * kChunkKV + r * 128 + ((u ^ (r & 7)) << 4),
-                          reinterpret_cast<const void*>(a + 512 * rank + 16 * lane),
-                          (m[h] >> i) & 1 ? 16u : 0u);
-            }
+        for (int part = 0; part <= kLatChunks; ++part) {
+          if (kFp8) {
+            unsigned char* stg = sm + C::OFF_STG + s * kStgBytes;
+            if (part < kLatChunks)
+              tma_gather4(stg + part * kTile * 64 + 4 * q * 64, tm_kv,
+                          256 * (int)rank + 64 * part, y[0], y[1], y[2], y[3], full);
+            else
+              tma_gather4(stg + kLatChunks * kTile * 64 + 4 * q * 32, tm_kv_rope,
+                          512 + 32 * (int)rank, y[0], y[1], y[2], y[3], full);
+          } else {
+            unsigned char* stage = sm + OFF_KV + s * kStageBytes;
+            if (part < kLatChunks)
+              tma_gather4(stage + part * kChunkKV + 4 * q * 128, tm_kv,
+                          256 * (int)rank + 64 * part, y[0], y[1], y[2], y[3], full);
+            else
+              tma_gather4(stage + kLatChunks * kChunkKV + 4 * q * 64, tm_kv_rope,
+                          512 + 32 * (int)rank, y[0], y[1], y[2], y[3], full);
           }
-          // RoPE dims [512 + 32 r, +32): 64 bytes a row, eight rows per instruction
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int r = 8 * k + (lane >> 2);
-            const uint32_t u4 = lane & 3;
-            const unsigned long long a = __shfl_sync(0xffffffffu, src[k >> 2], r & 31);
-            cp_async_16(st + kLatChunks * kChunkKV + r * 64 + ((u4 ^ ((r >> 1) & 3)) << 4),
-                        reinterpret_cast<const void*>(a + 1024 + 64 * rank + 16 * u4),
-                        (m[k >> 2] >> (r & 31)) & 1 ? 16u : 0u);
-          }
-        } else {
-          const uint32_t st = smem_u32(sm + C::OFF_STG + s * kStgBytes);
-          // latent: 256 bytes a row, two rows per instruction (unit u = lane
-          // mod 16: chunk u / 4, 16-byte column u mod 4 of its 64-byte row)
-          const uint32_t u = lane & 15;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll 8
-            for (int i = 0; i < 16; ++i) {
-              const int ri = 2 * i + (lane >> 4), r = 32 * h + ri;
-              const unsigned long long a = __shfl_sync(0xffffffffu, src[h], ri);
-              cp_async_16(st + (u >> 2) * (kTile * 64) + r * 64 + (u & 3) * 16,
-                          reinterpret_cast<const void*>(a + 256 * rank + 16 * u),
-                          (m[h] >> ri) & 1 ? 16u : 0u);
-            }
-          }
-          // RoPE: 32 bytes a row, sixteen rows per instruction
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int r = 16 * k + (lane >> 1);
-            const uint32_t u2 = lane & 1;
-            const unsigned long long a = __shfl_sync(0xffffffffu, src[k >> 1], r & 31);
-            cp_async_16(st + kLatChunks * kTile * 64 + r * 32 + u2 * 16,
-                        reinterpret_cast<const void*>(a + 512 + 32 * rank + 16 * u2),
-                        (m[k >> 1] >> (r & 31)) & 1 ? 16u : 0u);
-          }
-        }
-        cp_async_commit();
-        if (g + 1 - g_sig > kLag) {  // tile g_sig's copies are now the oldest in flight
-          cp_async_wait_group<kLag>();
-          fence_proxy_async_smem();
-          __syncwarp();
-          signal(g_sig++);
         }
       }
+      finish(j1, pg1, row, word);
+      j1 = j2;
+      j2 = j3;
+      pg1 = pg2;
     }
   }
-  flush();
-  if (lane == 0 && n_item > 0) drain_wait(&c.bars[Q_FULL], (uint32_t)(n_item - 1) & 1);
-  return;
 out:
-  // a wait gave up: none of this warp's copies may still be landing in shared
-  // memory when the CTA leaves
-  cp_async_wait_all();
-  if (lane == 0 && n_item > 0) drain_wait(&c.bars[Q_FULL], (uint32_t)(n_item - 1) & 1);
+  // however the loop ended, no copy issued here may still be landing in shared
+  // memory when the CTA leaves: wait for the last tiles of the ring and the
+  // last query load (phases already complete pass at once)
+  if (lane == 0) {
+    const uint32_t depth = kFp8 ? 2u : (uint32_t)kStages;
+    for (uint32_t d = 0; d < depth && d < g; ++d) {
+      const uint32_t gi = g - 1 - d;
+      const int s = kFp8 ? (int)(gi & 1) : (int)(gi % kStages);
+      const uint32_t use = kFp8 ? (gi >> 1) : gi / kStages;
+      drain_wait(&c.bars[kFp8 ? STG_FULL0 + s : KV_FULL0 + s], use & 1);
+    }
+    if (role == 0 && n_item > 0) drain_wait(&c.bars[Q_FULL], (uint32_t)(n_item - 1) & 1);
+  }
 }
 
-template <bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8>::kThreads, 1)
+template <bool kFp8, bool kSparse>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8, kSparse>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                     const __grid_constant__ CUtensorMap tm_q_rope,
                     const __grid_constant__ CUtensorMap tm_kv,
                     const __grid_constant__ CUtensorMap tm_kv_rope) {
-  using C = Cfg<kFp8>;
+  using C = Cfg<kFp8, kSparse>;
   constexpr int kStages = C::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -470,6 +472,12 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kConvThreads / 32;
       counts[STG_EMPTY0] = counts[STG_EMPTY1] = kConvThreads / 32;
     }
+    if (kSparse) {  // one arrival per gather warp on the ring the rows land in
+      if (kFp8)
+        counts[STG_FULL0] = counts[STG_FULL1] = kGatherWarps;
+      else
+        for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kGatherWarps;
+    }
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(&c.bars[i], counts[i]);
     *c.abort = 0;
     for (int k = 0; k < 32; ++k) flags[k] = -1;
@@ -496,8 +504,9 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   const int H = p.num_heads;
   const int R = lay.rows_per_group;  // query rows of a work item: 128, or H (sparse top-k)
 
-  if (warp == 0 && p.sparse_k > 0) {
-    gather_producer<kFp8>(c, p, items, item_begin, item_end, sm, rank, R, &tm_q_rope);
+  if (kSparse && (warp == 0 || warp >= C::kFirstExtraGatherWarp)) {
+    gather_producer<kFp8>(warp == 0 ? 0 : 1 + warp - C::kFirstExtraGatherWarp, c, p, items,
+                          item_begin, item_end, sm, rank, R, &tm_q_rope, &tm_kv, &tm_kv_rope);
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // Lane 0 waits for ring slots and issues the copies.  The whole warp
@@ -734,7 +743,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const uint32_t flag_peer0 = map_to_rank(smem_u32(sm + OFF_FLAG), peer);
     const uint32_t lrow_peer = map_to_rank(smem_u32(sm + OFF_LROW), peer);
     const int W = max(p.cp_world, 1);
-    const bool sparse = p.sparse_k > 0;
+    constexpr bool sparse = kSparse;
     const unsigned long long* vmask = reinterpret_cast<const unsigned long long*>(sm + OFF_VMASK);
     uint32_t g = 0;
     int n_item = 0;
@@ -813,7 +822,10 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         if (sparse) {
           // the mask was written before the tile's full barrier completed
           if (!wait_bar(c, KV_FULL0 + (int)(g % kStages), (g / kStages) & 1)) goto done_softmax;
-          usable = (uint32_t)(vmask[g & 7] >> (32 * hh));
+          unsigned long long u = 0;
+#pragma unroll
+          for (int r = 0; r < kGatherWarps; ++r) u |= vmask[kGatherWarps * (g & 7) + r];
+          usable = (uint32_t)(u >> (32 * hh));
         }
         float m_tile = -INFINITY;
         if (row_ok) {
@@ -1246,10 +1258,10 @@ bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int e
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kSparse>
 cudaError_t setup_one(int sm_count, int* n_pairs) {
-  using C = Cfg<kFp8>;
-  auto kernel = decode_sm103_kernel<kFp8>;
+  using C = Cfg<kFp8, kSparse>;
+  auto kernel = decode_sm103_kernel<kFp8, kSparse>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1273,10 +1285,10 @@ cudaError_t setup_one(int sm_count, int* n_pairs) {
 }
 
 // Launch as a programmatic dependent of the previous kernel in the stream.
-template <bool kFp8>
+template <bool kFp8, bool kSparse>
 cudaError_t launch_pdl(int grid, cudaStream_t stream, const Problem& p, const Layout& lay, char* ws,
                        const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c) {
-  using C = Cfg<kFp8>;
+  using C = Cfg<kFp8, kSparse>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -1287,18 +1299,17 @@ cudaError_t launch_pdl(int grid, cudaStream_t stream, const Problem& p, const La
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kFp8>, p, lay, ws, a, b, c);
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kFp8, kSparse>, p, lay, ws, a, b, c);
 }
 
 }  // namespace
 
-cudaError_t decode_sm103_setup(int kv_dtype, int num_heads, int max_q, int packed, int sm_count,
-                               int* n_pairs) {
-  (void)num_heads;
-  (void)max_q;
-  (void)packed;
-  if (kv_dtype == 1) return setup_one<true>(sm_count, n_pairs);
-  return setup_one<false>(sm_count, n_pairs);
+cudaError_t decode_sm103_setup(int kv_dtype, int sparse, int sm_count, int* n_pairs) {
+  if (kv_dtype == 1)
+    return sparse ? setup_one<true, true>(sm_count, n_pairs)
+                  : setup_one<true, false>(sm_count, n_pairs);
+  return sparse ? setup_one<false, true>(sm_count, n_pairs)
+                : setup_one<false, false>(sm_count, n_pairs);
 }
 
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
@@ -1306,6 +1317,8 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
   CUtensorMap tm_q_rope, tm_kv, tm_kv_rope;
   const uint64_t q_rows = std::max<uint64_t>(1, (uint64_t)p.total_q * p.num_heads);
   const uint64_t kv_rows = (uint64_t)p.num_pages * p.page_size;
+  // sparse top-k gathers single rows (four per copy); otherwise pages are copied
+  const uint32_t box_rows = p.sparse_k > 0 ? 1u : (uint32_t)p.page_size;
   // (an e4m3 query is read with plain loads; its map is encoded but unused)
   if (!(p.q_fp8 ? encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_rows, 32,
                             kRows, CU_TENSOR_MAP_SWIZZLE_NONE)
@@ -1314,21 +1327,29 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
     return cudaErrorInvalidValue;
   if (p.kv_dtype == 1) {
     // e4m3 bytes land row-major in the staging ring; the converter swizzles
-    if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 64,
-                   p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 64, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 32,
-                   p.page_size, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    return launch_pdl<true>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv,
-                            tm_kv_rope);
+    return p.sparse_k > 0 ? launch_pdl<true, true>(lay.n_ctas, stream, p, lay,
+                                                   static_cast<char*>(ws), tm_q_rope, tm_kv,
+                                                   tm_kv_rope)
+                          : launch_pdl<true, false>(lay.n_ctas, stream, p, lay,
+                                                    static_cast<char*>(ws), tm_q_rope, tm_kv,
+                                                    tm_kv_rope);
   }
-  if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64,
-                 p.page_size, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 64, box_rows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_rows, 32,
-                 p.page_size, CU_TENSOR_MAP_SWIZZLE_64B))
+                 box_rows, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  return launch_pdl<false>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws), tm_q_rope, tm_kv,
-                           tm_kv_rope);
+  return p.sparse_k > 0 ? launch_pdl<false, true>(lay.n_ctas, stream, p, lay,
+                                                  static_cast<char*>(ws), tm_q_rope, tm_kv,
+                                                  tm_kv_rope)
+                        : launch_pdl<false, false>(lay.n_ctas, stream, p, lay,
+                                                   static_cast<char*>(ws), tm_q_rope, tm_kv,
+                                                   tm_kv_rope);
 }
 
 }  // namespace mla
