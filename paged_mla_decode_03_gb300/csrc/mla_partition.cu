@@ -18,8 +18,9 @@
 // writing the output directly.  So workers are balanced to within one tile
 // plus one overhead, and there are at most n + #groups items and n - 1 cut
 // points.  Under sparse top-k selection a group is one token's H rows and its
-// KV range is the token's list of k positions (T = ceil(k / 64)).  One CTA of 128-1024 threads; the range boundaries are tabulated in
-// shared memory once, so cut points and owners are table lookups.
+// KV range is the token's list of k positions (T = ceil(k / 64)).  One CTA
+// of 128-1024 threads; the range boundaries are tabulated in shared memory
+// once, so cut points and owners are table lookups.
 #include <algorithm>
 
 #include "mla_common.cuh"

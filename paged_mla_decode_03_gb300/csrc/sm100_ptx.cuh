@@ -56,13 +56,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false (and leaves the barrier alone) if the phase did
-// not complete within `max_iters` polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_iters) {
-  for (uint32_t i = 0; i < max_iters; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
 
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -182,18 +175,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
       "r"(r[15])
       : "memory");
 }
-// 16 lanes x 32 bit, two column halves: threads 0-15 read lanes 0-15 at
-// columns [col, col + 16), threads 16-31 the same lanes at [col + 32, col + 48)
-// (half split offset 32 columns).
-__device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16], 32;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -218,11 +199,6 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
   asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ uint32_t nclusters_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
@@ -232,16 +208,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_saddr, uint32_t r
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
   return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
-               : "memory");
-}
-// Arrive (release at cluster scope) on an mbarrier given by a shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -263,31 +229,6 @@ namespace ptx {
 
 constexpr uint32_t kSwizzle64B = 4;
 
-// expect-tx without an arrival
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-// Asynchronous 16-byte store into a peer CTA's shared memory that completes
-// `bytes` of the transaction count of the peer's mbarrier `remote_bar`.
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
-          "r"(remote_addr),
-      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
-      : "memory");
-}
-// Bulk copy from this CTA's shared memory into a peer CTA's shared memory,
-// completing the transaction count of the peer's mbarrier.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const void* src,
-                                                  uint32_t bytes, uint32_t remote_bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(remote_dst),
-      "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
-      : "memory");
-}
 // Relaxed remote arrive: orders nothing, only counts (for write-after-read
 // hand-offs whose reads have already returned their values).
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
@@ -302,16 +243,6 @@ __device__ __forceinline__ uint4 ld_volatile_shared_v4(const void* p) {
                : "r"(smem_u32(p))
                : "memory");
   return v;
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Named barrier over `nthreads` threads (id 1..15).
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -379,18 +310,6 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// 16 lanes x 32 bit, two column halves, 16 repetitions: threads 0-15 write
-// lanes 0-15 of the address at columns [col, col + 16), threads 16-31 the
-// same lanes at columns [col + 16, col + 32).
-__device__ __forceinline__ void tmem_st_16x32bx2_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], 16, {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
 
 }  // namespace ptx
 }  // namespace mla
@@ -411,18 +330,6 @@ __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, u
       "r"(v), "r"(remote_bar)
       : "memory");
 }
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
-  float a, b;
-  asm("{\n .reg .b16 x, y;\n mov.b32 {x, y}, %2;\n cvt.f32.f16 %0, x;\n cvt.f32.f16 %1, y;\n}"
-      : "=f"(a), "=f"(b)
-      : "r"(v));
-  return make_float2(a, b);
-}
 
 }  // namespace ptx
 }  // namespace mla
@@ -438,18 +345,6 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta
       " [%0], %1;" ::"r"(smem_u32(bar)),
       "h"(cta_mask)
       : "memory");
-}
-// 16 lanes x 32 bit, two column halves, 16 repetitions: threads 0-15 read
-// lanes 0-15 of the address at columns [col, col + 16), threads 16-31 the same
-// lanes at columns [col + 16, col + 32) (half split offset 16 columns).
-__device__ __forceinline__ void tmem_ld_16x32bx2_x16_s16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16], 16;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
 }
 
 }  // namespace ptx
