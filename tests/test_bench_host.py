@@ -30,6 +30,32 @@ def test_work_model_counts_visible_pairs_by_enumeration():
     assert bench.work_model(wd)["n_vis"] == 2 * 5 + 2 * 9
 
 
+def test_sparse_work_model_counts_usable_entries_and_distinct_rows():
+    """Under sparse top-k the FLOPs count every usable listed entry (repeats
+    included), the KV bytes only the distinct rows of each request, and a
+    list of every position once gives the dense non-causal counts."""
+    w = mi.build("wms", 4, num_heads=4, page_size=32, seq_lens=[50, 70], q_lens=[2, 2],
+                 packed=False, causal=False)
+    dense = bench.work_model(w)
+    idx = np.full((4, 70), -1, np.int32)
+    for t in range(4):
+        L = int(w.seq_lens[t // 2])
+        idx[t, :L] = np.random.default_rng(t).permutation(L)
+    full = bench.work_model(dataclasses.replace(w, sparse_idx=idx))
+    assert full["n_vis"] == dense["n_vis"] and full["flops"] == dense["flops"]
+    assert full["kv_bytes"] == dense["kv_bytes"]
+    # repeats, -1 and past-the-end entries: 3 + 1 usable for token 0, 2 usable for the rest
+    idx2 = np.full((4, 6), -1, np.int32)
+    idx2[0] = [3, 3, 7, 50, -1, 9]
+    idx2[1] = [0, 1, -1, -1, -1, 70]
+    idx2[2] = [5, 6, -1, -1, -1, -1]
+    idx2[3] = [5, 6, 70, -1, -1, -1]
+    wm = bench.work_model(dataclasses.replace(w, sparse_idx=idx2))
+    assert wm["n_vis"] == 4 + 2 + 2 + 2
+    # distinct rows: request 0 {0, 1, 3, 7, 9}, request 1 {5, 6}
+    assert wm["kv_bytes"] == (5 + 2) * 576 * 2
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))

@@ -212,3 +212,40 @@ def test_sparse_topk_through_decode_api():
     ref_o, ref_l = oracle.run(w)
     check("bf16", out.float().cpu().numpy().reshape(-1, w.num_heads, 512), ref_o,
           lse.cpu().numpy(), ref_l, what="decode api")
+
+
+def test_sparse_profiled_entry_times_the_decode_and_equals_the_plain_entry():
+    """The bench's entry point (events around the decode kernel) takes the
+    lists too and gives the same bits as mla_decode_run_sparse."""
+    w = topk(2018, 256, seq_lens=[900, 2000, 400], q_lens=[1] * 3)
+    d = to_device(w)
+    run(w, d)
+    ref = d.out.clone()
+    out = torch.full_like(d.out, float("nan"))
+    ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    mla.mla_decode_run_profiled(d.plan.handle, d.query, d.kv_cache, d.block_tables, d.seq_lens,
+                                None, 0, w.bmm1_scale, w.bmm2_scale, out, d.lse, d.workspace,
+                                events=ev, sparse_indices=d.sparse_idx)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert ev[0].elapsed_time(ev[1]) > 0.0
+    with pytest.raises(mla.MlaDecodeError):  # a sparse plan needs its lists here too
+        mla.mla_decode_run_profiled(d.plan.handle, d.query, d.kv_cache, d.block_tables,
+                                    d.seq_lens, None, 0, w.bmm1_scale, w.bmm2_scale, out, d.lse,
+                                    d.workspace)
+
+
+def test_sparse_plan_is_refused_by_the_allocation_free_entry():
+    import ctypes
+    w = topk(2019, 64, seq_lens=[300], q_lens=[1])
+    d = to_device(w)
+    lib = mla.load_library()
+    fn = lib.mla_decode_run_static_workspace
+    vp = ctypes.c_void_p
+    fn.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.c_float, ctypes.c_float, vp, vp,
+                   vp]
+    fn.restype = ctypes.c_int
+    rc = fn(d.plan.handle, d.query.data_ptr(), d.kv_cache.data_ptr(), d.block_tables.data_ptr(),
+            d.seq_lens.data_ptr(), None, 0, w.bmm1_scale, w.bmm2_scale, d.out.data_ptr(),
+            d.lse.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert rc == -1  # MLA_ERR_INVALID_ARG: the static entry has no list argument
