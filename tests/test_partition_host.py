@@ -1,0 +1,134 @@
+"""The partition kernel's own source, run on CPU threads, against the host model.
+
+The partitioner's arithmetic is pinned twice: by ``tests/partition_model.py``
+(a Python restatement, checked for its invariants on CPU and compared with the
+kernel's work list on the GPU), and here. The test compiles the CUDA source
+of ``partition_kernel`` as C++ with host stand-ins for the barrier and warp
+shuffles (``tests/partition_host/shim.h``), under AddressSanitizer and
+UndefinedBehaviorSanitizer. It runs one std::thread per CUDA thread of the
+launch and requires the work list the kernel leaves in a dirty workspace to
+equal the host model's, item by item and worker range by worker range. An
+out-of-range index or a race on the shared scratch shows up here, on CPU,
+before any GPU run.
+"""
+import os
+import re
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import mla_inputs as mi
+from partition_model import partition
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HERE = os.path.join(ROOT, "tests", "partition_host")
+CSRC = os.path.join(ROOT, "paged_mla_decode_03_gb300", "csrc")
+
+
+def _function_text(src, head):
+    """The text of the function that starts at `head`, through its closing brace."""
+    i = src.index(head)
+    j = src.index("{", i)
+    depth = 0
+    for k in range(j, len(src)):
+        depth += {"{": 1, "}": -1}.get(src[k], 0)
+        if depth == 0:
+            return src[i:k + 1]
+    raise ValueError(head)
+
+
+@pytest.fixture(scope="module")
+def emulator(tmp_path_factory):
+    cxx = shutil.which("g++")
+    if cxx is None:
+        pytest.skip("no g++")
+    out = tmp_path_factory.mktemp("partition_host")
+    common = open(os.path.join(CSRC, "mla_common.cuh")).read()
+    common = common.replace("#include <cuda_runtime.h>\n", "")
+    common = common.replace("#pragma once", "#pragma once\ninline unsigned char* g_scratch = nullptr;", 1)
+    (out / "mla_common_host.h").write_text(common)
+    src = open(os.path.join(CSRC, "mla_partition.cu")).read()
+    src = src.replace('#include "mla_common.cuh"\n#include "sm100_ptx.cuh"\n',
+                      '#include "shim.h"\n#include "mla_common_host.h"\n')
+    src = src.replace("ptx::pdl_launch_dependents();", "")
+    src = src.replace("extern __shared__ __align__(16) unsigned char scratch_smem[];",
+                      "unsigned char* scratch_smem = g_scratch;")
+    src = src[:src.index("cudaError_t launch_partition(")] + "}  // namespace mla\n"
+    assert "asm" not in src and "__ldg" not in src
+    (out / "partition_host.inc").write_text(src)
+    api = open(os.path.join(CSRC, "mla_api.cu")).read()
+    (out / "make_layout.inc").write_text(_function_text(api, "int make_layout(") + "\n")
+    exe = out / "partition_host"
+    cmd = [cxx, "-std=c++20", "-O1", "-g", "-fsanitize=address,undefined",
+           "-fno-sanitize-recover=undefined", "-pthread", "-I", str(out), "-I", HERE,
+           "-I", os.path.join(ROOT, "include"), os.path.join(HERE, "driver.cpp"), "-o", str(exe)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0 and ("No such file" in r.stderr or "cannot find -l" in r.stderr):
+        pytest.skip("host toolchain lacks C++20 <barrier> or the sanitizers: " + r.stderr[-300:])
+    assert r.returncode == 0, r.stderr[-3000:]
+    return exe, out
+
+
+def _run(emulator, w, n_workers):
+    exe, out = emulator
+    inp, res = out / "in.txt", out / "out.txt"
+    with open(inp, "w") as f:
+        f.write(f"{w.batch} {w.num_heads} {int(w.packed)} {w.max_seq_len_q} {w.max_seq_len} "
+                f"{n_workers} {w.sparse_k} {int(w.causal)} {w.total_q}\n")
+        f.write(" ".join(str(int(x)) for x in w.seq_lens) + "\n")
+        if w.packed:
+            f.write(" ".join(str(int(x)) for x in w.qo_indptr) + "\n")
+    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0:abort_on_error=1")
+    r = subprocess.run([str(exe), str(inp), str(res)], capture_output=True, text=True, env=env,
+                       timeout=300)
+    assert r.returncode == 0, (r.returncode, r.stderr[-3000:])
+    lines = open(res).read().split("\n")
+    status, n_items, _ = (int(x) for x in lines[0].split())
+    vals = [int(x) for x in lines[1].split()]
+    got = [vals[10 * i:10 * i + 10] for i in range(n_items)]
+    wb = [int(x) for x in lines[2].split()]
+    items, ref_wb, _ = partition(w.seq_lens, w.q_lens, w.q_start()[:-1], w.num_heads, n_workers,
+                                 w.seq_lens.astype(np.int64) - w.q_lens, sparse_k=w.sparse_k)
+    assert status == 0
+    assert got == [list(t) for t in items]
+    assert wb == ref_wb
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek_v3", "mtp", "ragged", "fp8_long",
+                                  "sparse_topk"])
+def test_kernel_source_work_list_equals_host_model_on_bench_workloads(emulator, name):
+    _run(emulator, mi.WORKLOADS[name](), 76)
+
+
+class _Shape:
+    """Just the fields the partitioner reads (no KV pool is drawn)."""
+
+    def __init__(self, seq_lens, q_lens, H, packed, sparse_k):
+        self.seq_lens = np.asarray(seq_lens, np.int32)
+        self.q_lens = np.asarray(q_lens, np.int32)
+        self.batch = len(self.seq_lens)
+        self.num_heads = H
+        self.packed = packed
+        self.causal = True
+        self.sparse_k = sparse_k
+        self.max_seq_len = int(self.seq_lens.max())
+        self.max_seq_len_q = int(self.q_lens.max())
+        self.total_q = int(self.q_lens.sum())
+        self.qo_indptr = np.concatenate([[0], np.cumsum(self.q_lens)]).astype(np.int32)
+
+    def q_start(self):
+        return self.qo_indptr.astype(np.int64)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_kernel_source_work_list_equals_host_model_on_random_shapes(emulator, seed):
+    rng = np.random.default_rng(7000 + seed)
+    B = int(rng.integers(1, 200))
+    H = int(rng.choice([16, 32, 64, 128]))
+    packed = bool(rng.integers(2))
+    q = (rng.integers(1, 9, size=B) if packed else np.full(B, int(rng.integers(1, 5))))
+    L = rng.integers(q, int(rng.choice([100, 3000, 40000])), endpoint=True)
+    sparse_k = int(rng.choice([64, 100, 2048])) if rng.random() < 0.3 else 0
+    _run(emulator, _Shape(L, q, H, packed, sparse_k), int(rng.choice([1, 7, 76, 148, 600])))
