@@ -276,7 +276,9 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   __syncthreads();
   if (threadIdx.x == 0) sh.carry_ll = 0;
   __syncthreads();
-  atomicAdd(reinterpret_cast<unsigned long long*>(&sh.carry_ll), (unsigned long long)W_total);
+  // only threads holding cost add (contended 64-bit shared atomics are slow)
+  if (W_total != 0)
+    atomicAdd(reinterpret_cast<unsigned long long*>(&sh.carry_ll), (unsigned long long)W_total);
   __syncthreads();
   W_total = sh.carry_ll;
   const long long n_eff = max(1LL, min(n, W_total / kMinUnits));
