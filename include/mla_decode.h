@@ -88,6 +88,16 @@ typedef struct mla_decode_params {
   int32_t sparse_top_k;      /* sparse top-k selection: entries k per query token of the
                                 position list (0: off; > 0: run with mla_decode_run_sparse;
                                 not with cp_world > 1) */
+  int32_t e4m3_widen;        /* e4m3 cache only.  0: the e4m3 tiles go straight to the
+                                FP8 tensor cores (kind::f8f6f4).  The query enters them
+                                as e4m3: an e4m3 query as it is; a bf16 query row
+                                scaled by a power of two and split into two e4m3 parts
+                                whose sum is the row (exact for every element of at
+                                least 2^-9 of the row's largest magnitude, within 2^-17
+                                of that magnitude below).  P enters as two e4m3 parts
+                                (about 2^-8 relative).  Nonzero: every e4m3 value is
+                                widened exactly to bf16 before bf16 MMAs (P in bf16).
+                                Sparse top-k always widens. */
 } mla_decode_params;
 
 typedef struct mla_plan_s mla_plan_t; /* opaque; host memory only */

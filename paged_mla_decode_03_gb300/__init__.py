@@ -67,6 +67,7 @@ class MlaDecodeParams(ctypes.Structure):
         ("cp_world", ctypes.c_int32),
         ("cp_rank", ctypes.c_int32),
         ("sparse_top_k", ctypes.c_int32),
+        ("e4m3_widen", ctypes.c_int32),
     ]
 
 
@@ -337,7 +338,8 @@ class Plan:
                  page_size: int, max_pages_per_req: int, num_pages: int, packed: bool,
                  max_total_q: int = 0, kv_dtype: str = "bf16", causal: bool = True,
                  return_lse: bool = False, device: int = 0, q_dtype: str = "bf16",
-                 cp_world: int = 1, cp_rank: int = 0, sparse_top_k: int = 0):
+                 cp_world: int = 1, cp_rank: int = 0, sparse_top_k: int = 0,
+                 e4m3_widen: bool = False):
         self.params = MlaDecodeParams(
             batch=batch, num_heads=num_heads, max_seq_len_q=max_seq_len_q,
             max_seq_len=max_seq_len, page_size=page_size, max_pages_per_req=max_pages_per_req,
@@ -346,7 +348,8 @@ class Plan:
             mask=MASK_CAUSAL if causal else MASK_DENSE, return_lse=int(bool(return_lse)),
             device=device,
             q_dtype=Q_FP8_E4M3 if q_dtype in ("e4m3", "fp8", torch.float8_e4m3fn) else Q_BF16,
-            cp_world=cp_world, cp_rank=cp_rank, sparse_top_k=sparse_top_k)
+            cp_world=cp_world, cp_rank=cp_rank, sparse_top_k=sparse_top_k,
+            e4m3_widen=int(bool(e4m3_widen)))
         self.cp_world = cp_world
         self.sparse_top_k = sparse_top_k
         self.handle, self.workspace_bytes = mla_decode_plan(self.params)
@@ -417,7 +420,7 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
            bmm1_scale=1.0, bmm2_scale=1.0, mask_type: str = "causal",
            return_lse: bool = False, cp_world: int = 1, cp_rank: int = 0,
            causal_seqlens_kv_global: Optional[torch.Tensor] = None,
-           sparse_indices: Optional[torch.Tensor] = None):
+           sparse_indices: Optional[torch.Tensor] = None, e4m3_widen: bool = False):
     """Paged MLA decode.  Returns ``out`` (and ``lse`` when ``return_lse``).
 
     ``query``: bf16 or float8_e4m3fn (quantised with a q_scale the caller folds
@@ -433,6 +436,9 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
     ``sparse_indices``: int32 ``[tokens, k]`` logical KV positions per query
     token (sparse top-k, ``sparse_mla_top_k`` = k); the listed positions in
     ``[0, seq_lens[b])`` replace the mask.
+    ``e4m3_widen``: with an e4m3 cache, widen every e4m3 value exactly to bf16
+    and multiply on bf16 tensor cores instead of the FP8 ones (see
+    ``mla_decode_params.e4m3_widen`` in ``include/mla_decode.h``).
     """
     if query.dtype not in (torch.bfloat16, torch.float8_e4m3fn) or not query.is_cuda:
         raise ValueError("query must be a bf16 or float8_e4m3fn CUDA tensor")
@@ -471,7 +477,7 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
     key = (B, H, sq, int(max_seq_len), int(kv_cache.shape[1]), int(block_tables.shape[1]),
            int(kv_cache.shape[0]), packed, total_q if packed else 0, kv_dtype, causal,
            bool(return_lse), query.device.index or 0, q_dtype, int(cp_world), int(cp_rank),
-           top_k)
+           top_k, bool(e4m3_widen))
     plan = _plans.get(key)
     if plan is None:
         plan = Plan(batch=B, num_heads=H, max_seq_len_q=sq, max_seq_len=int(max_seq_len),
@@ -479,7 +485,7 @@ def decode(query: torch.Tensor, kv_cache: torch.Tensor, workspace_buffer: torch.
                     num_pages=int(kv_cache.shape[0]), packed=packed, max_total_q=total_q,
                     kv_dtype=kv_dtype, causal=causal, return_lse=return_lse,
                     device=query.device.index or 0, q_dtype=q_dtype, cp_world=int(cp_world),
-                    cp_rank=int(cp_rank), sparse_top_k=top_k)
+                    cp_rank=int(cp_rank), sparse_top_k=top_k, e4m3_widen=e4m3_widen)
         _plans[key] = plan
     if workspace_buffer.numel() * workspace_buffer.element_size() < plan.workspace_bytes:
         raise ValueError(f"workspace_buffer needs {plan.workspace_bytes} bytes")

@@ -19,7 +19,7 @@ cudaError_t launch_partition(const Problem& p, const Layout& lay, void* ws, cuda
 cudaError_t partition_setup();
 cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int grid,
                            cudaStream_t stream);
-cudaError_t decode_sm103_setup(int kv_dtype, int sparse, int sm_count, int* n_pairs);
+cudaError_t decode_sm103_setup(int kv_dtype, int sparse, int f8_mma, int sm_count, int* n_pairs);
 cudaError_t launch_merge_states(const void* o_parts, const float* lse_parts, int n, long long rows,
                                 float scale, void* out, float* lse_out, cudaStream_t stream);
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
@@ -38,6 +38,12 @@ namespace {
 constexpr size_t kHeaderBytes = sizeof(int) * mla::kHdrWords;
 
 bool supported_heads(int h) { return h == 16 || h == 32 || h == 64 || h == 128; }
+
+// An e4m3 cache runs on the FP8 MMAs unless widening was asked for (sparse
+// top-k always widens).
+bool uses_f8_mma(const mla_decode_params& p) {
+  return p.kv_dtype == MLA_KV_FP8_E4M3 && p.sparse_top_k == 0 && p.e4m3_widen == 0;
+}
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -131,7 +137,7 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   int sms = 0, n_pairs = 0;
   cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p.device);
   if (e == cudaSuccess)
-    e = mla::decode_sm103_setup(p.kv_dtype, p.sparse_top_k > 0, sms, &n_pairs);
+    e = mla::decode_sm103_setup(p.kv_dtype, p.sparse_top_k > 0, uses_f8_mma(p), sms, &n_pairs);
   if (e == cudaSuccess) e = mla::partition_setup();
   cudaSetDevice(prev);
   if (e != cudaSuccess || sms <= 0) return MLA_ERR_CUDA;
@@ -247,6 +253,7 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
   p.packed = prm.packed;
   p.kv_dtype = prm.kv_dtype;
   p.q_fp8 = prm.q_dtype == MLA_Q_FP8_E4M3;
+  p.f8_mma = uses_f8_mma(prm);
   p.cp_world = dcp ? prm.cp_world : 1;
   p.cp_rank = dcp ? prm.cp_rank : 0;
   p.seq_lens_global = seq_lens_global;

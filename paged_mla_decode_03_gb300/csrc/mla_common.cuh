@@ -24,7 +24,8 @@ constexpr int kStatusSeqLen = 1, kStatusQLen = 2, kStatusCausal = 4, kStatusCapa
 struct Problem {
   int batch, num_heads, max_q, max_seq_len, page_size, max_pages;
   int packed, kv_dtype, causal, return_lse;
-  int q_fp8;                     // 1: query is e4m3 (widened to bf16 on load)
+  int q_fp8;                     // 1: query is e4m3
+  int f8_mma;                    // 1: e4m3 cache on FP8 MMAs (else widened to bf16)
   int cp_world, cp_rank;         // decode-context parallelism (cp_world 1: off)
   int sparse_k;                  // > 0: sparse top-k, k listed KV positions per token
   long long num_pages, total_q;  // total_q: rows of the query tensor (tokens)

@@ -86,6 +86,12 @@ constexpr uint32_t kRopeKV = kTile * 64;    // 32-dim RoPE half of a KV tile
 constexpr uint32_t kStageBytes = kLatChunks * kChunkKV + kRopeKV;  // 36 KB
 constexpr uint32_t kPBytes = kRows * 128;   // P: 128 rows x 64 KV rows bf16, 128B-swizzled
 constexpr uint32_t kStgBytes = kLatChunks * kTile * 64 + kTile * 32;  // e4m3 tile, 18 KB
+// e4m3 tiles read by FP8 MMAs: two 128-dim latent chunks (128B-swizzled rows)
+// and the 32 RoPE dims (32B-swizzled rows)
+constexpr uint32_t kChunk8 = kTile * 128;
+constexpr uint32_t kRope8 = kTile * 32;
+constexpr uint32_t kStage8Bytes = 2 * kChunk8 + kRope8;  // 18 KB
+constexpr uint32_t kPart8 = kRows * 64;  // one e4m3 part of a P tile (64B-swizzled rows)
 // peer's partial scores of the owned rows: [64 rows][64] fp32 per tile parity
 // (16-byte units of a row XOR-swizzled by the row index)
 constexpr uint32_t kXRowBytes = kTile * 4;
@@ -104,17 +110,22 @@ constexpr uint32_t OFF_ABORT = OFF_TMEM + 16;
 // uint64 [8][3]: usable rows of a sparse tile, by g mod 8 and gather warp
 constexpr uint32_t OFF_VMASK = OFF_ABORT + 16;
 constexpr int kGatherWarps = 3;  // sparse top-k: warps that gather KV rows
-constexpr uint32_t OFF_KV = (OFF_VMASK + 8 * kGatherWarps * 8 + 1023) / 1024 * 1024;
+// float [2][128]: per-row query scale 2^-k of the FP8 path, by item parity
+constexpr uint32_t OFF_QSCALE = OFF_VMASK + 8 * kGatherWarps * 8;
+constexpr uint32_t OFF_KV = (OFF_QSCALE + 2 * kRows * 4 + 1023) / 1024 * 1024;
 
-// bf16 cache: a 4-stage ring.  e4m3 cache: 3 bf16 stages and a 2-deep e4m3
-// staging ring in the fourth stage's space.  Sparse top-k: two more warps
-// (the last two) gather rows beside warp 0.
-template <bool kFp8, bool kSparse = false> struct Cfg {
-  static constexpr int kStages = kFp8 ? 3 : 4;
+// bf16 cache: a 4-stage ring.  e4m3 cache widened to bf16 (kFp8): 3 bf16
+// stages and a 2-deep e4m3 staging ring in the fourth stage's space.  e4m3
+// cache on FP8 MMAs (kF8): an 8-stage ring of e4m3 tiles.  Sparse top-k: two
+// more warps (the last two) gather rows beside warp 0.
+template <bool kFp8, bool kSparse = false, bool kF8 = false> struct Cfg {
+  static_assert(!(kF8 && (kFp8 || kSparse)), "FP8 MMAs: dense e4m3 cache only");
+  static constexpr int kStages = kF8 ? 8 : (kFp8 ? 3 : 4);
+  static constexpr uint32_t kStage = kF8 ? kStage8Bytes : kStageBytes;  // bytes of a stage
   static constexpr int kThreads =
       (kFp8 ? 704 : 448) + (kSparse ? 32 * (kGatherWarps - 1) : 0);  // + 8 converter warps
   static constexpr int kFirstExtraGatherWarp = kThreads / 32 - (kGatherWarps - 1);
-  static constexpr uint32_t OFF_STG = OFF_KV + kStages * kStageBytes;  // e4m3 staging
+  static constexpr uint32_t OFF_STG = OFF_KV + kStages * kStage;  // e4m3 staging
   static constexpr uint32_t kRingEnd = OFF_STG + (kFp8 ? 2 * kStgBytes : 0);
   static constexpr uint32_t kSmemBytes = kRingEnd + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -122,7 +133,8 @@ template <bool kFp8, bool kSparse = false> struct Cfg {
 };
 static_assert(OFF_KV % 1024 == 0 && kStageBytes % 1024 == 0 && OFF_P % 1024 == 0 &&
                   kPBytes % 1024 == 0 && OFF_FLAG % 16 == 0 && OFF_X % 16 == 0 &&
-                  2 * kStgBytes == kStageBytes && OFF_VMASK % 8 == 0,
+                  2 * kStgBytes == kStageBytes && OFF_VMASK % 8 == 0 &&
+                  kStage8Bytes % 1024 == 0 && 2 * kPart8 == kPBytes && OFF_QSCALE % 16 == 0,
               "alignment");
 // bytes the peer pushes into this CTA's P tile per KV tile (P rows, factors,
 // the group's four flags), plus the row sums on an item's last tile
@@ -137,9 +149,9 @@ constexpr uint32_t TM_Q = 384;  // Q latent: 128 rows x 256 dims (bf16 pairs)
 
 enum Bar {
   Q_FULL, Q_FREE, QT_FULL,
-  KV_FULL0, KV_FULL1, KV_FULL2, KV_FULL3,
-  KV_EMPTY0, KV_EMPTY1, KV_EMPTY2, KV_EMPTY3,
-  S_FULL0, S_FULL1, S_FREE0, S_FREE1,
+  KV_FULL0, KV_EMPTY0 = KV_FULL0 + 8,  // 8 each: one per ring stage
+  S_FULL0 = KV_EMPTY0 + 8, S_FULL1,
+  S_FREE0, S_FREE1,
   X_FULL0, X_FULL1, PEER_X_FREE0, PEER_X_FREE1,
   P_FULL0, P_FULL1, P_FREE0, P_FREE1,
   MREF0,                       // 8: [tile parity][subpartition], running max published
@@ -148,6 +160,7 @@ enum Bar {
   O_STABLE, CORR_DONE, O_FINAL, EPI_DONE,
   STG_FULL0, STG_FULL1, STG_EMPTY0, STG_EMPTY1,
   MMA_DRAIN,                   // the issuer's last commit: every MMA it issued has completed
+  QS_FULL0, QS_FULL1,          // FP8 path: the item's query row scales written, by item parity
   NUM_BARS
 };
 static_assert(NUM_BARS * 8 <= 512, "barrier area");
@@ -264,6 +277,119 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
         make_uint4(o[4], o[5], o[6], o[7]);
   }
   fence_proxy_async_smem();  // read by the RoPE MMAs
+}
+
+// Row `q` of a work item's query for the FP8 MMAs, for the CTA of cluster rank
+// `rank`: its latent dims [256 rank, 256 rank + 256) as e4m3 codes into the
+// TMEM columns at `tmem_q` (four codes a column; A operand of the ts QK MMAs)
+// and its RoPE dims [512 + 32 rank, +32) into the 32B-swizzled smem tile at
+// `q_rope`.  An e4m3 query is copied as it is (one part).  A bf16 query row
+// is scaled by 2^k, the largest power of two with max|q| 2^k <= 448 (taken
+// over all 576 dims, so both CTAs of the pair agree), and split into two
+// parts, hi = e4m3(x) at columns [0, 64) and lo = e4m3(x - hi) at [64, 128)
+// (RoPE: the second 4 KB of `q_rope`).  hi + lo equals x exactly wherever
+// |x| >= 2^-2 (x is a bf16 value times a power of two, and x - hi has at most
+// four significant bits at or above 2^-9) and to within 2^-10 below that.
+// Returns 2^-k, the factor the row's scores need.  Rows past the query
+// tensor are zero (factor 1).
+__device__ __noinline__ float load_q_row_split_e4m3(const Problem& p, long long qrow, bool in,
+                                                    int q, uint32_t rank, uint32_t tmem_q,
+                                                    unsigned char* q_rope) {
+  const int sw = (q >> 2) & 1;  // 32B swizzle: 16-byte unit u of row q sits at u ^ sw
+  if (p.q_fp8) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        reinterpret_cast<const unsigned char*>(p.query) + (in ? qrow : 0) * kQkDim);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t w[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 x = in ? __ldg(src + 16 * (int)rank + 8 * half + u) : make_uint4(0, 0, 0, 0);
+        w[4 * u] = x.x;
+        w[4 * u + 1] = x.y;
+        w[4 * u + 2] = x.z;
+        w[4 * u + 3] = x.w;
+      }
+      tmem_st_32x32b_x16(tmem_q + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(w));
+      tmem_st_32x32b_x16(tmem_q + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(w + 16));
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint4 x = in ? __ldg(src + 32 + 2 * (int)rank + u) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(q_rope + q * 32 + ((u ^ sw) << 4)) = x;
+    }
+    fence_proxy_async_smem();  // read by the RoPE MMA
+    return 1.f;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(
+      reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim);
+  float amax = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < kQkDim / 8; ++i) {
+    const uint4 x = in ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
+                               fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+  }
+  int k = 0;
+  if (amax > 0.f && amax <= 3.4028235e38f) {
+    const uint32_t ab = __float_as_uint(amax);
+    const int E = (int)(ab >> 23);  // biased exponent, 0 for a subnormal
+    k = E == 0 ? 126 : ((ab & 0x7FFFFFu) <= 0x600000u ? 135 - E : 134 - E);  // 448 = 1.75 * 2^8
+    k = min(126, max(-126, k));
+  }
+  const float up = __uint_as_float((uint32_t)(127 + k) << 23);
+  // eight bf16 values (one uint4) -> two words of hi codes and two of lo codes
+  auto split8 = [&](const uint4 x, uint32_t* hi, uint32_t* lo) {
+    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float a = __uint_as_float(w4[2 * e] << 16) * up;
+      const float b = __uint_as_float(w4[2 * e] & 0xFFFF0000u) * up;
+      const float c = __uint_as_float(w4[2 * e + 1] << 16) * up;
+      const float d = __uint_as_float(w4[2 * e + 1] & 0xFFFF0000u) * up;
+      const uint32_t hab = f32x2_to_e4m3x2(a, b), hcd = f32x2_to_e4m3x2(c, d);
+      float fa, fb, fc, fd;
+      e4m3x2_to_f32x2(hab, fa, fb);
+      e4m3x2_to_f32x2(hcd, fc, fd);
+      hi[e] = hab | (hcd << 16);
+      lo[e] = f32x2_to_e4m3x2(a - fa, b - fb) | (f32x2_to_e4m3x2(c - fc, d - fd) << 16);
+    }
+  };
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {  // 128 latent dims = 16 uint4 = 32 columns a part
+    uint32_t hw[32], lw[32];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const uint4 x = in ? __ldg(src + 32 * (int)rank + 16 * half + u) : make_uint4(0, 0, 0, 0);
+      split8(x, hw + 2 * u, lw + 2 * u);
+    }
+    tmem_st_32x32b_x16(tmem_q + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(hw));
+    tmem_st_32x32b_x16(tmem_q + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(hw + 16));
+    tmem_st_32x32b_x16(tmem_q + 64 + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(lw));
+    tmem_st_32x32b_x16(tmem_q + 64 + 32 * half + 16,
+                       *reinterpret_cast<const uint32_t(*)[16]>(lw + 16));
+  }
+  {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // RoPE dims 512 + 32 r + [8 u, 8 u + 8)
+      const uint4 x = in ? __ldg(src + 64 + 4 * (int)rank + u) : make_uint4(0, 0, 0, 0);
+      split8(x, hw + 2 * u, lw + 2 * u);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int off = q * 32 + ((u ^ sw) << 4);
+      *reinterpret_cast<uint4*>(q_rope + off) =
+          make_uint4(hw[4 * u], hw[4 * u + 1], hw[4 * u + 2], hw[4 * u + 3]);
+      *reinterpret_cast<uint4*>(q_rope + kRopeQ / 2 + off) =
+          make_uint4(lw[4 * u], lw[4 * u + 1], lw[4 * u + 2], lw[4 * u + 3]);
+    }
+  }
+  fence_proxy_async_smem();  // read by the RoPE MMAs
+  return __uint_as_float((uint32_t)(127 - k) << 23);
 }
 
 // Producer of a sparse top-k decode: kGatherWarps warps (role 0 = warp 0,
@@ -425,13 +551,13 @@ out:
   }
 }
 
-template <bool kFp8, bool kSparse>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8, kSparse>::kThreads, 1)
+template <bool kFp8, bool kSparse, bool kF8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kFp8, kSparse, kF8>::kThreads, 1)
 decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                     const __grid_constant__ CUtensorMap tm_q_rope,
                     const __grid_constant__ CUtensorMap tm_kv,
                     const __grid_constant__ CUtensorMap tm_kv_rope) {
-  using C = Cfg<kFp8, kSparse>;
+  using C = Cfg<kFp8, kSparse, kF8>;
   constexpr int kStages = C::kStages;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -468,6 +594,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     counts[P_FREE0] = counts[P_FREE1] = 2;                        // both CTAs' PV
     counts[LROW_FREE] = 2 * kCeWarps;                             // both CTAs' epilogues
     counts[CORR_DONE] = counts[EPI_DONE] = counts[QT_FULL] = kCeWarps;
+    counts[QS_FULL0] = counts[QS_FULL1] = kCeWarps;
     if (kFp8) {
       for (int i = 0; i < kStages; ++i) counts[KV_FULL0 + i] = kConvThreads / 32;
       counts[STG_EMPTY0] = counts[STG_EMPTY1] = kConvThreads / 32;
@@ -535,8 +662,10 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       if (!__shfl_sync(0xffffffffu, q_ok, 0)) goto done_producer;
       ++n_item;
       if (lane == 0) {
-        if (p.q_fp8) {
-          mbar_arrive(&c.bars[Q_FULL]);  // the RoPE half is widened into smem with the latent part
+        if (p.q_fp8 || kF8) {
+          // the RoPE half is written into smem with the latent part (widened,
+          // or split into e4m3 parts)
+          mbar_arrive(&c.bars[Q_FULL]);
         } else {
           mbar_arrive_expect_tx(&c.bars[Q_FULL], kRopeQ);
           tma_load_2d(sm + OFF_QROPE, &tm_q_rope, 512 + 32 * (int)rank,
@@ -572,14 +701,22 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               pages[pg] = -1;
               continue;
             }
-            bytes += ps * (kLatChunks * 64 + 32) * (kFp8 ? 1 : 2);
+            bytes += ps * (kLatChunks * 64 + 32) * (kFp8 || kF8 ? 1 : 2);
           }
           uint64_t* full = &c.bars[kFp8 ? STG_FULL0 + s : KV_FULL0 + s];
           mbar_arrive_expect_tx(full, bytes);
           for (int pg = 0; pg < npg; ++pg) {
             if (pages[pg] < 0) continue;
             const int y = pages[pg] * ps;
-            if (kFp8) {
+            if (kF8) {
+              // e4m3 rows straight into the ring, in the layouts the FP8 MMAs read
+              unsigned char* stage = sm + OFF_KV + s * C::kStage;
+              for (int lc = 0; lc < 2; ++lc)
+                tma_load_2d(stage + lc * kChunk8 + pg * ps * 128, &tm_kv, 256 * (int)rank + 128 * lc,
+                            y, full);
+              tma_load_2d(stage + 2 * kChunk8 + pg * ps * 32, &tm_kv_rope, 512 + 32 * (int)rank, y,
+                          full);
+            } else if (kFp8) {
               unsigned char* stg = sm + C::OFF_STG + s * kStgBytes;
               for (int lc = 0; lc < kLatChunks; ++lc)
                 tma_load_2d(stg + lc * kTile * 64 + pg * ps * 64, &tm_kv, 256 * (int)rank + 64 * lc,
@@ -617,8 +754,12 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     // Within an item QK(g) is issued as soon as its KV tile and S buffer are
     // ready (up to two tiles ahead of PV), PV(g) as soon as P(g) is complete.
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_f16(128, 64, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(128, 256, false, true);
+      constexpr uint32_t idesc_qk = kF8 ? idesc_e4m3(128, 64, false, false)
+                                        : idesc_f16(128, 64, false, false);
+      constexpr uint32_t idesc_pv = kF8 ? idesc_e4m3(128, 256, false, true)
+                                        : idesc_f16(128, 256, false, true);
+      // FP8 path: a bf16 query is two e4m3 parts (hi, lo), an e4m3 query one
+      const int q_parts = p.q_fp8 ? 1 : 2;
       const uint32_t qr_base = smem_u32(sm + OFF_QROPE);
       const uint32_t kv_base = smem_u32(sm + OFF_KV);
       const uint32_t p_base = smem_u32(sm + OFF_P);
@@ -662,12 +803,24 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
               // them before this thread's MMA reads (async proxy)
               fence_proxy_async_smem();
               const int s = gp % kStages;
-              const uint32_t stage = kv_base + s * kStageBytes;
-              for (int ks = 0; ks < kTile / 16; ++ks) {
-                const uint64_t a =
-                    smem_desc(p_base + pb * kPBytes + ks * 32, 16, 1024, kSwizzle128B);
-                const uint64_t b = smem_desc(stage + ks * 16 * 128, 8192, 1024, kSwizzle128B);
-                mma_bf16_ss(tmem + TM_O, a, b, idesc_pv, (pv == 0 && ks == 0) ? 0u : 1u);
+              const uint32_t stage = kv_base + s * C::kStage;
+              if (kF8) {
+                // P as two e4m3 parts (64B-swizzled rows) against V read
+                // MN-major from the two 128-dim chunks, K = 32 KV rows a step
+                for (int k = 0; k < 2 * (kTile / 32); ++k) {
+                  const int part = k >> 1, ks = k & 1;
+                  const uint64_t a = smem_desc(p_base + pb * kPBytes + part * kPart8 + ks * 32, 16,
+                                               512, kSwizzle64B);
+                  const uint64_t b = smem_desc(stage + ks * 32 * 128, kChunk8, 1024, kSwizzle128B);
+                  mma_e4m3_ss(tmem + TM_O, a, b, idesc_pv, (pv == 0 && k == 0) ? 0u : 1u);
+                }
+              } else {
+                for (int ks = 0; ks < kTile / 16; ++ks) {
+                  const uint64_t a =
+                      smem_desc(p_base + pb * kPBytes + ks * 32, 16, 1024, kSwizzle128B);
+                  const uint64_t b = smem_desc(stage + ks * 16 * 128, 8192, 1024, kSwizzle128B);
+                  mma_bf16_ss(tmem + TM_O, a, b, idesc_pv, (pv == 0 && ks == 0) ? 0u : 1u);
+                }
               }
               mma_commit(&c.bars[KV_EMPTY0 + s]);
               // both CTAs' P tiles (of this parity) are free
@@ -685,18 +838,35 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
                 mbar_test_wait(&c.bars[S_FREE0 + sb], ((gq >> 1) & 1) ^ 1)) {
               tc_fence_after();
               const uint32_t d = tmem + TM_S + 64 * sb;
-              const uint32_t stage = kv_base + s * kStageBytes;
-              for (int k = 0; k < 4 * kLatChunks; ++k) {
-                const int lc = k >> 2, ks = k & 3;
-                const uint64_t b = smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
-                // 16 dims = 8 TMEM columns of bf16 pairs
-                mma_bf16_ts(d, tmem + TM_Q + 32 * lc + 8 * ks, b, idesc_qk, k > 0 ? 1u : 0u);
-              }
-              for (int ks = 0; ks < 2; ++ks) {
-                const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
-                const uint64_t b = smem_desc(stage + kLatChunks * kChunkKV + ks * 32, 16, 512,
-                                             kSwizzle64B);
-                mma_bf16_ss(d, a, b, idesc_qk, 1u);
+              const uint32_t stage = kv_base + s * C::kStage;
+              if (kF8) {
+                for (int part = 0; part < q_parts; ++part) {
+                  for (int k = 0; k < 8; ++k) {
+                    const int lc = k >> 2, ks = k & 3;
+                    const uint64_t b =
+                        smem_desc(stage + lc * kChunk8 + ks * 32, 16, 1024, kSwizzle128B);
+                    // 32 dims = 8 TMEM columns of four e4m3 codes
+                    mma_e4m3_ts(d, tmem + TM_Q + 64 * part + 32 * lc + 8 * ks, b, idesc_qk,
+                                (part | k) != 0 ? 1u : 0u);
+                  }
+                  const uint64_t a = smem_desc(qr_base + part * (kRopeQ / 2), 16, 256, kSwizzle32B);
+                  const uint64_t b = smem_desc(stage + 2 * kChunk8, 16, 256, kSwizzle32B);
+                  mma_e4m3_ss(d, a, b, idesc_qk, 1u);
+                }
+              } else {
+                for (int k = 0; k < 4 * kLatChunks; ++k) {
+                  const int lc = k >> 2, ks = k & 3;
+                  const uint64_t b =
+                      smem_desc(stage + lc * kChunkKV + ks * 32, 16, 1024, kSwizzle128B);
+                  // 16 dims = 8 TMEM columns of bf16 pairs
+                  mma_bf16_ts(d, tmem + TM_Q + 32 * lc + 8 * ks, b, idesc_qk, k > 0 ? 1u : 0u);
+                }
+                for (int ks = 0; ks < 2; ++ks) {
+                  const uint64_t a = smem_desc(qr_base + ks * 32, 16, 512, kSwizzle64B);
+                  const uint64_t b = smem_desc(stage + kLatChunks * kChunkKV + ks * 32, 16, 512,
+                                               kSwizzle64B);
+                  mma_bf16_ss(d, a, b, idesc_qk, 1u);
+                }
               }
               mma_commit(&c.bars[S_FULL0 + sb]);
               if (++qk == nt) mma_commit(&c.bars[Q_FREE]);
@@ -733,7 +903,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const uint32_t lane_addr = (uint32_t)(32 * sp + 16 * (int)rank) << 16;
     const bool designated = fw == 0 && lane == 0;
     const int g_tid = fw * 32 + lane;  // thread within the group
-    const float scale = run_bmm1(p, c.status) * kLog2e;
+    const float bmm1_log2e = run_bmm1(p, c.status) * kLog2e;
+    const float* qscale = reinterpret_cast<const float*>(sm + OFF_QSCALE);
     float* mref = reinterpret_cast<float*>(sm + OFF_MREF);  // [tile parity][row]
     float* lx = reinterpret_cast<float*>(sm + OFF_LX);      // [item parity][l, m][row]
     const uint32_t xfree_peer0 = map_to_rank(smem_u32(&c.bars[PEER_X_FREE0]), peer);
@@ -773,10 +944,19 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       // this group's share of the row sum (this thread's 32 columns), relative
       // to the reference m_grp of the group's latest tile of the item
       float l_part = 0.f, m_grp = -INFINITY;
+      // bmm1 * log2(e), times the row's query scale 2^-k on the FP8 path (the
+      // MMAs saw the query times 2^k), read at the group's first tile of the item
+      float scale = bmm1_log2e;
+      bool have_scale = !kF8;
       for (int t = 0; t < nt; ++t, ++g) {
         if ((int)(g & 1) != grp) continue;
         const int sb = grp;
         float sv[32];
+        if (!have_scale) {
+          if (!wait_bar(c, QS_FULL0 + (n_item & 1), (n_item >> 1) & 1)) goto done_softmax;
+          scale = bmm1_log2e * qscale[(n_item & 1) * kRows + q];
+          have_scale = true;
+        }
         if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
         tc_fence_after();
         {
@@ -884,11 +1064,13 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         // zero V rows past the end of the KV range (last tile of the item)
         const int valid = it.kv_end - j0;
         if (valid < kTile) {
-          unsigned char* stage = sm + OFF_KV + (g % kStages) * kStageBytes;
-          const int nz = (kTile - valid) * kLatChunks * 8;  // 16-byte units
+          unsigned char* stage = sm + OFF_KV + (g % kStages) * C::kStage;
+          constexpr int kChunks = kF8 ? 2 : kLatChunks;  // 128-byte rows per KV row
+          constexpr uint32_t kChunkBytes = kF8 ? kChunk8 : kChunkKV;
+          const int nz = (kTile - valid) * kChunks * 8;  // 16-byte units
           for (int e = g_tid; e < nz; e += kGroupWarps * 32) {
-            const int row = valid + e / 32, ch = (e / 8) % 4, u = e % 8;
-            *reinterpret_cast<uint4*>(stage + ch * kChunkKV + row * 128 + u * 16) =
+            const int row = valid + e / (8 * kChunks), ch = (e / 8) % kChunks, u = e % 8;
+            *reinterpret_cast<uint4*>(stage + ch * kChunkBytes + row * 128 + u * 16) =
                 make_uint4(0, 0, 0, 0);
           }
         }
@@ -896,18 +1078,47 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         // CTAs' PV of tile g - 2 read them
         if (!wait_bar(c, P_FREE0 + sb, ((g >> 1) & 1) ^ 1)) goto done_softmax;
         {
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
           const uint32_t pbar = pfull_peer0 + 8u * sb;
           unsigned char* ptile = sm + OFF_P + sb * kPBytes;
           const uint32_t ppeer = p_peer0 + sb * kPBytes;
+          if (kF8) {
+            // two e4m3 parts: hi = e4m3(p), lo = e4m3(p - hi); their sum is p to
+            // about 2^-8 relative (64B-swizzled rows of 64 codes per part)
+            uint32_t hw[8], lw[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t off = q * 128 + (((4 * hh + u) ^ (q & 7)) << 4);
-            const uint4 val = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            *reinterpret_cast<uint4*>(ptile + off) = val;
-            st_async_v4_b32(ppeer + off, val, pbar);
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t h01 = f32x2_to_e4m3x2(sv[4 * e], sv[4 * e + 1]);
+              const uint32_t h23 = f32x2_to_e4m3x2(sv[4 * e + 2], sv[4 * e + 3]);
+              float f0, f1, f2, f3;
+              e4m3x2_to_f32x2(h01, f0, f1);
+              e4m3x2_to_f32x2(h23, f2, f3);
+              hw[e] = h01 | (h23 << 16);
+              lw[e] = f32x2_to_e4m3x2(sv[4 * e] - f0, sv[4 * e + 1] - f1) |
+                      (f32x2_to_e4m3x2(sv[4 * e + 2] - f2, sv[4 * e + 3] - f3) << 16);
+            }
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              const uint32_t* w = part ? lw : hw;
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const uint32_t off =
+                    part * kPart8 + q * 64 + (((2 * hh + u) ^ ((q >> 1) & 3)) << 4);
+                const uint4 val = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                *reinterpret_cast<uint4*>(ptile + off) = val;
+                st_async_v4_b32(ppeer + off, val, pbar);
+              }
+            }
+          } else {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t off = q * 128 + (((4 * hh + u) ^ (q & 7)) << 4);
+              const uint4 val = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+              *reinterpret_cast<uint4*>(ptile + off) = val;
+              st_async_v4_b32(ppeer + off, val, pbar);
+            }
           }
           if (hh == 0) {
             fac[sb * kRows + q] = f;
@@ -1020,10 +1231,15 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     // item is pending.
     const long long q_rows = p.total_q * H;
     const float bmm2 = run_bmm2(p);
-    auto write_q = [&](const WorkItem& it) {
+    // `ordinal`: the item's place among this worker's items (its scale slot)
+    float* qscale = reinterpret_cast<float*>(sm + OFF_QSCALE);
+    auto write_q = [&](const WorkItem& it, int ordinal) {
       const long long qrow = (long long)it.q_start * H + (long long)it.g * R + q;
       const bool in = qrow < q_rows;
-      if (!p.q_fp8) {
+      if (kF8) {
+        qscale[(ordinal & 1) * kRows + q] = load_q_row_split_e4m3(
+            p, qrow, in, q, rank, tmem + lane_base + TM_Q, sm + OFF_QROPE);
+      } else if (!p.q_fp8) {
         const uint4* src = reinterpret_cast<const uint4*>(
             reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim +
             256 * (int)rank);
@@ -1049,7 +1265,10 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c.bars[QT_FULL]);
+      if (lane == 0) {
+        mbar_arrive(&c.bars[QT_FULL]);
+        if (kF8) mbar_arrive(&c.bars[QS_FULL0 + (ordinal & 1)]);
+      }
     };
     auto correct = [&](uint32_t gc, bool first) -> bool {
       if (!wait_bar(c, P_FULL0 + (gc & 1), (gc >> 1) & 1)) return false;
@@ -1079,7 +1298,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       const WorkItem it = items[idx];
       const int nt = n_tiles_of(it);
       if (nt <= 0) continue;
-      if (n_item == 0) write_q(it);
+      if (n_item == 0) write_q(it, 0);
       for (int t = 0; t < nt; ++t, ++g) {
         if (!send(g, it.kv_end - (it.kv_begin + t * kTile))) goto done_epi;
         if (t > 0 && !correct(g - 1, t == 1)) goto done_epi;
@@ -1089,7 +1308,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       for (int nx = idx + 1; nx < item_end; ++nx) {
         const WorkItem itn = items[nx];
         if (n_tiles_of(itn) > 0) {
-          write_q(itn);
+          write_q(itn, n_item + 1);
           break;
         }
       }
@@ -1258,10 +1477,10 @@ bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int e
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kFp8, bool kSparse>
+template <bool kFp8, bool kSparse, bool kF8 = false>
 cudaError_t setup_one(int sm_count, int* n_pairs) {
-  using C = Cfg<kFp8, kSparse>;
-  auto kernel = decode_sm103_kernel<kFp8, kSparse>;
+  using C = Cfg<kFp8, kSparse, kF8>;
+  auto kernel = decode_sm103_kernel<kFp8, kSparse, kF8>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1285,10 +1504,10 @@ cudaError_t setup_one(int sm_count, int* n_pairs) {
 }
 
 // Launch as a programmatic dependent of the previous kernel in the stream.
-template <bool kFp8, bool kSparse>
+template <bool kFp8, bool kSparse, bool kF8 = false>
 cudaError_t launch_pdl(int grid, cudaStream_t stream, const Problem& p, const Layout& lay, char* ws,
                        const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c) {
-  using C = Cfg<kFp8, kSparse>;
+  using C = Cfg<kFp8, kSparse, kF8>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -1299,12 +1518,13 @@ cudaError_t launch_pdl(int grid, cudaStream_t stream, const Problem& p, const La
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kFp8, kSparse>, p, lay, ws, a, b, c);
+  return cudaLaunchKernelEx(&cfg, decode_sm103_kernel<kFp8, kSparse, kF8>, p, lay, ws, a, b, c);
 }
 
 }  // namespace
 
-cudaError_t decode_sm103_setup(int kv_dtype, int sparse, int sm_count, int* n_pairs) {
+cudaError_t decode_sm103_setup(int kv_dtype, int sparse, int f8_mma, int sm_count, int* n_pairs) {
+  if (kv_dtype == 1 && f8_mma && !sparse) return setup_one<false, false, true>(sm_count, n_pairs);
   if (kv_dtype == 1)
     return sparse ? setup_one<true, true>(sm_count, n_pairs)
                   : setup_one<true, false>(sm_count, n_pairs);
@@ -1319,12 +1539,25 @@ cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
   const uint64_t kv_rows = (uint64_t)p.num_pages * p.page_size;
   // sparse top-k gathers single rows (four per copy); otherwise pages are copied
   const uint32_t box_rows = p.sparse_k > 0 ? 1u : (uint32_t)p.page_size;
-  // (an e4m3 query is read with plain loads; its map is encoded but unused)
+  // (an e4m3 query, and any query on the FP8 MMA path, is read with plain
+  // loads; its map is encoded but unused)
   if (!(p.q_fp8 ? encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q_rows, 32,
                             kRows, CU_TENSOR_MAP_SWIZZLE_NONE)
                 : encode_2d(&tm_q_rope, p.query, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q_rows, 32,
                             kRows, CU_TENSOR_MAP_SWIZZLE_64B)))
     return cudaErrorInvalidValue;
+  if (p.f8_mma) {
+    // e4m3 rows straight into the ring for the FP8 MMAs: 128-dim latent chunks
+    // (128B swizzle) and the 32 RoPE dims (32B swizzle)
+    if (p.kv_dtype != 1 || p.sparse_k > 0 ||
+        !encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 128, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tm_kv_rope, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 32,
+                   box_rows, CU_TENSOR_MAP_SWIZZLE_32B))
+      return cudaErrorInvalidValue;
+    return launch_pdl<false, false, true>(lay.n_ctas, stream, p, lay, static_cast<char*>(ws),
+                                          tm_q_rope, tm_kv, tm_kv_rope);
+  }
   if (p.kv_dtype == 1) {
     // e4m3 bytes land row-major in the staging ring; the converter swizzles
     if (!encode_2d(&tm_kv, p.kv_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kv_rows, 64, box_rows,

@@ -364,3 +364,57 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 }  // namespace ptx
 }  // namespace mla
+
+namespace mla {
+namespace ptx {
+
+// ------------------------------------------------------------------ FP8 (kind::f8f6f4)
+constexpr uint32_t kSwizzle32B = 6;
+
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0) and
+// fp32 accumulation; the other fields as in idesc_f16.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// A in tensor memory: one row per lane, four 8-bit elements per 32-bit column
+// (element k in byte k mod 4 of column k / 4).
+__device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Two fp32 values -> two e4m3 codes (round to nearest even, saturating to
+// +-448), `a` in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
+  uint32_t r;
+  asm("{\n .reg .b16 h;\n cvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n cvt.u32.u16 %0, h;\n}"
+      : "=r"(r)
+      : "f"(a), "f"(b));
+  return r;
+}
+// Two e4m3 codes (low byte first) -> their exact fp32 values.
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t two_bytes, float& a, float& b) {
+  uint32_t h2;
+  asm("{\n .reg .b16 lo;\n mov.b32 {lo, _}, %1;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n}"
+      : "=r"(h2)
+      : "r"(two_bytes));
+  asm("{\n .reg .b16 x, y;\n mov.b32 {x, y}, %2;\n cvt.f32.f16 %0, x;\n cvt.f32.f16 %1, y;\n}"
+      : "=f"(a), "=f"(b)
+      : "r"(h2));
+}
+
+}  // namespace ptx
+}  // namespace mla

@@ -43,7 +43,7 @@ class DeviceCase:
 
 
 def to_device(w, *, return_lse=None, causal=None, workspace_fill=None, max_total_q=None,
-              plan_batch=None):
+              plan_batch=None, e4m3_widen=False):
     dev = torch.device("cuda", 0)
     if getattr(w, "q_dtype", "bf16") == "e4m3":
         q = torch.from_numpy(w.query).to(dev).view(torch.float8_e4m3fn)
@@ -65,7 +65,7 @@ def to_device(w, *, return_lse=None, causal=None, workspace_fill=None, max_total
                     packed=w.packed, max_total_q=max_total_q if max_total_q else tokens,
                     kv_dtype=w.kv_dtype, causal=cz, return_lse=ret,
                     q_dtype=getattr(w, "q_dtype", "bf16"), cp_world=w.cp_world,
-                    cp_rank=w.cp_rank, sparse_top_k=w.sparse_k)
+                    cp_rank=w.cp_rank, sparse_top_k=w.sparse_k, e4m3_widen=e4m3_widen)
     sp = torch.from_numpy(w.sparse_idx).to(dev) if w.sparse_idx is not None else None
     slg = None
     if w.cp_world > 1 and cz:

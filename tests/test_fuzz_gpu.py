@@ -3,6 +3,7 @@
 Each case draws one launch at random:
 - shape: head count, page size, batch, fixed or packed query lengths;
 - mask (causal or dense), cache and query dtypes, LSE or none, bmm1;
+- for an e4m3 cache, the FP8-MMA path or the exact widening path;
 - sparse top-k lists, with random padding, repeated and out-of-range entries;
 - a workspace filled with a random byte.
 
@@ -65,13 +66,15 @@ def draw(seed):
                     else:
                         idx[t, p_] = int(w.seq_lens[b]) + int(rng.integers(0, 5))
         w = dataclasses.replace(w, sparse_idx=idx)
-    return w, int(rng.integers(0, 256))
+    fill = int(rng.integers(0, 256))
+    widen = w.kv_dtype == "e4m3" and bool(rng.integers(2))
+    return w, fill, widen
 
 
 @pytest.mark.parametrize("seed", range(N_CASES))
 def test_random_configuration_matches_oracle(seed):
-    w, fill = draw(seed)
-    d = to_device(w, workspace_fill=fill)
+    w, fill, widen = draw(seed)
+    d = to_device(w, workspace_fill=fill, e4m3_widen=widen)
     run(w, d)
     out, lse = results(d)
     assert device_status(d) == 0, f"{w.name}: status {device_status(d)}"

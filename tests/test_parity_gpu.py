@@ -23,6 +23,7 @@ def full_parity(w, **kw):
     d = to_device(w, **kw)
     run(w, d)
     out, lse = results(d)
+    assert device_status(d) == 0
     ref_o, ref_l = oracle.run(w, causal=kw.get("causal"))
     H = w.num_heads
     rel = check(w.kv_dtype, out.reshape(-1, H, 512), ref_o, lse, ref_l if lse is not None else None,
@@ -44,14 +45,25 @@ def test_reduced_workload_full_parity(name):
     full_parity(REDUCED[name]())
 
 
-@pytest.mark.parametrize("name", ["deepseek_v3", "mtp", "ragged", "fp8_long", "sparse_topk"])
+@pytest.mark.parametrize("name", ["fp8_long", "fp8_long_e4m3q"])
+def test_reduced_e4m3_cache_widened_path(name):
+    """The e4m3 cache widened exactly to bf16 (the path asked for with
+    e4m3_widen; the default runs FP8 MMAs), with a bf16 and an e4m3 query."""
+    w = (REDUCED["fp8_long"]() if name == "fp8_long"
+         else mi.fp8_long(batch=3, lo=500, hi=1500, return_lse=True, q_dtype="e4m3"))
+    full_parity(w, e4m3_widen=True)
+
+
+@pytest.mark.parametrize("name", ["deepseek_v3", "mtp", "ragged", "fp8_long", "fp8_long_widened",
+                                  "sparse_topk"])
 def test_full_size_workload_sampled_parity(name):
     """The full-size workloads in the launch shapes the bench times (many-way
     lanes, long split items, every worker busy), checked on sampled pairs
     with their LSE (at long lengths |O| is small, so the LSE and the
     relative-L2 gate carry most of the check)."""
-    w = mi.WORKLOADS[name]()
-    d = to_device(w, return_lse=True)
+    widen = name == "fp8_long_widened"
+    w = mi.WORKLOADS["fp8_long" if widen else name]()
+    d = to_device(w, return_lse=True, e4m3_widen=widen)
     run(w, d)
     out, lse = results(d)
     sel = sample_pairs(w, 48, seed=1)
@@ -247,10 +259,12 @@ def test_host_side_errors():
 
 
 def test_e4m3_widening_is_exact_for_every_code():
-    """The kernel widens e4m3 KV to bf16 in shared memory.  With Q = 0 and a
-    single KV row, P = 1 exactly and O is that row's V, so every output
-    element must be the bf16 value of its e4m3 code, bit for bit, for all
-    254 non-NaN codes (subnormals included).  The sign of a zero does not
+    """Both e4m3 paths: widened to bf16 in shared memory, and read by the FP8
+    MMAs as they are (V MN-major from the 128-dim chunks).  With Q = 0 and a
+    single KV row, P = 1 exactly (on the FP8 path its hi part is 1 and its lo
+    part 0) and O is that row's V, so every output element must be the bf16
+    value of its e4m3 code, bit for bit, for all 254 non-NaN codes
+    (subnormals included), each at its own V dim.  The sign of a zero does not
     survive the fp32 accumulation of P V (1 * -0 + 0 * v = +0), so zeros are
     compared by value.  A NaN code would turn the scores NaN, so it cannot be
     read back this way."""
@@ -267,18 +281,20 @@ def test_e4m3_widening_is_exact_for_every_code():
     q = torch.zeros((1, H, 576), dtype=torch.bfloat16, device=dev)
     bt = torch.zeros((1, 1), dtype=torch.int32, device=dev)
     sl = torch.ones(1, dtype=torch.int32, device=dev)
-    plan = mla.Plan(batch=1, num_heads=H, max_seq_len_q=1, max_seq_len=1, page_size=64,
-                    max_pages_per_req=1, num_pages=1, packed=False, kv_dtype="e4m3")
-    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
-    out = torch.full((1, H, 512), float("nan"), dtype=torch.bfloat16, device=dev)
-    plan.run(q, kv_t, bt, sl, out, workspace=ws)
-    torch.cuda.synchronize()
-    want = torch.from_numpy(row[:512].copy()).view(torch.float8_e4m3fn).to(torch.bfloat16)
-    got = out.cpu()
-    nz = want != 0
-    for h in range(H):
-        assert torch.equal(got[0, h].float(), want.float()), h
-        assert torch.equal(got[0, h][nz].view(torch.int16), want[nz].view(torch.int16)), h
+    for widen in (True, False):
+        plan = mla.Plan(batch=1, num_heads=H, max_seq_len_q=1, max_seq_len=1, page_size=64,
+                        max_pages_per_req=1, num_pages=1, packed=False, kv_dtype="e4m3",
+                        e4m3_widen=widen)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+        out = torch.full((1, H, 512), float("nan"), dtype=torch.bfloat16, device=dev)
+        plan.run(q, kv_t, bt, sl, out, workspace=ws)
+        torch.cuda.synchronize()
+        want = torch.from_numpy(row[:512].copy()).view(torch.float8_e4m3fn).to(torch.bfloat16)
+        got = out.cpu()
+        nz = want != 0
+        for h in range(H):
+            assert torch.equal(got[0, h].float(), want.float()), (widen, h)
+            assert torch.equal(got[0, h][nz].view(torch.int16), want[nz].view(torch.int16)), (widen, h)
 
 
 def _index_encoded(w):
@@ -469,7 +485,8 @@ def test_zero_bmm1_gives_the_mean_of_the_visible_rows(name):
 ])
 def test_e4m3_query_full_parity(make):
     """e4m3 query (q_scale folded into bmm1), with bf16 and e4m3 caches: the
-    kernel widens Q exactly, so the cache's tolerance applies unchanged."""
+    kernel uses the codes exactly (widened for a bf16 cache, as they are on
+    the FP8 MMAs), so the cache's tolerance applies unchanged."""
     w = make()
     assert w.q_dtype == "e4m3"
     full_parity(w)
@@ -550,6 +567,7 @@ def test_wide_logits_full_parity(name, bmm1):
     full_parity(w)
 
 
+@pytest.mark.parametrize("widen", [False, True])
 @pytest.mark.parametrize("case", [
     dict(name="e4m3_ps32_h128_q2", num_heads=128, page_size=32, seq_lens=[40, 300, 129, 777],
          q_lens=[2] * 4, packed=False),
@@ -563,13 +581,14 @@ def test_wide_logits_full_parity(name, bmm1):
     dict(name="e4m3_dense_ragged_h64_ps32", num_heads=64, page_size=32, seq_lens=[33, 250, 5],
          q_lens=[2, 1, 4], packed=True, causal=False, max_seq_len_q=4),
 ])
-def test_e4m3_cache_page_sizes_packed_and_dense(case):
-    """The e4m3 cache's own staging path at page size 32, with packed ragged
-    queries and with the dense mask."""
+def test_e4m3_cache_page_sizes_packed_and_dense(case, widen):
+    """The e4m3 cache at page size 32, with packed ragged queries and with the
+    dense mask, on both paths (FP8 MMAs, and widening through the staging
+    ring)."""
     case = dict(case)
     name = case.pop("name")
     w = mi.build(name, 95, kv_dtype="e4m3", return_lse=True, **case)
-    full_parity(w)
+    full_parity(w, e4m3_widen=widen)
 
 
 def _dcp_case(world, make):
