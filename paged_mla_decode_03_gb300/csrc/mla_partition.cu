@@ -276,8 +276,10 @@ partition_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   __syncthreads();
   if (threadIdx.x == 0) sh.carry_ll = 0;
   __syncthreads();
-  // only threads holding cost add (contended 64-bit shared atomics are slow)
-  if (W_total != 0)
+  // summed within each warp first, then one add per warp: contended 64-bit
+  // shared atomics serialise (one per request cost a few microseconds at B = 64)
+  for (int o = 16; o > 0; o >>= 1) W_total += __shfl_xor_sync(0xffffffffu, W_total, o);
+  if ((threadIdx.x & 31) == 0 && W_total != 0)
     atomicAdd(reinterpret_cast<unsigned long long*>(&sh.carry_ll), (unsigned long long)W_total);
   __syncthreads();
   W_total = sh.carry_ll;
