@@ -568,6 +568,38 @@ def test_wide_logits_full_parity(name, bmm1):
 
 
 @pytest.mark.parametrize("widen", [False, True])
+def test_e4m3_cache_query_rows_of_any_magnitude(widen):
+    """The FP8 path scales each bf16 query row by a power of two before it
+    splits it into e4m3 parts.  Rows multiplied by 2^-6 .. 2^3 (exact in bf16,
+    so the oracle sees the same values) and an all-zero row per token (factor
+    1 on the device, a uniform softmax) must all match the oracle."""
+    w = REDUCED["fp8_long"]()
+    rows = w.query_rows()  # [tokens, H, 576] bf16 bits
+    q32 = (rows.astype(np.uint32) << 16).view(np.float32)
+    rng = np.random.default_rng(5)
+    e = rng.integers(-6, 4, size=q32.shape[:2]).astype(np.float32)
+    q32 = q32 * np.exp2(e)[:, :, None]
+    q32[:, 0, :] = 0.0
+    bits = (q32.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), q32)  # exact
+    w = dataclasses.replace(w, query=bits.reshape(w.query.shape), return_lse=True)
+    full_parity(w, e4m3_widen=widen)
+
+
+@pytest.mark.parametrize("widen", [False, True])
+@pytest.mark.parametrize("factor", [10.0, 30.0])
+def test_wide_logits_e4m3_cache(factor, widen):
+    """The e4m3 cache at wide logits (bmm1 * |s| up to ~100-150): on the FP8
+    path the bf16 query enters the MMAs as two e4m3 parts, which must keep the
+    scores, and so the LSE, at the bf16 query's precision; the widened path
+    is exact.  Same bounds as the bf16 wide-logit cases."""
+    w = REDUCED["fp8_long"]()
+    w.bmm1_scale = mi.f32(w.bmm1_scale * factor)
+    w.return_lse = True
+    full_parity(w, e4m3_widen=widen)
+
+
+@pytest.mark.parametrize("widen", [False, True])
 @pytest.mark.parametrize("case", [
     dict(name="e4m3_ps32_h128_q2", num_heads=128, page_size=32, seq_lens=[40, 300, 129, 777],
          q_lens=[2] * 4, packed=False),
