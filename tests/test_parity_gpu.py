@@ -686,19 +686,24 @@ def test_dcp_causal_plan_refuses_the_plain_entry_point():
     assert e.value.status == -1
 
 
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "e4m3_widen"])
 @pytest.mark.parametrize("H,B,qlo,qhi,lhi", [(128, 512, 24, 48, 2048), (16, 4096, 1, 8, 300)])
-def test_prefill_scale_packed_launch(H, B, qlo, qhi, lhi):
+def test_prefill_scale_packed_launch(H, B, qlo, qhi, lhi, kv):
     """Prefill through the decode path (the FlashInfer issue "Support
     cum_seq_lens_q in trtllm_batch_decode_with_kv_cache_mla", point 1): more
     than 16k packed query tokens.  At this size the partitioner's per-group
-    scratch no longer fits its shared memory and lives in the workspace."""
+    scratch no longer fits its shared memory and lives in the workspace, and
+    every worker runs hundreds of items back to back (the e4m3 cases take the
+    FP8 path's per-item query scales through both of their slots many times)."""
     rng = np.random.default_rng(86 + H)
     q = rng.integers(qlo, qhi, size=B, endpoint=True).astype(np.int32)
     L = rng.integers(q + 1, lhi, endpoint=True).astype(np.int32)
-    w = mi.build(f"prefill_h{H}", 86 + H, num_heads=H, page_size=64 if H == 128 else 32,
-                 seq_lens=L, q_lens=q, packed=True, return_lse=True, max_seq_len_q=int(qhi))
+    kv_dtype = "bf16" if kv == "bf16" else "e4m3"
+    w = mi.build(f"prefill_h{H}_{kv}", 86 + H, num_heads=H, page_size=64 if H == 128 else 32,
+                 seq_lens=L, q_lens=q, packed=True, return_lse=True, max_seq_len_q=int(qhi),
+                 kv_dtype=kv_dtype)
     assert w.total_q >= 16384
-    d = to_device(w)
+    d = to_device(w, e4m3_widen=kv == "e4m3_widen")
     assert d.plan.workspace_bytes > 0
     run(w, d)
     out, lse = results(d)
@@ -706,8 +711,8 @@ def test_prefill_scale_packed_launch(H, B, qlo, qhi, lhi):
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     sel = sample_pairs(w, 96, seed=3)
     ref_o, ref_l = oracle.run(w, sel=sel)
-    check("bf16", out[sel[:, 0], sel[:, 1]], ref_o, lse[sel[:, 0], sel[:, 1]], ref_l,
-          what=f"prefill H={H}")
+    check(kv_dtype, out[sel[:, 0], sel[:, 1]], ref_o, lse[sel[:, 0], sel[:, 1]], ref_l,
+          what=f"prefill H={H} {kv}")
 
 
 def test_prefill_scale_repeats_are_finite_and_bitwise_equal():
