@@ -40,9 +40,13 @@
 // group of an item's last tile merges the two.  Warps 10-13 are the
 // partial-score senders (the peer-owned lanes), O correction, epilogue and
 // the Q latent load into TMEM (thread = query row = TMEM lane).
-// With an e4m3 cache eight more warps (14-21) widen each staged e4m3 tile to
-// bf16 in shared memory (exact; the k_scale lives in bmm1/bmm2), and the
-// bf16 ring is 3 deep beside a 2-deep e4m3 staging ring.
+// An e4m3 cache runs by default on FP8 MMAs (kind::f8f6f4, a separate
+// instantiation): the e4m3 tiles go from the TMA straight into an 8-deep ring
+// in the operand layouts, the query enters as e4m3 (a bf16 row as two parts
+// under a power-of-two row scale the softmax folds into bmm1), and so does P
+// (two parts).  Widening on request: eight more warps (14-21) widen each
+// staged e4m3 tile to bf16 in shared memory (exact; the k_scale lives in
+// bmm1/bmm2), and the bf16 ring is 3 deep beside a 2-deep e4m3 staging ring.
 // Under sparse top-k selection (a separate instantiation, two warps more) a
 // work item is one token's H query rows and its KV tiles are 64 entries of
 // the token's position list: warp 0 and the two extra warps gather the listed
