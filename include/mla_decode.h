@@ -243,9 +243,12 @@ size_t mla_decode_host_staging_bytes(const mla_plan_t *plan, int64_t total_q);
 /*
  * One decode step whose per-step inputs and results live in HOST memory: the
  * query and the metadata are copied host-to-device into `staging`, the decode
- * runs as mla_decode_run, and out (and lse) are copied device-to-host, all
- * enqueued on `stream` with one cudaMemcpyAsync per buffer.  The KV cache
- * stays in device memory (the persistent state of a serving loop).
+ * runs as mla_decode_run, and out (and lse) are copied device-to-host, with
+ * one cudaMemcpyAsync per buffer.  Everything is ordered on `stream` except
+ * the query's copy, which runs on a stream the plan owns so that it overlaps
+ * the partitioner: it starts after `stream`'s earlier work and the decode
+ * waits for it (event fork and join, also under stream capture).  The KV
+ * cache stays in device memory (the persistent state of a serving loop).
  *
  * This entry point is the exception to the device-pointers rule above: it
  * exists for callers that hold the step's query and metadata on the host.

@@ -31,6 +31,12 @@ struct mla_plan_s {
   mla::Layout lay;
   int sm_count;
   int combine_grid;
+  // mla_decode_run_host copies the query on this stream while the
+  // partitioner runs (created with the plan, on its device)
+  cudaStream_t side_stream = nullptr;
+  ~mla_plan_s() {
+    if (side_stream) cudaStreamDestroy(side_stream);
+  }
 };
 
 namespace {
@@ -139,11 +145,20 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   if (e == cudaSuccess)
     e = mla::decode_sm103_setup(p.kv_dtype, p.sparse_top_k > 0, uses_f8_mma(p), sms, &n_pairs);
   if (e == cudaSuccess) e = mla::partition_setup();
+  cudaStream_t side = nullptr;
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking);
   cudaSetDevice(prev);
-  if (e != cudaSuccess || sms <= 0) return MLA_ERR_CUDA;
+  if (e != cudaSuccess || sms <= 0) {
+    if (side) cudaStreamDestroy(side);
+    return MLA_ERR_CUDA;
+  }
 
   mla_plan_s* pl = new (std::nothrow) mla_plan_s;
-  if (!pl) return MLA_ERR_INVALID_ARG;
+  if (!pl) {
+    cudaStreamDestroy(side);
+    return MLA_ERR_INVALID_ARG;
+  }
+  pl->side_stream = side;
   pl->prm = p;
   pl->sm_count = sms;
   // one work item = 128 query rows on one CTA pair; under sparse top-k one
@@ -207,7 +222,7 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
              const float* bmm2_dev, void* out, float* lse, void* workspace,
              size_t workspace_bytes, void* stream, void* event_before_decode,
              void* event_after_decode, const int32_t* seq_lens_global = nullptr,
-             const int32_t* sparse_idx = nullptr) {
+             const int32_t* sparse_idx = nullptr, cudaEvent_t join_before_decode = nullptr) {
   if (!plan) return MLA_ERR_INVALID_ARG;
   const mla_decode_params& prm = plan->prm;
   // a sparse plan needs its position lists; no other plan takes them
@@ -285,6 +300,9 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
     if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
   }
   if (mla::launch_partition(p, plan->lay, workspace, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // work enqueued elsewhere that the decode needs (the host entry's query copy)
+  if (join_before_decode && cudaStreamWaitEvent(s, join_before_decode, 0) != cudaSuccess)
+    return MLA_ERR_CUDA;
   if (event_before_decode &&
       cudaEventRecordWithFlags(static_cast<cudaEvent_t>(event_before_decode), s, ev_flags) !=
           cudaSuccess)
@@ -420,17 +438,35 @@ int mla_decode_run_host(const mla_plan_t* plan, const void* h_query, const void*
   void* d_out = base + st.out;
   float* d_lse = prm.return_lse ? reinterpret_cast<float*>(base + st.lse) : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // one copy per buffer, in stream order with the decode
-  auto h2d = [&](void* dst, const void* src, size_t n) {
-    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  // One copy per buffer.  The metadata goes first on the caller's stream (the
+  // partitioner reads nothing else); the query goes on the plan's side stream,
+  // forked after the caller's earlier work (which may still read the staging
+  // buffer) and joined before the decode, so it overlaps the partitioner.
+  auto h2d = [&](void* dst, const void* src, size_t n, cudaStream_t on) {
+    return n == 0 || cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, on) == cudaSuccess;
   };
-  if (!h2d(d_query, h_query, st.query_bytes) || !h2d(d_bt, h_block_tables, st.block_tables_bytes) ||
-      !h2d(d_sl, h_seq_lens, st.seq_lens_bytes) ||
-      (d_qo && !h2d(d_qo, h_qo_indptr, st.qo_indptr_bytes)))
+  if (!h2d(d_bt, h_block_tables, st.block_tables_bytes, s) ||
+      !h2d(d_sl, h_seq_lens, st.seq_lens_bytes, s) ||
+      (d_qo && !h2d(d_qo, h_qo_indptr, st.qo_indptr_bytes, s)))
     return MLA_ERR_CUDA;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  auto release = [&]() {  // pending events are released once their work completes
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+  };
+  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventRecord(fork, s) != cudaSuccess ||
+      cudaStreamWaitEvent(plan->side_stream, fork, 0) != cudaSuccess ||
+      !h2d(d_query, h_query, st.query_bytes, plan->side_stream) ||
+      cudaEventRecord(join, plan->side_stream) != cudaSuccess) {
+    release();
+    return MLA_ERR_CUDA;
+  }
   const int rc = run_impl(plan, d_query, kv_cache, d_bt, d_sl, d_qo, total_q, bmm1_scale,
                           bmm2_scale, nullptr, nullptr, d_out, d_lse, workspace, workspace_bytes,
-                          stream, nullptr, nullptr);
+                          stream, nullptr, nullptr, nullptr, nullptr, join);
+  release();
   if (rc != MLA_OK) return rc;
   if (st.out_bytes &&
       cudaMemcpyAsync(h_out, d_out, st.out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
@@ -441,7 +477,15 @@ int mla_decode_run_host(const mla_plan_t* plan, const void* h_query, const void*
   return MLA_OK;
 }
 
-void mla_decode_destroy(mla_plan_t* plan) { delete plan; }
+void mla_decode_destroy(mla_plan_t* plan) {
+  if (!plan) return;
+  // the plan's side stream belongs to its device
+  int prev = -1;
+  const bool swap = cudaGetDevice(&prev) == cudaSuccess && prev != plan->prm.device &&
+                    cudaSetDevice(plan->prm.device) == cudaSuccess;
+  delete plan;
+  if (swap) cudaSetDevice(prev);
+}
 
 size_t mla_decode_workspace_size(const mla_plan_t* plan) { return plan ? plan->lay.total : 0; }
 

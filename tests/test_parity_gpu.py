@@ -411,6 +411,34 @@ def test_host_buffer_entry_equals_device_entry(name):
     want = d.out.cpu().view(torch.int16).numpy()
     assert np.array_equal(got.reshape(want.shape), want)
     assert np.array_equal(h_lse.numpy(), d.lse.cpu().numpy())
+    want_lse = d.lse.cpu().numpy()
+
+    # Two steps back to back on one stream with different queries: the library
+    # copies a step's query on its own side stream, which must wait for the
+    # previous step's decode (it reads the same staging buffer).
+    q2 = d.query * 0.5  # exact in bf16
+    d.query.copy_(q2)
+    run(w, d)
+    torch.cuda.synchronize()
+    want2 = d.out.cpu().view(torch.int16).numpy()
+    want2_lse = d.lse.cpu().numpy()
+    h_q2 = q2.cpu().pin_memory()
+    h_out2 = torch.full_like(h_out, float("nan")).pin_memory()
+    h_lse2 = torch.full_like(h_lse, float("nan")).pin_memory()
+    h_out.fill_(float("nan"))
+    for _ in range(3):
+        d.plan.run_host(h_q, d.kv_cache, h_bt, h_sl, h_out, staging=staging, workspace=d.workspace,
+                        h_qo_indptr=h_qo, total_q=total_q, h_lse=h_lse, bmm1_scale=w.bmm1_scale,
+                        bmm2_scale=w.bmm2_scale, stream=stream)
+        d.plan.run_host(h_q2, d.kv_cache, h_bt, h_sl, h_out2, staging=staging,
+                        workspace=d.workspace, h_qo_indptr=h_qo, total_q=total_q, h_lse=h_lse2,
+                        bmm1_scale=w.bmm1_scale, bmm2_scale=w.bmm2_scale, stream=stream)
+    stream.synchronize()
+    assert device_status(d) == 0
+    assert np.array_equal(h_out.view(torch.int16).numpy().reshape(want.shape), want)
+    assert np.array_equal(h_lse.numpy(), want_lse)
+    assert np.array_equal(h_out2.view(torch.int16).numpy().reshape(want2.shape), want2)
+    assert np.array_equal(h_lse2.numpy(), want2_lse)
 
 
 def test_device_scales_equal_host_scales_and_follow_graph_replays():
