@@ -288,10 +288,11 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
 // TMEM columns at `tmem_q` (four codes a column; A operand of the ts QK MMAs)
 // and its RoPE dims [512 + 32 rank, +32) into the 32B-swizzled smem tile at
 // `q_rope`.  An e4m3 query is copied as it is (one part).  A bf16 query row
-// is scaled by 2^k, the largest power of two with max|q| 2^k <= 448 (taken
-// over all 576 dims, so both CTAs of the pair agree), and split into two
-// parts, hi = e4m3(x) at columns [0, 64) and lo = e4m3(x - hi) at [64, 128)
-// (RoPE: the second 4 KB of `q_rope`).  hi + lo equals x exactly wherever
+// is scaled by 2^k, the largest power of two with max|q| 2^k <= 448 over this
+// CTA's 288 dims (each CTA of the pair has its own k; the partial scores are
+// brought back to true units on each side before they are added), and split
+// into two parts, hi = e4m3(x) at columns [0, 64) and lo = e4m3(x - hi) at
+// [64, 128) (RoPE: the second 4 KB of `q_rope`).  hi + lo equals x exactly wherever
 // |x| >= 2^-2 (x is a bf16 value times a power of two, and x - hi has at most
 // four significant bits at or above 2^-9) and to within 2^-10 below that.
 // Returns 2^-k, the factor the row's scores need.  Rows past the query
@@ -327,15 +328,23 @@ __device__ __noinline__ float load_q_row_split_e4m3(const Problem& p, long long 
   }
   const uint4* src = reinterpret_cast<const uint4*>(
       reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim);
+  // this CTA's 36 16-byte units: latent [32 r, 32 r + 32), RoPE [64 + 4 r, +4);
+  // loaded in three batches of 12 so that each batch is one memory round trip
+  auto unit = [&](int i) { return i < 32 ? 32 * (int)rank + i : 64 + 4 * (int)rank + (i - 32); };
   float amax = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < kQkDim / 8; ++i) {
-    const uint4 x = in ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
-                               fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+  for (int b0 = 0; b0 < 36; b0 += 12) {
+    uint4 x[12];
+#pragma unroll
+    for (int u = 0; u < 12; ++u) x[u] = in ? __ldg(src + unit(b0 + u)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 12; ++u) {
+      const uint32_t w4[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
+                                 fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
+    }
   }
   int k = 0;
   if (amax > 0.f && amax <= 3.4028235e38f) {
@@ -948,9 +957,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       // this group's share of the row sum (this thread's 32 columns), relative
       // to the reference m_grp of the group's latest tile of the item
       float l_part = 0.f, m_grp = -INFINITY;
-      // bmm1 * log2(e), times the row's query scale 2^-k on the FP8 path (the
-      // MMAs saw the query times 2^k), read at the group's first tile of the item
-      float scale = bmm1_log2e;
+      // FP8 path: this CTA's partial scores are 2^k times the true ones (the
+      // MMAs saw its half of the query times 2^k); the factor 2^-k of the
+      // item's row is read at the group's first tile of the item
+      const float scale = bmm1_log2e;
+      float qs_own = 1.f;
       bool have_scale = !kF8;
       for (int t = 0; t < nt; ++t, ++g) {
         if ((int)(g & 1) != grp) continue;
@@ -958,7 +969,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         float sv[32];
         if (!have_scale) {
           if (!wait_bar(c, QS_FULL0 + (n_item & 1), (n_item >> 1) & 1)) goto done_softmax;
-          scale = bmm1_log2e * qscale[(n_item & 1) * kRows + q];
+          qs_own = qscale[(n_item & 1) * kRows + q];
           have_scale = true;
         }
         if (!wait_bar(c, S_FULL0 + sb, (g >> 1) & 1)) goto done_softmax;
@@ -968,7 +979,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           tmem_ld_16x32bx2_x32(tmem + lane_addr + TM_S + 64 * sb, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(v[j]) * qs_own;  // exact: 2^-k
         }
         tc_fence_before();
         __syncwarp();
@@ -1204,6 +1215,8 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     int n_item = 0;
     // `valid`: KV rows of the tile inside the item's range; the others may hold
     // stale shared memory (an unloaded page) and are masked by the softmax
+    // FP8 path: per-row factors 2^-k of the query halves, by item parity
+    float* qscale = reinterpret_cast<float*>(sm + OFF_QSCALE);
     auto send = [&](uint32_t gs, int valid) -> bool {
       const int sb = gs & 1;
       if (!wait_bar(c, S_FULL0 + sb, (gs >> 1) & 1)) return false;
@@ -1215,7 +1228,14 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.bars[S_FREE0 + sb]);
       // the scores go over unrounded (fp32): the logits' error stays that of
-      // the MMA's fp32 accumulation whatever the size of bmm1 * |S|
+      // the MMA's fp32 accumulation whatever the size of bmm1 * |S|.  FP8
+      // path: in true units, i.e. times this CTA's factor 2^-k of the row
+      // (written by this warp's lane of that row with the item's query)
+      if (kF8) {
+        const float qs = qscale[(n_item & 1) * kRows + 32 * sp + 16 * (int)peer + (lane & 15)];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * qs);
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (32 * hh + j >= valid) v[j] = 0u;
@@ -1236,7 +1256,6 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     const long long q_rows = p.total_q * H;
     const float bmm2 = run_bmm2(p);
     // `ordinal`: the item's place among this worker's items (its scale slot)
-    float* qscale = reinterpret_cast<float*>(sm + OFF_QSCALE);
     auto write_q = [&](const WorkItem& it, int ordinal) {
       const long long qrow = (long long)it.q_start * H + (long long)it.g * R + q;
       const bool in = qrow < q_rows;
