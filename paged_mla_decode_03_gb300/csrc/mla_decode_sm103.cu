@@ -116,7 +116,10 @@ constexpr uint32_t OFF_VMASK = OFF_ABORT + 16;
 constexpr int kGatherWarps = 3;  // sparse top-k: warps that gather KV rows
 // float [2][128]: per-row query scale 2^-k of the FP8 path, by item parity
 constexpr uint32_t OFF_QSCALE = OFF_VMASK + 8 * kGatherWarps * 8;
-constexpr uint32_t OFF_KV = (OFF_QSCALE + 2 * kRows * 4 + 1023) / 1024 * 1024;
+// float [128]: an item's final running max of the owned rows (log2 units),
+// beside lrow, for the epilogue's split-chunk LSE
+constexpr uint32_t OFF_MROW = OFF_QSCALE + 2 * kRows * 4;
+constexpr uint32_t OFF_KV = (OFF_MROW + kRows * 4 + 1023) / 1024 * 1024;
 
 // bf16 cache: a 4-stage ring.  e4m3 cache widened to bf16 (kFp8): 3 bf16
 // stages and a 2-deep e4m3 staging ring in the fourth stage's space.  e4m3
@@ -594,6 +597,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_TMEM);
   float* fac = reinterpret_cast<float*>(sm + OFF_FAC);
   float* lrow = reinterpret_cast<float*>(sm + OFF_LROW);
+  float* mrow = reinterpret_cast<float*>(sm + OFF_MROW);
   volatile int* flags = reinterpret_cast<volatile int*>(sm + OFF_FLAG);
 
   if (tid == 0) {
@@ -1160,16 +1164,11 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
           if (n_item > 0 && !wait_bar_cluster(c, LROW_FREE, (n_item - 1) & 1)) goto done_softmax;
           if (hh == 0) {
             lrow[q] = l_row;
+            mrow[q] = m_new;  // a split chunk's LSE is written by the epilogue warps
             st_async_b32(lrow_peer + 4u * q, __float_as_uint(l_row), pfull_peer0 + 8u * sb);
-            if (row_ok) {
+            if (row_ok && it.slot < 0 && p.return_lse) {
               const float lse = l_row > 0.f ? (m_new + log2f(l_row)) * kLn2 : -INFINITY;
-              const size_t grow = (size_t)it.q_start * H + row0 + q;
-              if (it.slot < 0) {
-                if (p.return_lse) p.lse[grow] = lse;
-              } else {
-                part_lse[(size_t)it.slot * R + q] = lse;
-                __threadfence();  // visible GPU-wide before the epilogue counts the chunk
-              }
+              p.lse[(size_t)it.q_start * H + row0 + q] = lse;
             }
           }
         }
@@ -1344,13 +1343,18 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
         const int row0 = it.g * R;
         const bool row_ok = q < min(R, rows_total - row0);
         const float l = lrow[q];
+        const float m = mrow[q];  // meaningful for the rows this CTA owns
         __syncwarp();
-        if (lane == 0) {  // both CTAs' softmax may overwrite l for the next item
+        if (lane == 0) {  // both CTAs' softmax may overwrite l (and m) for the next item
           mbar_arrive(&c.bars[LROW_FREE]);
           mbar_arrive_cluster_relaxed(lfree_peer);
         }
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const size_t grow = (size_t)it.q_start * H + row0 + q;
+        // a split chunk's natural-log LSE of the rows this CTA owns (lane q is
+        // owned by CTA (q / 16) mod 2); made visible with the partial O below
+        if (it.slot >= 0 && row_ok && ((q >> 4) & 1) == (int)rank)
+          part_lse[(size_t)it.slot * R + q] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll 1
         for (int c16 = 0; c16 < 16; ++c16) {
           uint32_t x[16];
