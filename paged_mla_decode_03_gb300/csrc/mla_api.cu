@@ -97,7 +97,7 @@ int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int row
   lay->scratch_bytes = req_bytes + grp_bytes;
   lay->scratch_in_smem = lay->scratch_bytes <= kPartitionSmemMax ? 1 : 0;
   lay->part_o = off;
-  off = align_up(off + sizeof(float) * R * kVDim * (size_t)lay->max_partials, 256);
+  off = align_up(off + kPartBytesPerRow * R * (size_t)lay->max_partials, 256);
   lay->part_lse = off;
   off = align_up(off + sizeof(float) * R * (size_t)lay->max_partials, 256);
   lay->comb_done = off;

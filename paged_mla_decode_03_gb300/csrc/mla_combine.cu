@@ -59,7 +59,7 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   const int* done = reinterpret_cast<const int*>(ws + lay.comb_done);
   const int* hdr = reinterpret_cast<const int*>(ws);
   const CombineItem* comb = reinterpret_cast<const CombineItem*>(ws + lay.combine);
-  const float* part_o = reinterpret_cast<const float*>(ws + lay.part_o);
+  const uint4* part_o = reinterpret_cast<const uint4*>(ws + lay.part_o);  // see part_unit
   const float* part_lse = reinterpret_cast<const float*>(ws + lay.part_lse);
   const int n_combine = hdr[kHdrNumCombine];
   const int H = p.num_heads;
@@ -91,10 +91,21 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
           l[u] = -INFINITY;
           if (k0 + u < c.n_chunks) {
             const size_t slot = (size_t)(c.first_slot + (k0 + u) * c.stride);
-            const float4* src =
-                reinterpret_cast<const float4*>(part_o + (slot * R + r) * kVDim) + 4 * t;
+            if (kPartialBf16) {
+              const uint4 a = part_o[part_unit(slot, R, t, 0, r)];
+              const uint4 b = part_o[part_unit(slot, R, t, 1, r)];
+              const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int v = 0; v < 4; ++v) x[u][v] = src[v];
+              for (int v = 0; v < 4; ++v)  // bf16 pairs, low half first
+                x[u][v] = make_float4(__uint_as_float(w[2 * v] << 16),
+                                      __uint_as_float(w[2 * v] & 0xFFFF0000u),
+                                      __uint_as_float(w[2 * v + 1] << 16),
+                                      __uint_as_float(w[2 * v + 1] & 0xFFFF0000u));
+            } else {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                x[u][v] = reinterpret_cast<const float4*>(part_o)[part_unit(slot, R, t, v, r)];
+            }
             l[u] = part_lse[slot * R + r];
           } else {
 #pragma unroll

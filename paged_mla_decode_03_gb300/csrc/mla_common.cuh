@@ -109,7 +109,7 @@ struct Layout {
   size_t group_scratch;  // partitioner scratch per row group / item
   size_t scratch_bytes;  // bytes of the two scratch areas
   int scratch_in_smem;   // 1: the partitioner keeps its scratch in shared memory
-  size_t part_o;         // float[max_partials][rows_per_group][512]
+  size_t part_o;         // split partials of O, see part_unit
   size_t part_lse;       // float[max_partials][rows_per_group]
   size_t comb_done;      // int[max_combine]: CTAs that finished a chunk of each split group
   size_t total;
@@ -120,5 +120,17 @@ struct Layout {
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Split partials of O (normalised by their own softmax sum): bf16, or fp32
+// when kPartialBf16 is false.  A slot holds R rows x 512 dims as 32 chunks of
+// 16 dims; chunk c of row q is kPartUnits 16-byte units, stored unit-major
+// over the rows, [slot][c][unit][row], so the epilogue's threads (one row
+// each) write consecutive 16-byte units.
+constexpr bool kPartialBf16 = true;
+constexpr int kPartUnits = kPartialBf16 ? 2 : 4;  // 16-byte units of a 16-dim chunk
+constexpr size_t kPartBytesPerRow = 32 * kPartUnits * 16;
+__host__ __device__ inline size_t part_unit(size_t slot, int R, int c, int u, int q) {
+  return ((slot * 32 + (size_t)c) * kPartUnits + (size_t)u) * (size_t)R + (size_t)q;
+}
 
 }  // namespace mla

@@ -585,7 +585,7 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
   int* hdr = reinterpret_cast<int*>(ws);
   const WorkItem* items = reinterpret_cast<const WorkItem*>(ws + lay.items);
   const int* worker_begin = reinterpret_cast<const int*>(ws + lay.worker_ranges);
-  float* part_o = reinterpret_cast<float*>(ws + lay.part_o);
+  uint4* part_o = reinterpret_cast<uint4*>(ws + lay.part_o);  // see part_unit
   float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   int* comb_done = reinterpret_cast<int*>(ws + lay.comb_done);
 
@@ -1373,11 +1373,23 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
             dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
             dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
           } else {
-            float4* dst = reinterpret_cast<float4*>(part_o + ((size_t)it.slot * R + q) * kVDim + vd);
+            // this row's chunk of the split partial (consecutive rows store
+            // consecutive 16-byte units: coalesced)
+            const int cidx = 16 * (int)rank + c16;
+            if (kPartialBf16) {
+              uint32_t o[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              dst[k] = make_float4(__uint_as_float(x[4 * k]) * inv, __uint_as_float(x[4 * k + 1]) * inv,
-                                   __uint_as_float(x[4 * k + 2]) * inv, __uint_as_float(x[4 * k + 3]) * inv);
+              for (int k = 0; k < 8; ++k)
+                o[k] = pack_bf16(__uint_as_float(x[2 * k]) * inv, __uint_as_float(x[2 * k + 1]) * inv);
+              part_o[part_unit(it.slot, R, cidx, 0, q)] = make_uint4(o[0], o[1], o[2], o[3]);
+              part_o[part_unit(it.slot, R, cidx, 1, q)] = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                reinterpret_cast<float4*>(part_o)[part_unit(it.slot, R, cidx, k, q)] =
+                    make_float4(__uint_as_float(x[4 * k]) * inv, __uint_as_float(x[4 * k + 1]) * inv,
+                                __uint_as_float(x[4 * k + 2]) * inv, __uint_as_float(x[4 * k + 3]) * inv);
+            }
           }
         }
       }

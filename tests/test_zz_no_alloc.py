@@ -65,8 +65,8 @@ def test_static_workspace_matches_caller_workspace_twice(make):
 
 def test_static_workspace_rejects_plans_that_do_not_fit():
     # A packed plan with a huge total_q bound needs more scratch than the array holds.
-    plan = mla.Plan(batch=4096, num_heads=128, max_seq_len_q=64, max_seq_len=4096, page_size=64,
-                    max_pages_per_req=64, num_pages=16, packed=True, max_total_q=1 << 20)
+    plan = mla.Plan(batch=16384, num_heads=128, max_seq_len_q=64, max_seq_len=4096, page_size=64,
+                    max_pages_per_req=64, num_pages=16, packed=True, max_total_q=1 << 21)
     assert plan.workspace_bytes > mla.MLA_STATIC_WORKSPACE_BYTES
     rc = _entry()(plan.handle, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 16, 1.0, 1.0, 1 << 20,
                   None, torch.cuda.current_stream().cuda_stream)
