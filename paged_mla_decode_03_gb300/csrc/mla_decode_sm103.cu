@@ -286,6 +286,16 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
   fence_proxy_async_smem();  // read by the RoPE MMAs
 }
 
+// The lines of a bf16 query row that the CTA of cluster rank `rank` reads (its
+// latent half [256 rank, +256): bytes [512 rank, +512); its RoPE half: inside
+// bytes [1024, 1152)) are brought into L2.  A row is 1152 bytes, nine lines.
+__device__ __forceinline__ void prefetch_q_row_bf16(const Problem& p, long long qrow, uint32_t rank) {
+  const unsigned char* row = reinterpret_cast<const unsigned char*>(p.query) + qrow * (2 * kQkDim);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) prefetch_l2(row + 512 * rank + 128 * k);
+  prefetch_l2(row + 1024);
+}
+
 // Row `q` of a work item's query for the FP8 MMAs, for the CTA of cluster rank
 // `rank`: its latent dims [256 rank, 256 rank + 256) as e4m3 codes into the
 // TMEM columns at `tmem_q` (four codes a column; A operand of the ts QK MMAs)
@@ -331,24 +341,29 @@ __device__ __noinline__ float load_q_row_split_e4m3(const Problem& p, long long 
   }
   const uint4* src = reinterpret_cast<const uint4*>(
       reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim);
-  // this CTA's 36 16-byte units: latent [32 r, 32 r + 32), RoPE [64 + 4 r, +4);
-  // loaded in three batches of 12 so that each batch is one memory round trip
+  // every line first (the batches below then wait for one DRAM round trip,
+  // not one each; the caller may have prefetched them already)
+  if (in) prefetch_q_row_bf16(p, qrow, rank);
+  // this CTA's 36 16-byte units: latent [32 r, 32 r + 32), RoPE [64 + 4 r, +4),
+  // in two batches of 18.  The largest magnitude is taken on the bf16 bit
+  // patterns with the sign cleared (their integer order is their magnitude
+  // order), two values an instruction.  This runs once per item from a cold
+  // instruction cache, so the code is kept short: loops over batches and
+  // halves are not unrolled.
   auto unit = [&](int i) { return i < 32 ? 32 * (int)rank + i : 64 + 4 * (int)rank + (i - 32); };
-  float amax = 0.f;
+  uint32_t mbits = 0;
+#pragma unroll 1
+  for (int b0 = 0; b0 < 36; b0 += 18) {
+    uint4 x[18];
 #pragma unroll
-  for (int b0 = 0; b0 < 36; b0 += 12) {
-    uint4 x[12];
+    for (int u = 0; u < 18; ++u) x[u] = in ? __ldg(src + unit(b0 + u)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int u = 0; u < 12; ++u) x[u] = in ? __ldg(src + unit(b0 + u)) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < 12; ++u) {
-      const uint32_t w4[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
-                                 fabsf(__uint_as_float(w4[e] & 0xFFFF0000u))));
-    }
+    for (int u = 0; u < 18; ++u)
+      mbits = __vmaxu2(mbits, __vmaxu2(__vmaxu2(x[u].x & 0x7FFF7FFFu, x[u].y & 0x7FFF7FFFu),
+                                       __vmaxu2(x[u].z & 0x7FFF7FFFu, x[u].w & 0x7FFF7FFFu)));
   }
+  // a NaN or infinite element fails the range check below, hence k = 0
+  const float amax = __uint_as_float(max(mbits & 0xFFFFu, mbits >> 16) << 16);
   int k = 0;
   if (amax > 0.f && amax <= 3.4028235e38f) {
     const uint32_t ab = __float_as_uint(amax);
@@ -374,27 +389,28 @@ __device__ __noinline__ float load_q_row_split_e4m3(const Problem& p, long long 
       lo[e] = f32x2_to_e4m3x2(a - fa, b - fb) | (f32x2_to_e4m3x2(c - fc, d - fd) << 16);
     }
   };
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {  // 128 latent dims = 16 uint4 = 32 columns a part
-    uint32_t hw[32], lw[32];
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const uint4 x = in ? __ldg(src + 32 * (int)rank + 16 * half + u) : make_uint4(0, 0, 0, 0);
-      split8(x, hw + 2 * u, lw + 2 * u);
-    }
-    tmem_st_32x32b_x16(tmem_q + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(hw));
-    tmem_st_32x32b_x16(tmem_q + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(hw + 16));
-    tmem_st_32x32b_x16(tmem_q + 64 + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(lw));
-    tmem_st_32x32b_x16(tmem_q + 64 + 32 * half + 16,
-                       *reinterpret_cast<const uint32_t(*)[16]>(lw + 16));
-  }
   {
+    // RoPE dims 512 + 32 r + [8 u, 8 u + 8), loaded with the first latent half
+    uint4 xr[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) xr[u] = in ? __ldg(src + 64 + 4 * (int)rank + u) : make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {  // 128 latent dims = 16 uint4 = 32 columns a part
+      uint32_t hw[32], lw[32];
+      uint4 x[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) x[u] = in ? __ldg(src + 32 * (int)rank + 16 * half + u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) split8(x[u], hw + 2 * u, lw + 2 * u);
+      tmem_st_32x32b_x16(tmem_q + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(hw));
+      tmem_st_32x32b_x16(tmem_q + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(hw + 16));
+      tmem_st_32x32b_x16(tmem_q + 64 + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(lw));
+      tmem_st_32x32b_x16(tmem_q + 64 + 32 * half + 16,
+                         *reinterpret_cast<const uint32_t(*)[16]>(lw + 16));
+    }
     uint32_t hw[8], lw[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {  // RoPE dims 512 + 32 r + [8 u, 8 u + 8)
-      const uint4 x = in ? __ldg(src + 64 + 4 * (int)rank + u) : make_uint4(0, 0, 0, 0);
-      split8(x, hw + 2 * u, lw + 2 * u);
-    }
+    for (int u = 0; u < 4; ++u) split8(xr[u], hw + 2 * u, lw + 2 * u);
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int off = q * 32 + ((u ^ sw) << 4);

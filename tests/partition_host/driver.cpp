@@ -1,4 +1,4 @@
-// Runs the partition kernel's source on host threads for one problem read
+// Runs a partition kernel's source (the block or the single-warp form) on host threads for one problem read
 // from a text file and writes the work list it leaves in the workspace.
 // Built by tests/test_partition_host.py from generated copies of the kernel
 // source (partition_host.inc) and of the plan's layout arithmetic
@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <deque>
+#include <string>
 
 #include "partition_host.inc"
 #include "mla_decode.h"
@@ -18,7 +19,9 @@ enum { MLA_OK = 0, MLA_ERR_UNSUPPORTED = -2 };
 }  // namespace
 
 int main(int argc, char** argv) {
-  if (argc != 3) return 2;
+  // argv[3] = "warp": run the single-warp kernel (exit 4 if the plan does not fit it)
+  if (argc != 3 && argc != 4) return 2;
+  const bool warp_kernel = argc == 4 && std::string(argv[3]) == "warp";
   FILE* f = std::fopen(argv[1], "r");
   if (!f) return 2;
   int B, H, packed, max_q, max_seq_len, n_workers, sparse_k, causal;
@@ -62,8 +65,10 @@ int main(int argc, char** argv) {
   // the launch's block size (launch_partition)
   const long long need = std::max<long long>(std::max<long long>(B, lay.max_groups),
                                              (long long)lay.n_workers + 1);
+  if (warp_kernel && !mla::partition_warp_fits(p, lay)) return 4;
   const int threads =
-      (int)std::min<long long>(1024, std::max<long long>(128, (need + 31) / 32 * 32));
+      warp_kernel ? 32
+                  : (int)std::min<long long>(1024, std::max<long long>(128, (need + 31) / 32 * 32));
   blockDim.x = threads;
   std::barrier<> block_bar(threads);
   g_block_barrier = &block_bar;
@@ -78,7 +83,10 @@ int main(int argc, char** argv) {
   for (int t = 0; t < threads; ++t)
     th.emplace_back([&, t] {
       threadIdx.x = t;
-      mla::partition_kernel(p, lay, reinterpret_cast<char*>(ws.data()));
+      if (warp_kernel)
+        mla::partition_warp_kernel(p, lay, reinterpret_cast<char*>(ws.data()));
+      else
+        mla::partition_kernel(p, lay, reinterpret_cast<char*>(ws.data()));
     });
   for (auto& x : th) x.join();
   const int* hdr = reinterpret_cast<const int*>(ws.data());

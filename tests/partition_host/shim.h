@@ -1,7 +1,7 @@
 // Host stand-ins for the CUDA constructs the partition kernel uses, so that
 // its source compiles as C++ and runs with one std::thread per CUDA thread
-// (one block): __syncthreads is a std::barrier over the block, a warp
-// shuffle is an exchange through a per-warp array between two barriers of
+// (one block): __syncthreads is a std::barrier over the block, __syncwarp one
+// over the warp's 32 threads, a warp shuffle is an exchange through a per-warp array between two barriers of
 // the warp's 32 threads, and atomics are std::atomic_ref operations.
 #pragma once
 #include <algorithm>
@@ -56,6 +56,11 @@ template <typename T>
 T __shfl_xor_sync(unsigned, T v, int d) {
   return host_exchange(v, (threadIdx.x & 31) ^ d);
 }
+template <typename T>
+T __shfl_sync(unsigned, T v, int src_lane) {
+  return host_exchange(v, src_lane & 31);
+}
+inline void __syncwarp(unsigned = 0xffffffffu) { g_warps[threadIdx.x >> 5]->bar->arrive_and_wait(); }
 template <typename T>
 T __shfl_up_sync(unsigned, T v, int d) {
   const int lane = threadIdx.x & 31;

@@ -1,9 +1,10 @@
-"""The partition kernel's own source, run on CPU threads, against the host model.
+"""The partition kernels' own source, run on CPU threads, against the host model.
 
 The partitioner's arithmetic is pinned twice: by ``tests/partition_model.py``
 (a Python restatement, checked for its invariants on CPU and compared with the
 kernel's work list on the GPU), and here. The test compiles the CUDA source
-of ``partition_kernel`` as C++ with host stand-ins for the barrier and warp
+of both kernel forms (``partition_kernel``, one block, and
+``partition_warp_kernel``, one warp, which the launch picks for small plans) as C++ with host stand-ins for the barriers and warp
 shuffles (``tests/partition_host/shim.h``), under AddressSanitizer and
 UndefinedBehaviorSanitizer. It runs one std::thread per CUDA thread of the
 launch and requires the work list the kernel leaves in a dirty workspace to
@@ -71,7 +72,9 @@ def emulator(tmp_path_factory):
     return exe, out
 
 
-def _run(emulator, w, n_workers):
+def _run(emulator, w, n_workers, kernel="block"):
+    """Runs one kernel form on `w`; returns False if the single-warp form was
+    asked for and the plan does not fit it."""
     exe, out = emulator
     inp, res = out / "in.txt", out / "out.txt"
     with open(inp, "w") as f:
@@ -81,8 +84,10 @@ def _run(emulator, w, n_workers):
         if w.packed:
             f.write(" ".join(str(int(x)) for x in w.qo_indptr) + "\n")
     env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0:abort_on_error=1")
-    r = subprocess.run([str(exe), str(inp), str(res)], capture_output=True, text=True, env=env,
-                       timeout=300)
+    args = [str(exe), str(inp), str(res)] + (["warp"] if kernel == "warp" else [])
+    r = subprocess.run(args, capture_output=True, text=True, env=env, timeout=300)
+    if kernel == "warp" and r.returncode == 4:
+        return False
     assert r.returncode == 0, (r.returncode, r.stderr[-3000:])
     lines = open(res).read().split("\n")
     status, n_items, _ = (int(x) for x in lines[0].split())
@@ -94,12 +99,16 @@ def _run(emulator, w, n_workers):
     assert status == 0
     assert got == [list(t) for t in items]
     assert wb == ref_wb
+    return True
 
 
+@pytest.mark.parametrize("kernel", ["block", "warp"])
 @pytest.mark.parametrize("name", ["tiny", "deepseek_v3", "mtp", "ragged", "fp8_long",
                                   "sparse_topk"])
-def test_kernel_source_work_list_equals_host_model_on_bench_workloads(emulator, name):
-    _run(emulator, mi.WORKLOADS[name](), 76)
+def test_kernel_source_work_list_equals_host_model_on_bench_workloads(emulator, name, kernel):
+    # every one of these plans fits the single-warp form (the launch picks it
+    # for tiny and fp8_long)
+    assert _run(emulator, mi.WORKLOADS[name](), 76, kernel)
 
 
 class _Shape:
@@ -122,8 +131,9 @@ class _Shape:
         return self.qo_indptr.astype(np.int64)
 
 
+@pytest.mark.parametrize("kernel", ["block", "warp"])
 @pytest.mark.parametrize("seed", range(10))
-def test_kernel_source_work_list_equals_host_model_on_random_shapes(emulator, seed):
+def test_kernel_source_work_list_equals_host_model_on_random_shapes(emulator, seed, kernel):
     rng = np.random.default_rng(7000 + seed)
     B = int(rng.integers(1, 200))
     H = int(rng.choice([16, 32, 64, 128]))
@@ -131,4 +141,43 @@ def test_kernel_source_work_list_equals_host_model_on_random_shapes(emulator, se
     q = (rng.integers(1, 9, size=B) if packed else np.full(B, int(rng.integers(1, 5))))
     L = rng.integers(q, int(rng.choice([100, 3000, 40000])), endpoint=True)
     sparse_k = int(rng.choice([64, 100, 2048])) if rng.random() < 0.3 else 0
-    _run(emulator, _Shape(L, q, H, packed, sparse_k), int(rng.choice([1, 7, 76, 148, 600])))
+    _run(emulator, _Shape(L, q, H, packed, sparse_k), int(rng.choice([1, 7, 76, 148, 600])),
+         kernel)
+
+
+def _plan_groups(q, H, packed, sparse_k):
+    """The plan's bound on row groups (make_layout): R = 128 rows, or H under
+    sparse top-k, where a group is one token's heads."""
+    R = H if sparse_k else 128
+    B, max_q = len(q), int(np.max(q))
+    groups = B * -(-max_q * H // R)
+    if packed:
+        groups = min(groups, B + -(-int(np.sum(q)) * H // R))
+    return groups
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_single_warp_kernel_on_shapes_near_its_bounds(emulator, seed):
+    """The single-warp form on shapes up to its table bounds (512 requests,
+    512 row groups, 512 workers), with lengths that make many short groups,
+    one group longer than all the others, or groups shorter than the overhead;
+    every shape must fit it and give the host model's work list."""
+    rng = np.random.default_rng(9100 + seed)
+    H = int(rng.choice([16, 32, 64, 128]))
+    packed = bool(rng.integers(2))
+    sparse_k = int(rng.choice([64, 2048])) if rng.random() < 0.25 else 0
+    B = int(rng.integers(1, 513))
+    q = rng.integers(1, 9, size=B) if packed else np.full(B, int(rng.integers(1, 5)))
+    while _plan_groups(q, H, packed, sparse_k) > 512:
+        q = q[:max(1, len(q) * 3 // 4)]
+    B = len(q)
+    kind = seed % 3
+    if kind == 0:
+        L = rng.integers(q, q + 200, endpoint=True)
+    elif kind == 1:
+        L = rng.integers(q, 2000, endpoint=True)
+        L[int(rng.integers(B))] = 120000
+    else:
+        L = rng.integers(q, 40000, endpoint=True)
+    n_workers = int(rng.choice([1, 2, 76, 148, 511, 512]))
+    assert _run(emulator, _Shape(L, q, H, packed, sparse_k), n_workers, "warp")
