@@ -1,5 +1,6 @@
-// Split-KV combine: merges the normalised fp32 partials of every split
-// (request, row group) by their natural-log LSEs.
+// Split-KV combine: merges the normalised partials of every split
+// (request, row group), stored in bf16 (part_unit in mla_common.cuh), by
+// their natural-log LSEs (fp32), accumulating in fp32.
 //
 // For chunks k with partial output O_k (already divided by its own softmax
 // denominator) and lse_k = ln sum_{j in chunk k} exp(s_j):

@@ -61,7 +61,7 @@ __device__ __forceinline__ float run_bmm2(const Problem& p) {
 // [kv_begin, kv_end).  Under sparse top-k selection R = H (one token, q_start
 // + g) and [kv_begin, kv_end) indexes the token's position list.
 // slot < 0: the item covers the whole KV range and writes `out` directly;
-// otherwise it writes a normalised fp32 partial (O and natural-log LSE) into
+// otherwise it writes a normalised partial (bf16 O, fp32 natural-log LSE) into
 // partial slot `slot` for the combine kernel.
 struct WorkItem {
   int b, g, kv_begin, kv_end;
