@@ -363,7 +363,8 @@ def gpu_case(w, dev, steps, warmup, with_e2e):
     res = {"ms_per_step": total_ms / steps, "kernel_ms": statistics.mean(kernel_ms),
            "kernel_ms_median": statistics.median(kernel_ms),
            "call_ms_median": statistics.median(call_ms), "n_median": n_prof,
-           "ms_per_step_with_events": prof_total_ms / steps, "launches_per_step": 3}
+           "ms_per_step_with_events": prof_total_ms / steps,
+           "launches_per_step": mla.mla_decode_kernels_per_run(plan.handle)}
 
     if with_e2e:
         # end to end through the public API with host buffers: per-step inputs
@@ -552,7 +553,8 @@ def run_profile_target(args):
     torch.cuda.synchronize()
     status = int(ws[:4].view(torch.int32).item())
     print(json.dumps({"profile_target": w.name, "calls": args.warmup + args.steps,
-                      "launches_per_call": 3, "status_word": status}), flush=True)
+                      "launches_per_call": mla.mla_decode_kernels_per_run(plan.handle),
+                      "status_word": status}), flush=True)
     if status != 0:
         raise SystemExit(f"device status word {status}")
 

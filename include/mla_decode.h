@@ -390,6 +390,15 @@ int mla_decode_work_list_layout(const mla_plan_t *plan, size_t *items_offset,
                                 size_t *worker_ranges_offset, int32_t *n_workers);
 
 /*
+ * Number of kernels one run of `plan` launches on the caller's stream (a
+ * plan property; batch 0 launches none): the partitioner, the decode kernel
+ * and the combine kernel, plus, on the FP8 MMA path with a bf16 query (an
+ * e4m3 cache, no sparse top-k, e4m3_widen 0), the query split that precedes
+ * the decode.  Returns -1 for a NULL plan.
+ */
+int32_t mla_decode_kernels_per_run(const mla_plan_t *plan);
+
+/*
  * Byte offset, inside the workspace, of the int32 device status word the last
  * run left behind.  0: every device-side value was within the contract.
  * Bits (values are clamped and never read out of bounds):

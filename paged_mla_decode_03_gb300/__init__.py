@@ -117,6 +117,8 @@ def load_library():
     lib.mla_decode_work_list_layout.argtypes = [vp, ctypes.POINTER(sz), ctypes.POINTER(sz),
                                                 ctypes.POINTER(i32)]
     lib.mla_decode_work_list_layout.restype = ctypes.c_int
+    lib.mla_decode_kernels_per_run.argtypes = [vp]
+    lib.mla_decode_kernels_per_run.restype = i32
     lib.mla_decode_status_offset.argtypes = []
     lib.mla_decode_status_offset.restype = sz
     lib.mla_decode_status_string.argtypes = [ctypes.c_int]
@@ -162,6 +164,11 @@ def mla_decode_work_list_layout(plan: int) -> Tuple[int, int, int]:
     if rc != MLA_OK:
         raise MlaDecodeError(rc, "mla_decode_work_list_layout")
     return a.value, b.value, n.value
+
+
+def mla_decode_kernels_per_run(plan: int) -> int:
+    """Kernels one run of the plan launches (see include/mla_decode.h)."""
+    return int(load_library().mla_decode_kernels_per_run(ctypes.c_void_p(plan)))
 
 
 def _nbytes(x) -> int:

@@ -22,6 +22,8 @@ cudaError_t launch_combine(const Problem& p, const Layout& lay, void* ws, int gr
 cudaError_t decode_sm103_setup(int kv_dtype, int sparse, int f8_mma, int sm_count, int* n_pairs);
 cudaError_t launch_merge_states(const void* o_parts, const float* lse_parts, int n, long long rows,
                                 float scale, void* out, float* lse_out, cudaStream_t stream);
+cudaError_t launch_qsplit(const Problem& p, const Layout& lay, void* ws, int sm_count,
+                          cudaStream_t stream);
 cudaError_t launch_decode_sm103(const Problem& p, const Layout& lay, void* ws,
                                 cudaStream_t stream);
 }  // namespace mla
@@ -49,6 +51,11 @@ bool supported_heads(int h) { return h == 16 || h == 32 || h == 64 || h == 128; 
 // top-k always widens).
 bool uses_f8_mma(const mla_decode_params& p) {
   return p.kv_dtype == MLA_KV_FP8_E4M3 && p.sparse_top_k == 0 && p.e4m3_widen == 0;
+}
+
+// the FP8 MMA path with a bf16 query: the query is split before the decode
+bool uses_q_split(const mla_decode_params& p) {
+  return uses_f8_mma(p) && p.q_dtype == MLA_Q_BF16;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -102,6 +109,14 @@ int make_layout(const mla_decode_params& prm, int n_workers, int n_ctas, int row
   off = align_up(off + sizeof(float) * R * (size_t)lay->max_partials, 256);
   lay->comb_done = off;
   off = align_up(off + sizeof(int) * (size_t)std::max(lay->max_combine, 1), 256);
+  // the FP8 MMA path (e4m3 cache, dense, not widened) with a bf16 query: the
+  // query's e4m3 parts, split once per call before the decode (q_split_offset)
+  if (prm.kv_dtype == MLA_KV_FP8_E4M3 && prm.sparse_top_k == 0 && prm.e4m3_widen == 0 &&
+      prm.q_dtype == MLA_Q_BF16) {
+    const long long tokens = prm.packed ? prm.max_total_q : B * prm.max_seq_len_q;
+    const size_t halves = 2 * (size_t)std::max(tokens, 1LL) * (size_t)prm.num_heads;
+    off = align_up(off + halves * kQSplitUnits * 16, 256);
+  }
   lay->total = off;
   return MLA_OK;
 }
@@ -303,6 +318,9 @@ int run_impl(const mla_plan_t* plan, const void* query, const void* kv_cache,
   // work enqueued elsewhere that the decode needs (the host entry's query copy)
   if (join_before_decode && cudaStreamWaitEvent(s, join_before_decode, 0) != cudaSuccess)
     return MLA_ERR_CUDA;
+  if (uses_q_split(prm) &&
+      mla::launch_qsplit(p, plan->lay, workspace, plan->sm_count, s) != cudaSuccess)
+    return MLA_ERR_CUDA;
   if (event_before_decode &&
       cudaEventRecordWithFlags(static_cast<cudaEvent_t>(event_before_decode), s, ev_flags) !=
           cudaSuccess)
@@ -497,6 +515,12 @@ int mla_decode_work_list_layout(const mla_plan_t* plan, size_t* items_offset,
   *worker_ranges_offset = plan->lay.worker_ranges;
   *n_workers = plan->lay.n_workers;
   return MLA_OK;
+}
+
+int32_t mla_decode_kernels_per_run(const mla_plan_t* plan) {
+  if (!plan) return -1;
+  if (plan->prm.batch == 0) return 0;
+  return uses_q_split(plan->prm) ? 4 : 3;
 }
 
 size_t mla_decode_status_offset(void) { return sizeof(int) * mla::kHdrStatus; }

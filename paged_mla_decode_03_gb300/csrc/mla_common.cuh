@@ -121,6 +121,20 @@ struct Layout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The query split of the FP8 MMA path with a bf16 query (mla_qsplit.cu), one
+// record of kQSplitUnits 16-byte units per (query row, CTA half): latent hi
+// codes (units 0-15), latent lo codes (16-31), RoPE hi (32-33), RoPE lo
+// (34-35), each in dim order, then the half's factor 2^-k (the float in the
+// first word of unit 36).  The records follow the combine counters; the plans
+// that use them size the workspace to hold one per (row, half) of their
+// largest query.  (Kept out of Layout: the decode kernel measured 1.5% slower
+// on the MTP workload with two more Layout fields, for no reason found.)
+constexpr int kQSplitUnits = 37;
+__host__ __device__ inline size_t q_split_offset(const Layout& lay) {
+  return align_up(lay.comb_done + sizeof(int) * (size_t)(lay.max_combine > 1 ? lay.max_combine : 1),
+                  256);
+}
+
 // Split partials of O (normalised by their own softmax sum): bf16, or fp32
 // when kPartialBf16 is false.  A slot holds R rows x 512 dims as 32 chunks of
 // 16 dims; chunk c of row q is kPartUnits 16-byte units, stored unit-major

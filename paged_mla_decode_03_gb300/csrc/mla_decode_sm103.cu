@@ -286,33 +286,20 @@ __device__ __noinline__ void load_q_row_e4m3(const Problem& p, long long qrow, b
   fence_proxy_async_smem();  // read by the RoPE MMAs
 }
 
-// The lines of a bf16 query row that the CTA of cluster rank `rank` reads (its
-// latent half [256 rank, +256): bytes [512 rank, +512); its RoPE half: inside
-// bytes [1024, 1152)) are brought into L2.  A row is 1152 bytes, nine lines.
-__device__ __forceinline__ void prefetch_q_row_bf16(const Problem& p, long long qrow, uint32_t rank) {
-  const unsigned char* row = reinterpret_cast<const unsigned char*>(p.query) + qrow * (2 * kQkDim);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) prefetch_l2(row + 512 * rank + 128 * k);
-  prefetch_l2(row + 1024);
-}
-
 // Row `q` of a work item's query for the FP8 MMAs, for the CTA of cluster rank
 // `rank`: its latent dims [256 rank, 256 rank + 256) as e4m3 codes into the
-// TMEM columns at `tmem_q` (four codes a column; A operand of the ts QK MMAs)
-// and its RoPE dims [512 + 32 rank, +32) into the 32B-swizzled smem tile at
-// `q_rope`.  An e4m3 query is copied as it is (one part).  A bf16 query row
-// is scaled by 2^k, the largest power of two with max|q| 2^k <= 448 over this
-// CTA's 288 dims (each CTA of the pair has its own k; the partial scores are
-// brought back to true units on each side before they are added), and split
-// into two parts, hi = e4m3(x) at columns [0, 64) and lo = e4m3(x - hi) at
-// [64, 128) (RoPE: the second 4 KB of `q_rope`).  hi + lo equals x exactly wherever
-// |x| >= 2^-2 (x is a bf16 value times a power of two, and x - hi has at most
-// four significant bits at or above 2^-9) and to within 2^-10 below that.
-// Returns 2^-k, the factor the row's scores need.  Rows past the query
-// tensor are zero (factor 1).
-__device__ __noinline__ float load_q_row_split_e4m3(const Problem& p, long long qrow, bool in,
-                                                    int q, uint32_t rank, uint32_t tmem_q,
-                                                    unsigned char* q_rope) {
+// TMEM columns at `tmem_q` (four codes a column, in dim order; A operand of the
+// ts QK MMAs) and its RoPE dims [512 + 32 rank, +32) into the 32B-swizzled
+// smem tile at `q_rope`.  An e4m3 query is copied as it is (one part).  A
+// bf16 query comes split (mla_qsplit.cu; records at q_split_offset) into hi
+// codes, copied to columns [0, 64) and the first 4 KB of `q_rope`, and lo
+// codes, to [64, 128) and the second 4 KB, with the factor 2^-k that the
+// row's partial scores need.
+// Returns that factor (1 for an e4m3 query).  Rows past the query tensor are
+// zero (factor 1).  Called once per item, kept out of line.
+__device__ __noinline__ float load_q_row_fp8_mma(const Problem& p, const uint4* split,
+                                                 long long qrow, bool in, int q, uint32_t rank,
+                                                 uint32_t tmem_q, unsigned char* q_rope) {
   const int sw = (q >> 2) & 1;  // 32B swizzle: 16-byte unit u of row q sits at u ^ sw
   if (p.q_fp8) {
     const uint4* src = reinterpret_cast<const uint4*>(
@@ -339,89 +326,26 @@ __device__ __noinline__ float load_q_row_split_e4m3(const Problem& p, long long 
     fence_proxy_async_smem();  // read by the RoPE MMA
     return 1.f;
   }
-  const uint4* src = reinterpret_cast<const uint4*>(
-      reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim);
-  // every line first (the batches below then wait for one DRAM round trip,
-  // not one each; the caller may have prefetched them already)
-  if (in) prefetch_q_row_bf16(p, qrow, rank);
-  // this CTA's 36 16-byte units: latent [32 r, 32 r + 32), RoPE [64 + 4 r, +4),
-  // in two batches of 18.  The largest magnitude is taken on the bf16 bit
-  // patterns with the sign cleared (their integer order is their magnitude
-  // order), two values an instruction.  This runs once per item from a cold
-  // instruction cache, so the code is kept short: loops over batches and
-  // halves are not unrolled.
-  auto unit = [&](int i) { return i < 32 ? 32 * (int)rank + i : 64 + 4 * (int)rank + (i - 32); };
-  uint32_t mbits = 0;
+  // this (row, half)'s units: latent hi [0, 16), latent lo [16, 32), RoPE hi
+  // [32, 34), RoPE lo [34, 36); one part per round of 18 loads
+  const uint4* src = split + ((in ? qrow : 0) * 2 + rank) * kQSplitUnits;
 #pragma unroll 1
-  for (int b0 = 0; b0 < 36; b0 += 18) {
+  for (int part = 0; part < 2; ++part) {
     uint4 x[18];
 #pragma unroll
-    for (int u = 0; u < 18; ++u) x[u] = in ? __ldg(src + unit(b0 + u)) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < 16; ++u) x[u] = in ? __ldg(src + 16 * part + u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int u = 0; u < 18; ++u)
-      mbits = __vmaxu2(mbits, __vmaxu2(__vmaxu2(x[u].x & 0x7FFF7FFFu, x[u].y & 0x7FFF7FFFu),
-                                       __vmaxu2(x[u].z & 0x7FFF7FFFu, x[u].w & 0x7FFF7FFFu)));
-  }
-  // a NaN or infinite element fails the range check below, hence k = 0
-  const float amax = __uint_as_float(max(mbits & 0xFFFFu, mbits >> 16) << 16);
-  int k = 0;
-  if (amax > 0.f && amax <= 3.4028235e38f) {
-    const uint32_t ab = __float_as_uint(amax);
-    const int E = (int)(ab >> 23);  // biased exponent, 0 for a subnormal
-    k = E == 0 ? 126 : ((ab & 0x7FFFFFu) <= 0x600000u ? 135 - E : 134 - E);  // 448 = 1.75 * 2^8
-    k = min(126, max(-126, k));
-  }
-  const float up = __uint_as_float((uint32_t)(127 + k) << 23);
-  // eight bf16 values (one uint4) -> two words of hi codes and two of lo codes
-  auto split8 = [&](const uint4 x, uint32_t* hi, uint32_t* lo) {
-    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+    for (int u = 0; u < 2; ++u) x[16 + u] = in ? __ldg(src + 32 + 2 * part + u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float a = __uint_as_float(w4[2 * e] << 16) * up;
-      const float b = __uint_as_float(w4[2 * e] & 0xFFFF0000u) * up;
-      const float c = __uint_as_float(w4[2 * e + 1] << 16) * up;
-      const float d = __uint_as_float(w4[2 * e + 1] & 0xFFFF0000u) * up;
-      const uint32_t hab = f32x2_to_e4m3x2(a, b), hcd = f32x2_to_e4m3x2(c, d);
-      float fa, fb, fc, fd;
-      e4m3x2_to_f32x2(hab, fa, fb);
-      e4m3x2_to_f32x2(hcd, fc, fd);
-      hi[e] = hab | (hcd << 16);
-      lo[e] = f32x2_to_e4m3x2(a - fa, b - fb) | (f32x2_to_e4m3x2(c - fc, d - fd) << 16);
-    }
-  };
-  {
-    // RoPE dims 512 + 32 r + [8 u, 8 u + 8), loaded with the first latent half
-    uint4 xr[4];
+    for (int j = 0; j < 4; ++j)
+      tmem_st_32x32b_x16(tmem_q + 64 * part + 16 * j,
+                         *reinterpret_cast<const uint32_t(*)[16]>(&x[4 * j]));
 #pragma unroll
-    for (int u = 0; u < 4; ++u) xr[u] = in ? __ldg(src + 64 + 4 * (int)rank + u) : make_uint4(0, 0, 0, 0);
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {  // 128 latent dims = 16 uint4 = 32 columns a part
-      uint32_t hw[32], lw[32];
-      uint4 x[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) x[u] = in ? __ldg(src + 32 * (int)rank + 16 * half + u) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int u = 0; u < 16; ++u) split8(x[u], hw + 2 * u, lw + 2 * u);
-      tmem_st_32x32b_x16(tmem_q + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(hw));
-      tmem_st_32x32b_x16(tmem_q + 32 * half + 16, *reinterpret_cast<const uint32_t(*)[16]>(hw + 16));
-      tmem_st_32x32b_x16(tmem_q + 64 + 32 * half, *reinterpret_cast<const uint32_t(*)[16]>(lw));
-      tmem_st_32x32b_x16(tmem_q + 64 + 32 * half + 16,
-                         *reinterpret_cast<const uint32_t(*)[16]>(lw + 16));
-    }
-    uint32_t hw[8], lw[8];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) split8(xr[u], hw + 2 * u, lw + 2 * u);
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int off = q * 32 + ((u ^ sw) << 4);
-      *reinterpret_cast<uint4*>(q_rope + off) =
-          make_uint4(hw[4 * u], hw[4 * u + 1], hw[4 * u + 2], hw[4 * u + 3]);
-      *reinterpret_cast<uint4*>(q_rope + kRopeQ / 2 + off) =
-          make_uint4(lw[4 * u], lw[4 * u + 1], lw[4 * u + 2], lw[4 * u + 3]);
-    }
+    for (int u = 0; u < 2; ++u)
+      *reinterpret_cast<uint4*>(q_rope + part * (kRopeQ / 2) + q * 32 + ((u ^ sw) << 4)) = x[16 + u];
   }
   fence_proxy_async_smem();  // read by the RoPE MMAs
-  return __uint_as_float((uint32_t)(127 - k) << 23);
+  return in ? __ldg(reinterpret_cast<const float*>(src + 36)) : 1.f;
 }
 
 // Producer of a sparse top-k decode: kGatherWarps warps (role 0 = warp 0,
@@ -1274,9 +1198,10 @@ decode_sm103_kernel(const Problem p, const Layout lay, char* __restrict__ ws,
     auto write_q = [&](const WorkItem& it, int ordinal) {
       const long long qrow = (long long)it.q_start * H + (long long)it.g * R + q;
       const bool in = qrow < q_rows;
-      if (kF8) {
-        qscale[(ordinal & 1) * kRows + q] = load_q_row_split_e4m3(
-            p, qrow, in, q, rank, tmem + lane_base + TM_Q, sm + OFF_QROPE);
+      if constexpr (kF8) {
+        qscale[(ordinal & 1) * kRows + q] = load_q_row_fp8_mma(
+            p, reinterpret_cast<const uint4*>(ws + q_split_offset(lay)), qrow, in, q, rank,
+            tmem + lane_base + TM_Q, sm + OFF_QROPE);
       } else if (!p.q_fp8) {
         const uint4* src = reinterpret_cast<const uint4*>(
             reinterpret_cast<const __nv_bfloat16*>(p.query) + (in ? qrow : 0) * kQkDim +

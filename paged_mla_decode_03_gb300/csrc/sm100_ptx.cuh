@@ -69,11 +69,6 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // ------------------------------------------------------------------ TMA
-// Starts bringing the 128-byte line holding `ptr` (global memory) into L2.
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)) : "memory");
-}
-
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

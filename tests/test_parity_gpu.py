@@ -839,3 +839,21 @@ def test_back_to_back_calls_do_not_disturb_each_other(name):
         ro, rl = refs[k % 2]
         assert torch.equal(outs[k].view(torch.int16), ro.view(torch.int16)), k
         assert torch.equal(lses[k], rl), k
+
+
+def test_kernels_per_run_reports_the_query_split():
+    """A plan on the FP8 MMA path with a bf16 query launches the query split
+    before the decode (four kernels a run); an e4m3 query, the widened path, a
+    bf16 cache and a sparse plan launch three."""
+    import paged_mla_decode_03_gb300 as mla
+    base = dict(batch=2, num_heads=16, max_seq_len_q=1, max_seq_len=64, page_size=32,
+                max_pages_per_req=2, num_pages=4, packed=False)
+    cases = [(dict(kv_dtype="e4m3"), 4), (dict(kv_dtype="e4m3", q_dtype="e4m3"), 3),
+             (dict(kv_dtype="e4m3", e4m3_widen=True), 3), (dict(kv_dtype="bf16"), 3),
+             (dict(kv_dtype="e4m3", sparse_top_k=64), 3)]
+    for extra, want in cases:
+        plan = mla.Plan(**base, **extra)
+        try:
+            assert mla.mla_decode_kernels_per_run(plan.handle) == want, extra
+        finally:
+            plan.close()
