@@ -5,7 +5,8 @@
 // q_len / KV-length / total_q bounds) and the device's SM count.
 // mla_decode_run checks what the host can check and enqueues three kernels
 // on the caller's stream: the split-KV partitioner, the decode kernel and the
-// combine kernel.  Grid sizes depend only on plan-time values, and nothing
+// combine kernel, with the query split between the first two on the FP8 MMA
+// path with a bf16 query.  Grid sizes depend only on plan-time values, and nothing
 // here allocates, copies or synchronises, so a run can be captured in a CUDA
 // graph and replayed with new seq_lens / qo_indptr values.
 #include <algorithm>
