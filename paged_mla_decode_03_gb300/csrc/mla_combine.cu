@@ -54,7 +54,7 @@ __device__ bool wait_count(const int* counter, int target, int* status) {
 // kernel, whose CTAs release it right after their prologue, the combine's
 // CTAs run on SMs the decode kernel has finished with and merge a group as
 // soon as both CTAs of every chunk of it have counted their partial.
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
   int* status = reinterpret_cast<int*>(ws) + kHdrStatus;
   const int* done = reinterpret_cast<const int*>(ws + lay.comb_done);
@@ -85,32 +85,27 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) acc[e] = 0.f;
       for (int k0 = 0; k0 < c.n_chunks; k0 += kBatch) {
-        float4 x[kBatch][4];
+        // this row's 16 dims of each chunk as stored (8 words of bf16 pairs,
+        // or 16 fp32 words), widened where they are used: half the registers
+        // of widening them here, so more blocks fit on an SM
+        uint32_t xw[kBatch][4 * kPartUnits];
         float l[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           l[u] = -INFINITY;
+#pragma unroll
+          for (int v = 0; v < 4 * kPartUnits; ++v) xw[u][v] = 0u;
           if (k0 + u < c.n_chunks) {
             const size_t slot = (size_t)(c.first_slot + (k0 + u) * c.stride);
-            if (kPartialBf16) {
-              const uint4 a = part_o[part_unit(slot, R, t, 0, r)];
-              const uint4 b = part_o[part_unit(slot, R, t, 1, r)];
-              const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-              for (int v = 0; v < 4; ++v)  // bf16 pairs, low half first
-                x[u][v] = make_float4(__uint_as_float(w[2 * v] << 16),
-                                      __uint_as_float(w[2 * v] & 0xFFFF0000u),
-                                      __uint_as_float(w[2 * v + 1] << 16),
-                                      __uint_as_float(w[2 * v + 1] & 0xFFFF0000u));
-            } else {
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                x[u][v] = reinterpret_cast<const float4*>(part_o)[part_unit(slot, R, t, v, r)];
+            for (int v = 0; v < kPartUnits; ++v) {
+              const uint4 a = part_o[part_unit(slot, R, t, v, r)];
+              xw[u][4 * v] = a.x;
+              xw[u][4 * v + 1] = a.y;
+              xw[u][4 * v + 2] = a.z;
+              xw[u][4 * v + 3] = a.w;
             }
             l[u] = part_lse[slot * R + r];
-          } else {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) x[u][v] = make_float4(0.f, 0.f, 0.f, 0.f);
           }
         }
         float m_new = m;
@@ -125,9 +120,14 @@ combine_kernel(Problem p, Layout lay, char* __restrict__ ws) {
         for (int u = 0; u < kBatch; ++u) {
           const float w = expf(l[u] - m_use);  // absent chunks: l = -inf, w = 0
           sum += w;
-          const float* xv = reinterpret_cast<const float*>(x[u]);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) acc[e] += w * xv[e];
+          for (int e = 0; e < 16; ++e) {
+            // bf16: dim e is the low half of word e / 2 for even e, the high half for odd e
+            const float xe = kPartialBf16 ? __uint_as_float((e & 1) ? (xw[u][e >> 1] & 0xFFFF0000u)
+                                                                   : (xw[u][e >> 1] << 16))
+                                          : __uint_as_float(xw[u][e]);
+            acc[e] += w * xe;
+          }
         }
         m = m_new;
       }
