@@ -43,8 +43,9 @@
 // An e4m3 cache runs by default on FP8 MMAs (kind::f8f6f4, a separate
 // instantiation): the e4m3 tiles go from the TMA straight into an 8-deep ring
 // in the operand layouts, the query enters as e4m3 (a bf16 row as two parts
-// under a power-of-two row scale the softmax folds into bmm1), and so does P
-// (two parts).  Widening on request: eight more warps (14-21) widen each
+// under a power-of-two scale per CTA half, split before this kernel by
+// mla_qsplit.cu; the scores are brought back by it before the halves are
+// added), and so does P (two parts).  Widening on request: eight more warps (14-21) widen each
 // staged e4m3 tile to bf16 in shared memory (exact; the k_scale lives in
 // bmm1/bmm2), and the bf16 ring is 3 deep beside a 2-deep e4m3 staging ring.
 // Under sparse top-k selection (a separate instantiation, two warps more) a
