@@ -374,11 +374,12 @@ def test_ragged_request_equals_its_own_single_request_launch():
         assert np.abs(l1 - lb).max() <= 1e-3, b
 
 
-@pytest.mark.parametrize("name", ["deepseek_v3", "ragged"])
+@pytest.mark.parametrize("name", ["deepseek_v3", "ragged", "fp8_long"])
 def test_host_buffer_entry_equals_device_entry(name):
     """mla_decode_run_host (host query, metadata and results, staged by the
     library) gives bitwise the device entry's results: same kernels, same
-    inputs, fixed and packed launches."""
+    inputs, fixed and packed launches, and the FP8 path, whose query split
+    runs after the staged query's copy."""
     import paged_mla_decode_03_gb300 as mla
 
     w = REDUCED[name]()
