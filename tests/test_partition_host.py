@@ -181,3 +181,43 @@ def test_single_warp_kernel_on_shapes_near_its_bounds(emulator, seed):
         L = rng.integers(q, 40000, endpoint=True)
     n_workers = int(rng.choice([1, 2, 76, 148, 511, 512]))
     assert _run(emulator, _Shape(L, q, H, packed, sparse_k), n_workers, "warp")
+
+
+def test_workspace_layout_regions_hold_what_the_kernels_write(emulator):
+    """The plan's layout arithmetic (make_layout) on plans of every kind: bf16
+    and e4m3 caches (FP8 MMAs with a bf16 or an e4m3 query, and widened),
+    fixed and packed queries from one token to prefill sizes, sparse top-k,
+    decode-context parallelism, and worker counts from 1 to 600.  Every region
+    must be 256-byte aligned, in order, and large enough for what the kernels
+    write (tests/partition_host/layout_check.cpp states the checks)."""
+    exe_dir = emulator[1]
+    cxx = shutil.which("g++")
+    exe = exe_dir / "layout_check"
+    r = subprocess.run([cxx, "-std=c++20", "-O1", "-fsanitize=address,undefined",
+                        "-fno-sanitize-recover=undefined", "-pthread", "-I", str(exe_dir), "-I",
+                        HERE, "-I", os.path.join(ROOT, "include"),
+                        os.path.join(HERE, "layout_check.cpp"), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    rows = []
+    # B H packed max_q max_total_q max_seq_len n_workers sparse_k kv q widen cp_world
+    for kv, q, widen in ((0, 0, 0), (1, 0, 0), (1, 1, 0), (1, 0, 1)):
+        rows += [
+            (2, 16, 0, 1, 0, 64, 76, 0, kv, q, widen, 1),            # tiny
+            (64, 128, 0, 1, 0, 8192, 76, 0, kv, q, widen, 1),        # headline
+            (32, 128, 0, 4, 0, 16384, 76, 0, kv, q, widen, 1),       # MTP
+            (128, 16, 1, 8, 576, 32768, 76, 0, kv, q, widen, 1),     # ragged
+            (8, 128, 0, 2, 0, 131072, 76, 0, kv, q, widen, 1),       # long context
+            (512, 128, 1, 48, 18432, 2048, 76, 0, kv, q, widen, 1),  # prefill
+            (64, 128, 0, 1, 0, 12288, 76, 2048, kv, q, widen, 1),    # sparse top-k
+            (16, 64, 0, 2, 0, 4096, 76, 0, kv, q, widen, 2),         # DCP rank
+            (1, 16, 1, 1, 1, 1, 1, 0, kv, q, widen, 1),              # one token, one worker
+            (200, 32, 1, 8, 900, 40000, 600, 100, kv, q, widen, 1),  # sparse, many workers
+            (300, 128, 1, 8, 2400, 5000, 148, 0, kv, q, widen, 1),
+        ]
+    inp = exe_dir / "layouts.txt"
+    inp.write_text("\n".join(" ".join(str(v) for v in row) for row in rows) + "\n")
+    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=0:abort_on_error=1")
+    r = subprocess.run([str(exe), str(inp)], capture_output=True, text=True, env=env, timeout=60)
+    assert r.returncode == 0, (r.stdout, r.stderr[-2000:])
+    assert r.stdout.strip() == f"ok {len(rows)}"
