@@ -93,10 +93,10 @@ struct CombineItem {
 enum HeaderWord {
   kHdrStatus = 0,     // contract-violation bits (see mla_decode_status_offset)
   kHdrNumItems = 1,
-  kHdrWorkCounter = 2,
+  kHdrWorkCounter = 2,     // reserved: zeroed by the partitioner, read by no kernel
   kHdrNumCombine = 3,
-  kHdrChunkTiles = 4,
-  kHdrCombineCounter = 5,
+  kHdrChunkTiles = 4,      // the partition's total cost in units (a diagnostic)
+  kHdrCombineCounter = 5,  // reserved: zeroed by the partitioner, read by no kernel
   kHdrWords = 64
 };
 
