@@ -193,6 +193,43 @@ def test_cuda_graph_replay_with_new_lengths():
         check("bf16", out, ref_o, lse, ref_l, what="graph replay")
 
 
+def test_cuda_graph_replay_fp8_path_follows_new_query_and_lengths():
+    """The FP8 MMA path with a bf16 query splits the query in a kernel of its
+    own before the decode.  Captured once and replayed with new query values
+    and new lengths written in place, every replay matches the oracle: the
+    split runs inside the graph on each replay, not once at capture."""
+    import paged_mla_decode_03_gb300 as mla
+    mk = lambda seed, lens: mi.build("graph_fp8", seed, num_heads=32, page_size=32,
+                                     seq_lens=lens, q_lens=[2, 2, 2], packed=False,
+                                     return_lse=True, kv_dtype="e4m3")
+    w = mk(85, [300, 120, 77])
+    d = to_device(w)
+    assert mla.mla_decode_kernels_per_run(d.plan.handle) == 4
+    run(w, d)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            run(w, d, stream=s)
+    # new lengths stay within the first draw's (its block tables cover them)
+    for seed, lens in ((86, [250, 64, 77]), (87, [300, 2, 40])):
+        w2 = mk(seed, lens)  # a new query; the first draw's cache, tables and scales kept
+        w2 = dataclasses.replace(w2, kv_cache=w.kv_cache, block_tables=w.block_tables,
+                                 max_seq_len=w.max_seq_len, bmm1_scale=w.bmm1_scale,
+                                 bmm2_scale=w.bmm2_scale, k_scale=w.k_scale)
+        d.query.copy_(torch.from_numpy(w2.query.view(np.int16)).to(d.query.device)
+                      .view(torch.bfloat16))
+        d.seq_lens.copy_(torch.from_numpy(w2.seq_lens))
+        d.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert device_status(d) == 0
+        out, lse = results(d)
+        ref_o, ref_l = oracle.run(w2)
+        check("e4m3", out, ref_o, lse, ref_l, what="fp8 graph replay")
+
+
 def test_large_packed_total_q():
     """Prefill-through-decode shape: thousands of packed query tokens."""
     rng = np.random.default_rng(84)
