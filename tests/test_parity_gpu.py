@@ -836,6 +836,42 @@ def test_partition_work_list_matches_host_model(name):
     assert got_wb == wb
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_small_plans_work_list_matches_host_model(seed):
+    """Plans of up to 32 requests and 32 row groups run the one-warp form of
+    the partitioner; its work list equals the host model's, item by item and
+    worker range by worker range, on seeded shapes (fixed and packed queries,
+    every head count, short and long requests, one request much longer than
+    the others), and the decode's status word stays clear."""
+    import paged_mla_decode_03_gb300 as mla
+    from partition_model import partition
+    rng = np.random.default_rng(9300 + seed)
+    H = int(rng.choice([16, 32, 64, 128]))
+    packed = bool(rng.integers(2))
+    while True:
+        B = int(rng.integers(1, 33))
+        q = rng.integers(1, 5, size=B) if packed else np.full(B, int(rng.integers(1, 3)))
+        if B * -(-int(q.max()) * H // 128) <= 32:
+            break
+    L = rng.integers(q, int(rng.choice([70, 900, 5000])), endpoint=True)
+    if seed % 3 == 0:
+        L[int(rng.integers(B))] = 20000
+    w = mi.build(f"small{seed}", 9300 + seed, num_heads=H, page_size=int(rng.choice([32, 64])),
+                 seq_lens=L, q_lens=q, packed=packed)
+    d = to_device(w)
+    run(w, d)
+    torch.cuda.synchronize()
+    assert device_status(d) == 0
+    items_off, wr_off, n_workers = mla.mla_decode_work_list_layout(d.plan.handle)
+    n_items = int(d.workspace[4:8].view(torch.int32).item())
+    got = d.workspace[items_off:items_off + 40 * n_items].view(torch.int32).cpu().numpy()
+    got_wb = d.workspace[wr_off:wr_off + 4 * (n_workers + 1)].view(torch.int32).cpu().tolist()
+    items, wb, _ = partition(w.seq_lens, w.q_lens, w.q_start()[:-1], w.num_heads, n_workers,
+                             w.seq_lens.astype(np.int64) - w.q_lens, sparse_k=w.sparse_k)
+    assert got.reshape(-1, 10).tolist() == [list(x) for x in items]
+    assert got_wb == wb
+
+
 @pytest.mark.parametrize("name", ["tiny", "uniform76", "deepseek_v3"])
 def test_back_to_back_calls_do_not_disturb_each_other(name):
     """Sixteen calls on one stream and one workspace with no synchronisation
