@@ -179,8 +179,22 @@ int mla_decode_plan(const mla_decode_params* params, mla_plan_t** plan, size_t* 
   pl->sm_count = sms;
   // one work item = 128 query rows on one CTA pair; under sparse top-k one
   // token's H rows (its own position list)
-  const int rc =
-      make_layout(p, n_pairs, 2 * n_pairs, p.sparse_top_k > 0 ? p.num_heads : 128, &pl->lay);
+  const int rows_per_group = p.sparse_top_k > 0 ? p.num_heads : 128;
+  // No run of this plan keeps more workers busy than its largest possible
+  // work allows (the partitioner gives a busy worker at least kMinUnits units
+  // of kOverheadTiles + tiles per row group), so a small plan launches a
+  // smaller grid; the work list is the same as with every pair.
+  {
+    const long long g_max = ceil_div((long long)p.max_seq_len_q * p.num_heads, rows_per_group);
+    long long groups = (long long)p.batch * g_max;
+    if (p.packed)
+      groups = std::min(groups, (long long)p.batch +
+                                    ceil_div(p.max_total_q * p.num_heads, rows_per_group));
+    const long long kv_rows = p.sparse_top_k > 0 ? p.sparse_top_k : p.max_seq_len;
+    const long long units = std::max(groups, 1LL) * (mla::kOverheadTiles + ceil_div(kv_rows, mla::kKvTile));
+    n_pairs = (int)std::max(1LL, std::min<long long>(n_pairs, units / mla::kMinUnits));
+  }
+  const int rc = make_layout(p, n_pairs, 2 * n_pairs, rows_per_group, &pl->lay);
   if (rc != MLA_OK) {
     delete pl;
     return rc;

@@ -121,6 +121,12 @@ struct Layout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The partitioner's cost model: a row group costs kOverheadTiles + its KV
+// tiles (the overhead is the query load and the epilogue, in tile units;
+// measured ~3.2), and every busy worker gets at least kMinUnits units.
+constexpr long long kOverheadTiles = 3;
+constexpr long long kMinUnits = 4;
+
 // The query split of the FP8 MMA path with a bf16 query (mla_qsplit.cu), one
 // record of kQSplitUnits 16-byte units per (query row, CTA half): latent hi
 // codes (units 0-15), latent lo codes (16-31), RoPE hi (32-33), RoPE lo

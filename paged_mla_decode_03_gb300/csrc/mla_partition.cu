@@ -33,8 +33,8 @@ namespace {
 // One CTA of 128..1024 threads, sized by the launch from the plan's bounds
 // (fewer warps make the block-wide steps cheaper on small problems).
 constexpr int kMaxThreads = 1024;
-constexpr long long kOverheadTiles = 3;  // c0: query load + epilogue, in tile units (measured ~3.2)
-constexpr long long kMinUnits = 4;       // least work per busy worker: one item of one tile
+// the cost model's kOverheadTiles and kMinUnits are in mla_common.cuh (the
+// plan bounds its worker count with them)
 constexpr int kBoundTable = 512;         // workers whose range boundaries are tabulated
 
 struct Shared {
