@@ -27,7 +27,8 @@
 //  * O = P V with P from shared memory: M = 128 query rows, N = 256 (CTA r's
 //    V dims, read MN-major from its latent chunks), K = 64 KV rows, into a
 //    128 x 256 fp32 TMEM accumulator.  The PV commit is multicast to both CTAs,
-//    so the (single) P tile is rewritten only after both CTAs' PV read it.
+//    so each of the two P tiles (one per tile parity) is rewritten only after
+//    both CTAs' PV read it.
 // Warp roles (448 threads, 704 with e4m3): warp 0 TMA producer (4-stage KV
 // ring), warp 1 MMA issuer and TMEM owner (QK runs up to two tiles ahead of
 // PV), warps 2-9 softmax of the 64 owned rows in two groups of four that take
@@ -45,9 +46,10 @@
 // in the operand layouts, the query enters as e4m3 (a bf16 row as two parts
 // under a power-of-two scale per CTA half, split before this kernel by
 // mla_qsplit.cu; the scores are brought back by it before the halves are
-// added), and so does P (two parts).  Widening on request: eight more warps (14-21) widen each
-// staged e4m3 tile to bf16 in shared memory (exact; the k_scale lives in
-// bmm1/bmm2), and the bf16 ring is 3 deep beside a 2-deep e4m3 staging ring.
+// added), and so does P (two parts).  Widening on request: eight more warps
+// (14-21) widen each staged e4m3 tile to bf16 in shared memory (exact; the
+// k_scale lives in bmm1/bmm2), and the bf16 ring is 3 deep beside a 2-deep
+// e4m3 staging ring.
 // Under sparse top-k selection (a separate instantiation, two warps more) a
 // work item is one token's H query rows and its KV tiles are 64 entries of
 // the token's position list: warp 0 and the two extra warps gather the listed
