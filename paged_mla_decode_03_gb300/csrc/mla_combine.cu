@@ -15,12 +15,12 @@
 // An entry with no chunk (a decode-context-parallel rank that holds no row of
 // the request) writes the empty sum: O = 0 and lse = -inf.
 //
-// Grid: (row blocks of 8 rows) x (combine entries), 256 threads; 32 threads
-// per row, 16 output dims per thread.  Every load of a thread (the LSEs and
-// the 16-dim slices of up to kBatch chunks) is issued before any is used, so
-// a row costs one memory round trip per kBatch chunks, and the grid fits one
-// wave.  Blocks past the live number of entries exit at once, so the grid
-// depends only on plan-time bounds.
+// Grid: (row blocks of 8 rows) x min(entry bound, 4 x SMs), 256 threads; a
+// block takes entries blockIdx.y, + gridDim.y, ...; 32 threads per row, 16
+// output dims per thread.  Every load of a thread (the LSEs and the 16-dim
+// slices of up to kBatch chunks) is issued before any is used, so a row costs
+// one memory round trip per kBatch chunks.  Blocks past the live number of
+// entries exit at once, so the grid depends only on plan-time bounds.
 #include <cuda_bf16.h>
 
 #include <algorithm>
